@@ -1,0 +1,374 @@
+"""Pins of the CPU oracle to facts outside itself (closed forms, brute force,
+library routines, invariants).  Each test is chosen so that a plausible slip
+in the oracle -- a swapped nibble, a wrong code offset, a dropped term, a
+wrong tie rule, a transposed operand -- fails at least one of them."""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import workload as W
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- scalar conversions
+
+def test_half_to_double_matches_numpy_for_every_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(b) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def _nearest_bf16_exact(v: float) -> int:
+    """Brute force: the bf16 value nearest to v (ties to even mantissa)."""
+    f32 = np.float32(v)
+    base = int(np.array([f32]).view(np.uint32)[0] >> 16)
+    best = None
+    for cand in range(max(0, base - 2) if v >= 0 else base - 2, base + 3):
+        cand &= 0xFFFF
+        cv = float(np.array([cand << 16], np.uint32).view(np.float32)[0])
+        if not math.isfinite(cv) or (cv < 0) != (v < 0) and cv != 0:
+            continue
+        d = abs(Fraction(cv) - Fraction(v))
+        key = (d, cand & 1)
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return best[1]
+
+
+def test_bf16_rounding_single_rounding_from_double():
+    r = rng(1)
+    vals = list(r.standard_normal(300) * 10.0 ** r.uniform(-30, 30, 300))
+    # values just above a bf16 rounding midpoint that a double->float->bf16
+    # path would round the wrong way
+    for base in (1.0, 3.0, -7.5, 1e-20, 6e30):
+        b = np.float32(base).view(np.uint32) & 0xFFFF0000
+        mid = float(np.uint32(b | 0x8000).view(np.float32))
+        vals += [mid + abs(mid) * 2.0 ** -40, mid - abs(mid) * 2.0 ** -40, mid]
+    for v in vals:
+        assert oracle.round_bf16(np.array([v]))[0] == _nearest_bf16_exact(v), v
+
+
+def test_bf16_rounding_matches_torch_on_float32_inputs():
+    x = torch.randn(100000, generator=torch.Generator().manual_seed(3)) * 50
+    ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_bf16(x.double().numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_silu_closed_forms():
+    assert oracle.silu(0.0) == 0.0
+    for g in (-30.0, -3.0, -0.5, 0.25, 2.0, 40.0):
+        assert oracle.silu(g) == pytest.approx(g * scipy.special.expit(g), rel=1e-14, abs=1e-300)
+    assert oracle.silu(2.0) == pytest.approx(2.0 / (1.0 + math.exp(-2.0)), rel=1e-15)
+
+
+# ---------------------------------------------------------------- dequantization
+
+def test_dequant_roundtrip_bound_against_generator_weights():
+    cfg = W.CONFIGS["tiny"]
+    rows, K = 64, 256
+    q, s = W.quant_matrix(cfg, 0, W.T_GATE, 3, rows, K)
+    wf = np.empty((rows, K), np.float32)
+    lib = W._hostlib()
+    assert lib.gen_dense_matrix(cfg.seed, cfg.wset, 0, W.T_GATE, 3, rows, K, cfg.weight_sigma,
+                                wf.ctypes.data, None, 1) == 0
+    scale = s.view(np.float16).astype(np.float64)
+    for r in range(rows):
+        wq = oracle.dequant_row(q[r], s[r])
+        bound = 0.5 * np.repeat(scale[r], 32) * (1 + 1e-6) + 1e-30
+        err = np.abs(wq - wf[r].astype(np.float64))
+        assert np.all(err <= bound), (r, np.max(err / bound))
+    # and the codes use the full range: the block maximum maps to +-7
+    codes = np.stack([q & 15, q >> 4], -1).reshape(rows, K // 32, 32).astype(int) - 8
+    assert np.all(np.abs(codes).max(-1) == 7)
+
+
+def test_dequant_exact_for_representable_blocks():
+    r = rng(2)
+    for trial in range(50):
+        sc = 2.0 ** r.integers(-12, 3)
+        codes = r.integers(-7, 8, 32)
+        codes[r.integers(0, 32)] = 7 * (1 if r.random() < 0.5 else -1)
+        w = (codes * sc).astype(np.float32)
+        q = np.zeros(16, np.uint8)
+        sbits = W._hostlib().gen_quant_block(w.ctypes.data, q.ctypes.data)
+        assert np.float16(sc).view(np.uint16) == sbits
+        got = oracle.dequant_row(q, np.array([sbits], np.uint16))
+        assert np.array_equal(got, w.astype(np.float64))
+
+
+def test_dequant_nibble_order_one_hot():
+    # row: element k has code (k % 16) - 8; byte i = code(2i) low | code(2i+1) high
+    K = 64
+    nib = np.arange(K) % 16
+    q = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    s = np.array([np.float16(0.5).view(np.uint16)] * (K // 32), np.uint16)
+    w = oracle.dequant_row(q, s)
+    for k in range(K):
+        assert w[k] == ((k % 16) - 8) * 0.5
+
+
+# ---------------------------------------------------------------- router + top-k
+
+def test_router_logits_one_hot_picks_a_column():
+    E, H = 16, 64
+    Wr = rng(4).standard_normal((E, H)).astype(np.float32)
+    b = rng(5).standard_normal(E).astype(np.float32)
+    x = np.zeros((3, H), np.uint16)
+    one = np.float32(1.0).view(np.uint32) >> 16
+    x[0, 5] = one
+    x[1, 63] = one
+    z = oracle.router_logits(Wr, b, x)
+    assert np.array_equal(z[0], Wr[:, 5].astype(np.float64) + b)
+    assert np.array_equal(z[1], Wr[:, 63].astype(np.float64) + b)
+    assert np.array_equal(z[2], b.astype(np.float64))
+
+
+def _brute_rank_select(z, k):
+    E = len(z)
+    rank = [sum(1 for f in range(E) if z[f] > z[e] or (z[f] == z[e] and f < e)) for e in range(E)]
+    sel = sorted([e for e in range(E) if rank[e] < k], key=lambda e: rank[e])
+    return sel
+
+
+@pytest.mark.parametrize("E,k", [(8, 1), (8, 3), (16, 2), (64, 8), (256, 8), (512, 10)])
+def test_topk_matches_brute_force_rank_selection(E, k):
+    r = rng(E * 7 + k)
+    z = r.standard_normal((20, E))
+    z[:10] = np.round(z[:10] * 2) / 2  # many exact ties
+    ids, w, margin = oracle.topk_softmax(z, k)
+    for t in range(20):
+        sel = _brute_rank_select(list(z[t]), k)
+        assert list(ids[t]) == sel
+        srt = sorted(z[t], reverse=True)
+        if k < E:
+            assert margin[t] == srt[k - 1] - srt[k]
+
+
+def test_routing_weights_closed_form_k2():
+    z = np.array([[1.5, -0.25, 0.75, 3.0]])
+    ids, w, _ = oracle.topk_softmax(z, 2)
+    assert list(ids[0]) == [3, 0]
+    assert w[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(1.5 - 3.0)), rel=1e-15)
+    assert w[0, 1] == pytest.approx(1.0 / (1.0 + math.exp(3.0 - 1.5)), rel=1e-15)
+
+
+def test_routing_weights_sum_to_one_positive_descending_and_full_softmax_identity():
+    z = rng(6).standard_normal((50, 256)) * 3
+    ids, w, _ = oracle.topk_softmax(z, 8)
+    ids2, w2 = oracle.topk_softmax_full(z, 8)
+    assert np.array_equal(ids, ids2)
+    assert np.allclose(w, w2, rtol=1e-13, atol=0)
+    assert np.all(np.abs(w.sum(1) - 1) < 1e-12)
+    assert np.all(w > 0)
+    assert np.all(np.diff(w, axis=1) <= 0)
+    # the selection's weights are scipy's softmax restricted to it
+    for t in range(5):
+        p = scipy.special.softmax(z[t][ids[t]])
+        assert np.allclose(w[t], p, rtol=1e-13)
+
+
+def test_softmax_is_shift_invariant_in_the_bias():
+    z = rng(7).standard_normal((4, 32))
+    a = oracle.topk_softmax(z, 4)
+    b = oracle.topk_softmax(z + 1000.0, 4)
+    assert np.array_equal(a[0], b[0])
+    assert np.allclose(a[1], b[1], rtol=1e-9)
+
+
+# ---------------------------------------------------------------- bucketing
+
+def test_bucket_invariants_and_brute_force_grouping():
+    r = rng(8)
+    T, k, E = 37, 5, 16
+    ids = np.stack([r.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, pt, pj = oracle.bucket(ids, E)
+    assert counts.sum() == T * k
+    assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts)
+    ref = sorted((ids[t, j], t, j) for t in range(T) for j in range(k))
+    assert [(ids[t, j], t, j) for t, j in zip(pt, pj)] == ref
+    assert len(set(zip(pt, pj))) == T * k
+
+
+# ---------------------------------------------------------------- expert FFN
+
+def _pack(codes):
+    """codes in -8..7, shape [..., K] -> bytes [..., K/2]."""
+    n = (np.asarray(codes) + 8).astype(np.uint8)
+    return (n[..., 0::2] | (n[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _hbits(v, shape):
+    return np.full(shape, np.float16(v).view(np.uint16), np.uint16)
+
+
+def test_expert_ffn_hand_computed_example():
+    H = F = 32
+    ex = dict(gate_q=_pack(np.ones((F, H), int)), gate_s=_hbits(2 ** -4, (F, 1)),
+              up_q=_pack(2 * np.ones((F, H), int)), up_s=_hbits(2 ** -4, (F, 1)),
+              down_q=_pack(np.ones((H, F), int)), down_s=_hbits(2 ** -5, (H, 1)))
+    y = oracle.expert_ffn(ex, np.ones(H))
+    # g = 32 * 1/16 = 2, u = 32 * 2/16 = 4, h = silu(2) * 4, y_i = 32 * h / 32
+    h = 2.0 / (1.0 + math.exp(-2.0)) * 4.0
+    assert np.allclose(y, h, rtol=1e-15)
+
+
+def test_expert_ffn_operand_orientation():
+    # gate/up rows index the FFN dim, down rows index the hidden dim: an
+    # asymmetric example with H != F catches a transposed operand
+    H, F = 64, 32
+    gcode = np.zeros((F, H), int)
+    gcode[3, 10] = 4  # g_3 = 4 * s * x_10
+    ucode = np.zeros((F, H), int)
+    ucode[3, 10] = 2
+    dcode = np.zeros((H, F), int)
+    dcode[40, 3] = -3  # y_40 = -3 * s * h_3
+    ex = dict(gate_q=_pack(gcode), gate_s=_hbits(0.5, (F, H // 32)),
+              up_q=_pack(ucode), up_s=_hbits(0.5, (F, H // 32)),
+              down_q=_pack(dcode), down_s=_hbits(0.25, (H, F // 32)))
+    x = np.zeros(H)
+    x[10] = 1.5
+    y = oracle.expert_ffn(ex, x)
+    g, u = 4 * 0.5 * 1.5, 2 * 0.5 * 1.5
+    h3 = g / (1 + math.exp(-g)) * u
+    expect = np.zeros(H)
+    expect[40] = -3 * 0.25 * h3
+    assert np.allclose(y, expect, rtol=1e-15, atol=0)
+
+
+def _np_dequant(q, s):
+    lo = (q & 15).astype(np.float64) - 8
+    hi = (q >> 4).astype(np.float64) - 8
+    codes = np.empty(q.shape[:-1] + (q.shape[-1] * 2,))
+    codes[..., 0::2], codes[..., 1::2] = lo, hi
+    sc = s.view(np.float16).astype(np.float64)
+    return (codes.reshape(*codes.shape[:-1], -1, 32) * sc[..., None]).reshape(codes.shape)
+
+
+def _tiny_layer(permuted=False, top_k=None, shared=True):
+    cfg = W.CONFIGS["tiny"].replace(permuted_slots=permuted)
+    if not shared:
+        cfg = cfg.replace(shared_ffn=0)
+    L = W.layer(cfg, 0)
+    return cfg, L
+
+
+def test_top1_layer_equals_dense_swiglu_of_the_chosen_expert():
+    cfg, L = _tiny_layer(shared=False)
+    x = W.activations(cfg)
+    y, ids, w, _ = oracle.moe_forward(L, 1, x)
+    assert np.all(w == 1.0)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(x.shape[0]):
+        s = L["slot_of_expert"][ids[t, 0]]
+        Wg = _np_dequant(L["gate_q"][s], L["gate_s"][s])
+        Wu = _np_dequant(L["up_q"][s], L["up_s"][s])
+        Wd = _np_dequant(L["down_q"][s], L["down_s"][s])
+        g, u = Wg @ xf[t], Wu @ xf[t]
+        ref = Wd @ (g * scipy.special.expit(g) * u)
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_dense_identity_k_equals_E():
+    cfg, L = _tiny_layer()
+    E = cfg.n_experts
+    x = W.activations(cfg)
+    y, ids, w, _ = oracle.moe_forward(L, E, x)
+    z = oracle.router_logits(L["router_w"], L["router_b"], x)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    sh = {k[3:]: v for k, v in L.items() if k.startswith("sh_")}
+    for t in range(x.shape[0]):
+        p = scipy.special.softmax(z[t])
+        ref = sum(p[e] * oracle.expert_ffn({n: L[n][L["slot_of_expert"][e]] for n in
+                                            ("gate_q", "gate_s", "up_q", "up_s", "down_q",
+                                             "down_s")}, xf[t]) for e in range(E))
+        ref = ref + oracle.expert_ffn(sh, xf[t])
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_slot_permutation_invariance_is_bit_exact():
+    cfg, L0 = _tiny_layer(permuted=False)
+    _, L1 = _tiny_layer(permuted=True)
+    assert not np.array_equal(L0["slot_of_expert"], L1["slot_of_expert"])
+    x = W.activations(cfg)
+    y0 = oracle.moe_forward(L0, cfg.top_k, x)[0]
+    y1 = oracle.moe_forward(L1, cfg.top_k, x)[0]
+    assert np.array_equal(y0, y1)
+
+
+def test_token_independence_is_exact():
+    cfg, L = _tiny_layer()
+    x = W.activations(cfg)
+    yall = oracle.moe_forward(L, cfg.top_k, x)[0]
+    for t in range(x.shape[0]):
+        assert np.array_equal(oracle.moe_forward(L, cfg.top_k, x[t:t + 1])[0][0], yall[t])
+
+
+def test_combine_token_matches_layer():
+    cfg, L = _tiny_layer(permuted=True)
+    x = W.activations(cfg)
+    y, ids, w, _ = oracle.moe_forward(L, cfg.top_k, x)
+    names = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+    sh = {n: L["sh_" + n] for n in names}
+    for t in range(x.shape[0]):
+        exs = [W.expert(cfg, 0, int(e)) for e in ids[t]]
+        yt = oracle.combine_token(exs, w[t], sh, x[t])
+        assert np.array_equal(yt, y[t])
+
+
+def test_swiglu_zero_gate_or_up_gives_shared_only():
+    cfg, L = _tiny_layer()
+    x = W.activations(cfg)
+    names = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+    sh = {n: L["sh_" + n] for n in names}
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    for zero in ("gate_s", "up_s"):
+        Lz = dict(L)
+        Lz[zero] = np.zeros_like(L[zero])
+        y = oracle.moe_forward(Lz, cfg.top_k, x)[0]
+        for t in range(x.shape[0]):
+            assert np.array_equal(y[t], oracle.expert_ffn(sh, xf[t]))
+
+
+def test_forced_ids_reproduce_own_selection():
+    cfg, L = _tiny_layer()
+    x = W.activations(cfg)
+    y, ids, w, _ = oracle.moe_forward(L, cfg.top_k, x)
+    y2, ids2, w2, _ = oracle.moe_forward(L, cfg.top_k, x, forced_ids=ids)
+    assert np.array_equal(ids, ids2) and np.array_equal(y, y2)
+
+
+# ---------------------------------------------------------------- stack
+
+def test_residual_with_zero_output_is_identity_and_stack_composes():
+    cfg, L = _tiny_layer()
+    x = W.activations(cfg)
+    assert np.array_equal(oracle.residual(x, np.zeros(x.shape)), x)
+    Lz = dict(L)
+    for n in ("gate_s", "up_s", "sh_gate_s", "sh_up_s"):
+        Lz[n] = np.zeros_like(L[n])
+    out, trace, _ = oracle.stack_forward([Lz, Lz, Lz], cfg.top_k, x)
+    assert np.array_equal(out, x)
+    # two real layers = two single-layer steps with the residual between
+    L1 = W.layer(cfg, 1)
+    out, trace, ids = oracle.stack_forward([L, L1], cfg.top_k, x)
+    h1 = oracle.residual(x, oracle.moe_forward(L, cfg.top_k, x)[0])
+    h2 = oracle.residual(h1, oracle.moe_forward(L1, cfg.top_k, h1)[0])
+    assert np.array_equal(trace[0], h1) and np.array_equal(out, h2)
+    # residual: one rounding of h + bf16(y)
+    hf = W.bf16_bits_to_f32(x).astype(np.float64)
+    y0 = oracle.moe_forward(L, cfg.top_k, x)[0]
+    yb = oracle.bf16_to_f64(oracle.round_bf16(y0))
+    assert np.array_equal(h1, oracle.round_bf16(hf + yb))
