@@ -1,0 +1,148 @@
+/*
+ * moe.h -- C ABI of the GB300 routed Mixture-of-Experts FFN layer.
+ *
+ * What a layer computes (the hot path of the local-inference engines
+ * described in "nano-cuda-moe-qwen38" -- memory-hierarchy and prefill
+ * paragraphs --, "cyber-on-strata" -- two-tier memory section -- and the
+ * Strata / Project Maya page -- "MoE architecture and hierarchical caching"
+ * and "Strata tiers" sections): per token,
+ *   z   = W_r x + b                       router logits (fp32 weights)
+ *   S   = top-k of z (ties: lower id)     the experts that run
+ *   w   = softmax of z over S             routing weights, sum to 1
+ *   y   = sum_{e in S} w_e FFN_{slot(e)}(x) + FFN_shared(x)
+ *   FFN(x) = W_d (silu(W_g x) * (W_u x))  SwiGLU expert
+ * Every expert is reached through a resident slot table (the pages' VRAM
+ * expert cache, here sized to hold all experts in HBM).  Expert weights are
+ * symmetric 4-bit codes in blocks of 32 along the reduction dimension with
+ * one binary16 scale per block (the block-scale idea of the pages' int8 KV
+ * cache, one scale per 32 values): weight = (nibble - 8) * scale.
+ *
+ * Conventions for every entry point:
+ *  - No C++ exceptions cross this boundary; errors are moe_status codes and
+ *    a thread-local message from moe_last_error().
+ *  - All work is asynchronous on the given CUDA stream (a cudaStream_t
+ *    passed as void*, NULL = legacy default stream), except where stated.
+ *  - Activation pointers (x, y, ids, weights) may be device pointers or host
+ *    pointers (pinned or pageable).  Host inputs are copied into library
+ *    buffers on the stream; when an output is a host pointer the call copies
+ *    it back and synchronises the stream before returning.
+ *  - The library owns all device memory it uses (weights and workspaces are
+ *    allocated in moe_layer_create); no other call allocates device memory.
+ *  - Calls that use the same layer object must not run concurrently (they
+ *    share its workspace); stack calls use the first layer's workspace.
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_layer moe_layer; /* opaque, owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,  /* bad argument, config or weight table */
+  MOE_ERR_CUDA = -2,     /* a CUDA runtime call failed */
+  MOE_ERR_OOM = -3,      /* device allocation failed (create only) */
+  MOE_ERR_CAPACITY = -4, /* n_tokens outside [1, max_tokens] */
+  MOE_ERR_BOUNDS = -5,   /* a kernel met an out-of-range slot */
+  MOE_ERR_TIMEOUT = -6   /* a bounded device-side wait ran out */
+} moe_status;
+
+/* Layer shape.  Limits: hidden % 128 == 0 and 128 <= hidden <= 8192;
+ * 1 <= n_experts <= 1024; 1 <= top_k <= min(16, n_experts);
+ * ffn % 128 == 0 and 128 <= ffn <= 4096; shared_ffn == 0 or a multiple of
+ * 128 up to 4096; n_slots == n_experts (the slot table holds every expert);
+ * 1 <= max_tokens <= 65536 (sizes the workspaces). */
+typedef struct {
+  int32_t hidden;     /* H */
+  int32_t n_experts;  /* E */
+  int32_t top_k;      /* k */
+  int32_t ffn;        /* F: routed expert intermediate size */
+  int32_t shared_ffn; /* Fs: shared expert intermediate size, 0 = none */
+  int32_t n_slots;    /* S: expert-cache slots */
+  int32_t max_tokens; /* largest n_tokens any call will pass */
+} moe_layer_config;
+
+/* Packed weights, all row-major with the reduction dimension contiguous.
+ * A packed row of K weights is K/2 bytes of codes (byte i holds element 2i
+ * in its low nibble and element 2i+1 in its high nibble) and K/32 binary16
+ * scales (raw bits).  Routed tensors are indexed by slot:
+ *   gate_q, up_q  [S][F][H/2]   gate_s, up_s  [S][F][H/32]
+ *   down_q        [S][H][F/2]   down_s        [S][H][F/32]
+ *   sh_gate_q, sh_up_q [Fs][H/2], sh_*_s [Fs][H/32]
+ *   sh_down_q [H][Fs/2], sh_down_s [H][Fs/32]        (NULL when Fs == 0)
+ *   router_w [E][H] fp32, router_bias [E] fp32 or NULL (zero bias)
+ *   slot_of_expert [E]: a permutation of 0..S-1 (validated at create). */
+typedef struct {
+  const float* router_w;
+  const float* router_bias;
+  const int32_t* slot_of_expert;
+  const uint8_t* gate_q;
+  const uint16_t* gate_s;
+  const uint8_t* up_q;
+  const uint16_t* up_s;
+  const uint8_t* down_q;
+  const uint16_t* down_s;
+  const uint8_t* sh_gate_q;
+  const uint16_t* sh_gate_s;
+  const uint8_t* sh_up_q;
+  const uint16_t* sh_up_s;
+  const uint8_t* sh_down_q;
+  const uint16_t* sh_down_s;
+} moe_layer_weights;
+
+/* Creates a layer: validates cfg and the slot table, allocates the layer's
+ * HBM (weights + workspaces) and copies the weights in.  weights_on_device
+ * = 1: every pointer in w is a device pointer, 0: host pointers.  The caller
+ * keeps ownership of its buffers and may free them after the call returns
+ * (the call synchronises the device).  On success *out owns everything and
+ * must be released with moe_layer_destroy. */
+moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights* w,
+                            int weights_on_device, moe_layer** out);
+
+/* Frees a layer (NULL is a no-op).  Synchronises the device first. */
+void moe_layer_destroy(moe_layer* layer);
+
+/* Router + top-k only.  x_bf16 [T][H] (bf16 bits); outputs topk_ids [T][k]
+ * (logical expert ids, descending logit, ties to the lower id) and topk_w
+ * [T][k] (softmax over the selected logits). */
+moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t* topk_ids,
+                     float* topk_w, void* stream);
+
+/* One layer: y_bf16 [T][H] = layer(x_bf16 [T][H]).  x and y must not
+ * overlap.  n_tokens <= 4 runs the decode path (fused dequant GEMVs);
+ * larger batches run the prefill path (bucketed grouped GEMM on tcgen05). */
+moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void* y_bf16,
+                       void* stream);
+
+/* Residual stack: h_0 = x, h_{l+1} = bf16(h_l + bf16(layer_l(h_l))),
+ * y = h_L.  All layers must share one config.  x == y is allowed. */
+moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,
+                             int n_tokens, void* y_bf16, void* stream);
+
+/* moe_stack_forward that also records, when the pointers are not NULL,
+ * every layer's output h_{l+1} into h_trace [L][T][H] (bf16 bits) and every
+ * layer's top-k ids into ids_trace [L][T][k]. */
+moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
+                                    int n_tokens, void* y_bf16, void* h_trace_bf16,
+                                    int32_t* ids_trace, void* stream);
+
+/* Synchronises `stream`, then returns and clears the layer's device error
+ * word (MOE_ERR_BOUNDS or MOE_ERR_TIMEOUT if a kernel recorded one). */
+moe_status moe_status_sync(moe_layer* layer, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

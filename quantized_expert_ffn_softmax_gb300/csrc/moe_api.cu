@@ -1,0 +1,490 @@
+// C ABI of the routed MoE FFN layer: validation, HBM ownership, staging of
+// host buffers, and dispatch to the decode (1..4 tokens) and prefill paths.
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();
+  return fail(e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "%s: %s", what,
+              cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(call, what)                  \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+uint64_t wait_timeout_ns() {
+  const char* s = getenv("MOE_WAIT_TIMEOUT_US");
+  if (s && *s) {
+    long long us = atoll(s);
+    if (us > 0) return (uint64_t)us * 1000ull;
+  }
+  return 1000000000ull;  // 1 s
+}
+
+moe_status validate_config(const moe_layer_config* c) {
+  if (!c) return fail(MOE_ERR_INVALID, "config is NULL");
+  if (c->hidden < 128 || c->hidden > 8192 || c->hidden % 128)
+    return fail(MOE_ERR_INVALID, "hidden=%d: need a multiple of 128 in [128, 8192]", c->hidden);
+  if (c->n_experts < 1 || c->n_experts > moe::kMaxExperts)
+    return fail(MOE_ERR_INVALID, "n_experts=%d: need 1..%d", c->n_experts, moe::kMaxExperts);
+  if (c->top_k < 1 || c->top_k > moe::kMaxTopK || c->top_k > c->n_experts)
+    return fail(MOE_ERR_INVALID, "top_k=%d: need 1..min(16, n_experts)", c->top_k);
+  if (c->ffn < 128 || c->ffn > 4096 || c->ffn % 128)
+    return fail(MOE_ERR_INVALID, "ffn=%d: need a multiple of 128 in [128, 4096]", c->ffn);
+  if (c->shared_ffn < 0 || c->shared_ffn > 4096 || c->shared_ffn % 128)
+    return fail(MOE_ERR_INVALID, "shared_ffn=%d: need 0 or a multiple of 128 up to 4096",
+                c->shared_ffn);
+  if (c->n_slots != c->n_experts)
+    return fail(MOE_ERR_INVALID, "n_slots=%d must equal n_experts=%d", c->n_slots, c->n_experts);
+  if (c->max_tokens < 1 || c->max_tokens > 65536)
+    return fail(MOE_ERR_INVALID, "max_tokens=%d: need 1..65536", c->max_tokens);
+  return MOE_OK;
+}
+
+struct Stage {
+  const uint16_t* x = nullptr;
+  uint16_t* y = nullptr;
+  bool y_host = false;
+};
+
+}  // namespace
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights* w,
+                            int weights_on_device, moe_layer** out) {
+  if (!out) return fail(MOE_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  moe_status st = validate_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!w || !w->router_w || !w->slot_of_expert || !w->gate_q || !w->gate_s || !w->up_q ||
+      !w->up_s || !w->down_q || !w->down_s)
+    return fail(MOE_ERR_INVALID, "a required weight pointer is NULL");
+  if (cfg->shared_ffn > 0 && (!w->sh_gate_q || !w->sh_gate_s || !w->sh_up_q || !w->sh_up_s ||
+                              !w->sh_down_q || !w->sh_down_s))
+    return fail(MOE_ERR_INVALID, "shared_ffn > 0 but a shared-expert pointer is NULL");
+  const char* fault = getenv("MOE_FAULT_ALLOC");
+  if (fault && atoi(fault) == 1) return fail(MOE_ERR_OOM, "allocation failure injected by MOE_FAULT_ALLOC");
+
+  const int H = cfg->hidden, E = cfg->n_experts, F = cfg->ffn, Fs = cfg->shared_ffn;
+  const int S = cfg->n_slots, k = cfg->top_k, Tm = cfg->max_tokens;
+  const cudaMemcpyKind kind = weights_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+
+  // slot table: must be a permutation of 0..S-1
+  std::vector<int32_t> slots(E);
+  CUDA_TRY(cudaMemcpy(slots.data(), w->slot_of_expert, sizeof(int32_t) * E,
+                      weights_on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost),
+           "read slot table");
+  {
+    std::vector<char> seen(S, 0);
+    for (int e = 0; e < E; ++e) {
+      const int s = slots[e];
+      if (s < 0 || s >= S || seen[s])
+        return fail(MOE_ERR_INVALID, "slot_of_expert is not a permutation (expert %d -> %d)", e, s);
+      seen[s] = 1;
+    }
+  }
+
+  moe_layer* L = new moe_layer();
+  L->cfg = *cfg;
+  cudaGetDevice(&L->device);
+  cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+
+  // ---- weights: one allocation, 256-B aligned sub-buffers
+  struct Piece {
+    const void* src;
+    size_t bytes;
+    size_t off;
+  };
+  std::vector<Piece> pieces;
+  size_t off = 0;
+  auto add = [&](const void* src, size_t bytes) {
+    off = align_up(off, 256);
+    pieces.push_back({src, bytes, off});
+    off += bytes;
+    return pieces.size() - 1;
+  };
+  const size_t gq = (size_t)S * F * (H / 2), gs = (size_t)S * F * (H / 32) * 2;
+  const size_t dq = (size_t)S * H * (F / 2), ds = (size_t)S * H * (F / 32) * 2;
+  size_t i_rw = add(w->router_w, sizeof(float) * E * H);
+  size_t i_rb = add(w->router_bias, sizeof(float) * E);
+  size_t i_sl = add(w->slot_of_expert, sizeof(int32_t) * E);
+  size_t i_gq = add(w->gate_q, gq), i_gs = add(w->gate_s, gs);
+  size_t i_uq = add(w->up_q, gq), i_us = add(w->up_s, gs);
+  size_t i_dq = add(w->down_q, dq), i_ds = add(w->down_s, ds);
+  size_t i_sgq = 0, i_sgs = 0, i_suq = 0, i_sus = 0, i_sdq = 0, i_sds = 0;
+  if (Fs > 0) {
+    i_sgq = add(w->sh_gate_q, (size_t)Fs * (H / 2));
+    i_sgs = add(w->sh_gate_s, (size_t)Fs * (H / 32) * 2);
+    i_suq = add(w->sh_up_q, (size_t)Fs * (H / 2));
+    i_sus = add(w->sh_up_s, (size_t)Fs * (H / 32) * 2);
+    i_sdq = add(w->sh_down_q, (size_t)H * (Fs / 2));
+    i_sds = add(w->sh_down_s, (size_t)H * (Fs / 32) * 2);
+  }
+  L->weights_bytes = align_up(off, 256);
+  cudaError_t e = cudaMalloc(&L->weights_block, L->weights_bytes);
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail(e, "cudaMalloc(weights)");
+  }
+  char* base = static_cast<char*>(L->weights_block);
+  for (const Piece& p : pieces) {
+    if (p.src)
+      e = cudaMemcpy(base + p.off, p.src, p.bytes, kind);
+    else
+      e = cudaMemset(base + p.off, 0, p.bytes);  // router bias omitted: zero
+    if (e != cudaSuccess) {
+      moe_layer_destroy(L);
+      return cuda_fail(e, "copy weights");
+    }
+  }
+  auto at = [&](size_t i) { return static_cast<const void*>(base + pieces[i].off); };
+  L->dev.router_w = (const float*)at(i_rw);
+  L->dev.router_b = (const float*)at(i_rb);
+  L->dev.slot_of = (const int32_t*)at(i_sl);
+  L->dev.gate_q = (const uint8_t*)at(i_gq);
+  L->dev.gate_s = (const uint16_t*)at(i_gs);
+  L->dev.up_q = (const uint8_t*)at(i_uq);
+  L->dev.up_s = (const uint16_t*)at(i_us);
+  L->dev.down_q = (const uint8_t*)at(i_dq);
+  L->dev.down_s = (const uint16_t*)at(i_ds);
+  if (Fs > 0) {
+    L->dev.sh_gate_q = (const uint8_t*)at(i_sgq);
+    L->dev.sh_gate_s = (const uint16_t*)at(i_sgs);
+    L->dev.sh_up_q = (const uint8_t*)at(i_suq);
+    L->dev.sh_up_s = (const uint16_t*)at(i_sus);
+    L->dev.sh_down_q = (const uint8_t*)at(i_sdq);
+    L->dev.sh_down_s = (const uint16_t*)at(i_sds);
+  }
+
+  // ---- workspace
+  const int Fmax = F > Fs ? F : Fs;
+  const int routed_max = (moe::kMaxDecodeTokens * k < E) ? moe::kMaxDecodeTokens * k : E;
+  size_t wo = 0;
+  auto wadd = [&](size_t bytes) {
+    wo = align_up(wo, 256);
+    size_t r = wo;
+    wo += bytes;
+    return r;
+  };
+  size_t o_xbuf = wadd(sizeof(uint16_t) * 2 * moe::kMaxDecodeTokens * H);
+  size_t o_z = wadd(sizeof(float) * moe::kMaxDecodeTokens * E);
+  size_t o_h = wadd(sizeof(float) * moe::kMaxDecodeTokens * ((size_t)routed_max * F + Fmax));
+  size_t o_bar = wadd(sizeof(moe::GridBarrier));
+  size_t o_err = wadd(sizeof(int) * 4);
+  size_t o_xs = wadd(sizeof(uint16_t) * (size_t)Tm * H);
+  size_t o_ys = wadd(sizeof(uint16_t) * (size_t)Tm * H);
+  size_t o_yl = wadd(sizeof(uint16_t) * (size_t)Tm * H);
+  size_t o_is = wadd(sizeof(int32_t) * (size_t)Tm * k);
+  size_t o_ws = wadd(sizeof(float) * (size_t)Tm * k);
+  size_t o_pf = wadd(moe::prefill_workspace_bytes(*cfg));
+  L->ws.bytes = align_up(wo, 256);
+  e = cudaMalloc(&L->ws_block, L->ws.bytes);
+  if (e != cudaSuccess) {
+    moe_layer_destroy(L);
+    return cuda_fail(e, "cudaMalloc(workspace)");
+  }
+  char* wb = static_cast<char*>(L->ws_block);
+  L->ws.xbuf = (uint16_t*)(wb + o_xbuf);
+  L->ws.z = (float*)(wb + o_z);
+  L->ws.hbuf = (float*)(wb + o_h);
+  L->ws.bar = (moe::GridBarrier*)(wb + o_bar);
+  L->ws.err = (int*)(wb + o_err);
+  L->ws.x_stage = (uint16_t*)(wb + o_xs);
+  L->ws.y_stage = (uint16_t*)(wb + o_ys);
+  L->ws.y_layer = (uint16_t*)(wb + o_yl);
+  L->ws.ids_stage = (int32_t*)(wb + o_is);
+  L->ws.w_stage = (float*)(wb + o_ws);
+  L->ws.scratch = wb + o_pf;
+  e = cudaMemset(L->ws_block, 0, L->ws.bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    moe_layer_destroy(L);
+    return cuda_fail(e, "initialise workspace");
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer* layer) {
+  if (!layer) return;
+  cudaDeviceSynchronize();
+  if (layer->weights_block) cudaFree(layer->weights_block);
+  if (layer->ws_block) cudaFree(layer->ws_block);
+  cudaGetLastError();
+  delete layer;
+}
+
+moe_status moe_status_sync(moe_layer* layer, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID, "layer is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  int err = 0;
+  CUDA_TRY(cudaMemcpy(&err, layer->ws.err, sizeof(int), cudaMemcpyDeviceToHost), "read error word");
+  if (err != 0) {
+    CUDA_TRY(cudaMemset(layer->ws.err, 0, sizeof(int)), "clear error word");
+    return fail((moe_status)err, "a kernel recorded error %d", err);
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
+  moe::DecodeParams p;
+  memset(&p, 0, sizeof p);
+  const moe_layer_config& c = L0->cfg;
+  p.H = c.hidden;
+  p.E = c.n_experts;
+  p.k = c.top_k;
+  p.F = c.ffn;
+  p.Fs = c.shared_ffn;
+  p.T = T;
+  p.mode = mode;
+  p.max_units = ((T * c.top_k < c.n_experts) ? T * c.top_k : c.n_experts) + 1;
+  p.xbuf = L0->ws.xbuf;
+  p.z = L0->ws.z;
+  p.hbuf = L0->ws.hbuf;
+  p.bar = L0->ws.bar;
+  p.err = L0->ws.err;
+  p.timeout_ns = wait_timeout_ns();
+  const char* dbg = getenv("MOE_DEBUG_UNREACHABLE_BARRIER");
+  p.debug_extra_arrivals = (dbg && atoi(dbg) == 1) ? 1 : 0;
+  return p;
+}
+
+// Runs `n_layers` layers on <= 4 tokens with the decode kernel (chunks of
+// kMaxLayersPerLaunch layers per launch).
+moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x, int T,
+                      uint16_t* y, uint16_t* h_trace, int32_t* ids_trace, float* w_out, int mode,
+                      cudaStream_t stream) {
+  moe_layer* L0 = layers[0];
+  const int H = L0->cfg.hidden;
+  const uint16_t* cur = x;
+  for (int l0 = 0; l0 < n_layers; l0 += moe::kMaxLayersPerLaunch) {
+    const int nl = (n_layers - l0 < moe::kMaxLayersPerLaunch) ? n_layers - l0 : moe::kMaxLayersPerLaunch;
+    moe::DecodeParams p = decode_params(L0, T, mode);
+    p.n_layers = nl;
+    p.x_in = cur;
+    p.y_out = y;
+    p.h_trace = h_trace ? h_trace + (size_t)l0 * T * H : nullptr;
+    p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
+    p.w_out = w_out;
+    for (int l = 0; l < nl; ++l) p.layers[l] = layers[l0 + l]->dev;
+    const char* why = "";
+    moe_status st = moe::launch_decode(p, stream, L0->num_sms, &why);
+    if (st != MOE_OK) return fail(st, "decode launch: %s", why);
+    cur = y;
+  }
+  return MOE_OK;
+}
+
+__global__ void residual_kernel(const uint16_t* __restrict__ h, const uint16_t* __restrict__ y,
+                                uint16_t* __restrict__ out, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float a = __bfloat162float(__ushort_as_bfloat16(h[i]));
+    const float b = __bfloat162float(__ushort_as_bfloat16(y[i]));
+    out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a + b));
+  }
+}
+
+// One layer on any token count: decode kernel for <= 4 tokens, the prefill
+// path above that.
+moe_status forward_device(moe_layer* L, const uint16_t* x, int T, uint16_t* y, cudaStream_t s) {
+  if (T <= moe::kMaxDecodeTokens) {
+    moe_layer* one[1] = {L};
+    return run_decode(one, 1, x, T, y, nullptr, nullptr, nullptr, moe::kModeForward, s);
+  }
+  const char* why = "";
+  moe_status st = moe::launch_prefill(L, x, T, y, nullptr, nullptr, false, s, &why);
+  if (st != MOE_OK) return fail(st, "prefill: %s", why);
+  return MOE_OK;
+}
+
+moe_status check_common(moe_layer* L, const void* x, int T) {
+  if (!L) return fail(MOE_ERR_INVALID, "layer is NULL");
+  if (!x) return fail(MOE_ERR_INVALID, "x is NULL");
+  if (T < 1 || T > L->cfg.max_tokens)
+    return fail(MOE_ERR_CAPACITY, "n_tokens=%d outside [1, %d]", T, L->cfg.max_tokens);
+  return MOE_OK;
+}
+
+// Brings x to the device (staging host input) and picks the y target.
+moe_status stage_in(moe_layer* L, const void* x, int T, void* y, Stage* st, cudaStream_t s) {
+  const size_t bytes = sizeof(uint16_t) * (size_t)T * L->cfg.hidden;
+  if (is_device_ptr(x)) {
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+      st->x = static_cast<const uint16_t*>(x);
+    } else {  // the kernels read x with 16-byte loads: realign through the staging buffer
+      CUDA_TRY(cudaMemcpyAsync(L->ws.x_stage, x, bytes, cudaMemcpyDeviceToDevice, s), "realign x");
+      st->x = L->ws.x_stage;
+    }
+  } else {
+    CUDA_TRY(cudaMemcpyAsync(L->ws.x_stage, x, bytes, cudaMemcpyHostToDevice, s), "copy x to device");
+    st->x = L->ws.x_stage;
+  }
+  if (y) {
+    st->y_host = !is_device_ptr(y);
+    st->y = st->y_host ? L->ws.y_stage : static_cast<uint16_t*>(y);
+  }
+  return MOE_OK;
+}
+
+moe_status stage_out(moe_layer* L, int T, void* y, const Stage& st, cudaStream_t s) {
+  if (!st.y_host) return MOE_OK;
+  const size_t bytes = sizeof(uint16_t) * (size_t)T * L->cfg.hidden;
+  CUDA_TRY(cudaMemcpyAsync(y, st.y, bytes, cudaMemcpyDeviceToHost, s), "copy y to host");
+  CUDA_TRY(cudaStreamSynchronize(s), "synchronise after copying y");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t* topk_ids,
+                     float* topk_w, void* stream) {
+  moe_status st = check_common(layer, x_bf16, n_tokens);
+  if (st != MOE_OK) return st;
+  if (!topk_ids || !topk_w) return fail(MOE_ERR_INVALID, "topk_ids / topk_w is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  Stage sg;
+  if ((st = stage_in(layer, x_bf16, n_tokens, nullptr, &sg, s)) != MOE_OK) return st;
+  const int k = layer->cfg.top_k;
+  const bool ids_host = !is_device_ptr(topk_ids), w_host = !is_device_ptr(topk_w);
+  int32_t* ids = ids_host ? layer->ws.ids_stage : topk_ids;
+  float* w = w_host ? layer->ws.w_stage : topk_w;
+  if (n_tokens <= moe::kMaxDecodeTokens) {
+    moe_layer* one[1] = {layer};
+    st = run_decode(one, 1, sg.x, n_tokens, nullptr, nullptr, ids, w, moe::kModeRoute, s);
+  } else {
+    const char* why = "";
+    st = moe::launch_prefill(layer, sg.x, n_tokens, nullptr, ids, w, true, s, &why);
+    if (st != MOE_OK) st = fail(st, "prefill route: %s", why);
+  }
+  if (st != MOE_OK) return st;
+  if (ids_host)
+    CUDA_TRY(cudaMemcpyAsync(topk_ids, ids, sizeof(int32_t) * n_tokens * k, cudaMemcpyDeviceToHost, s),
+             "copy ids to host");
+  if (w_host)
+    CUDA_TRY(cudaMemcpyAsync(topk_w, w, sizeof(float) * n_tokens * k, cudaMemcpyDeviceToHost, s),
+             "copy weights to host");
+  if (ids_host || w_host) CUDA_TRY(cudaStreamSynchronize(s), "synchronise after route");
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void* y_bf16,
+                       void* stream) {
+  moe_status st = check_common(layer, x_bf16, n_tokens);
+  if (st != MOE_OK) return st;
+  if (!y_bf16) return fail(MOE_ERR_INVALID, "y is NULL");
+  if (x_bf16 == y_bf16) return fail(MOE_ERR_INVALID, "x and y must not overlap");
+  cudaStream_t s = (cudaStream_t)stream;
+  Stage sg;
+  if ((st = stage_in(layer, x_bf16, n_tokens, y_bf16, &sg, s)) != MOE_OK) return st;
+  if ((st = forward_device(layer, sg.x, n_tokens, sg.y, s)) != MOE_OK) return st;
+  return stage_out(layer, n_tokens, y_bf16, sg, s);
+}
+
+moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
+                                    int n_tokens, void* y_bf16, void* h_trace_bf16,
+                                    int32_t* ids_trace, void* stream) {
+  if (!layers || n_layers < 1) return fail(MOE_ERR_INVALID, "need at least one layer");
+  moe_status st = check_common(layers[0], x_bf16, n_tokens);
+  if (st != MOE_OK) return st;
+  if (!y_bf16) return fail(MOE_ERR_INVALID, "y is NULL");
+  const moe_layer_config& c0 = layers[0]->cfg;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!layers[l]) return fail(MOE_ERR_INVALID, "layer %d is NULL", l);
+    const moe_layer_config& c = layers[l]->cfg;
+    if (c.hidden != c0.hidden || c.n_experts != c0.n_experts || c.top_k != c0.top_k ||
+        c.ffn != c0.ffn || c.shared_ffn != c0.shared_ffn)
+      return fail(MOE_ERR_INVALID, "layer %d has a different shape from layer 0", l);
+  }
+  if ((h_trace_bf16 && !is_device_ptr(h_trace_bf16)) || (ids_trace && !is_device_ptr(ids_trace)))
+    return fail(MOE_ERR_INVALID, "trace buffers must be device memory");
+  cudaStream_t s = (cudaStream_t)stream;
+  Stage sg;
+  if ((st = stage_in(layers[0], x_bf16, n_tokens, y_bf16, &sg, s)) != MOE_OK) return st;
+  const int H = c0.hidden, k = c0.top_k;
+  if (n_tokens <= moe::kMaxDecodeTokens) {
+    st = run_decode(layers, n_layers, sg.x, n_tokens, sg.y, (uint16_t*)h_trace_bf16, ids_trace,
+                    nullptr, moe::kModeStack, s);
+    if (st != MOE_OK) return st;
+  } else {
+    // prefill-sized stack: layer by layer, residual kernel between layers.
+    // h ping-pongs between the two staging buffers; y_l has its own buffer.
+    moe_layer* L0 = layers[0];
+    const size_t n = (size_t)n_tokens * H;
+    uint16_t* P = L0->ws.x_stage;
+    uint16_t* Q = L0->ws.y_stage;
+    uint16_t* Y = L0->ws.y_layer;
+    const uint16_t* cur = sg.x;
+    for (int l = 0; l < n_layers; ++l) {
+      const char* why = "";
+      st = moe::launch_prefill(layers[l], cur, n_tokens, Y,
+                               ids_trace ? ids_trace + (size_t)l * n_tokens * k : nullptr, nullptr,
+                               false, s, &why);
+      if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
+      uint16_t* dst = (l == n_layers - 1) ? sg.y : (cur == P ? Q : P);
+      residual_kernel<<<2 * L0->num_sms, 256, 0, s>>>(cur, Y, dst, n);  // elementwise: in place is safe
+      CUDA_TRY(cudaGetLastError(), "residual kernel");
+      if (h_trace_bf16)
+        CUDA_TRY(cudaMemcpyAsync((uint16_t*)h_trace_bf16 + (size_t)l * n, dst, n * 2,
+                                 cudaMemcpyDeviceToDevice, s),
+                 "trace copy");
+      cur = dst;
+    }
+  }
+  return stage_out(layers[0], n_tokens, y_bf16, sg, s);
+}
+
+moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,
+                             int n_tokens, void* y_bf16, void* stream) {
+  return moe_stack_forward_traced(layers, n_layers, x_bf16, n_tokens, y_bf16, nullptr, nullptr,
+                                  stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+// Internal definitions shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxLayersPerLaunch = 64;
+constexpr int kMaxDecodeTokens = 4;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kDecodeThreads = 256;
+constexpr int kMaxUnits = kMaxDecodeTokens * kMaxTopK + 1;  // routed + shared
+
+// Device pointers of one layer's weights (library-owned copies).
+struct LayerDev {
+  const float* router_w;  // [E][H]
+  const float* router_b;  // [E]
+  const int32_t* slot_of; // [E]
+  const uint8_t* gate_q;  // [S][F][H/2]
+  const uint16_t* gate_s; // [S][F][H/32]
+  const uint8_t* up_q;
+  const uint16_t* up_s;
+  const uint8_t* down_q;  // [S][H][F/2]
+  const uint16_t* down_s; // [S][H][F/32]
+  const uint8_t* sh_gate_q;
+  const uint16_t* sh_gate_s;
+  const uint8_t* sh_up_q;
+  const uint16_t* sh_up_s;
+  const uint8_t* sh_down_q;
+  const uint16_t* sh_down_s;
+};
+
+// Generation-counting grid barrier state (one per workspace, 128-B aligned).
+struct GridBarrier {
+  unsigned int count;
+  unsigned int gen;
+  unsigned int pad[30];
+};
+
+enum DecodeMode : int { kModeForward = 0, kModeStack = 1, kModeRoute = 2 };
+
+struct DecodeParams {
+  int H, E, k, F, Fs;
+  int T;          // real tokens (1..4)
+  int n_layers;
+  int mode;       // DecodeMode
+  int max_units;  // min(T*k, E) routed units + shared
+  const uint16_t* x_in;  // [T][H] bf16 (device)
+  uint16_t* y_out;       // forward: y [T][H]; stack: h_L [T][H]
+  uint16_t* h_trace;     // [L][T][H] or null
+  int32_t* ids_out;      // [L][T][k] or null
+  float* w_out;          // [L][T][k] or null
+  uint16_t* xbuf;        // [2][4][H] residual ping-pong
+  float* z;              // [4][E]
+  float* hbuf;           // [max_units-ish][4][Fmax] fp32
+  GridBarrier* bar;
+  int* err;
+  unsigned long long timeout_ns;
+  // Test hook: every grid barrier waits for this many arrivals more than the
+  // grid has, so the bounded wait runs out and records MOE_ERR_TIMEOUT.
+  int debug_extra_arrivals;
+  LayerDev layers[kMaxLayersPerLaunch];
+};
+
+// Workspace of one layer object.
+struct Workspace {
+  uint16_t* xbuf = nullptr;
+  float* z = nullptr;
+  float* hbuf = nullptr;
+  GridBarrier* bar = nullptr;
+  int* err = nullptr;
+  uint16_t* x_stage = nullptr;  // [max_tokens][H] staging for host inputs
+  uint16_t* y_stage = nullptr;  // [max_tokens][H] staging for host outputs
+  uint16_t* y_layer = nullptr;  // [max_tokens][H] per-layer output in prefill-sized stacks
+  int32_t* ids_stage = nullptr; // [max_tokens][k]
+  float* w_stage = nullptr;     // [max_tokens][k]
+  // prefill
+  float* zf = nullptr;          // [max_tokens][E] router logits
+  int32_t* topk_ids = nullptr;  // [max_tokens][k]
+  float* topk_w = nullptr;      // [max_tokens][k]
+  int32_t* counts = nullptr;    // [E] (+ scratch)
+  int32_t* offsets = nullptr;   // [E+1]
+  int32_t* perm_tok = nullptr;  // [max_tokens*k] token of each bucketed row
+  float* perm_w = nullptr;      // [max_tokens*k] routing weight of each bucketed row
+  int32_t* tiles = nullptr;     // tile list
+  void* hmid = nullptr;         // bf16 [max_tokens*k + max_tokens][Fmax]
+  float* yacc = nullptr;        // [max_tokens][H]
+  void* scratch = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace moe
+
+struct moe_layer {
+  moe_layer_config cfg;
+  moe::LayerDev dev;
+  void* weights_block = nullptr;  // one allocation holding all weight copies
+  size_t weights_bytes = 0;
+  void* ws_block = nullptr;       // one allocation holding the workspace
+  moe::Workspace ws;
+  int device = 0;
+  int num_sms = 0;
+};
+
+namespace moe {
+// decode.cu
+moe_status launch_decode(const DecodeParams& p, cudaStream_t stream, int num_sms,
+                         const char** why);
+size_t decode_smem_bytes(const DecodeParams& p);
+// prefill.cu
+moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
+                          float* w_out, bool route_only, cudaStream_t stream, const char** why);
+size_t prefill_workspace_bytes(const moe_layer_config& c);
+}  // namespace moe

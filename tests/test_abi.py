@@ -1,0 +1,70 @@
+"""The C-ABI library loads, exports every entry point include/moe.h declares,
+and its host-side validation rejects bad arguments (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_expert_ffn_softmax_gb300 as moe
+from quantized_expert_ffn_softmax_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "moe_forward" in names and "moe_layer_create" in names
+    raw = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_version_and_empty_error(lib):
+    assert moe.moe_version() == 100
+    assert isinstance(moe.moe_last_error(), str)
+
+
+def _cfg(**kw):
+    c = dict(hidden=256, n_experts=16, top_k=2, ffn=128, shared_ffn=128, max_tokens=8)
+    c.update(kw)
+    return c
+
+
+@pytest.mark.parametrize("bad", [dict(hidden=100), dict(hidden=0), dict(n_experts=0),
+                                 dict(n_experts=2000), dict(top_k=0), dict(top_k=17),
+                                 dict(top_k=20, n_experts=16), dict(ffn=96), dict(shared_ffn=64),
+                                 dict(max_tokens=0), dict(n_slots=8)])
+def test_create_rejects_bad_configs_before_touching_the_device(lib, bad):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_create(_cfg(**bad), {}, False)
+    assert ei.value.status == moe.MOE_ERR_INVALID
+
+
+def test_create_rejects_missing_weights(lib):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_create(_cfg(), {"router_w": 1}, False)
+    assert ei.value.status == moe.MOE_ERR_INVALID
+    assert "NULL" in moe.moe_last_error()
+
+
+def test_calls_reject_null_layer(lib):
+    L = lib
+    assert L.moe_forward(None, None, 1, None, None) == moe.MOE_ERR_INVALID
+    assert L.moe_route(None, None, 1, None, None, None) == moe.MOE_ERR_INVALID
+    assert L.moe_status_sync(None, None) == moe.MOE_ERR_INVALID
+    arr = (ctypes.c_void_p * 1)(None)
+    assert L.moe_stack_forward(arr, 0, None, 1, None, None) == moe.MOE_ERR_INVALID
+    L.moe_layer_destroy(None)

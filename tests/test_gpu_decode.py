@@ -1,0 +1,235 @@
+"""GPU parity of the decode / MTP-verify path (1..4 tokens) against the oracle,
+through the C ABI, on the seeded workloads: the tiny layer, the 40-layer
+35B-A3B-shaped stack (1 token and the 1+3-token verify batch) and the
+48-layer 125B-A6B-shaped stack with permuted slot tables."""
+import gc
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_expert_ffn_softmax_gb300 as moe
+import workload as W
+from parity import (bf16_f64, check_topk, make_layer_device, make_layer_host, oracle_token,
+                    to_dev, to_host_bits, y_tol)
+
+pytestmark = pytest.mark.gpu
+
+
+def _tiny(permuted=True, **kw):
+    return W.CONFIGS["tiny"].replace(permuted_slots=permuted, **kw)
+
+
+# ----------------------------------------------------------------- generator
+
+def test_generator_device_bytes_equal_host_bytes(cuda_device):
+    cfg = _tiny()
+    host = W.layer(cfg, 0)
+    dev = W.device_layer(cfg, 0)
+    torch.cuda.synchronize()
+    for k, v in dev.items():
+        d = v.cpu().numpy()
+        h = host[k]
+        if d.dtype == np.int16:
+            d = d.view(np.uint16)
+        assert np.array_equal(d.reshape(h.shape), h), k
+    # a few experts of a full-size layer
+    big = W.CONFIGS["decode125b"]
+    dq = W.device_layer(big, 3)
+    slots = W.slot_table(big, 3)
+    for e in (0, 77, 511):
+        ex = W.expert(big, 3, e)
+        s = slots[e]
+        for n in ("gate_q", "up_s", "down_q", "down_s"):
+            d = dq[n][s].cpu().numpy()
+            if d.dtype == np.int16:
+                d = d.view(np.uint16)
+            assert np.array_equal(d, ex[n]), (e, n)
+    del dq
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------- tiny layer
+
+@pytest.mark.parametrize("permuted", [False, True])
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_tiny_forward_and_route(cuda_device, permuted, T):
+    cfg = _tiny(permuted)
+    layer, Ld = make_layer_host(cfg, 0)
+    for idx in range(3):
+        x = W.activations(cfg, idx, n_tokens=T)
+        xd = to_dev(x)
+        y = layer.forward(xd)
+        ids, w = layer.route(xd)
+        assert moe.moe_status_sync(layer.handle) == moe.MOE_OK
+        ids = ids.cpu().numpy()
+        w = w.cpu().numpy()
+        z = oracle.router_logits(Ld["router_w"], Ld["router_b"], x)
+        adopt = [check_topk(ids[t], z[t], cfg.top_k) for t in range(T)]
+        forced = ids if any(adopt) else None
+        y_ref, ids_ref, w_ref, _ = oracle.moe_forward(Ld, cfg.top_k, x, forced_ids=forced)
+        assert np.max(np.abs(w - w_ref)) < 1e-5
+        assert np.allclose(w.sum(1), 1.0, atol=1e-5)
+        yg = bf16_f64(to_host_bits(y))
+        assert np.max(np.abs(yg - y_ref)) <= y_tol(y_ref)
+    layer.close()
+
+
+def test_tiny_host_pointers_match_device_pointers(cuda_device):
+    cfg = _tiny()
+    layer, Ld = make_layer_host(cfg, 0)
+    x = W.activations(cfg, 5)
+    y_dev = to_host_bits(layer.forward(to_dev(x)))
+    y_host = np.zeros_like(x)
+    moe.moe_forward(layer.handle, x, x.shape[0], y_host)
+    assert np.array_equal(y_host, y_dev)
+    ids = np.zeros((x.shape[0], cfg.top_k), np.int32)
+    w = np.zeros((x.shape[0], cfg.top_k), np.float32)
+    moe.moe_route(layer.handle, x, x.shape[0], ids, w)
+    ids_d, w_d = layer.route(to_dev(x))
+    assert np.array_equal(ids, ids_d.cpu().numpy()) and np.array_equal(w, w_d.cpu().numpy())
+    layer.close()
+
+
+def test_tiny_no_shared_expert_and_top1(cuda_device):
+    cfg = _tiny(shared_ffn=0, top_k=1)
+    layer, Ld = make_layer_host(cfg, 0)
+    x = W.activations(cfg, 1)
+    y = bf16_f64(to_host_bits(layer.forward(to_dev(x))))
+    y_ref = oracle.moe_forward(Ld, 1, x)[0]
+    assert np.max(np.abs(y - y_ref)) <= y_tol(y_ref)
+    layer.close()
+
+
+def test_tiny_stack_teacher_forced(cuda_device):
+    cfg = _tiny()
+    L = 5
+    made = [make_layer_host(cfg, l) for l in range(L)]
+    layers = [m[0] for m in made]
+    x = W.activations(cfg, 2)
+    y, h_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+    assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
+    h_trace = to_host_bits(h_trace)
+    ids_trace = ids_trace.cpu().numpy()
+    assert np.array_equal(to_host_bits(y), h_trace[-1])
+    h_prev = x
+    for l in range(L):
+        Ld = made[l][1]
+        z = oracle.router_logits(Ld["router_w"], Ld["router_b"], h_prev)
+        adopt = [check_topk(ids_trace[l, t], z[t], cfg.top_k) for t in range(cfg.n_tokens)]
+        y_ref = oracle.moe_forward(Ld, cfg.top_k, h_prev,
+                                   forced_ids=ids_trace[l] if any(adopt) else None)[0]
+        h_ref = bf16_f64(oracle.residual(h_prev, y_ref))
+        hg = bf16_f64(h_trace[l])
+        tol = y_tol(y_ref) + 2.0 ** -8 * np.abs(h_ref).max()
+        assert np.max(np.abs(hg - h_ref)) <= tol, l
+        h_prev = h_trace[l]
+    # in place: x == y is allowed for stacks
+    xd = to_dev(x)
+    moe.moe_stack_forward([l.handle for l in layers], L, xd, cfg.n_tokens, xd)
+    assert np.array_equal(to_host_bits(xd), h_trace[-1])
+    for l in layers:
+        l.close()
+
+
+def test_errors_and_timeout_status(cuda_device):
+    cfg = _tiny()
+    layer, Ld = make_layer_host(cfg, 0, max_tokens=4)
+    x = to_dev(W.activations(cfg, 0))
+    y = torch.empty_like(x)
+    for bad_T in (0, 5, -1):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(layer.handle, x, bad_T, y)
+        assert ei.value.status == moe.MOE_ERR_CAPACITY
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward(layer.handle, x, 4, x)  # aliasing
+    # a bad slot table is rejected at create
+    w = dict(Ld)
+    bad = Ld["slot_of_expert"].copy()
+    bad[3] = bad[4]
+    from parity import host_weights, config_dict
+    hw = host_weights(Ld)
+    hw["slot_of_expert"] = bad
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_create(config_dict(cfg, 4), hw, False)
+    assert ei.value.status == moe.MOE_ERR_INVALID
+    # bounded device wait: a barrier that can never fill must time out,
+    # record MOE_ERR_TIMEOUT and leave the context usable
+    os.environ["MOE_DEBUG_UNREACHABLE_BARRIER"] = "1"
+    os.environ["MOE_WAIT_TIMEOUT_US"] = "20000"
+    try:
+        moe.moe_forward(layer.handle, x, 4, y)
+        st = moe.moe_status_sync(layer.handle)
+    finally:
+        del os.environ["MOE_DEBUG_UNREACHABLE_BARRIER"]
+        del os.environ["MOE_WAIT_TIMEOUT_US"]
+    assert st == moe.MOE_ERR_TIMEOUT
+    assert moe.moe_status_sync(layer.handle) == moe.MOE_OK  # cleared
+    y2 = layer.forward(x)
+    y_ref = oracle.moe_forward(Ld, cfg.top_k, W.activations(cfg, 0))[0]
+    assert np.max(np.abs(bf16_f64(to_host_bits(y2)) - y_ref)) <= y_tol(y_ref)
+    layer.close()
+
+
+# ----------------------------------------------------------------- full-size stacks
+
+def _stack_check(cfg, n_check_layers=None, tokens_to_check=None, input_index=0):
+    """Runs the full stack (device-generated weights) once with traces and
+    checks every layer's top-k and a sample of layers' outputs with teacher
+    forcing (the oracle takes the GPU's bf16 input of that layer)."""
+    layers = [make_layer_device(cfg, l, max_tokens=8) for l in range(cfg.n_layers)]
+    try:
+        x = W.activations(cfg, input_index)
+        y, h_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+        assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
+        h_trace = to_host_bits(h_trace)
+        ids_trace = ids_trace.cpu().numpy()
+    finally:
+        for l in layers:
+            l.close()
+        del layers
+        gc.collect()
+        torch.cuda.empty_cache()
+    T = cfg.n_tokens
+    toks = range(T) if tokens_to_check is None else tokens_to_check
+    check_layers = set(range(cfg.n_layers)) if n_check_layers is None else set(n_check_layers)
+    h_in = [x] + [h_trace[l] for l in range(cfg.n_layers - 1)]
+    n_adopted = 0
+    for l in range(cfg.n_layers):
+        Wr, b = W.router(cfg, l)
+        z = oracle.router_logits(Wr, b, h_in[l])
+        for t in range(T):
+            n_adopted += check_topk(ids_trace[l, t], z[t], cfg.top_k)
+        if l not in check_layers:
+            continue
+        sh = W.shared_expert(cfg, l)
+        cache = {}
+        for t in toks:
+            y_ref, _, _ = oracle_token(cfg, l, h_in[l][t], gpu_ids=ids_trace[l, t], router=(Wr, b),
+                                       shared=sh, expert_cache=cache)
+            h_ref = bf16_f64(oracle.residual(h_in[l][t], y_ref))
+            hg = bf16_f64(h_trace[l][t])
+            tol = y_tol(y_ref) + 2.0 ** -8 * np.abs(h_ref).max()
+            err = np.max(np.abs(hg - h_ref))
+            assert err <= tol, (l, t, err, tol)
+    return ids_trace, n_adopted
+
+
+def test_decode35b_stack_parity(cuda_device):
+    cfg = W.CONFIGS["decode35b"]
+    _stack_check(cfg, n_check_layers=list(range(0, 40, 3)) + [39])
+
+
+def test_mtp35b_verify_batch_parity(cuda_device):
+    cfg = W.CONFIGS["mtp35b"]
+    ids, _ = _stack_check(cfg, n_check_layers=[0, 1, 20, 39])
+    # the calibrated drafts overlap token 0's selection by about one half
+    ov = [len(set(ids[0, 0]) & set(ids[0, t])) / cfg.top_k for t in range(1, 4)]
+    assert 0.2 <= np.mean(ov) <= 0.85
+
+
+def test_decode125b_stack_parity(cuda_device):
+    cfg = W.CONFIGS["decode125b"]
+    _stack_check(cfg, n_check_layers=[0, 1, 23, 46, 47])
