@@ -48,7 +48,7 @@ typedef enum {
   MOE_ERR_CUDA = -2,     /* a CUDA runtime call failed */
   MOE_ERR_OOM = -3,      /* device allocation failed (create only) */
   MOE_ERR_CAPACITY = -4, /* n_tokens outside [1, max_tokens] */
-  MOE_ERR_BOUNDS = -5,   /* a kernel met an out-of-range slot */
+  MOE_ERR_BOUNDS = -5,   /* a kernel met an out-of-range slot or non-finite logits */
   MOE_ERR_TIMEOUT = -6   /* a bounded device-side wait ran out */
 } moe_status;
 
@@ -119,17 +119,22 @@ moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t
 moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void* y_bf16,
                        void* stream);
 
-/* Residual stack: h_0 = x, h_{l+1} = bf16(h_l + bf16(layer_l(h_l))),
- * y = h_L.  All layers must share one config.  x == y is allowed. */
+/* Pre-norm residual stack: h_0 = x and, for l = 0..L-1,
+ *   u_l     = bf16(h_l / sqrt(mean(h_l^2) + 1e-6))   (RMS norm, unit gain)
+ *   h_{l+1} = bf16(h_l + bf16(layer_l(u_l)))
+ * y = h_L.  The norm keeps the stack finite: without it the SwiGLU output,
+ * which grows with the square of its input, makes a deep residual stack of
+ * these layers diverge.  All layers must share one shape.  x == y is
+ * allowed. */
 moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,
                              int n_tokens, void* y_bf16, void* stream);
 
-/* moe_stack_forward that also records, when the pointers are not NULL,
- * every layer's output h_{l+1} into h_trace [L][T][H] (bf16 bits) and every
- * layer's top-k ids into ids_trace [L][T][k]. */
+/* moe_stack_forward that also records, for every pointer that is not NULL
+ * (device memory only): h_trace [L][T][H] = h_{l+1}, in_trace [L][T][H] =
+ * u_l (bf16 bits), ids_trace [L][T][k] = each layer's top-k ids. */
 moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
-                                    int32_t* ids_trace, void* stream);
+                                    void* in_trace_bf16, int32_t* ids_trace, void* stream);
 
 /* Synchronises `stream`, then returns and clears the layer's device error
  * word (MOE_ERR_BOUNDS or MOE_ERR_TIMEOUT if a kernel recorded one). */

@@ -19,6 +19,8 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   moe_forward        dense identity (k = E), slot-permutation invariance,
                      token independence, SwiGLU zero cases
   residual / stack   zero-expert identity; bf16 rounding vs torch
+  rmsnorm            numpy RMS of the row; constant rows; power-of-two scale
+                     invariance
 """
 from __future__ import annotations
 
@@ -83,6 +85,7 @@ def lib():
         L.oracle_moe_forward.argtypes = [ctypes.POINTER(OracleLayer), i32, vp, vp, vp, vp, vp, vp]
         L.oracle_moe_forward.restype = i32
         L.oracle_residual.argtypes = [vp, vp, vp, i64]
+        L.oracle_rmsnorm.argtypes = [vp, i32, i32, d, vp]
         L.oracle_stack_forward.argtypes = [ctypes.POINTER(OracleLayer), i32, i32, vp, vp, vp, vp]
         L.oracle_stack_forward.restype = i32
         _lib = L
@@ -266,8 +269,17 @@ def residual(h_bf16, y) -> np.ndarray:
     return out
 
 
+def rmsnorm(h_bf16, eps: float = 1e-6) -> np.ndarray:
+    """Unit-gain RMS normalisation of each row, rounded once to bf16."""
+    h = _c(h_bf16, np.uint16)
+    T, H = h.shape
+    out = np.empty(h.shape, np.uint16)
+    lib().oracle_rmsnorm(_p(h), T, H, float(eps), _p(out))
+    return out
+
+
 def stack_forward(layers: list, top_k: int, x_bf16):
-    """Residual stack over in-memory layers: returns h_L, h trace, id trace."""
+    """Pre-norm residual stack over in-memory layers: h_L, h trace, id trace."""
     x = _c(x_bf16, np.uint16)
     T, H = x.shape
     structs, keeps = zip(*[_layer_struct(Ld, top_k) for Ld in layers])

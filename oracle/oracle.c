@@ -25,7 +25,10 @@
  *    scale; byte i of a row holds element 2i (low nibble), 2i+1 (high);
  *  - layer output y = sum_j w_j y_{e_j} + y_shared, shared weight 1,
  *    rounded to bf16 only at the output;
- *  - stack: h_{l+1} = bf16(h_l + bf16(y_l)).
+ *  - stack (pre-norm residual, RMSNorm with unit gain; a plain residual
+ *    stack of these layers diverges -- the SwiGLU output grows with the
+ *    square of its input): u_l = bf16(h_l / sqrt(mean(h_l^2) + 1e-6)),
+ *    h_{l+1} = bf16(h_l + bf16(MoE_l(u_l))).
  */
 #include <math.h>
 #include <stdint.h>
@@ -343,24 +346,43 @@ void oracle_residual(const uint16_t* h_bf16, const double* y, uint16_t* h_next, 
   }
 }
 
-/* L layers of the residual stack: h_0 = x, h_{l+1} = bf16(h_l + bf16(y_l)).
- * Writes h_L to out; h_trace (optional) receives h_1..h_L [L][T][H]. */
+/* RMS normalisation with unit gain, per row of H: one rounding to bf16 of
+ * h / sqrt(mean(h^2) + eps). */
+void oracle_rmsnorm(const uint16_t* h_bf16, int T, int H, double eps, uint16_t* out) {
+  for (int t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int i = 0; i < H; ++i) {
+      double v = oracle_bf16_to_double(h_bf16[(size_t)t * H + i]);
+      ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / H + eps);
+    for (int i = 0; i < H; ++i)
+      out[(size_t)t * H + i] = oracle_double_to_bf16(oracle_bf16_to_double(h_bf16[(size_t)t * H + i]) * inv);
+  }
+}
+
+/* L layers of the pre-norm residual stack: h_0 = x, u_l = rmsnorm(h_l),
+ * h_{l+1} = bf16(h_l + bf16(MoE_l(u_l))).  Writes h_L to out; h_trace
+ * (optional) receives h_1..h_L [L][T][H], ids_trace the selections. */
 int oracle_stack_forward(const oracle_layer* layers, int n_layers, int T, const uint16_t* x_bf16,
                          uint16_t* out, uint16_t* h_trace, int32_t* ids_trace) {
   const int H = layers[0].hidden;
   const size_t n = (size_t)T * H;
   uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * n);
+  uint16_t* u = (uint16_t*)malloc(sizeof(uint16_t) * n);
   double* y = (double*)malloc(sizeof(double) * n);
   memcpy(h, x_bf16, sizeof(uint16_t) * n);
   int rc = 0;
   for (int l = 0; l < n_layers && rc == 0; ++l) {
     int32_t* ids = ids_trace ? ids_trace + (size_t)l * T * layers[l].top_k : NULL;
-    rc = oracle_moe_forward(&layers[l], T, h, NULL, y, ids, NULL, NULL);
+    oracle_rmsnorm(h, T, H, 1e-6, u);
+    rc = oracle_moe_forward(&layers[l], T, u, NULL, y, ids, NULL, NULL);
     oracle_residual(h, y, h, (int64_t)n);
     if (h_trace) memcpy(h_trace + (size_t)l * n, h, sizeof(uint16_t) * n);
   }
   memcpy(out, h, sizeof(uint16_t) * n);
   free(h);
+  free(u);
   free(y);
   return rc;
 }

@@ -77,7 +77,8 @@ def lib():
         L.moe_forward.restype = i32
         L.moe_stack_forward.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp]
         L.moe_stack_forward.restype = i32
-        L.moe_stack_forward_traced.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp, vp, vp]
+        L.moe_stack_forward_traced.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp, vp, vp,
+                                               vp]
         L.moe_stack_forward_traced.restype = i32
         L.moe_status_sync.argtypes = [vp, vp]
         L.moe_status_sync.restype = i32
@@ -165,10 +166,10 @@ def moe_stack_forward(layers: Sequence[int], n_layers: int, x, n_tokens: int, y,
 
 
 def moe_stack_forward_traced(layers: Sequence[int], n_layers: int, x, n_tokens: int, y, h_trace,
-                             ids_trace, stream=None) -> None:
+                             in_trace, ids_trace, stream=None) -> None:
     _check(lib().moe_stack_forward_traced(_layer_array(layers), n_layers, _ptr(x), n_tokens,
-                                          _ptr(y), _ptr(h_trace), _ptr(ids_trace),
-                                          _stream(stream)))
+                                          _ptr(y), _ptr(h_trace), _ptr(in_trace),
+                                          _ptr(ids_trace), _stream(stream)))
 
 
 def moe_status_sync(layer: int, stream=None) -> int:
@@ -222,6 +223,7 @@ def stack_forward(layers: Sequence[MoELayer], x, stream=None, trace: bool = Fals
     L, T, H = len(hs), x.shape[0], x.shape[1]
     k = layers[0].config["top_k"]
     h_trace = torch.empty((L, T, H), dtype=x.dtype, device=x.device)
+    in_trace = torch.empty((L, T, H), dtype=x.dtype, device=x.device)
     ids = torch.empty((L, T, k), dtype=torch.int32, device=x.device)
-    moe_stack_forward_traced(hs, L, x, T, y, h_trace, ids, stream)
-    return y, h_trace, ids
+    moe_stack_forward_traced(hs, L, x, T, y, h_trace, in_trace, ids, stream)
+    return y, h_trace, in_trace, ids

@@ -1,12 +1,13 @@
 // Decode / MTP-verify path (1..4 tokens): one persistent cooperative kernel
 // runs a whole stack of MoE layers.  Per layer:
-//   phase R  router GEMV (fp32, one warp per expert row)        -> z
+//   phase R  (stacks: RMS-normalise the residual stream h -> u)
+//            router GEMV (fp32, one warp per expert row)        -> z
 //   barrier
 //   top-k + softmax + unit list, computed redundantly by every CTA
 //   phase G  fused dequant + gate/up GEMV + SwiGLU              -> h
 //   barrier
 //   phase D  fused dequant + down GEMV + weighted combine
-//            (+ residual for stacks)                            -> y / h_{l+1}
+//            (+ residual h + bf16(y) for stacks)                -> y / h_{l+1}
 //   barrier
 // The expert weights are streamed once with 128-bit non-allocating loads;
 // the per-block binary16 scales of each tile are staged in shared memory by
@@ -217,7 +218,7 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
 struct DecodeSmem {
-  size_t mbar, misc, red, xb, xp, sc, hp, total;
+  size_t mbar, misc, red, xb, hres, xp, sc, hp, total;
   __host__ __device__ static DecodeSmem make(int H, int F, int Fs, int TT, int max_units) {
     DecodeSmem s;
     const int C = H / 32;
@@ -230,6 +231,8 @@ struct DecodeSmem {
     s.red = o;
     o += 8 * 32 * 4;
     s.xb = o;
+    o += (size_t)TT * H * 2;
+    s.hres = o;
     o += (size_t)TT * H * 2;
     s.xp = o;
     o += (size_t)TT * H * 2;
@@ -261,6 +264,7 @@ struct DecodeMisc {
   unsigned bitmap[kMaxExperts / 32];
   int prefix[kMaxExperts / 32 + 1];
   float tok_max[8][4];
+  float inv_rms[4];
 };
 static_assert(sizeof(DecodeMisc) <= 8192, "misc region too small");
 
@@ -276,7 +280,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
   DecodeMisc& M = *reinterpret_cast<DecodeMisc*>(smem + L.misc);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.xb);
+  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.xb);      // layer input (u)
+  uint16_t* hres = reinterpret_cast<uint16_t*>(smem + L.hres);  // residual stream (stacks)
   uint4* xp = reinterpret_cast<uint4*>(smem + L.xp);
   __half* sc = reinterpret_cast<__half*>(smem + L.sc);
   uint4* hp = reinterpret_cast<uint4*>(smem + L.hp);
@@ -295,13 +300,48 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
     const uint16_t* xsrc = (l == 0) ? p.x_in : (p.xbuf + (size_t)(l & 1) * kMaxDecodeTokens * H);
 
     // ------------------------------------------------ phase R: stage x, router
+    const bool stack = (p.mode == kModeStack);
+    uint16_t* stage_dst = stack ? hres : xb;
     for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
       const int t = i / (H / 8);
       uint4 v = make_uint4(0, 0, 0, 0);
       if (t < T) v = __ldcg(reinterpret_cast<const uint4*>(xsrc + (size_t)t * H) + (i - t * (H / 8)));
-      reinterpret_cast<uint4*>(xb)[i] = v;
+      reinterpret_cast<uint4*>(stage_dst)[i] = v;
     }
     __syncthreads();
+    if (stack) {
+      // pre-norm: u = bf16(h / sqrt(mean(h^2) + eps)), unit gain
+      float ss[TT];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) ss[t] = 0.0f;
+      for (int i = tid; i < H; i += kDecodeThreads) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float v = __bfloat162float(__ushort_as_bfloat16(hres[t * H + i]));
+          ss[t] = fmaf(v, v, ss[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const float v = warp_sum(ss[t]);
+        if (lane == 0) M.tok_max[warp][t] = v;
+      }
+      __syncthreads();
+      if (tid < TT) {
+        float v = 0.0f;
+        for (int w = 0; w < kDecodeThreads / 32; ++w) v += M.tok_max[w][tid];
+        M.inv_rms[tid] = rsqrtf(v / (float)H + 1e-6f);
+      }
+      __syncthreads();
+      for (int i = tid; i < TT * H; i += kDecodeThreads) {
+        const int t = i / H;
+        const float v = __bfloat162float(__ushort_as_bfloat16(hres[i])) * M.inv_rms[t];
+        xb[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+      __syncthreads();
+      if (blockIdx.x == 0 && p.in_trace)
+        for (int i = tid; i < T * H; i += kDecodeThreads) p.in_trace[(size_t)l * T * H + i] = xb[i];
+    }
     {
       // per-token |x| max -> power-of-two shift for the fp16 activations
       float m[TT];
@@ -723,7 +763,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
             if (p.mode == kModeForward) {
               p.y_out[(size_t)t * H + i] = __bfloat16_as_ushort(yb);
             } else {
-              const float xv = __bfloat162float(__ushort_as_bfloat16(xb[t * H + i]));
+              const float xv = __bfloat162float(__ushort_as_bfloat16(hres[t * H + i]));
               const uint16_t xn = __bfloat16_as_ushort(__float2bfloat16_rn(xv + __bfloat162float(yb)));
               uint16_t* dst = (l == p.n_layers - 1)
                                   ? p.y_out

@@ -215,6 +215,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   size_t o_xs = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_ys = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_yl = wadd(sizeof(uint16_t) * (size_t)Tm * H);
+  size_t o_ul = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_is = wadd(sizeof(int32_t) * (size_t)Tm * k);
   size_t o_ws = wadd(sizeof(float) * (size_t)Tm * k);
   size_t o_pf = wadd(moe::prefill_workspace_bytes(*cfg));
@@ -233,6 +234,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->ws.x_stage = (uint16_t*)(wb + o_xs);
   L->ws.y_stage = (uint16_t*)(wb + o_ys);
   L->ws.y_layer = (uint16_t*)(wb + o_yl);
+  L->ws.u_layer = (uint16_t*)(wb + o_ul);
   L->ws.ids_stage = (int32_t*)(wb + o_is);
   L->ws.w_stage = (float*)(wb + o_ws);
   L->ws.scratch = wb + o_pf;
@@ -298,8 +300,8 @@ moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
 // Runs `n_layers` layers on <= 4 tokens with the decode kernel (chunks of
 // kMaxLayersPerLaunch layers per launch).
 moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x, int T,
-                      uint16_t* y, uint16_t* h_trace, int32_t* ids_trace, float* w_out, int mode,
-                      cudaStream_t stream) {
+                      uint16_t* y, uint16_t* h_trace, uint16_t* in_trace, int32_t* ids_trace,
+                      float* w_out, int mode, cudaStream_t stream) {
   moe_layer* L0 = layers[0];
   const int H = L0->cfg.hidden;
   const uint16_t* cur = x;
@@ -310,6 +312,7 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
     p.x_in = cur;
     p.y_out = y;
     p.h_trace = h_trace ? h_trace + (size_t)l0 * T * H : nullptr;
+    p.in_trace = in_trace ? in_trace + (size_t)l0 * T * H : nullptr;
     p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
     p.w_out = w_out;
     for (int l = 0; l < nl; ++l) p.layers[l] = layers[l0 + l]->dev;
@@ -330,12 +333,30 @@ __global__ void residual_kernel(const uint16_t* __restrict__ h, const uint16_t* 
   }
 }
 
+// u = bf16(h / sqrt(mean(h^2) + 1e-6)) per row (one warp per row).
+__global__ void rmsnorm_kernel(const uint16_t* __restrict__ h, int T, int H,
+                               uint16_t* __restrict__ u) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint16_t* row = h + (size_t)t * H;
+  float ss = 0.0f;
+  for (int i = lane; i < H; i += 32) {
+    const float v = __bfloat162float(__ushort_as_bfloat16(row[i]));
+    ss = fmaf(v, v, ss);
+  }
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = rsqrtf(ss / (float)H + 1e-6f);
+  for (int i = lane; i < H; i += 32)
+    u[(size_t)t * H + i] = __bfloat16_as_ushort(
+        __float2bfloat16_rn(__bfloat162float(__ushort_as_bfloat16(row[i])) * inv));
+}
+
 // One layer on any token count: decode kernel for <= 4 tokens, the prefill
 // path above that.
 moe_status forward_device(moe_layer* L, const uint16_t* x, int T, uint16_t* y, cudaStream_t s) {
   if (T <= moe::kMaxDecodeTokens) {
     moe_layer* one[1] = {L};
-    return run_decode(one, 1, x, T, y, nullptr, nullptr, nullptr, moe::kModeForward, s);
+    return run_decode(one, 1, x, T, y, nullptr, nullptr, nullptr, nullptr, moe::kModeForward, s);
   }
   const char* why = "";
   moe_status st = moe::launch_prefill(L, x, T, y, nullptr, nullptr, false, s, &why);
@@ -398,7 +419,7 @@ moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t
   float* w = w_host ? layer->ws.w_stage : topk_w;
   if (n_tokens <= moe::kMaxDecodeTokens) {
     moe_layer* one[1] = {layer};
-    st = run_decode(one, 1, sg.x, n_tokens, nullptr, nullptr, ids, w, moe::kModeRoute, s);
+    st = run_decode(one, 1, sg.x, n_tokens, nullptr, nullptr, nullptr, ids, w, moe::kModeRoute, s);
   } else {
     const char* why = "";
     st = moe::launch_prefill(layer, sg.x, n_tokens, nullptr, ids, w, true, s, &why);
@@ -430,7 +451,7 @@ moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void*
 
 moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
-                                    int32_t* ids_trace, void* stream) {
+                                    void* in_trace_bf16, int32_t* ids_trace, void* stream) {
   if (!layers || n_layers < 1) return fail(MOE_ERR_INVALID, "need at least one layer");
   moe_status st = check_common(layers[0], x_bf16, n_tokens);
   if (st != MOE_OK) return st;
@@ -443,28 +464,36 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
         c.ffn != c0.ffn || c.shared_ffn != c0.shared_ffn)
       return fail(MOE_ERR_INVALID, "layer %d has a different shape from layer 0", l);
   }
-  if ((h_trace_bf16 && !is_device_ptr(h_trace_bf16)) || (ids_trace && !is_device_ptr(ids_trace)))
+  if ((h_trace_bf16 && !is_device_ptr(h_trace_bf16)) || (ids_trace && !is_device_ptr(ids_trace)) ||
+      (in_trace_bf16 && !is_device_ptr(in_trace_bf16)))
     return fail(MOE_ERR_INVALID, "trace buffers must be device memory");
   cudaStream_t s = (cudaStream_t)stream;
   Stage sg;
   if ((st = stage_in(layers[0], x_bf16, n_tokens, y_bf16, &sg, s)) != MOE_OK) return st;
   const int H = c0.hidden, k = c0.top_k;
   if (n_tokens <= moe::kMaxDecodeTokens) {
-    st = run_decode(layers, n_layers, sg.x, n_tokens, sg.y, (uint16_t*)h_trace_bf16, ids_trace,
-                    nullptr, moe::kModeStack, s);
+    st = run_decode(layers, n_layers, sg.x, n_tokens, sg.y, (uint16_t*)h_trace_bf16,
+                    (uint16_t*)in_trace_bf16, ids_trace, nullptr, moe::kModeStack, s);
     if (st != MOE_OK) return st;
   } else {
-    // prefill-sized stack: layer by layer, residual kernel between layers.
-    // h ping-pongs between the two staging buffers; y_l has its own buffer.
+    // prefill-sized stack: layer by layer.  h ping-pongs between the two
+    // staging buffers, u_l = rmsnorm(h_l) and y_l have buffers of their own.
     moe_layer* L0 = layers[0];
     const size_t n = (size_t)n_tokens * H;
     uint16_t* P = L0->ws.x_stage;
     uint16_t* Q = L0->ws.y_stage;
+    uint16_t* U = L0->ws.u_layer;
     uint16_t* Y = L0->ws.y_layer;
     const uint16_t* cur = sg.x;
     for (int l = 0; l < n_layers; ++l) {
+      rmsnorm_kernel<<<(n_tokens + 7) / 8, 256, 0, s>>>(cur, n_tokens, H, U);
+      CUDA_TRY(cudaGetLastError(), "rmsnorm kernel");
+      if (in_trace_bf16)
+        CUDA_TRY(cudaMemcpyAsync((uint16_t*)in_trace_bf16 + (size_t)l * n, U, n * 2,
+                                 cudaMemcpyDeviceToDevice, s),
+                 "trace copy");
       const char* why = "";
-      st = moe::launch_prefill(layers[l], cur, n_tokens, Y,
+      st = moe::launch_prefill(layers[l], U, n_tokens, Y,
                                ids_trace ? ids_trace + (size_t)l * n_tokens * k : nullptr, nullptr,
                                false, s, &why);
       if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
@@ -484,7 +513,7 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
 moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,
                              int n_tokens, void* y_bf16, void* stream) {
   return moe_stack_forward_traced(layers, n_layers, x_bf16, n_tokens, y_bf16, nullptr, nullptr,
-                                  stream);
+                                  nullptr, stream);
 }
 
 }  // extern "C"

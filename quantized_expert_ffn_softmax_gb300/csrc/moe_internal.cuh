@@ -1,6 +1,7 @@
 // Internal definitions shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -54,6 +55,7 @@ struct DecodeParams {
   const uint16_t* x_in;  // [T][H] bf16 (device)
   uint16_t* y_out;       // forward: y [T][H]; stack: h_L [T][H]
   uint16_t* h_trace;     // [L][T][H] or null
+  uint16_t* in_trace;    // [L][T][H] or null: each layer's normalised input
   int32_t* ids_out;      // [L][T][k] or null
   float* w_out;          // [L][T][k] or null
   uint16_t* xbuf;        // [2][4][H] residual ping-pong
@@ -78,19 +80,25 @@ struct Workspace {
   uint16_t* x_stage = nullptr;  // [max_tokens][H] staging for host inputs
   uint16_t* y_stage = nullptr;  // [max_tokens][H] staging for host outputs
   uint16_t* y_layer = nullptr;  // [max_tokens][H] per-layer output in prefill-sized stacks
+  uint16_t* u_layer = nullptr;  // [max_tokens][H] per-layer normalised input (same)
   int32_t* ids_stage = nullptr; // [max_tokens][k]
   float* w_stage = nullptr;     // [max_tokens][k]
   // prefill
+  __half* x16 = nullptr;        // [max_tokens][H] fp16, per-token scaled, K-permuted
+  int32_t* xshift = nullptr;    // [max_tokens] per-token power-of-two shift
   float* zf = nullptr;          // [max_tokens][E] router logits
   int32_t* topk_ids = nullptr;  // [max_tokens][k]
   float* topk_w = nullptr;      // [max_tokens][k]
-  int32_t* counts = nullptr;    // [E] (+ scratch)
-  int32_t* offsets = nullptr;   // [E+1]
+  int32_t* offsets = nullptr;   // [E+1] bucket offsets
   int32_t* perm_tok = nullptr;  // [max_tokens*k] token of each bucketed row
   float* perm_w = nullptr;      // [max_tokens*k] routing weight of each bucketed row
-  int32_t* tiles = nullptr;     // tile list
-  void* hmid = nullptr;         // bf16 [max_tokens*k + max_tokens][Fmax]
-  float* yacc = nullptr;        // [max_tokens][H]
+  int4* gu_units = nullptr;     // gate/up work units
+  int4* dn_units = nullptr;     // down work units
+  int32_t* n_units = nullptr;   // [2] counts of the two lists
+  __half* hmid_r = nullptr;     // [max_tokens*k][F] routed SwiGLU output (bucket order)
+  __half* hmid_s = nullptr;     // [max_tokens][Fs] shared-expert SwiGLU output
+  float* yacc = nullptr;        // [max_tokens][H] fp32 combine accumulator
+  int max_gu_units = 0, max_dn_units = 0;
   void* scratch = nullptr;
   size_t bytes = 0;
 };
@@ -100,6 +108,10 @@ struct Workspace {
 struct moe_layer {
   moe_layer_config cfg;
   moe::LayerDev dev;
+  alignas(64) CUtensorMap tmap_x16;   // x16 rows, box {64, 1}, 128B swizzle (gather4)
+  alignas(64) CUtensorMap tmap_hr;    // hmid_r rows
+  alignas(64) CUtensorMap tmap_hs;    // hmid_s rows
+  int router_shift = 0;               // router weights are scaled by 2^router_shift
   void* weights_block = nullptr;  // one allocation holding all weight copies
   size_t weights_bytes = 0;
   void* ws_block = nullptr;       // one allocation holding the workspace
@@ -117,4 +129,6 @@ size_t decode_smem_bytes(const DecodeParams& p);
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
                           float* w_out, bool route_only, cudaStream_t stream, const char** why);
 size_t prefill_workspace_bytes(const moe_layer_config& c);
+// Carves the prefill workspace out of `scratch` and encodes the tensor maps.
+moe_status prefill_init(moe_layer* L, void* scratch, const char** why);
 }  // namespace moe

@@ -23,6 +23,14 @@ def y_tol(y_ref) -> float:
     return 1e-2 * float(np.abs(y_ref).max()) + 1e-3
 
 
+def h_tol(y_ref, h_ref) -> float:
+    """Tolerance on a stack output h = bf16(h_in + bf16(y)): the y tolerance,
+    plus one bf16 unit in the last place (2^-7 relative, upper bound) for each
+    of the two roundings, which may land on different sides of a rounding
+    boundary when y differs within its tolerance."""
+    return y_tol(y_ref) + 2.0 ** -7 * (float(np.abs(y_ref).max()) + float(np.abs(h_ref).max()))
+
+
 def config_dict(cfg: W.MoEConfig, max_tokens: int) -> dict:
     return dict(hidden=cfg.hidden, n_experts=cfg.n_experts, top_k=cfg.top_k, ffn=cfg.ffn,
                 shared_ffn=cfg.shared_ffn, max_tokens=max_tokens)

@@ -361,14 +361,35 @@ def test_residual_with_zero_output_is_identity_and_stack_composes():
         Lz[n] = np.zeros_like(L[n])
     out, trace, _ = oracle.stack_forward([Lz, Lz, Lz], cfg.top_k, x)
     assert np.array_equal(out, x)
-    # two real layers = two single-layer steps with the residual between
+    # two real layers = two pre-norm residual steps
     L1 = W.layer(cfg, 1)
     out, trace, ids = oracle.stack_forward([L, L1], cfg.top_k, x)
-    h1 = oracle.residual(x, oracle.moe_forward(L, cfg.top_k, x)[0])
-    h2 = oracle.residual(h1, oracle.moe_forward(L1, cfg.top_k, h1)[0])
+    h1 = oracle.residual(x, oracle.moe_forward(L, cfg.top_k, oracle.rmsnorm(x))[0])
+    h2 = oracle.residual(h1, oracle.moe_forward(L1, cfg.top_k, oracle.rmsnorm(h1))[0])
     assert np.array_equal(trace[0], h1) and np.array_equal(out, h2)
     # residual: one rounding of h + bf16(y)
     hf = W.bf16_bits_to_f32(x).astype(np.float64)
-    y0 = oracle.moe_forward(L, cfg.top_k, x)[0]
+    y0 = oracle.moe_forward(L, cfg.top_k, oracle.rmsnorm(x))[0]
     yb = oracle.bf16_to_f64(oracle.round_bf16(y0))
     assert np.array_equal(h1, oracle.round_bf16(hf + yb))
+
+
+def test_rmsnorm_against_numpy_and_closed_forms():
+    x = W.activations(W.CONFIGS["decode35b"], 3, n_tokens=3)
+    u = oracle.rmsnorm(x)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    ref = xf / np.sqrt(np.mean(xf ** 2, axis=1, keepdims=True) + 1e-6)
+    assert np.array_equal(u, oracle.round_bf16(ref))
+    # constant rows normalise to +-1/sqrt(1 + eps/c^2)
+    c = np.full((2, 64), 0, np.float64)
+    c[0] = 3.0
+    c[1] = -0.5
+    uc = oracle.bf16_to_f64(oracle.rmsnorm(oracle.round_bf16(c)))
+    assert np.all(uc[0] == 1.0) and np.all(uc[1] == -1.0)
+    # invariant under power-of-two scaling of the input (exact in bf16)
+    x4 = oracle.round_bf16(xf * 4.0)
+    assert np.array_equal(oracle.rmsnorm(x4), u)
+    # the stack stays finite over a deep 35B-shaped stack only with the norm
+    # (checked on the real workload in the GPU tests); a zero row stays zero
+    z = np.zeros((1, 64), np.uint16)
+    assert np.array_equal(oracle.rmsnorm(z), z)
