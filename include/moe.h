@@ -136,6 +136,15 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
                                     void* in_trace_bf16, int32_t* ids_trace, void* stream);
 
+/* Introspection of the prefill path's token bucketing: after a moe_forward
+ * or moe_route call with n_tokens > 4 on this layer, copies the bucket
+ * offsets [E+1] (exclusive scan of the per-expert counts; offsets[E] = T*k)
+ * and the token of every bucketed row [T*k] (rows sorted by expert, then by
+ * token).  Host or device pointers; synchronises the stream.  n_tokens must
+ * be the batch of that call. */
+moe_status moe_last_buckets(moe_layer* layer, int n_tokens, int32_t* offsets, int32_t* perm_token,
+                            void* stream);
+
 /* Synchronises `stream`, then returns and clears the layer's device error
  * word (MOE_ERR_BOUNDS or MOE_ERR_TIMEOUT if a kernel recorded one). */
 moe_status moe_status_sync(moe_layer* layer, void* stream);

@@ -80,6 +80,8 @@ def lib():
         L.moe_stack_forward_traced.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp, vp, vp,
                                                vp]
         L.moe_stack_forward_traced.restype = i32
+        L.moe_last_buckets.argtypes = [vp, i32, vp, vp, vp]
+        L.moe_last_buckets.restype = i32
         L.moe_status_sync.argtypes = [vp, vp]
         L.moe_status_sync.restype = i32
         _lib = L
@@ -170,6 +172,11 @@ def moe_stack_forward_traced(layers: Sequence[int], n_layers: int, x, n_tokens: 
     _check(lib().moe_stack_forward_traced(_layer_array(layers), n_layers, _ptr(x), n_tokens,
                                           _ptr(y), _ptr(h_trace), _ptr(in_trace),
                                           _ptr(ids_trace), _stream(stream)))
+
+
+def moe_last_buckets(layer: int, n_tokens: int, offsets, perm_token, stream=None) -> None:
+    _check(lib().moe_last_buckets(layer, n_tokens, _ptr(offsets), _ptr(perm_token),
+                                  _stream(stream)))
 
 
 def moe_status_sync(layer: int, stream=None) -> int:

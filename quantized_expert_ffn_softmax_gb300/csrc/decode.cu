@@ -19,57 +19,13 @@
 // conversion, so their range never overflows fp16.
 #include <math.h>
 
+#include "device_common.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint64_t global_timer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
+using namespace dev;
 
 // Bounded wait for a bulk-copy phase; on timeout records the error and
 // returns (the caller then computes on whatever is in shared memory).
@@ -83,18 +39,6 @@ __device__ __forceinline__ void mbar_wait_bounded(uint64_t* bar, uint32_t parity
       return;
     }
   }
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int ld_relaxed_i32(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
 }
 
 // Grid barrier on a counter zeroed before the launch: barrier number `n`
@@ -123,9 +67,6 @@ __device__ __forceinline__ void grid_sync(GridBarrier* b, unsigned& n, int* err,
   ++n;
   __syncthreads();
 }
-
-// 2^-s as a float, |s| <= 100.
-__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
 
 // Shift that brings amax into [32, 64).
 __device__ __forceinline__ int range_shift(float amax) {
@@ -200,18 +141,6 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
 #pragma unroll
   for (int k = 16 >> LOGN; k >= 1; k >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], k);
   return v[0];
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
-  return v;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, k));
-  return v;
 }
 
 }  // namespace
@@ -424,51 +353,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
     // ------------------------------------------------ top-k + softmax + units
     if (warp < T) {
       const int t = warp;
-      float v[kMaxExperts / 32];
-      const int nj = (E + 31) / 32;
-#pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = (j < nj && e < E) ? __ldcg(p.z + (size_t)t * E + e) : -INFINITY;
+      int id;
+      float wt;
+      // z was written by other CTAs before the barrier: read it through L2
+      if (!warp_topk_softmax_ldcg(p.z + (size_t)t * E, E, k, &id, &wt) && lane == 0)
+        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+      if (lane < k) {
+        M.sel_id[t][lane] = id;
+        M.sel_w[t][lane] = wt;
       }
-      uint32_t taken = 0;
-      for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < kMaxExperts / 32; ++j) {
-          if (j < nj && !((taken >> j) & 1u)) {
-            const int e = lane + 32 * j;
-            if (e < E && (v[j] > bv || (v[j] == bv && e < bi))) {
-              bv = v[j];
-              bi = e;
-            }
-          }
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if (bi < 0 || bi >= E) {  // only reachable with non-finite logits
-          if (lane == 0) atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-          bi = r;
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == 0) {
-          M.sel_id[t][r] = bi;
-          M.sel_z[t][r] = bv;
-        }
-      }
-      __syncwarp();
-      const float z0 = M.sel_z[t][0];
-      const float ex = (lane < k) ? __expf(M.sel_z[t][lane] - z0) : 0.0f;
-      const float den = warp_sum(ex);
-      if (lane < k) M.sel_w[t][lane] = ex / den;
     }
     if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
     for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)

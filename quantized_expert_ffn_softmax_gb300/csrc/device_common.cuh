@@ -1,0 +1,288 @@
+// Device helpers shared by the decode and prefill kernels: inline PTX for
+// mbarriers, bulk / tensor copies (TMA) and the 5th-generation tensor core
+// (tcgen05 + TMEM), bounded waits, and warp reductions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte streaming load of read-only data (no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_i32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the completion of the phase of `bar` with parity `parity`.
+// Bounded: gives up (returns false) when the layer's error word is already
+// set, or after timeout_ns, recording MOE_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          uint64_t timeout_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  unsigned spins = 0;
+  while (!mbar_test(bar, parity)) {
+    if ((++spins & 31u) == 0) {
+      if (ld_relaxed_i32(err) != 0) return false;
+      if (global_timer() - t0 > timeout_ns) {
+        atomicCAS(err, 0, (int)MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Non-tensor bulk copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tensor-map gather of 4 rows (box one row high) into consecutive 128-byte
+// rows of shared memory starting at dst; the map's swizzle is applied.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, int col, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (tensor core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------- tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulation.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on `bar` when all tcgen05 operations issued so far by this
+// thread have completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored in the 128-byte
+// swizzled canonical layout: rows of 64 fp16 (128 B), 8-row atoms of 1 KB
+// stacked at a 1 KB stride.  The tile base must be 1 KB aligned; moving the
+// start address by 32 B selects the next K=16 slice inside the atom.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1u << 16;                  // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;        // stride byte offset: 8-row atom
+  d |= (uint64_t)1u << 46;                  // descriptor version
+  d |= (uint64_t)2u << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp16 x fp16 -> fp32, both operands K-major, M=128.
+__device__ __forceinline__ uint32_t idesc_f16_m128(int n) {
+  return (1u << 4)                        // D format fp32
+         | (0u << 7) | (0u << 10)         // A, B format fp16
+         | ((uint32_t)(n >> 3) << 17)     // N
+         | ((uint32_t)(128 >> 4) << 24);  // M
+}
+
+// ------------------------------------------------------------- warp helpers
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, k));
+  return v;
+}
+
+// 2^s as a float, -126 <= s <= 127.
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
+
+// Top-k of one token's E logits (logit e read by lane e % 32), descending by
+// value, ties to the lower id; then softmax over the selected logits.  Lane
+// r < k receives id and weight r.  Returns false if a non-finite logit left
+// no valid candidate.  LDCG: read the logits through L2 only (they were
+// written by other CTAs of the same launch).
+template <bool LDCG>
+__device__ __forceinline__ bool warp_topk_softmax_impl(const float* z, int E, int k, int* id_out,
+                                                       float* w_out) {
+  const int lane = threadIdx.x & 31;
+  float v[kMaxExperts / 32];
+  const int nj = (E + 31) / 32;
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = (j < nj && e < E) ? (LDCG ? __ldcg(z + e) : z[e]) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  int my_id = 0;
+  float my_z = 0.0f, z0 = 0.0f;
+  bool ok = true;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      if (j < nj && !((taken >> j) & 1u)) {
+        const int e = lane + 32 * j;
+        if (e < E && (v[j] > bv || (v[j] == bv && e < bi))) {
+          bv = v[j];
+          bi = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < 0 || bi >= E) {  // only reachable with non-finite logits
+      ok = false;
+      bi = r;
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (r == 0) z0 = bv;
+    if (lane == r) {
+      my_id = bi;
+      my_z = bv;
+    }
+  }
+  const float ex = (lane < k) ? __expf(my_z - z0) : 0.0f;
+  const float den = warp_sum(ex);
+  *id_out = my_id;
+  *w_out = ex / den;
+  return ok;
+}
+
+__device__ __forceinline__ bool warp_topk_softmax(const float* z, int E, int k, int* id_out,
+                                                  float* w_out) {
+  return warp_topk_softmax_impl<false>(z, E, k, id_out, w_out);
+}
+__device__ __forceinline__ bool warp_topk_softmax_ldcg(const float* z, int E, int k, int* id_out,
+                                                       float* w_out) {
+  return warp_topk_softmax_impl<true>(z, E, k, id_out, w_out);
+}
+
+}  // namespace dev
+}  // namespace moe

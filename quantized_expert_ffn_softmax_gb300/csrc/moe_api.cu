@@ -1,5 +1,6 @@
 // C ABI of the routed MoE FFN layer: validation, HBM ownership, staging of
 // host buffers, and dispatch to the decode (1..4 tokens) and prefill paths.
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -243,6 +244,29 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (e != cudaSuccess) {
     moe_layer_destroy(L);
     return cuda_fail(e, "initialise workspace");
+  }
+  {
+    const char* why = "";
+    if ((st = moe::prefill_init(L, L->ws.scratch, &why)) != MOE_OK) {
+      moe_layer_destroy(L);
+      return fail(st, "prefill workspace: %s", why);
+    }
+  }
+  // The prefill router splits W_r * 2^shift into two fp16 terms; the shift
+  // puts max |W_r| in [16, 32) so neither term overflows or underflows.
+  {
+    std::vector<float> wr((size_t)E * H);
+    e = cudaMemcpy(wr.data(), L->dev.router_w, sizeof(float) * wr.size(), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      moe_layer_destroy(L);
+      return cuda_fail(e, "read router weights");
+    }
+    float m = 0.0f;
+    for (float v : wr) m = fabsf(v) > m ? fabsf(v) : m;
+    int ex = 0;
+    if (m > 0.0f && isfinite(m)) frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
+    int sh = 5 - ex;                             // m * 2^sh in [16, 32)
+    L->router_shift = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
   }
   *out = L;
   return MOE_OK;
@@ -508,6 +532,22 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
     }
   }
   return stage_out(layers[0], n_tokens, y_bf16, sg, s);
+}
+
+moe_status moe_last_buckets(moe_layer* layer, int n_tokens, int32_t* offsets, int32_t* perm_token,
+                            void* stream) {
+  if (!layer || !offsets || !perm_token) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (n_tokens <= moe::kMaxDecodeTokens || n_tokens > layer->cfg.max_tokens)
+    return fail(MOE_ERR_CAPACITY, "n_tokens=%d is not a prefill-path batch", n_tokens);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t nE = (size_t)layer->cfg.n_experts + 1;
+  const size_t nP = (size_t)n_tokens * layer->cfg.top_k;
+  const cudaMemcpyKind ko = is_device_ptr(offsets) ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost;
+  const cudaMemcpyKind kp = is_device_ptr(perm_token) ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost;
+  CUDA_TRY(cudaMemcpyAsync(offsets, layer->ws.offsets, sizeof(int32_t) * nE, ko, s), "copy offsets");
+  CUDA_TRY(cudaMemcpyAsync(perm_token, layer->ws.perm_tok, sizeof(int32_t) * nP, kp, s), "copy perm");
+  CUDA_TRY(cudaStreamSynchronize(s), "synchronise");
+  return MOE_OK;
 }
 
 moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,

@@ -108,9 +108,9 @@ struct Workspace {
 struct moe_layer {
   moe_layer_config cfg;
   moe::LayerDev dev;
-  alignas(64) CUtensorMap tmap_x16;   // x16 rows, box {64, 1}, 128B swizzle (gather4)
-  alignas(64) CUtensorMap tmap_hr;    // hmid_r rows
-  alignas(64) CUtensorMap tmap_hs;    // hmid_s rows
+  CUtensorMap tmap_x16;   // x16 rows, box {64, 1}, 128B swizzle (gather4)
+  CUtensorMap tmap_hr;    // hmid_r rows
+  CUtensorMap tmap_hs;    // hmid_s rows
   int router_shift = 0;               // router weights are scaled by 2^router_shift
   void* weights_block = nullptr;  // one allocation holding all weight copies
   size_t weights_bytes = 0;
