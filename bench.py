@@ -1,0 +1,487 @@
+"""Benchmark of the routed MoE FFN layer on GB300.
+
+Headline: single-token decode through the 40-layer 35B-A3B-shaped stack
+(hidden 2048, 256 experts/layer, top-8, expert FFN 512, shared FFN 512,
+int4/32-block/fp16-scale experts), as tokens/s, with the achieved HBM
+bandwidth of the decode kernel against the measured peak.  Also measured
+(under "extra"): the 1+3-token MTP verify batch on the same stack, the
+48-layer 125B-A6B-shaped stack with permuted slot tables, and the
+8192-token prefill chunk through one 125B-shaped layer (tokens/s and
+tensor-core utilisation of its grouped GEMMs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (decode tokens are independent: weak scaling, no collective on the
+data path); rank 0 prints one JSON line.  --impl reference times the CPU
+oracle (test infrastructure) on this host's cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workload as W  # noqa: E402
+
+HEADLINE = "decode35b"
+METRIC = "MoE decode tok/s (40-layer 35B-A3B-shaped stack, 1 token)"
+UNIT = "tokens/s"
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def decode_bytes_per_layer(cfg, n_units_routed: int) -> int:
+    """Algorithmic bytes of one layer: packed codes + scales of the routed
+    experts that run plus the shared expert (each byte read once)."""
+    b = n_units_routed * cfg.expert_bytes()
+    if cfg.shared_ffn:
+        b += cfg.expert_bytes(cfg.shared_ffn)
+    return b
+
+
+def router_bytes(cfg) -> int:
+    return cfg.n_experts * cfg.hidden * 4
+
+
+def prefill_flops(cfg, T) -> float:
+    H, F, Fs, k, E = cfg.hidden, cfg.ffn, cfg.shared_ffn, cfg.top_k, cfg.n_experts
+    return 2.0 * T * (k * 3 * H * F + 3 * H * Fs + E * H)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for i, nm in enumerate(names):
+                if r[5 + i].strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == src_hash:
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class Dist:
+    def __init__(self, n_gpus: int):
+        import torch
+
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.n = max(n_gpus, self.world)
+        self.pg = None
+        torch.cuda.set_device(self.local)
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def build_stack(cfg, max_tokens):
+    import quantized_expert_ffn_softmax_gb300 as moe
+    import torch
+
+    config = dict(hidden=cfg.hidden, n_experts=cfg.n_experts, top_k=cfg.top_k, ffn=cfg.ffn,
+                  shared_ffn=cfg.shared_ffn, max_tokens=max_tokens)
+    layers = []
+    for l in range(cfg.n_layers):
+        D = W.device_layer(cfg, l)
+        w = {n: D[n] for n in ("router_w", "slot_of_expert", "gate_q", "gate_s", "up_q", "up_s",
+                               "down_q", "down_s")}
+        w["router_bias"] = D["router_b"]
+        if cfg.shared_ffn:
+            for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+                w["sh_" + n] = D["sh_" + n]
+        torch.cuda.synchronize()
+        layers.append(moe.MoELayer(config, w, True))
+        del D, w
+    return layers
+
+
+def time_steps(fn, steps, warmup, dist, ring_len):
+    import torch
+
+    for i in range(warmup):
+        fn(i % ring_len)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(steps):
+        fn((warmup + i) % ring_len)
+    e.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    return dist.max(s.elapsed_time(e) / steps)
+
+
+def kernel_profile(fn, steps, ring_len):
+    import quantized_expert_ffn_softmax_gb300 as moe
+    import torch
+
+    torch.cuda.synchronize()
+    moe.moe_profile_read()
+    moe.moe_profile_enable(True)
+    for i in range(steps):
+        fn(i % ring_len)
+    torch.cuda.synchronize()
+    moe.moe_profile_enable(False)
+    return moe.moe_profile_read()
+
+
+def bench_decode(name, steps, warmup, dist, with_e2e=False):
+    import quantized_expert_ffn_softmax_gb300 as moe
+    import torch
+
+    cfg = W.CONFIGS[name]
+    T = cfg.n_tokens
+    layers = build_stack(cfg, max_tokens=8)
+    hs = [l.handle for l in layers]
+    ring = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).cuda() for i in range(64)]
+    y = torch.empty_like(ring[0])
+    # unique routed experts per layer for this input ring (from one traced pass)
+    L, k, H = cfg.n_layers, cfg.top_k, cfg.hidden
+    ids = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    hbuf = torch.empty((L, T, H), dtype=torch.int16, device="cuda")
+    ubuf = torch.empty_like(hbuf)
+    uniq = []
+    for i in range(8):
+        moe.moe_stack_forward_traced(hs, L, ring[i], T, y, hbuf, ubuf, ids)
+        a = ids.cpu().numpy()
+        uniq.append(sum(len(set(a[l].ravel().tolist())) for l in range(L)))
+    assert moe.moe_status_sync(hs[0]) == moe.MOE_OK
+    mean_unique_routed = float(np.mean(uniq))  # summed over layers
+    bytes_per_step = mean_unique_routed * cfg.expert_bytes() + L * (
+        cfg.expert_bytes(cfg.shared_ffn) if cfg.shared_ffn else 0)
+
+    def step(i):
+        moe.moe_stack_forward(hs, L, ring[i], T, y)
+
+    with ClockSampler(dist.local) as clk:
+        ms = time_steps(step, steps, warmup, dist, len(ring))
+    prof = kernel_profile(step, min(steps, 50), len(ring))
+    assert moe.moe_status_sync(hs[0]) == moe.MOE_OK
+    kcount, kms = prof.get("moe_decode_kernel", (0, 0.0))
+    k_avg = kms / max(kcount, 1)
+    launches_per_step = kcount / max(1, min(steps, 50))
+    out = {
+        "ms_per_step": ms,
+        "tok_s": dist.n * T / (ms / 1e3),
+        "bytes_per_step": bytes_per_step,
+        "gbs_step": bytes_per_step / (ms / 1e3) / 1e9,
+        "kernel_ms": k_avg,
+        "gbs_kernel": bytes_per_step / (k_avg / 1e3) / 1e9 if k_avg else None,
+        "bytes_incl_router": bytes_per_step + L * router_bytes(cfg),
+        "unique_routed_per_layer": mean_unique_routed / L,
+        "launches_per_step": launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if with_e2e:
+        xs = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).pin_memory() for i in range(8)]
+        yh = torch.empty_like(xs[0]).pin_memory()
+        for i in range(3):
+            moe.moe_stack_forward(hs, L, xs[i], T, yh)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            moe.moe_stack_forward(hs, L, xs[i % 8], T, yh)  # H2D, kernels, D2H, sync
+        dt = dist.max((time.perf_counter() - t0) / steps)
+        out["e2e"] = {"value": dist.n * T / dt, "unit": UNIT,
+                      "h2d_bytes_per_step": int(xs[0].numel() * 2),
+                      "d2h_bytes_per_step": int(yh.numel() * 2)}
+    for l in layers:
+        l.close()
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_prefill(name, steps, warmup, dist):
+    import quantized_expert_ffn_softmax_gb300 as moe
+    import torch
+
+    cfg = W.CONFIGS[name]
+    T = cfg.n_tokens
+    layer = build_stack(cfg, max_tokens=T)[0]
+    xs = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).cuda() for i in range(2)]
+    y = torch.empty_like(xs[0])
+
+    def step(i):
+        moe.moe_forward(layer.handle, xs[i], T, y)
+
+    ms = time_steps(step, steps, warmup, dist, 2)
+    prof = kernel_profile(step, min(steps, 20), 2)
+    assert moe.moe_status_sync(layer.handle) == moe.MOE_OK
+    # algorithmic FLOPs per GEMM kernel
+    H, F, Fs, k, E = cfg.hidden, cfg.ffn, cfg.shared_ffn, cfg.top_k, cfg.n_experts
+    fl = {"moe_gemm_gateup_swiglu": 2.0 * T * (k * 2 * H * F + 2 * H * Fs),
+          "moe_gemm_down_scatter": 2.0 * T * (k * H * F + H * Fs),
+          "moe_gemm_router": 2.0 * T * E * H}
+    kern = {}
+    total_k_ms = 0.0
+    for nm, (c, tms) in prof.items():
+        avg = tms / max(c, 1)
+        total_k_ms += tms
+        ent = {"launches": c, "avg_ms": avg}
+        if nm in fl:
+            ent["tflops"] = fl[nm] / (avg / 1e3) / 1e12
+        kern[nm] = ent
+    for nm in kern:
+        kern[nm]["share"] = prof[nm][1] / total_k_ms if total_k_ms else None
+    gemm_ms = sum(kern[n]["avg_ms"] for n in ("moe_gemm_gateup_swiglu", "moe_gemm_down_scatter")
+                  if n in kern)
+    gemm_fl = fl["moe_gemm_gateup_swiglu"] + fl["moe_gemm_down_scatter"]
+    out = {"ms_per_step": ms, "tok_s": dist.n * T / (ms / 1e3),
+           "tflops_step": prefill_flops(cfg, T) / (ms / 1e3) / 1e12,
+           "grouped_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "kernels": kern,
+           "launches_per_step": sum(v["launches"] for v in kern.values()) / max(1, min(steps, 20))}
+    layer.close()
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_decode_sample(cfg, n_tokens: int, n_layers: int):
+    """Times the oracle on `n_tokens` tokens through the first `n_layers`
+    layers of the stack (expert weights drawn before the timed region).
+    Returns (seconds per token for the full stack, description)."""
+    import oracle
+
+    routers = [W.router(cfg, l) for l in range(n_layers)]
+    shared = [W.shared_expert(cfg, l) for l in range(n_layers)]
+    xs = [W.activations(cfg, 100 + i) for i in range(n_tokens)]
+    # route once to know which experts to draw, then time the full pass
+    plans = []
+    for x in xs:
+        h = x.copy()
+        plan = []
+        for l in range(n_layers):
+            u = oracle.rmsnorm(h)
+            z = oracle.router_logits(*routers[l], u)
+            ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
+            plan.append([W.expert(cfg, l, int(e)) for e in ids[0]])
+            y = oracle.combine_token(plan[-1], w[0], shared[l], u[0])
+            h = oracle.residual(h, y[None, :])
+        plans.append(plan)
+    t0 = time.perf_counter()
+    for x, plan in zip(xs, plans):
+        h = x.copy()
+        for l in range(n_layers):
+            u = oracle.rmsnorm(h)
+            z = oracle.router_logits(*routers[l], u)
+            ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
+            y = oracle.combine_token(plan[l], w[0], shared[l], u[0])
+            h = oracle.residual(h, y[None, :])
+    dt = time.perf_counter() - t0
+    per_token_full = dt / n_tokens * (cfg.n_layers / n_layers)
+    desc = ("oracle (fp64 C, 1 thread) on %d token(s) x %d of %d layers; expert weights drawn "
+            "before timing; scaled to the full stack" % (n_tokens, n_layers, cfg.n_layers))
+    return per_token_full, desc
+
+
+def run_reference(args):
+    cfg = W.CONFIGS[HEADLINE]
+    import oracle
+
+    oracle.build()
+    # one step = one token through 8 of the 40 layers (about 1-2 s of CPU)
+    per = []
+    for _ in range(args.warmup):
+        oracle_decode_sample(cfg, 1, 8)
+    for _ in range(args.steps):
+        s, desc = oracle_decode_sample(cfg, 1, 8)
+        per.append(s)
+    sec = float(np.mean(per))
+    v = 1.0 / sec
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": HEADLINE},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    dist = Dist(args.gpus)
+    import quantized_expert_ffn_softmax_gb300 as moe
+
+    moe.lib()
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    head = bench_decode(HEADLINE, args.steps, args.warmup, dist, with_e2e=True)
+    extra = {}
+    if not args.no_extra:
+        for nm in ("mtp35b", "decode125b"):
+            r = bench_decode(nm, max(20, args.steps // 2), args.warmup, dist)
+            r["frac_of_peak_kernel"] = r["gbs_kernel"] / hbm if r["gbs_kernel"] else None
+            extra[nm] = r
+        pf = bench_prefill("prefill125b", max(10, args.steps // 10), args.warmup, dist)
+        g = pf["kernels"].get("moe_gemm_gateup_swiglu", {})
+        pf["roofline_gateup"] = {"bound": "tensor", "achieved": g.get("tflops"), "peak": bf16,
+                                 "unit": "TFLOP/s", "frac": (g.get("tflops") or 0) / bf16,
+                                 "note": "fp16 operands; fp16 dense peak = bf16 peak"}
+        pf["grouped_gemm_frac"] = (pf["grouped_gemm_tflops"] or 0) / bf16
+        extra["prefill125b"] = pf
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cfg = W.CONFIGS[HEADLINE]
+        sec, desc = oracle_decode_sample(cfg, 2, 10)
+        cpu = {"value": 1.0 / sec, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    src = source_hash("quantized_expert_ffn_softmax_gb300/csrc/decode.cu",
+                      "quantized_expert_ffn_softmax_gb300/csrc/device_common.cuh")
+    launches = head["launches_per_step"] * args.steps
+    if not args.no_extra:
+        launches += 0  # extras are timed separately and not part of the headline region
+    line = {
+        "metric": METRIC, "value": head["tok_s"], "unit": UNIT, "n_gpus": dist.n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "layers": 40, "hidden": 2048, "experts": 256, "top_k": 8,
+                   "ffn": 512, "shared_ffn": 512, "tokens_per_step": 1,
+                   "weights": "int4, 32-block, fp16 scale", "input_ring": 64,
+                   "l2": "expert bytes per step 637 MB > 129 MB L2; 64-input ring",
+                   "parallelism": "replica per GPU" if dist.n > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": head["gbs_kernel"], "peak": hbm, "unit": "GB/s",
+                     "frac": (head["gbs_kernel"] or 0) / hbm,
+                     "traffic": ncu_traffic("moe_decode_kernel:" + HEADLINE, src),
+                     "peak_kind": peak_kind, "kernel": "moe_decode_kernel",
+                     "bytes_per_launch": head["bytes_per_step"],
+                     "kernel_ms": head["kernel_ms"]},
+        "cpu_baseline": cpu,
+        "e2e": head["e2e"],
+        "gpu_launches": int(round(launches)),
+        "clocks": head["clocks"],
+        "extra": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

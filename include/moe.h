@@ -149,6 +149,16 @@ moe_status moe_last_buckets(moe_layer* layer, int n_tokens, int32_t* offsets, in
  * word (MOE_ERR_BOUNDS or MOE_ERR_TIMEOUT if a kernel recorded one). */
 moe_status moe_status_sync(moe_layer* layer, void* stream);
 
+/* Per-kernel timing of the library's own launches, for measurement (off by
+ * default; it adds two event records per launch).  While enabled, every
+ * kernel launch is bracketed by CUDA events on its stream.
+ * moe_profile_read synchronises on the recorded events, writes up to
+ * max_entries rows -- kernel name (NUL-terminated, name_len bytes per row),
+ * launch count, total milliseconds -- returns the number of rows and clears
+ * the totals. */
+moe_status moe_profile_enable(int enable);
+int moe_profile_read(char* names, int name_len, int* counts, float* total_ms, int max_entries);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);
 

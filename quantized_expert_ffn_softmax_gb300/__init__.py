@@ -82,6 +82,10 @@ def lib():
         L.moe_stack_forward_traced.restype = i32
         L.moe_last_buckets.argtypes = [vp, i32, vp, vp, vp]
         L.moe_last_buckets.restype = i32
+        L.moe_profile_enable.argtypes = [i32]
+        L.moe_profile_enable.restype = i32
+        L.moe_profile_read.argtypes = [ctypes.c_char_p, i32, vp, vp, i32]
+        L.moe_profile_read.restype = i32
         L.moe_status_sync.argtypes = [vp, vp]
         L.moe_status_sync.restype = i32
         _lib = L
@@ -182,6 +186,27 @@ def moe_last_buckets(layer: int, n_tokens: int, offsets, perm_token, stream=None
 def moe_status_sync(layer: int, stream=None) -> int:
     """Synchronises and returns (and clears) the layer's device error word."""
     return lib().moe_status_sync(layer, _stream(stream))
+
+
+def moe_profile_enable(enable: bool) -> None:
+    _check(lib().moe_profile_enable(int(bool(enable))))
+
+
+def moe_profile_read(max_entries: int = 64) -> dict:
+    """{kernel name: (launch count, total ms)} since the last read."""
+    import numpy as np
+
+    name_len = 64
+    names = ctypes.create_string_buffer(name_len * max_entries)
+    counts = np.zeros(max_entries, np.int32)
+    ms = np.zeros(max_entries, np.float32)
+    n = lib().moe_profile_read(names, name_len, counts.ctypes.data, ms.ctypes.data, max_entries)
+    raw = names.raw
+    out = {}
+    for i in range(n):
+        nm = raw[i * name_len:(i + 1) * name_len].split(b"\0", 1)[0].decode()
+        out[nm] = (int(counts[i]), float(ms[i]))
+    return out
 
 
 class MoELayer:

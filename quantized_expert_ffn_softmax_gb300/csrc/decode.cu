@@ -21,6 +21,7 @@
 
 #include "device_common.cuh"
 #include "moe_internal.cuh"
+#include "profile.cuh"
 
 namespace moe {
 namespace {
@@ -705,6 +706,7 @@ static moe_status launch_tt(const DecodeParams& p, cudaStream_t stream, int num_
     return MOE_ERR_CUDA;
   }
   void* args[] = {const_cast<DecodeParams*>(&p)};
+  prof::Scope scope("moe_decode_kernel", stream);
   cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kDecodeThreads),
                                               args, smem, stream);
   if (e != cudaSuccess) {

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "moe_internal.cuh"
+#include "profile.cuh"
 
 namespace {
 
@@ -510,7 +511,10 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
     uint16_t* Y = L0->ws.y_layer;
     const uint16_t* cur = sg.x;
     for (int l = 0; l < n_layers; ++l) {
-      rmsnorm_kernel<<<(n_tokens + 7) / 8, 256, 0, s>>>(cur, n_tokens, H, U);
+      {
+        moe::prof::Scope sc("moe_rmsnorm", s);
+        rmsnorm_kernel<<<(n_tokens + 7) / 8, 256, 0, s>>>(cur, n_tokens, H, U);
+      }
       CUDA_TRY(cudaGetLastError(), "rmsnorm kernel");
       if (in_trace_bf16)
         CUDA_TRY(cudaMemcpyAsync((uint16_t*)in_trace_bf16 + (size_t)l * n, U, n * 2,
@@ -522,7 +526,10 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
                                false, s, &why);
       if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
       uint16_t* dst = (l == n_layers - 1) ? sg.y : (cur == P ? Q : P);
-      residual_kernel<<<2 * L0->num_sms, 256, 0, s>>>(cur, Y, dst, n);  // elementwise: in place is safe
+      {
+        moe::prof::Scope sc("moe_residual", s);
+        residual_kernel<<<2 * L0->num_sms, 256, 0, s>>>(cur, Y, dst, n);  // elementwise: in place is safe
+      }
       CUDA_TRY(cudaGetLastError(), "residual kernel");
       if (h_trace_bf16)
         CUDA_TRY(cudaMemcpyAsync((uint16_t*)h_trace_bf16 + (size_t)l * n, dst, n * 2,

@@ -36,6 +36,7 @@
 
 #include "device_common.cuh"
 #include "moe_internal.cuh"
+#include "profile.cuh"
 
 namespace moe {
 namespace {
@@ -765,6 +766,9 @@ moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_
     *why = "cudaFuncSetAttribute(gemm smem)";
     return MOE_ERR_CUDA;
   }
+  static const char* const names[3] = {"moe_gemm_gateup_swiglu", "moe_gemm_down_scatter",
+                                       "moe_gemm_router"};
+  prof::Scope scope(names[MODE], s);
   kern<<<grid, kGemmThreads, smem, s>>>(gp, L->tmap_x16, L->tmap_hr, L->tmap_hs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -822,7 +826,10 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   const int H = c.hidden, E = c.n_experts, k = c.top_k;
   cudaError_t e;
 
-  prep_x16_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, ws.x16, ws.xshift);
+  {
+    prof::Scope sc("moe_prep_x16", s);
+    prep_x16_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, ws.x16, ws.xshift);
+  }
 
   GemmParams gp;
   memset(&gp, 0, sizeof gp);
@@ -854,7 +861,10 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
 
   int32_t* ids = (route_only && ids_out) ? ids_out : ws.topk_ids;
   float* wts = (route_only && w_out) ? w_out : ws.topk_w;
-  topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(ws.zf, T, E, k, ids, wts, ws.err);
+  {
+    prof::Scope sc("moe_topk", s);
+    topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(ws.zf, T, E, k, ids, wts, ws.err);
+  }
   if (route_only) {
     if ((e = cudaGetLastError()) != cudaSuccess) {
       *why = cudaGetErrorString(e);
@@ -890,7 +900,10 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
     *why = "cudaFuncSetAttribute(bucket smem)";
     return MOE_ERR_CUDA;
   }
-  bucket_kernel<<<1, kBucketThreads, bsmem, s>>>(bp);
+  {
+    prof::Scope sc("moe_bucket", s);
+    bucket_kernel<<<1, kBucketThreads, bsmem, s>>>(bp);
+  }
 
   gp.units = ws.gu_units;
   gp.n_units = ws.n_units;
@@ -902,7 +915,10 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.units = ws.dn_units;
   gp.n_units = ws.n_units + 1;
   if ((st = launch_gemm<kScatter>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;
-  finalize_kernel<<<2 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
+  {
+    prof::Scope sc("moe_finalize", s);
+    finalize_kernel<<<2 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) {
     *why = cudaGetErrorString(e);
     return MOE_ERR_CUDA;
