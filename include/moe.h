@@ -136,6 +136,29 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
                                     void* in_trace_bf16, int32_t* ids_trace, void* stream);
 
+/* Allocation-free decode of one layer (1..4 tokens), for callers that
+ * cannot allocate device memory when they need a layer evaluated: code
+ * that runs while a CUDA graph is being captured into a memory pool it does
+ * not own, plug-ins hosted by a framework whose allocator is the only one
+ * allowed to call cudaMalloc, and processes held to a fixed device-memory
+ * budget after start-up.  The pages have no counterpart of this entry point.
+ * Computes y = layer(x) like moe_forward, but from the caller's weights
+ * (device pointers, layout as in moe_layer_weights, router_bias required),
+ * x [n_tokens][H] bf16 (device, 16-byte aligned) and y (device).  All the
+ * scratch memory the kernel needs comes from one static 4 MiB device array
+ * inside the library, present on every GPU that loads it until the process
+ * exits; shapes whose scratch would not fit return MOE_ERR_CAPACITY.  No
+ * call allocates or frees device memory.  The first call on each device
+ * looks up the array's device address with that device current: make it
+ * before any stream capture.  Every call shares the array, so calls that
+ * overlap on the GPU (other streams, other host threads) race on it.
+ * status_out (optional, device int32) is zeroed, then receives any error a
+ * kernel records (MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS); the slot table is only
+ * bounds-checked by the kernel.  Asynchronous on `stream`. */
+moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weights* w,
+                               const void* x_bf16, int n_tokens, void* y_bf16,
+                               int32_t* status_out, void* stream);
+
 /* Introspection of the prefill path's token bucketing: after a moe_forward
  * or moe_route call with n_tokens > 4 on this layer, copies the bucket
  * offsets [E+1] (exclusive scan of the per-expert counts; offsets[E] = T*k)

@@ -80,6 +80,9 @@ def lib():
         L.moe_stack_forward_traced.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp, vp, vp,
                                                vp]
         L.moe_stack_forward_traced.restype = i32
+        L.moe_forward_noalloc.argtypes = [ctypes.POINTER(moe_layer_config),
+                                          ctypes.POINTER(moe_layer_weights), vp, i32, vp, vp, vp]
+        L.moe_forward_noalloc.restype = i32
         L.moe_last_buckets.argtypes = [vp, i32, vp, vp, vp]
         L.moe_last_buckets.restype = i32
         L.moe_profile_enable.argtypes = [i32]
@@ -146,6 +149,23 @@ def moe_layer_create(config: dict, weights: dict, weights_on_device: bool) -> in
     _check(lib().moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), int(bool(weights_on_device)),
                                   ctypes.byref(out)))
     return out.value
+
+
+def _cfg_struct(config: dict) -> moe_layer_config:
+    return moe_layer_config(config["hidden"], config["n_experts"], config["top_k"],
+                            config["ffn"], config.get("shared_ffn", 0),
+                            config.get("n_slots", config["n_experts"]),
+                            config.get("max_tokens", 4))
+
+
+def moe_forward_noalloc(config: dict, weights: dict, x, n_tokens: int, y, status_out=None,
+                        stream=None) -> None:
+    """Allocation-free decode (1..4 tokens) from caller-owned device weights;
+    scratch comes from the library's static device array."""
+    cfg = _cfg_struct(config)
+    w = moe_layer_weights(*[_ptr(weights.get(n)) for n in WEIGHT_FIELDS])
+    _check(lib().moe_forward_noalloc(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), n_tokens,
+                                     _ptr(y), _ptr(status_out), _stream(stream)))
 
 
 def moe_layer_destroy(layer: int) -> None:

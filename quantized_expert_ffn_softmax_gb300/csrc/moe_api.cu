@@ -87,6 +87,10 @@ struct Stage {
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace moe
+
 extern "C" {
 
 int moe_version(void) { return 100; }

@@ -121,6 +121,8 @@ struct moe_layer {
 };
 
 namespace moe {
+// moe_api.cu: message returned by moe_last_error() on this thread
+void set_last_error(const char* msg);
 // decode.cu
 moe_status launch_decode(const DecodeParams& p, cudaStream_t stream, int num_sms,
                          const char** why);
