@@ -416,6 +416,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="time one workload only (profiling cases): decode35b, mtp35b, "
+                         "decode125b or prefill125b")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="with --only on a decode workload: use the first N layers")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -429,6 +434,17 @@ def main():
     import quantized_expert_ffn_softmax_gb300 as moe
 
     moe.lib()
+    if args.only:
+        if args.layers:
+            W.CONFIGS[args.only] = W.CONFIGS[args.only].replace(n_layers=args.layers)
+        if args.only.startswith("prefill"):
+            r = bench_prefill(args.only, args.steps, args.warmup, dist)
+        else:
+            r = bench_decode(args.only, args.steps, args.warmup, dist)
+        if dist.rank == 0:
+            print(json.dumps({"only": args.only, "layers": args.layers, "result": r}), flush=True)
+        dist.close()
+        return
     hbm, bf16, bf16_sus, peak_kind = peaks()
     head = bench_decode(HEADLINE, args.steps, args.warmup, dist, with_e2e=True)
     extra = {}

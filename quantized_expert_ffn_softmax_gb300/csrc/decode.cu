@@ -1,22 +1,34 @@
 // Decode / MTP-verify path (1..4 tokens): one persistent cooperative kernel
-// runs a whole stack of MoE layers.  Per layer:
+// (one CTA per SM) runs a whole stack of MoE layers.  Per layer:
+//
 //   phase R  (stacks: RMS-normalise the residual stream h -> u)
-//            router GEMV (fp32, one warp per expert row)        -> z
+//            router GEMV (fp32) over this CTA's experts, whose W_r rows
+//            were prefetched into shared memory during the previous layer
 //   barrier
-//   top-k + softmax + unit list, computed redundantly by every CTA
-//   phase G  fused dequant + gate/up GEMV + SwiGLU              -> h
+//   top-k    two levels: every warp selects the top-k of one slice of the
+//            experts, one warp per token merges the slices; softmax over
+//            the selection; the expert-unit list.  Computed redundantly by
+//            every CTA.  Then the CTA starts the bulk copies (TMA) of the
+//            expert weights it reads in this layer: the gate/up rows of its
+//            first items and the down rows of its output rows, with their
+//            block-scale tiles
+//   phase G  fused dequant + gate/up GEMV + SwiGLU from shared memory -> h;
+//            each warp owns whole rows (no CTA-wide reduction); a stage is
+//            refilled as soon as all warps have read it
 //   barrier
-//   phase D  fused dequant + down GEMV + weighted combine
-//            (+ residual h + bf16(y) for stacks)                -> y / h_{l+1}
+//   phase D  fused dequant + down GEMV + weighted combine from shared
+//            memory (+ residual h + bf16(y) for stacks) -> y / h_{l+1};
+//            each warp owns whole output rows
 //   barrier
-// The expert weights are streamed once with 128-bit non-allocating loads;
-// the per-block binary16 scales of each tile are staged in shared memory by
-// the bulk-copy (TMA) engine.  Packed 4-bit codes become fp16 pairs with a
+//
+// Only the router logits, h and h_{l+1} cross between CTAs (through L2);
+// every weight byte is read from HBM once, by a bulk copy issued as soon as
+// its address is known.  Packed 4-bit codes become fp16 pairs with a
 // magic-exponent OR (0x6400 | n = 1024 + n, minus 1032 = n - 8, exact);
-// products with the fp16 activations are exact and summed within a 32-weight
-// block in fp16, then scaled by the block scale and summed in fp32.
-// Activations are rescaled by a per-token power of two before the fp16
-// conversion, so their range never overflows fp16.
+// products with the fp16 activations are exact and summed within a
+// 32-weight block in fp16, then scaled by the block scale and summed in
+// fp32.  Activations are rescaled by a per-token power of two before the
+// fp16 conversion, so their range never overflows fp16.
 #include <math.h>
 
 #include "device_common.cuh"
@@ -28,19 +40,8 @@ namespace {
 
 using namespace dev;
 
-// Bounded wait for a bulk-copy phase; on timeout records the error and
-// returns (the caller then computes on whatever is in shared memory).
-__device__ __forceinline__ void mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err,
-                                                  uint64_t timeout_ns) {
-  if (mbar_test(bar, parity)) return;
-  const uint64_t t0 = global_timer();
-  while (!mbar_test(bar, parity)) {
-    if (global_timer() - t0 > timeout_ns) {
-      atomicCAS(err, 0, (int)MOE_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
+constexpr int kWarps = kDecodeThreads / 32;
+constexpr int kMaxRowsPerWarp = 4;  // down-phase output rows one warp keeps in registers
 
 // Grid barrier on a counter zeroed before the launch: barrier number `n`
 // completes when the counter reaches (n + 1) * gridDim.x.  Waits are bounded
@@ -51,19 +52,20 @@ __device__ __forceinline__ void grid_sync(GridBarrier* b, unsigned& n, int* err,
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned target = (n + 1) * gridDim.x + (unsigned)extra;
-    __threadfence();
-    atomicAdd(&b->count, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&b->count) : "memory");
     if (ld_acquire_u32(&b->count) < target) {
       const uint64_t t0 = global_timer();
+      unsigned spins = 0;
       while (ld_acquire_u32(&b->count) < target) {
-        if (ld_relaxed_i32(err) != 0) break;
-        if (global_timer() - t0 > timeout_ns) {
-          atomicCAS(err, 0, (int)MOE_ERR_TIMEOUT);
-          break;
+        if ((++spins & 15u) == 0) {
+          if (ld_relaxed_i32(err) != 0) break;
+          if (global_timer() - t0 > timeout_ns) {
+            atomicCAS(err, 0, (int)MOE_ERR_TIMEOUT);
+            break;
+          }
         }
       }
     }
-    __threadfence();
   }
   ++n;
   __syncthreads();
@@ -144,93 +146,199 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
   return v[0];
 }
 
+// Monotonic 32-bit key of a float (larger float -> larger key, > 0); NaN -> 0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) return 0u;
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// k rounds of selection over NJ candidates per lane (keys, ids), descending
+// by key, ties to the lower id; key 0 marks an empty candidate.  Lane r < k
+// receives the r-th (key, id); (0, -1) when fewer than k candidates exist.
+template <int NJ>
+__device__ __forceinline__ void warp_select(uint32_t (&key)[NJ], const int (&id)[NJ], int k,
+                                            uint32_t* out_key, int* out_id) {
+  const int lane = threadIdx.x & 31;
+  uint32_t bk = 0u;
+  int bi = 0x7fffffff, bj = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
+      bk = key[j];
+      bi = id[j];
+      bj = j;
+    }
+  uint32_t mk = 0u;
+  int mi = -1;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == gk && gk != 0u) ? (uint32_t)bi : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == r) {
+      mk = gk;
+      mi = (win == 0xffffffffu) ? -1 : (int)win;
+    }
+    if (gk != 0u && cand == win) {  // this lane holds the winner: take it, find its next best
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if (j == bj) key[j] = 0u;
+      bk = 0u;
+      bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
+          bk = key[j];
+          bi = id[j];
+          bj = j;
+        }
+    }
+  }
+  *out_key = mk;
+  *out_id = mi;
+}
+
 }  // namespace
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
 struct DecodeSmem {
-  size_t mbar, misc, red, xb, hres, xp, sc, hp, total;
-  __host__ __device__ static DecodeSmem make(int H, int F, int Fs, int TT, int max_units) {
+  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dbuf, hp, total;
+  size_t g_stage, d_item;
+  int nmy, nd_items;
+  bool dprefetch;
+  __host__ __device__ static DecodeSmem make(int H, int E, int F, int Fs, int TT, int max_units,
+                                             int grid, int g_stages, bool want_dprefetch) {
     DecodeSmem s;
     const int C = H / 32;
     const int n_routed_max = max_units - 1;
+    s.nmy = (E + grid - 1) / grid;
+    s.nd_items = (H / 8 + grid - 1) / grid;
+    s.g_stage = (size_t)16 * H + (size_t)64 * C;  // gate+up rows (2 x 16 x H/2) + scales
+    s.d_item = (size_t)9 * ((size_t)n_routed_max * F + Fs) / 2;  // per unit: codes 4F_u, scales F_u/2
     size_t o = 0;
     s.mbar = o;
-    o += 16;
+    o += 128;
     s.misc = o;
-    o += 8192;
-    s.red = o;
-    o += 8 * 32 * 4;
+    o += 12288;
+    s.slots = o;
+    o += ((size_t)E * 4 + 15) & ~(size_t)15;
     s.xb = o;
     o += (size_t)TT * H * 2;
     s.hres = o;
     o += (size_t)TT * H * 2;
-    s.xp = o;
-    o += (size_t)TT * H * 2;
-    s.sc = o;
-    size_t sc_gu = (size_t)2 * 16 * C * 2;
-    size_t sc_dn = (size_t)n_routed_max * 8 * (F / 32) * 2 + (size_t)8 * (Fs / 32) * 2;
-    o += (sc_gu > sc_dn ? sc_gu : sc_dn);
+    s.wr = o;
+    o += (size_t)s.nmy * H * 4;
     o = (o + 127) & ~(size_t)127;
-    s.hp = o;
-    o += ((size_t)n_routed_max * F + Fs) * TT * 2;
+    // one region shared by phase G (x pair planes + gate/up stages) and
+    // phase D (w*h pair planes): the two are never live at the same time
+    const size_t region = o;
+    s.xp = region;
+    s.gbuf = (region + (size_t)TT * H * 2 + 127) & ~(size_t)127;
+    const size_t g_end = s.gbuf + (size_t)g_stages * s.g_stage;
+    s.hp = region;
+    const size_t h_end = region + ((size_t)n_routed_max * F + Fs) * TT * 2;
+    o = g_end > h_end ? g_end : h_end;
+    o = (o + 127) & ~(size_t)127;
+    s.dbuf = o;
+    const size_t with_d = o + (size_t)s.nd_items * s.d_item;
+    s.dprefetch = want_dprefetch && with_d <= (size_t)227 * 1024 && s.nd_items <= kMaxRowsPerWarp;
+    if (s.dprefetch) o = with_d;
     s.total = (o + 127) & ~(size_t)127;
     return s;
   }
 };
 
-// misc region layout (ints / floats, each array padded)
 struct DecodeMisc {
   int x_shift[4];
-  int d_shift[4];
   int n_routed;
   int n_units;
-  int pad0[6];
+  int pad0[2];
   int sel_id[kMaxDecodeTokens][kMaxTopK];
-  float sel_z[kMaxDecodeTokens][kMaxTopK];
   float sel_w[kMaxDecodeTokens][kMaxTopK];
   int unit_expert[kMaxUnits];
   int unit_slot[kMaxUnits];
   float unit_w[kMaxUnits][kMaxDecodeTokens];
   unsigned bitmap[kMaxExperts / 32];
   int prefix[kMaxExperts / 32 + 1];
-  float tok_max[8][4];
-  float inv_rms[4];
+  float red_ss[kWarps][4];
+  float red_mx[kWarps][4];
+  uint32_t cand_key[kWarps][kMaxTopK];  // top-k level 1: per-warp selections
+  int cand_id[kWarps][kMaxTopK];
 };
-static_assert(sizeof(DecodeMisc) <= 8192, "misc region too small");
+static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
+
+// mbarrier slots
+enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarD = 4, kBarR = 5 };
 
 template <int TT>
-__global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    moe_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = p.H, E = p.E, k = p.k, F = p.F, Fs = p.Fs, T = p.T;
   const int C = H / 32;
   const int CF = F / 32;
   const int CS = Fs / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const DecodeSmem L = DecodeSmem::make(H, F, Fs, TT, p.max_units);
+  const int grid = gridDim.x;
+  const DecodeSmem L =
+      DecodeSmem::make(H, E, F, Fs, TT, p.max_units, grid, p.g_stages, p.want_dprefetch != 0);
+  const int NG = p.g_stages;  // 1 or 2
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
   DecodeMisc& M = *reinterpret_cast<DecodeMisc*>(smem + L.misc);
-  float* red = reinterpret_cast<float*>(smem + L.red);
+  int* slots = reinterpret_cast<int*>(smem + L.slots);
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.xb);      // layer input (u)
   uint16_t* hres = reinterpret_cast<uint16_t*>(smem + L.hres);  // residual stream (stacks)
   uint4* xp = reinterpret_cast<uint4*>(smem + L.xp);
-  __half* sc = reinterpret_cast<__half*>(smem + L.sc);
+  float* wr = reinterpret_cast<float*>(smem + L.wr);
+  unsigned char* gbuf = smem + L.gbuf;
+  unsigned char* dbuf = smem + L.dbuf;
   uint4* hp = reinterpret_cast<uint4*>(smem + L.hp);
+  float* amax_g = reinterpret_cast<float*>(p.bar->pad);  // [2][4], zeroed with the counter
 
   if (tid == 0) {
-    mbar_init(mbar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int i = 0; i < 6; ++i) mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1) ? kWarps : 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  uint32_t phase = 0;
+  uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
+  uint32_t ph_d = 0u, ph_r = 0u;
   unsigned nbar = 0;
   const uint64_t tmo = p.timeout_ns;
+  const bool stack = (p.mode == kModeStack);
+  // experts of this CTA: e = blockIdx.x + j * grid, j < my_rows
+  const int my_rows = ((int)blockIdx.x < E) ? (E - (int)blockIdx.x + grid - 1) / grid : 0;
+
+  // Router rows of this CTA's experts for layer l (and the slot table when
+  // its size and alignment allow a bulk copy), into shared memory on the R
+  // barrier.
+  auto slots_bulk_of = [&](int l) {
+    return (E % 4) == 0 && (reinterpret_cast<uintptr_t>(p.layers[l].slot_of) & 15u) == 0;
+  };
+  auto prefetch_router = [&](int l) {
+    const LayerDev& W = p.layers[l];
+    const bool slots_bulk = slots_bulk_of(l);
+    if (warp == kWarps - 1) {
+      const uint32_t bytes = (uint32_t)my_rows * H * 4u + (slots_bulk ? (uint32_t)E * 4u : 0u);
+      if (lane == 0 && bytes) mbar_expect_tx(&mbar[kBarR], bytes);
+      __syncwarp();
+      for (int j = lane; j < my_rows; j += 32)
+        bulk_g2s(wr + (size_t)j * H, W.router_w + (size_t)(blockIdx.x + j * grid) * H, H * 4u,
+                 &mbar[kBarR]);
+      if (slots_bulk && lane == 31) bulk_g2s(slots, W.slot_of, (uint32_t)E * 4u, &mbar[kBarR]);
+    }
+    if (!slots_bulk)
+      for (int e = tid; e < E; e += kDecodeThreads) slots[e] = __ldg(W.slot_of + e);
+  };
+  prefetch_router(0);
 
   for (int l = 0; l < p.n_layers; ++l) {
     const LayerDev& W = p.layers[l];
     const uint16_t* xsrc = (l == 0) ? p.x_in : (p.xbuf + (size_t)(l & 1) * kMaxDecodeTokens * H);
 
     // ------------------------------------------------ phase R: stage x, router
-    const bool stack = (p.mode == kModeStack);
     uint16_t* stage_dst = stack ? hres : xb;
     for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
       const int t = i / (H / 8);
@@ -239,68 +347,67 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
       reinterpret_cast<uint4*>(stage_dst)[i] = v;
     }
     __syncthreads();
-    if (stack) {
-      // pre-norm: u = bf16(h / sqrt(mean(h^2) + eps)), unit gain
-      float ss[TT];
+    {
+      // one pass: sum of squares (stacks) and max |x| of the staged rows
+      float ss[TT], mx[TT];
 #pragma unroll
-      for (int t = 0; t < TT; ++t) ss[t] = 0.0f;
+      for (int t = 0; t < TT; ++t) ss[t] = mx[t] = 0.0f;
       for (int i = tid; i < H; i += kDecodeThreads) {
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
-          const float v = __bfloat162float(__ushort_as_bfloat16(hres[t * H + i]));
+          const float v = __bfloat162float(__ushort_as_bfloat16(stage_dst[t * H + i]));
           ss[t] = fmaf(v, v, ss[t]);
+          mx[t] = fmaxf(mx[t], fabsf(v));
         }
       }
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
-        const float v = warp_sum(ss[t]);
-        if (lane == 0) M.tok_max[warp][t] = v;
+        const float a = warp_sum(ss[t]), b = warp_max(mx[t]);
+        if (lane == 0) {
+          M.red_ss[warp][t] = a;
+          M.red_mx[warp][t] = b;
+        }
       }
       __syncthreads();
-      if (tid < TT) {
-        float v = 0.0f;
-        for (int w = 0; w < kDecodeThreads / 32; ++w) v += M.tok_max[w][tid];
-        M.inv_rms[tid] = rsqrtf(v / (float)H + 1e-6f);
-      }
-      __syncthreads();
-      for (int i = tid; i < TT * H; i += kDecodeThreads) {
-        const int t = i / H;
-        const float v = __bfloat162float(__ushort_as_bfloat16(hres[i])) * M.inv_rms[t];
-        xb[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-      }
-      __syncthreads();
-      if (blockIdx.x == 0 && p.in_trace)
-        for (int i = tid; i < T * H; i += kDecodeThreads) p.in_trace[(size_t)l * T * H + i] = xb[i];
-    }
-    {
-      // per-token |x| max -> power-of-two shift for the fp16 activations
-      float m[TT];
-#pragma unroll
-      for (int t = 0; t < TT; ++t) m[t] = 0.0f;
-      for (int i = tid; i < H; i += kDecodeThreads) {
-#pragma unroll
-        for (int t = 0; t < TT; ++t)
-          m[t] = fmaxf(m[t], fabsf(__bfloat162float(__ushort_as_bfloat16(xb[t * H + i]))));
-      }
+      float inv[TT], sc[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
-        float v = warp_max(m[t]);
-        if (lane == 0) M.tok_max[warp][t] = v;
+        float a = 0.0f, b = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          a += M.red_ss[w][t];
+          b = fmaxf(b, M.red_mx[w][t]);
+        }
+        // pre-norm: u = bf16(h / sqrt(mean(h^2) + eps)), unit gain
+        inv[t] = stack ? rsqrtf(a / (float)H + 1e-6f) : 1.0f;
+        // max |u| <= max |h| * inv, up to one bf16 rounding
+        const int s = range_shift(b * inv[t] * 1.0079f);
+        sc[t] = pow2f(-s);
+        if (tid == 0) M.x_shift[t] = s;
       }
-      __syncthreads();
-      if (tid < TT) {
-        float v = 0.0f;
-        for (int w = 0; w < kDecodeThreads / 32; ++w) v = fmaxf(v, M.tok_max[w][tid]);
-        M.x_shift[tid] = range_shift(v);
+      if (stack) {
+        for (int i = tid; i < TT * H; i += kDecodeThreads) {
+          const int t = i / H;
+          float v = __bfloat162float(__ushort_as_bfloat16(hres[i]));
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt)
+            if (tt == t) v *= inv[tt];
+          xb[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+        __syncthreads();
+        if (blockIdx.x == 0 && p.in_trace)
+          for (int i = tid; i < T * H; i += kDecodeThreads) p.in_trace[(size_t)l * T * H + i] = xb[i];
       }
-      __syncthreads();
       // fp16 pair planes: xp[(t*4 + q)*C + c] = pairs (x[32c+8q+j], x[32c+8q+j+4]), j < 4
       for (int i = tid; i < TT * C * 4; i += kDecodeThreads) {
         const int t = i / (4 * C);
         const int rem = i - t * 4 * C;
         const int q = rem / C;
         const int c = rem - q * C;
-        const float sc_t = pow2f(-M.x_shift[t]);
+        float sc_t = 1.0f;
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt)
+          if (tt == t) sc_t = sc[tt];
         const uint16_t* src = xb + t * H + 32 * c + 8 * q;
         uint32_t out[4];
 #pragma unroll
@@ -313,229 +420,315 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
         xp[(t * 4 + q) * C + c] = make_uint4(out[0], out[1], out[2], out[3]);
       }
     }
-    // router: expert e handled by warp (e / gridDim.x) % 8 of CTA e % gridDim.x
-    for (int e = blockIdx.x + warp * gridDim.x; e < E; e += 8 * gridDim.x) {
-      const float4* wr = reinterpret_cast<const float4*>(W.router_w + (size_t)e * H);
+    // router: warp j computes the logits of this CTA's j-th expert from the
+    // prefetched W_r row
+    if (my_rows > 0 || slots_bulk_of(l)) {  // the R barrier was armed for this layer
+      mbar_wait(&mbar[kBarR], ph_r, p.err, tmo);
+      ph_r ^= 1u;
+    }
+    for (int j = warp; j < my_rows; j += kWarps) {
+      const int e = blockIdx.x + j * grid;
+      const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)j * H);
       float acc[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-      for (int base = 0; base < H / 4; base += 32 * 8) {
-        float4 wv[8];
+      for (int idx = lane; idx < H / 4; idx += 32) {
+        const float4 wv = wrow[idx];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int idx = base + j * 32 + lane;
-          wv[j] = (idx < H / 4) ? __ldg(wr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int idx = base + j * 32 + lane;
-          if (idx < H / 4) {
-#pragma unroll
-            for (int t = 0; t < TT; ++t) {
-              const uint2 xv = *reinterpret_cast<const uint2*>(xb + t * H + 4 * idx);
-              const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
-              const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
-              acc[t] = fmaf(wv[j].x, x0, acc[t]);
-              acc[t] = fmaf(wv[j].y, x1, acc[t]);
-              acc[t] = fmaf(wv[j].z, x2, acc[t]);
-              acc[t] = fmaf(wv[j].w, x3, acc[t]);
-            }
-          }
+        for (int t = 0; t < TT; ++t) {
+          const uint2 xv = *reinterpret_cast<const uint2*>(xb + t * H + 4 * idx);
+          acc[t] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[t]);
+          acc[t] = fmaf(wv.y, __uint_as_float(xv.x & 0xffff0000u), acc[t]);
+          acc[t] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[t]);
+          acc[t] = fmaf(wv.w, __uint_as_float(xv.y & 0xffff0000u), acc[t]);
         }
       }
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         const float s = warp_sum(acc[t]);
-        if (lane == 0 && t < T) p.z[(size_t)t * E + e] = s + W.router_b[e];
+        if (lane == 0 && t < T) p.z[(size_t)t * E + e] = s + __ldg(W.router_b + e);
       }
     }
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
 
     // ------------------------------------------------ top-k + softmax + units
-    if (warp < T) {
-      const int t = warp;
-      int id;
-      float wt;
-      // z was written by other CTAs before the barrier: read it through L2
-      if (!warp_topk_softmax_ldcg(p.z + (size_t)t * E, E, k, &id, &wt) && lane == 0)
-        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+    {
+      // level 1: the warps of token t each select the top-k of one slice
+      constexpr int G = kWarps / TT;  // warps per token
+      constexpr int NJ1 = 4 * TT;     // logits per lane, E <= 1024
+      const int t = warp / G, g = warp - (warp / G) * G;
+      const int seg = (E + G - 1) / G;
+      const int e0 = g * seg;
+      uint32_t key[NJ1];
+      int id[NJ1];
+#pragma unroll
+      for (int j = 0; j < NJ1; ++j) {
+        const int e = e0 + lane + 32 * j;
+        const bool in = t < T && lane + 32 * j < seg && e < E;
+        key[j] = in ? order_key(__ldcg(p.z + (size_t)t * E + e)) : 0u;
+        id[j] = e;
+      }
+      uint32_t ok1;
+      int oi1;
+      warp_select<NJ1>(key, id, k, &ok1, &oi1);
       if (lane < k) {
-        M.sel_id[t][lane] = id;
-        M.sel_w[t][lane] = wt;
+        M.cand_key[warp][lane] = ok1;
+        M.cand_id[warp][lane] = oi1;
+      }
+    }
+    __syncthreads();
+    if (warp < T) {
+      // level 2: warp t merges the G slices of token t
+      constexpr int G = kWarps / TT;
+      constexpr int NJ2 = (G * kMaxTopK + 31) / 32;
+      uint32_t key[NJ2];
+      int id[NJ2];
+#pragma unroll
+      for (int j = 0; j < NJ2; ++j) {
+        const int c = lane + 32 * j;  // candidate c = (slice c / k, rank c % k)
+        const bool in = c < G * k;
+        const int wsrc = warp * G + (in ? c / k : 0), r = in ? c - (c / k) * k : 0;
+        key[j] = in ? M.cand_key[wsrc][r] : 0u;
+        id[j] = in ? M.cand_id[wsrc][r] : 0x7fffffff;
+      }
+      uint32_t ok2;
+      int oi2;
+      warp_select<NJ2>(key, id, k, &ok2, &oi2);
+      const bool bad = (lane < k) && (ok2 == 0u || oi2 < 0 || oi2 >= E);
+      if (__any_sync(0xffffffffu, bad)) {  // only reachable with non-finite logits
+        if (lane == 0) atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+        if (lane < k) {
+          oi2 = lane;
+          ok2 = 0x80000000u;
+        }
+      }
+      const float zv = key_value(ok2);
+      const float z0 = __shfl_sync(0xffffffffu, zv, 0);
+      const float ex = (lane < k) ? __expf(zv - z0) : 0.0f;
+      const float den = warp_sum(ex);
+      if (lane < k) {
+        M.sel_id[warp][lane] = oi2;
+        M.sel_w[warp][lane] = ex / den;
       }
     }
     if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
     for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)
       (&M.unit_w[0][0])[i] = 0.0f;
     __syncthreads();
-    if (tid < T * k) atomicOr(&M.bitmap[M.sel_id[tid / k][tid % k] >> 5], 1u << (M.sel_id[tid / k][tid % k] & 31));
-    __syncthreads();
-    if (tid == 0) {
-      int s = 0;
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        M.prefix[i] = s;
-        s += __popc(M.bitmap[i]);
+    if (TT == 1) {
+      // one token: the units are the selection itself, in selection order
+      if (tid < k) {
+        const int e = M.sel_id[0][tid];
+        M.unit_w[tid][0] = M.sel_w[0][tid];
+        M.unit_expert[tid] = e;
+        int s = slots[e];
+        if (s < 0 || s >= E) {
+          atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+          s = 0;
+        }
+        M.unit_slot[tid] = s;
       }
-      M.prefix[kMaxExperts / 32] = s;
-      M.n_routed = s;
-      M.n_units = s + (Fs > 0 ? 1 : 0);
-    }
-    __syncthreads();
-    if (tid < T * k) {
-      const int t = tid / k, r = tid % k;
-      const int e = M.sel_id[t][r];
-      const int u = M.prefix[e >> 5] + __popc(M.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-      M.unit_w[u][t] = M.sel_w[t][r];
-      M.unit_expert[u] = e;
-    }
-    __syncthreads();
-    const int n_routed = M.n_routed;
-    if (tid < n_routed) {
-      int s = W.slot_of[M.unit_expert[tid]];
-      if (s < 0 || s >= E) {
-        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-        s = 0;
+      if (tid == 0) {
+        M.n_routed = k;
+        M.n_units = k + (Fs > 0 ? 1 : 0);
       }
-      M.unit_slot[tid] = s;
+    } else {
+      if (tid < T * k) atomicOr(&M.bitmap[M.sel_id[tid / k][tid % k] >> 5], 1u << (M.sel_id[tid / k][tid % k] & 31));
+      __syncthreads();
+      if (warp == 0) {  // exclusive prefix of the bitmap's popcounts
+        const int c = __popc(M.bitmap[lane]);
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        M.prefix[lane] = x - c;
+        if (lane == 31) {
+          M.prefix[32] = x;
+          M.n_routed = x;
+          M.n_units = x + (Fs > 0 ? 1 : 0);
+        }
+      }
+      __syncthreads();
+      if (tid < T * k) {
+        const int t = tid / k, r = tid % k;
+        const int e = M.sel_id[t][r];
+        const int u = M.prefix[e >> 5] + __popc(M.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+        M.unit_w[u][t] = M.sel_w[t][r];
+        M.unit_expert[u] = e;
+        int s = slots[e];
+        if (s < 0 || s >= E) {
+          atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+          s = 0;
+        }
+        M.unit_slot[u] = s;
+      }
     }
-    if (Fs > 0 && tid < kMaxDecodeTokens) M.unit_w[n_routed][tid] = (tid < T) ? 1.0f : 0.0f;
     if (blockIdx.x == 0 && tid < T * k) {
       const int t = tid / k, r = tid % k;
       if (p.ids_out) p.ids_out[((size_t)l * T + t) * k + r] = M.sel_id[t][r];
       if (p.w_out) p.w_out[((size_t)l * T + t) * k + r] = M.sel_w[t][r];
     }
+    {
+      // the shared expert is the unit after the routed ones, weight 1
+      const int nr = (TT == 1) ? k : M.n_routed;
+      if (Fs > 0 && tid < kMaxDecodeTokens) M.unit_w[nr][tid] = (tid < T) ? 1.0f : 0.0f;
+    }
     __syncthreads();
     if (p.mode == kModeRoute) continue;
+    const int n_routed = M.n_routed;
+    const int n_units = M.n_units;
+
+    // ------------------------------------------------ bulk copies of this layer's weights
+    const int ipu = F / 16;  // gate/up items per routed unit
+    const int n_gitems = n_routed * ipu + Fs / 16;
+    auto issue_g = [&](int q) {  // gate/up item q of this CTA into stage q % NG
+      const int it = blockIdx.x + q * grid;
+      if (it >= n_gitems) return;
+      const uint8_t* gq;
+      const uint16_t* gs;
+      const uint8_t* uq;
+      const uint16_t* us;
+      if (it < n_routed * ipu) {
+        const int u = it / ipu;
+        const int f0 = (it - u * ipu) * 16;
+        const size_t slot = (size_t)M.unit_slot[u];
+        gq = W.gate_q + (slot * F + f0) * (H / 2);
+        uq = W.up_q + (slot * F + f0) * (H / 2);
+        gs = W.gate_s + (slot * F + f0) * C;
+        us = W.up_s + (slot * F + f0) * C;
+      } else {
+        const int f0 = (it - n_routed * ipu) * 16;
+        gq = W.sh_gate_q + (size_t)f0 * (H / 2);
+        uq = W.sh_up_q + (size_t)f0 * (H / 2);
+        gs = W.sh_gate_s + (size_t)f0 * C;
+        us = W.sh_up_s + (size_t)f0 * C;
+      }
+      unsigned char* st = gbuf + (size_t)(q % NG) * L.g_stage;
+      uint64_t* bar = &mbar[kBarG0 + (q % NG)];
+      mbar_expect_tx(bar, (uint32_t)L.g_stage);
+      bulk_g2s(st, gq, 16u * (H / 2), bar);
+      bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
+      bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
+      bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
+    };
+    // down items of this CTA: output rows i0 = (blockIdx.x + q * grid) * 8
+    const int n_ditems = ((int)blockIdx.x < H / 8) ? (H / 8 - (int)blockIdx.x + grid - 1) / grid : 0;
+    if (warp == 0 && lane == 0)
+      for (int q = 0; q < NG; ++q) issue_g(q);
+    if (warp == kWarps - 1 && L.dprefetch && n_ditems > 0) {
+      // per item: for each unit, codes (8 x F_u/2 bytes) then scales (8 x F_u/16 bytes)
+      if (lane == 0)
+        mbar_expect_tx(&mbar[kBarD], (uint32_t)((size_t)9 * ((size_t)n_routed * F + Fs) / 2 * n_ditems));
+      __syncwarp();
+      for (int job = lane; job < n_ditems * n_units; job += 32) {
+        const int q = job / n_units, u = job - (job / n_units) * n_units;
+        const int i0 = (blockIdx.x + q * grid) * 8;
+        unsigned char* base = dbuf + (size_t)q * L.d_item + (size_t)u * (9 * (size_t)F / 2);
+        if (u < n_routed) {
+          const size_t slot = (size_t)M.unit_slot[u];
+          bulk_g2s(base, W.down_q + (slot * H + i0) * (F / 2), 8u * (F / 2), &mbar[kBarD]);
+          bulk_g2s(base + 8 * (F / 2), W.down_s + (slot * H + i0) * CF, 8u * CF * 2u, &mbar[kBarD]);
+        } else {
+          bulk_g2s(base, W.sh_down_q + (size_t)i0 * (Fs / 2), 8u * (Fs / 2), &mbar[kBarD]);
+          bulk_g2s(base + 8 * (Fs / 2), W.sh_down_s + (size_t)i0 * CS, 8u * CS * 2u, &mbar[kBarD]);
+        }
+      }
+    }
 
     // ------------------------------------------------ phase G: gate/up + SwiGLU
     {
-      const int ipu = F / 16;  // items per routed unit
-      const int n_items = n_routed * ipu + Fs / 16;
-      const int rg = tid >> 6, cl = tid & 63;
-      const int mat = rg >> 1, rb = rg & 1;
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const uint8_t* gq;
-        const uint16_t* gs;
-        const uint8_t* uq;
-        const uint16_t* us;
-        int f0, Fu;
+      // warp w owns row pairs 2w, 2w+1 of every item (gate and up rows)
+      float* amax_l = amax_g + (l & 1) * 4;
+      for (int q = 0; (int)blockIdx.x + q * grid < n_gitems; ++q) {
+        const int it = blockIdx.x + q * grid;
+        int Fu, u, f0;
         size_t hoff;
         if (it < n_routed * ipu) {
-          const int u = it / ipu;
+          u = it / ipu;
           f0 = (it - u * ipu) * 16;
-          const size_t slot = (size_t)M.unit_slot[u];
-          gq = W.gate_q + slot * F * (H / 2);
-          uq = W.up_q + slot * F * (H / 2);
-          gs = W.gate_s + slot * F * C;
-          us = W.up_s + slot * F * C;
           Fu = F;
           hoff = (size_t)u * kMaxDecodeTokens * F;
         } else {
+          u = n_routed;
           f0 = (it - n_routed * ipu) * 16;
-          gq = W.sh_gate_q;
-          uq = W.sh_up_q;
-          gs = W.sh_gate_s;
-          us = W.sh_up_s;
           Fu = Fs;
           hoff = (size_t)(p.max_units - 1) * kMaxDecodeTokens * F;
         }
-        if (tid == 0) {
-          mbar_expect_tx(mbar, 2u * 16u * C * 2u);
-          bulk_g2s(sc, gs + (size_t)f0 * C, 16u * C * 2u, mbar);
-          bulk_g2s(sc + 16 * C, us + (size_t)f0 * C, 16u * C * 2u, mbar);
-        }
-        const uint8_t* qrow = (mat ? uq : gq) + (size_t)(f0 + rb * 8) * (H / 2);
-        float acc[8][TT];
+        const int sg = q % NG;
+        const uint32_t par = gcount[sg] & 1u;
+        ++gcount[sg];
+        const unsigned char* st = gbuf + (size_t)sg * L.g_stage;
+        mbar_wait(&mbar[kBarG0 + sg], par, p.err, tmo);
+        float acc[4][TT];  // rows: gate 2w, gate 2w+1, up 2w, up 2w+1
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
           for (int t = 0; t < TT; ++t) acc[r][t] = 0.0f;
-        bool waited = false;
-        for (int c = cl; c < C; c += 64) {
-          uint4 wv[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) wv[r] = ld_stream(qrow + (size_t)r * (H / 2) + c * 16);
-          if (!waited) {
-            mbar_wait_bounded(mbar, phase, p.err, tmo);
-            waited = true;
-          }
+        for (int c = lane; c < C; c += 32) {
           uint4 act[TT][4];
 #pragma unroll
           for (int t = 0; t < TT; ++t)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) act[t][q] = xp[(t * 4 + q) * C + c];
+            for (int qq = 0; qq < 4; ++qq) act[t][qq] = xp[(t * 4 + qq) * C + c];
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
+          for (int r = 0; r < 4; ++r) {
+            const int mat = r >> 1, row = 2 * warp + (r & 1);
+            const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)mat * 16 * (H / 2) +
+                                                             (size_t)row * (H / 2) + c * 16);
+            const float s =
+                __half2float(reinterpret_cast<const __half*>(st + 16 * H + mat * 32 * C)[row * C + c]);
             float d[TT];
-            dot_block<TT>(wv[r], act, d);
-            const float s = __half2float(sc[(mat * 16 + rb * 8 + r) * C + c]);
+            dot_block<TT>(wv, act, d);
 #pragma unroll
             for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(s, d[t], acc[r][t]);
           }
         }
-        // reduce the 8*TT sums of this 64-thread row group
-        {
-          float v[8 * TT];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mbar[kBarE0 + sg]);  // this warp is done with the stage
+        float v[4 * TT];
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
-          const float s = warp_reduce_scatter<8 * TT>(v, lane);
-          constexpr int REP = 32 / (8 * TT);
-          constexpr int SH = (REP == 8) ? 3 : (REP == 4) ? 2 : (REP == 2) ? 1 : 0;
-          if ((lane & (REP - 1)) == 0) red[warp * 32 + (lane >> SH)] = s;
-        }
-        __syncthreads();
-        if (tid < 16 * TT) {
-          const int f = tid / TT, t = tid - (tid / TT) * TT;
-          const int rbf = f >> 3, r = f & 7;
-          const int ig = r * TT + t;
-          const int wg = 2 * (0 * 2 + rbf), wu = 2 * (1 * 2 + rbf);
+          for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
+        // value idx = r*TT + t ends in lanes [idx*REP, (idx+1)*REP); the up row
+        // of the same (row pair, token) is 2*TT indices on: 16 lanes further
+        const float s = warp_reduce_scatter<4 * TT>(v, lane);
+        const float up = __shfl_down_sync(0xffffffffu, s, 16);
+        constexpr int REP = 32 / (4 * TT);
+        if (lane < 16 && (lane & (REP - 1)) == 0) {
+          const int idx = lane / REP;
+          const int rp = idx / TT, t = idx - (idx / TT) * TT;
           const float xs = pow2f(M.x_shift[t]);
-          const float g = (red[wg * 32 + ig] + red[(wg + 1) * 32 + ig]) * xs;
-          const float uu = (red[wu * 32 + ig] + red[(wu + 1) * 32 + ig]) * xs;
+          const float g = s * xs, uu = up * xs;
           const float h = g / (1.0f + __expf(-g)) * uu;
-          p.hbuf[hoff + (size_t)t * Fu + f0 + f] = h;
+          p.hbuf[hoff + (size_t)t * Fu + f0 + 2 * warp + rp] = h;
+          // per-token max |w h| over the layer, for the down phase's fp16 range
+          const float a = fabsf(h * M.unit_w[u][t]);
+          if (a > 0.0f && isfinite(a)) atomicMax(reinterpret_cast<int*>(amax_l + t), __float_as_int(a));
         }
-        if (!waited && tid == 0) mbar_wait_bounded(mbar, phase, p.err, tmo);
-        phase ^= 1u;
-        __syncthreads();
+        // refill this stage with item q + NG once every warp has read it
+        if (warp == 0 && lane == 0 && (int)blockIdx.x + (q + NG) * grid < n_gitems) {
+          mbar_wait(&mbar[kBarE0 + sg], par, p.err, tmo);
+          issue_g(q + NG);
+        }
       }
     }
+    if (l + 1 < p.n_layers) prefetch_router(l + 1);
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
 
     // ------------------------------------------------ phase D: down + combine
     {
-      const int n_units = M.n_units;
       const size_t sh_hoff = (size_t)(p.max_units - 1) * kMaxDecodeTokens * F;
-      // per-token max of |w * h| -> shift
-      float m[TT];
+      if (blockIdx.x == 0 && tid < 4) amax_g[((l + 1) & 1) * 4 + tid] = 0.0f;  // next layer's
+      int dsh[TT];
 #pragma unroll
-      for (int t = 0; t < TT; ++t) m[t] = 0.0f;
-      for (int u = 0; u < n_units; ++u) {
-        const int Fu = (u < n_routed) ? F : Fs;
-        const size_t ho = (u < n_routed) ? (size_t)u * kMaxDecodeTokens * F : sh_hoff;
-        for (int f = tid; f < Fu; f += kDecodeThreads) {
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-            m[t] = fmaxf(m[t], fabsf(M.unit_w[u][t] * __ldcg(p.hbuf + ho + (size_t)t * Fu + f)));
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        float v = warp_max(m[t]);
-        if (lane == 0) M.tok_max[warp][t] = v;
-      }
-      __syncthreads();
-      if (tid < TT) {
-        float v = 0.0f;
-        for (int w = 0; w < kDecodeThreads / 32; ++w) v = fmaxf(v, M.tok_max[w][tid]);
-        M.d_shift[tid] = range_shift(v);
-      }
-      __syncthreads();
+      for (int t = 0; t < TT; ++t) dsh[t] = range_shift(__ldcg(amax_g + (l & 1) * 4 + t));
       // stage w*h as fp16 pair planes: unit u base = u*TT*4*CF (shared: n_routed*TT*4*CF)
       {
         const int n_chunks = n_routed * CF + CS;
+#pragma unroll 2
         for (int i = tid; i < n_chunks * TT; i += kDecodeThreads) {
           const int t = i / n_chunks;
           const int pc = i - t * n_chunks;
@@ -552,7 +745,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
             Cu = CS;
             ho = sh_hoff;
           }
-          const float wt = M.unit_w[u][t] * pow2f(-M.d_shift[t]);
+          int sh = 0;
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt)
+            if (tt == t) sh = dsh[tt];
+          const float wt = M.unit_w[u][t] * pow2f(-sh);
           const float4* src = reinterpret_cast<const float4*>(p.hbuf + ho + (size_t)t * (Cu * 32) + c * 32);
           float vv[32];
 #pragma unroll
@@ -565,94 +762,90 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
           }
           uint4* dst = hp + (size_t)u * TT * 4 * CF + (size_t)t * 4 * Cu + c;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int qq = 0; qq < 4; ++qq) {
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              __half2 hh = __floats2half2_rn(vv[8 * q + j], vv[8 * q + j + 4]);
+              __half2 hh = __floats2half2_rn(vv[8 * qq + j], vv[8 * qq + j + 4]);
               o[j] = *reinterpret_cast<uint32_t*>(&hh);
             }
-            dst[q * Cu] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[qq * Cu] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }
       __syncthreads();
       const int P = n_routed * CF + CS;
-      const uint32_t sc_bytes = (uint32_t)(n_routed * 8 * CF * 2 + 8 * CS * 2);
-      for (int it = blockIdx.x; it < H / 8; it += gridDim.x) {
-        const int i0 = it * 8;
-        if (tid == 0) {
-          mbar_expect_tx(mbar, sc_bytes);
-          for (int u = 0; u < n_routed; ++u)
-            bulk_g2s(sc + u * 8 * CF, W.down_s + ((size_t)M.unit_slot[u] * H + i0) * CF, 8u * CF * 2u,
-                     mbar);
-          if (CS) bulk_g2s(sc + n_routed * 8 * CF, W.sh_down_s + (size_t)i0 * CS, 8u * CS * 2u, mbar);
-        }
-        float acc[8][TT];
+      if (L.dprefetch && n_ditems > 0) {
+        mbar_wait(&mbar[kBarD], ph_d, p.err, tmo);
+        ph_d ^= 1u;
+      }
+      // warp w owns row w of up to kMaxRowsPerWarp items at a time: rows
+      // i = (blockIdx.x + q * grid) * 8 + w
+      for (int q0 = 0; q0 < n_ditems; q0 += kMaxRowsPerWarp) {
+        const int nq = min(kMaxRowsPerWarp, n_ditems - q0);
+        float acc[kMaxRowsPerWarp][TT];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int q = 0; q < kMaxRowsPerWarp; ++q)
 #pragma unroll
-          for (int t = 0; t < TT; ++t) acc[r][t] = 0.0f;
-        bool waited = false;
-        for (int pp = tid; pp < P; pp += kDecodeThreads) {
+          for (int t = 0; t < TT; ++t) acc[q][t] = 0.0f;
+        for (int pp = lane; pp < P; pp += 32) {
           int u, c, Cu;
-          const uint8_t* base;
           if (pp < n_routed * CF) {
             u = pp / CF;
             c = pp - u * CF;
             Cu = CF;
-            base = W.down_q + (size_t)M.unit_slot[u] * H * (F / 2);
           } else {
             u = n_routed;
             c = pp - n_routed * CF;
             Cu = CS;
-            base = W.sh_down_q;
-          }
-          uint4 wv[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) wv[r] = ld_stream(base + (size_t)(i0 + r) * (Cu * 16) + c * 16);
-          if (!waited) {
-            mbar_wait_bounded(mbar, phase, p.err, tmo);
-            waited = true;
           }
           uint4 act[TT][4];
           const uint4* ap = hp + (size_t)u * TT * 4 * CF + c;
 #pragma unroll
           for (int t = 0; t < TT; ++t)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) act[t][q] = ap[(t * 4 + q) * Cu];
-          const __half* scu = sc + u * 8 * CF;
+            for (int qq = 0; qq < 4; ++qq) act[t][qq] = ap[(t * 4 + qq) * Cu];
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            float d[TT];
-            dot_block<TT>(wv[r], act, d);
-            const float s = __half2float(scu[r * Cu + c]);
+          for (int q = 0; q < kMaxRowsPerWarp; ++q) {
+            if (q < nq) {
+              uint4 wv;
+              float s;
+              if (L.dprefetch) {
+                const unsigned char* ub = dbuf + (size_t)(q0 + q) * L.d_item + (size_t)u * (9 * (size_t)F / 2);
+                wv = *reinterpret_cast<const uint4*>(ub + (size_t)warp * (Cu * 16) + c * 16);
+                s = __half2float(reinterpret_cast<const __half*>(ub + 8 * (Cu * 16))[warp * Cu + c]);
+              } else {
+                const int i = ((int)blockIdx.x + (q0 + q) * grid) * 8 + warp;
+                const size_t slot = (u < n_routed) ? (size_t)M.unit_slot[u] : 0;
+                const uint8_t* base = (u < n_routed) ? W.down_q + slot * H * (F / 2) : W.sh_down_q;
+                const uint16_t* sbase = (u < n_routed) ? W.down_s + slot * H * CF : W.sh_down_s;
+                wv = ld_stream(base + (size_t)i * (Cu * 16) + c * 16);
+                s = __half2float(__ushort_as_half(__ldg(sbase + (size_t)i * Cu + c)));
+              }
+              float d[TT];
+              dot_block<TT>(wv, act, d);
 #pragma unroll
-            for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(s, d[t], acc[r][t]);
+              for (int t = 0; t < TT; ++t) acc[q][t] = fmaf(s, d[t], acc[q][t]);
+            }
           }
         }
-        {
-          float v[8 * TT];
+        float v[kMaxRowsPerWarp * TT];
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+        for (int q = 0; q < kMaxRowsPerWarp; ++q)
 #pragma unroll
-            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
-          const float s = warp_reduce_scatter<8 * TT>(v, lane);
-          constexpr int REP = 32 / (8 * TT);
-          constexpr int SH = (REP == 8) ? 3 : (REP == 4) ? 2 : (REP == 2) ? 1 : 0;
-          if ((lane & (REP - 1)) == 0) red[warp * 32 + (lane >> SH)] = s;
-        }
-        if (!waited) mbar_wait_bounded(mbar, phase, p.err, tmo);
-        phase ^= 1u;
-        __syncthreads();
-        if (tid < 8 * TT) {
-          const int r = tid / TT, t = tid - (tid / TT) * TT;
-          float y = 0.0f;
+          for (int t = 0; t < TT; ++t) v[q * TT + t] = acc[q][t];
+        const float y0 = warp_reduce_scatter<kMaxRowsPerWarp * TT>(v, lane);
+        constexpr int REP = 32 / (kMaxRowsPerWarp * TT);
+        if ((lane & (REP - 1)) == 0) {
+          const int idx = lane / REP;
+          const int q = idx / TT, t = idx - (idx / TT) * TT;
+          if (q < nq && t < T) {
+            int sh = 0;
 #pragma unroll
-          for (int w = 0; w < kDecodeThreads / 32; ++w) y += red[w * 32 + tid];
-          y *= pow2f(M.d_shift[t]);
-          const int i = i0 + r;
-          if (t < T) {
+            for (int tt = 0; tt < TT; ++tt)
+              if (tt == t) sh = dsh[tt];
+            const float y = y0 * pow2f(sh);
+            const int i = ((int)blockIdx.x + (q0 + q) * grid) * 8 + warp;
             const __nv_bfloat16 yb = __float2bfloat16_rn(y);
             if (p.mode == kModeForward) {
               p.y_out[(size_t)t * H + i] = __bfloat16_as_ushort(yb);
@@ -667,27 +860,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) moe_decode_kernel(const __g
             }
           }
         }
-        __syncthreads();
       }
     }
+    // the next layer's bulk copies land in shared memory this phase wrote
+    // through the generic proxy: order those writes before them
+    fence_proxy_async_smem();
     if (l + 1 < p.n_layers) grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
   }
 }
 
 size_t decode_smem_bytes(const DecodeParams& p) {
   const int TT = p.T == 1 ? 1 : (p.T == 2 ? 2 : 4);
-  return DecodeSmem::make(p.H, p.F, p.Fs, TT, p.max_units).total;
+  return DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, 152, 1, false).total;
 }
 
 template <int TT>
-static moe_status launch_tt(const DecodeParams& p, cudaStream_t stream, int num_sms,
+static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int num_sms,
                             const char** why) {
   auto kern = moe_decode_kernel<TT>;
-  const size_t smem = DecodeSmem::make(p.H, p.F, p.Fs, TT, p.max_units).total;
-  if (smem > 227 * 1024) {
+  DecodeParams p = p_in;
+  const int grid = num_sms;  // one CTA per SM
+  // most staging that fits: 2 gate/up stages and the down weights in shared
+  // memory, else without the down weights, else one gate/up stage
+  const size_t cap = (size_t)227 * 1024;
+  p.g_stages = 2;
+  p.want_dprefetch = 1;
+  DecodeSmem sm = DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, grid, 2, true);
+  if (sm.total > cap) {
+    p.g_stages = 1;
+    sm = DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, grid, 1, true);
+  }
+  if (sm.total > cap) {
     *why = "decode shared-memory footprint exceeds 227 KB for this shape";
     return MOE_ERR_INVALID;
   }
+  const size_t smem = sm.total;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic smem) failed";
@@ -700,12 +907,11 @@ static moe_status launch_tt(const DecodeParams& p, cudaStream_t stream, int num_
     *why = "decode kernel cannot be resident (occupancy query)";
     return MOE_ERR_CUDA;
   }
-  int grid = num_sms * (per_sm > 2 ? 2 : per_sm);
-  if (cudaMemsetAsync(&p.bar->count, 0, sizeof(unsigned), stream) != cudaSuccess) {
+  if (cudaMemsetAsync(p.bar, 0, sizeof(GridBarrier), stream) != cudaSuccess) {
     *why = "cudaMemsetAsync(barrier) failed";
     return MOE_ERR_CUDA;
   }
-  void* args[] = {const_cast<DecodeParams*>(&p)};
+  void* args[] = {&p};
   prof::Scope scope("moe_decode_kernel", stream);
   cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kDecodeThreads),
                                               args, smem, stream);

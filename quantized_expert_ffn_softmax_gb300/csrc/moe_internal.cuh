@@ -67,6 +67,8 @@ struct DecodeParams {
   // Test hook: every grid barrier waits for this many arrivals more than the
   // grid has, so the bounded wait runs out and records MOE_ERR_TIMEOUT.
   int debug_extra_arrivals;
+  int want_dprefetch;  // set by the launcher: stage the down weights in shared memory
+  int g_stages;        // set by the launcher: gate/up shared-memory stages (1 or 2)
   LayerDev layers[kMaxLayersPerLaunch];
 };
 
