@@ -55,6 +55,7 @@ constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kGemmThreads = 14 * 32;
 constexpr int kBucketThreads = 1024;
+constexpr int kPrefetch = 4;       // K steps of weight codes each producer keeps in flight
 
 enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 
@@ -244,40 +245,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           q = (part ? Wd.up_q : Wd.gate_q) + (slot * p.F + f) * (H / 2);
           sc = (part ? Wd.up_s : Wd.gate_s) + (slot * p.F + f) * (H / 32);
         }
-        uint4 c0 = ld_stream(q), c1 = ld_stream(q + 16);
-        uint32_t s2 = __ldg(reinterpret_cast<const uint32_t*>(sc));
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          uint4 n0 = c0, n1 = c1;
-          uint32_t ns = s2;
-          if (ks + 1 < nks) {
-            n0 = ld_stream(q + (ks + 1) * 32);
-            n1 = ld_stream(q + (ks + 1) * 32 + 16);
-            ns = __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * (ks + 1)));
+        // a ring of kPrefetch K steps of codes and scales in registers keeps
+        // that many global loads in flight per thread
+        uint4 ca[kPrefetch], cb[kPrefetch];
+        uint32_t cs[kPrefetch];
+#pragma unroll
+        for (int i = 0; i < kPrefetch; ++i) {
+          if (i < nks) {
+            ca[i] = ld_stream(q + i * 32);
+            cb[i] = ld_stream(q + i * 32 + 16);
+            cs[i] = __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * i));
           }
-          const int s = it % kStages;
-          bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            alive = false;
-            break;
+        }
+        for (int ks0 = 0; ks0 < nks && alive; ks0 += kPrefetch) {
+#pragma unroll
+          for (int i = 0; i < kPrefetch; ++i) {
+            const int ks = ks0 + i;
+            if (ks < nks && alive) {
+              const int s = it % kStages;
+              bool ok = true;
+              if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) {
+                alive = false;
+              } else {
+                unsigned char* tile = smem + s * STAGE + part * kTileA;
+                const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(cs[i] & 0xffffu)));
+                const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(cs[i] >> 16)));
+                st_tile_chunk(tile, r, 0, dequant_word(ca[i].x, slo));
+                st_tile_chunk(tile, r, 1, dequant_word(ca[i].y, slo));
+                st_tile_chunk(tile, r, 2, dequant_word(ca[i].z, slo));
+                st_tile_chunk(tile, r, 3, dequant_word(ca[i].w, slo));
+                st_tile_chunk(tile, r, 4, dequant_word(cb[i].x, shi));
+                st_tile_chunk(tile, r, 5, dequant_word(cb[i].y, shi));
+                st_tile_chunk(tile, r, 6, dequant_word(cb[i].z, shi));
+                st_tile_chunk(tile, r, 7, dequant_word(cb[i].w, shi));
+                fence_proxy_async_smem();
+                mbar_arrive(&full_a[s]);
+                ++it;
+                if (ks + kPrefetch < nks) {
+                  ca[i] = ld_stream(q + (ks + kPrefetch) * 32);
+                  cb[i] = ld_stream(q + (ks + kPrefetch) * 32 + 16);
+                  cs[i] = __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * (ks + kPrefetch)));
+                }
+              }
+            }
           }
-          unsigned char* tile = smem + s * STAGE + part * kTileA;
-          const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(s2 & 0xffffu)));
-          const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(s2 >> 16)));
-          st_tile_chunk(tile, r, 0, dequant_word(c0.x, slo));
-          st_tile_chunk(tile, r, 1, dequant_word(c0.y, slo));
-          st_tile_chunk(tile, r, 2, dequant_word(c0.z, slo));
-          st_tile_chunk(tile, r, 3, dequant_word(c0.w, slo));
-          st_tile_chunk(tile, r, 4, dequant_word(c1.x, shi));
-          st_tile_chunk(tile, r, 5, dequant_word(c1.y, shi));
-          st_tile_chunk(tile, r, 6, dequant_word(c1.z, shi));
-          st_tile_chunk(tile, r, 7, dequant_word(c1.w, shi));
-          fence_proxy_async_smem();
-          mbar_arrive(&full_a[s]);
-          c0 = n0;
-          c1 = n1;
-          s2 = ns;
         }
       } else if (MODE == kScatter) {
         const int i = U.mt * 128 + r;  // output row of H
@@ -292,33 +305,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           q = Wd.down_q + (slot * p.H + i) * (K / 2);
           sc = Wd.down_s + (slot * p.H + i) * (K / 32);
         }
-        uint4 c = ld_stream(q + part * 16);
-        uint16_t sv = __ldg(sc + part);
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          uint4 nc = c;
-          uint16_t nsv = sv;
-          if (ks + 1 < nks) {
-            nc = ld_stream(q + (ks + 1) * 32 + part * 16);
-            nsv = __ldg(sc + 2 * (ks + 1) + part);
+        uint4 cc[kPrefetch];
+        uint16_t cv[kPrefetch];
+#pragma unroll
+        for (int j = 0; j < kPrefetch; ++j) {
+          if (j < nks) {
+            cc[j] = ld_stream(q + j * 32 + part * 16);
+            cv[j] = __ldg(sc + 2 * j + part);
           }
-          const int s = it % kStages;
-          bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            alive = false;
-            break;
+        }
+        for (int ks0 = 0; ks0 < nks && alive; ks0 += kPrefetch) {
+#pragma unroll
+          for (int j = 0; j < kPrefetch; ++j) {
+            const int ks = ks0 + j;
+            if (ks < nks && alive) {
+              const int s = it % kStages;
+              bool ok = true;
+              if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) {
+                alive = false;
+              } else {
+                unsigned char* tile = smem + s * STAGE;
+                const __half2 s2 = __half2half2(__ushort_as_half(cv[j]));
+                st_tile_chunk(tile, r, part * 4 + 0, dequant_word(cc[j].x, s2));
+                st_tile_chunk(tile, r, part * 4 + 1, dequant_word(cc[j].y, s2));
+                st_tile_chunk(tile, r, part * 4 + 2, dequant_word(cc[j].z, s2));
+                st_tile_chunk(tile, r, part * 4 + 3, dequant_word(cc[j].w, s2));
+                fence_proxy_async_smem();
+                mbar_arrive(&full_a[s]);
+                ++it;
+                if (ks + kPrefetch < nks) {
+                  cc[j] = ld_stream(q + (ks + kPrefetch) * 32 + part * 16);
+                  cv[j] = __ldg(sc + 2 * (ks + kPrefetch) + part);
+                }
+              }
+            }
           }
-          unsigned char* tile = smem + s * STAGE;
-          const __half2 s2 = __half2half2(__ushort_as_half(sv));
-          st_tile_chunk(tile, r, part * 4 + 0, dequant_word(c.x, s2));
-          st_tile_chunk(tile, r, part * 4 + 1, dequant_word(c.y, s2));
-          st_tile_chunk(tile, r, part * 4 + 2, dequant_word(c.z, s2));
-          st_tile_chunk(tile, r, part * 4 + 3, dequant_word(c.w, s2));
-          fence_proxy_async_smem();
-          mbar_arrive(&full_a[s]);
-          c = nc;
-          sv = nsv;
         }
       } else {
         // router: rows are experts; K' = 2H; step ks < H/64 writes the fp16
