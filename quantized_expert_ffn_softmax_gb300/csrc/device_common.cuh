@@ -114,6 +114,51 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// One 2-D tile of a tensor map (box given by the map) at (col, row); the
+// innermost coordinate times the element size must be a multiple of 16 B.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int col, int row,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 16-byte global -> shared copy that bypasses L1 (per-thread async copy).
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(dst_smem), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Named barrier over a subset of the block's warps (all of them must reach it).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Same, and returns the AND of every participating thread's v.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  int r;
+  asm volatile(
+      "{\n"
+      " .reg .pred pv, pr;\n"
+      " setp.ne.s32 pv, %1, 0;\n"
+      " bar.red.and.pred pr, %2, %3, pv;\n"
+      " selp.s32 %0, 1, 0, pr;\n"
+      "}"
+      : "=r"(r)
+      : "r"((int)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -173,6 +218,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -23,8 +23,11 @@
 //   warps 4-11  A producers: dequantise 4-bit codes (or split fp32 router
 //               weights) into fp16 128x64 tiles in the 128-byte swizzled
 //               K-major layout, straight into the stage's shared memory
-//   warp 12     B producer: TMA gather4 of the unit's token rows
-//   warp 13     TMEM allocator and single-thread tcgen05.mma issuer
+//   B loaders   gate/up: warps 12-13 gather the unit's token rows (bucket
+//               order) with per-thread 16-byte async copies into the same
+//               swizzled layout; down/router: warp 12 loads the unit's
+//               contiguous rows as one TMA tile per K step
+//   last warp   TMEM allocator and single-thread tcgen05.mma issuer
 // A 4-stage shared-memory ring (full/empty mbarriers) feeds the MMA; two
 // TMEM accumulators let the epilogue of one unit overlap the next unit's
 // MMAs.  Every wait is bounded and gives up once the error word is set.
@@ -51,13 +54,24 @@ constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 4;
 constexpr int kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kGemmThreads = 14 * 32;
+constexpr int kBWarp0 = 12;
 constexpr int kBucketThreads = 1024;
 constexpr int kPrefetch = 4;       // K steps of weight codes each producer keeps in flight
+constexpr int kBLag = 2;           // K steps of gathered token rows each B loader keeps in flight
 
 enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
+
+// Warp roles after the epilogue and A-producer warps: the gate/up GEMM
+// gathers its token rows with two warps of per-thread async copies; the
+// down and router GEMMs read contiguous rows with one TMA tile per K step.
+// At most 16 warps, so that no SM sub-partition holds more than four and a
+// thread may use 128 registers.
+template <int MODE>
+struct Roles {
+  static constexpr int kBWarps = (MODE == kSwiglu) ? 2 : 1;
+  static constexpr int kMmaWarp = kBWarp0 + kBWarps;
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;
+};
 
 struct GemmParams {
   int H, E, k, F, Fs, T, Tk;
@@ -65,6 +79,7 @@ struct GemmParams {
   const int32_t* n_units;    // gate/up or down: device count
   const int4* units;
   LayerDev W;
+  const __half* x16;
   const int32_t* perm_tok;
   const float* perm_w;
   const int32_t* xshift;
@@ -127,12 +142,13 @@ __device__ __forceinline__ void st_tile_chunk(unsigned char* tile, int r, int j,
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_hr,
                     const __grid_constant__ CUtensorMap tm_hs) {
   constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
   constexpr int STAGE = NA * kTileA + kTileB;
+  constexpr int kMmaWarp = Roles<MODE>::kMmaWarp;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -143,12 +159,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = bars + 3 * kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  // per-unit token metadata of the epilogue: two words per token column
+  int* meta_i = reinterpret_cast<int*>(smem + kStages * STAGE + 256);
+  float* meta_f = reinterpret_cast<float*>(meta_i + kNT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_a[s], kProdThreads);
-      mbar_init(&full_b[s], 1);
+      mbar_init(&full_b[s], MODE == kSwiglu ? Roles<MODE>::kBWarps * 32 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -170,51 +189,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
+    // Thread r owns accumulator row r (TMEM lane r).  The per-token factors
+    // of the unit (power-of-two input scales, routing weights, destination
+    // rows) are staged in shared memory once per unit, one token per thread.
     const int r = warp * 32 + lane;
     int j = 0;
+    float bias_r = 0.0f;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
       const UnitInfo U = unit_info<MODE>(p, u);
+      if (MODE == kRouter) {
+        const int e = U.mt * 128 + r;
+        bias_r = e < p.E ? __ldg(p.W.router_b + e) : 0.0f;
+      }
+      named_bar_sync(1, kEpiWarps * 32);  // the previous unit is done with meta
+      if (r < U.n) {
+        if (MODE == kSwiglu) {
+          const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
+          const int sx = __ldg(p.xshift + tok);
+          meta_i[r] = sx;  // D * 2^sx = x-scale restored; h stored * 2^-2sx
+        } else if (MODE == kScatter) {
+          const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
+          const float wgt = U.shared ? 1.0f : __ldg(p.perm_w + U.p0 + r);
+          meta_i[r] = tok;
+          meta_f[r] = wgt * pow2f(2 * __ldg(p.xshift + tok));
+        } else {
+          meta_f[r] = pow2f(__ldg(p.xshift + U.p0 + r) - p.router_shift);
+        }
+      }
       const int b = j & 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&tfull[b], (j >> 1) & 1, p.err, tmo);
-      ok = __shfl_sync(0xffffffffu, ok, 0);  // warp-uniform: tcgen05.ld is .sync.aligned
-      if (!ok) break;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // meta is ready, and the four warps agree on whether to go on (the
+      // break must be uniform: the named barriers wait for all of them)
+      if (!named_bar_and(1, kEpiWarps * 32, ok)) break;
       tc_fence_after();
       const int neff = (U.n + 15) & ~15;
       const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 256);
-      for (int c0 = 0; c0 < neff; c0 += 32) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tbase + c0, v0);
-        if (NA == 2) tmem_ld32(tbase + 128 + c0, v1);
+      int q = 0;
+      __half* hrow = nullptr;
+      size_t hstride = 0;
+      if (MODE == kSwiglu) {
+        const int f = U.mt * 128 + r;
+        q = (f & ~7) | ((f & 4) ? (((f & 3) << 1) | 1) : ((f & 3) << 1));
+        hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
+        hrow = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + q;
+      }
+      constexpr int CW = (NA == 2) ? 16 : 32;  // columns per TMEM load
+      for (int c0 = 0; c0 < neff; c0 += CW) {
+        uint32_t v0[CW], v1[CW];
+        tmem_ld(tbase + c0, v0);
+        if (NA == 2) tmem_ld(tbase + 128 + c0, v1);
         tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
+        for (int jj = 0; jj < CW; ++jj) {
           const int t = c0 + jj;
           if (t >= U.n) continue;
           if (MODE == kSwiglu) {
-            const int tok = U.shared ? (U.p0 + t) : __ldg(p.perm_tok + U.p0 + t);
-            const int s = __ldg(p.xshift + tok);
-            const float g = __uint_as_float(v0[jj]) * pow2f(s);
-            const float uu = __uint_as_float(v1[jj]) * pow2f(s);
-            const float h = g / (1.0f + __expf(-g)) * uu;
-            const int f = U.mt * 128 + r;
-            const int q = (f & ~7) | ((f & 4) ? (((f & 3) << 1) | 1) : ((f & 3) << 1));
-            __half* dst = U.shared ? p.hmid_s + (size_t)(U.p0 + t) * p.Fs
-                                   : p.hmid_r + (size_t)(U.p0 + t) * p.F;
-            dst[q] = __float2half_rn(h * pow2f(-2 * s));
+            const int sx = meta_i[t];
+            const float g = __uint_as_float(v0[jj]) * pow2f(sx);
+            const float uu = __uint_as_float(v1[jj]) * pow2f(sx);
+            const float h = __fdividef(g, 1.0f + __expf(-g)) * uu;
+            hrow[(size_t)t * hstride] = __float2half_rn(h * pow2f(-2 * sx));
           } else if (MODE == kScatter) {
-            const int tok = U.shared ? (U.p0 + t) : __ldg(p.perm_tok + U.p0 + t);
-            const float wgt = U.shared ? 1.0f : __ldg(p.perm_w + U.p0 + t);
-            const int s = __ldg(p.xshift + tok);
-            atomicAdd(p.yacc + (size_t)tok * p.H + U.mt * 128 + r,
-                      __uint_as_float(v0[jj]) * wgt * pow2f(2 * s));
+            atomicAdd(p.yacc + (size_t)meta_i[t] * p.H + U.mt * 128 + r,
+                      __uint_as_float(v0[jj]) * meta_f[t]);
           } else {
-            const int tok = U.p0 + t;
             const int e = U.mt * 128 + r;
-            const int s = __ldg(p.xshift + tok);
             if (e < p.E)
-              p.z[(size_t)tok * p.E + e] =
-                  __uint_as_float(v0[jj]) * pow2f(s - p.router_shift) + __ldg(p.W.router_b + e);
+              p.z[(size_t)(U.p0 + t) * p.E + e] = __uint_as_float(v0[jj]) * meta_f[t] + bias_r;
           }
         }
       }
@@ -390,49 +433,85 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ B producer
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ B loaders
     uint32_t it = 0;
     bool alive = true;
-    for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
-      const UnitInfo U = unit_info<MODE>(p, u);
-      const int neff = (U.n + 15) & ~15;
-      int rows[4];
+    if (MODE == kSwiglu) {
+      // lane l of B warp bw copies 16-byte chunk (l & 7) of rows
+      // bw*RW + 4i + (l >> 3), i < RW/4: every warp instruction moves four
+      // whole 128-byte rows.  A thread's copies of K step j form one async
+      // group; it retires step j (wait, proxy fence, arrive) kBLag steps later.
+      constexpr int RW = kNT / Roles<MODE>::kBWarps;  // rows per warp
+      const int bw = warp - kBWarp0;
+      const int c = lane & 7;
+      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        const int neff = (U.n + 15) & ~15;
+        uint32_t src[RW / 4];  // element offset of the chunk in x16
+        uint32_t dst[RW / 4];  // byte offset in the B tile, or ~0 if not loaded
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        int t = 4 * lane + i;
-        t = t < U.n ? t : U.n - 1;  // padding rows repeat a valid row
-        if (MODE == kSwiglu)
-          rows[i] = U.shared ? (U.p0 + t) : __ldg(p.perm_tok + U.p0 + t);
-        else
-          rows[i] = U.p0 + t;
-      }
-      const CUtensorMap* tm = (MODE == kScatter) ? (U.shared ? &tm_hs : &tm_hr) : &tm_x;
-      const int nks = U.K / 64;
-      const int kpp = p.H / 64;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % kStages;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          alive = false;
-          break;
+        for (int i = 0; i < RW / 4; ++i) {
+          const int row = bw * RW + 4 * i + (lane >> 3);
+          int t = row < U.n ? row : U.n - 1;  // padding rows repeat a valid row
+          const int tok = U.shared ? (U.p0 + t) : __ldg(p.perm_tok + U.p0 + t);
+          src[i] = (uint32_t)tok * (uint32_t)p.H + (uint32_t)(c * 8);
+          dst[i] = (row < neff) ? (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4)) : 0xffffffffu;
         }
-        if (lane == 0) mbar_expect_tx(&full_b[s], (uint32_t)neff * 128u);
-        __syncwarp();
-        const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-        if (4 * lane < neff)
-          tma_gather4(smem + s * STAGE + NA * kTileA + lane * 512, tm, col, rows[0], rows[1],
-                      rows[2], rows[3], &full_b[s]);
+        const int nks = U.K / 64;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % kStages;
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            alive = false;
+            break;
+          }
+          const uint32_t tile = smem_u32(smem + s * STAGE + NA * kTileA);
+#pragma unroll
+          for (int i = 0; i < RW / 4; ++i)
+            if (dst[i] != 0xffffffffu) cp_async_16(tile + dst[i], p.x16 + src[i] + ks * 64);
+          cp_async_commit();
+          if (it >= (uint32_t)kBLag) {
+            cp_async_wait<kBLag>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full_b[(it - kBLag) % kStages]);
+          }
+        }
       }
+      // every copy lands before the CTA can exit; retire the last steps
+      cp_async_wait<0>();
+      if (alive) {
+        fence_proxy_async_smem();
+        for (uint32_t q = it > (uint32_t)kBLag ? it - kBLag : 0u; q < it; ++q)
+          mbar_arrive(&full_b[q % kStages]);
+      }
+    } else {
+      if (lane == 0) {
+        const int kpp = p.H / 64;
+        for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+          const UnitInfo U = unit_info<MODE>(p, u);
+          const CUtensorMap* tm = (MODE == kScatter) ? (U.shared ? &tm_hs : &tm_hr) : &tm_x;
+          const int nks = U.K / 64;
+          for (int ks = 0; ks < nks; ++ks, ++it) {
+            const int s = it % kStages;
+            if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo)) {
+              alive = false;
+              break;
+            }
+            mbar_expect_tx(&full_b[s], (uint32_t)kTileB);
+            const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
+            tma_load_2d(smem + s * STAGE + NA * kTileA, tm, col, U.p0, &full_b[s]);
+          }
+        }
+        // let every copy this thread issued land before the CTA can exit
+        const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+        for (uint32_t q = first; q < it; ++q)
+          mbar_wait(&full_b[q % kStages], (q / kStages) & 1, p.err, tmo);
+      }
+      __syncwarp();
     }
-    // let every copy this warp issued land before the CTA can exit
-    if (lane == 0) {
-      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
-      for (uint32_t q = first; q < it; ++q) mbar_wait(&full_b[q % kStages], (q / kStages) & 1, p.err, tmo);
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -765,13 +844,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D fp16 row map [rows][cols], box {64, 1} (one 128-byte row), 128B swizzle.
+// 2-D fp16 map [rows][cols], box {64, 128} (128 rows of 128 bytes: one
+// K step of a B tile), 128B swizzle; rows past the end read as zero.
 bool encode_rows(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 1};
+  cuuint32_t box[2] = {64, (cuuint32_t)kNT};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -782,7 +862,7 @@ template <int MODE>
 moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_t s,
                        const char** why) {
   constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
-  const size_t smem = (size_t)kStages * (NA * kTileA + kTileB) + 1024 + 256;
+  const size_t smem = (size_t)kStages * (NA * kTileA + kTileB) + 1024 + 256 + 8 * kNT;
   auto kern = moe_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
@@ -792,7 +872,7 @@ moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_
   static const char* const names[3] = {"moe_gemm_gateup_swiglu", "moe_gemm_down_scatter",
                                        "moe_gemm_router"};
   prof::Scope scope(names[MODE], s);
-  kern<<<grid, kGemmThreads, smem, s>>>(gp, L->tmap_x16, L->tmap_hr, L->tmap_hs);
+  kern<<<grid, Roles<MODE>::kThreads, smem, s>>>(gp, L->tmap_x16, L->tmap_hr, L->tmap_hs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = cudaGetErrorString(e);
@@ -864,6 +944,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.T = T;
   gp.Tk = T * k;
   gp.W = L->dev;
+  gp.x16 = ws.x16;
   gp.perm_tok = ws.perm_tok;
   gp.perm_w = ws.perm_w;
   gp.xshift = ws.xshift;
