@@ -575,6 +575,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int nr = (TT == 1) ? k : M.n_routed;
       if (Fs > 0 && tid < kMaxDecodeTokens) M.unit_w[nr][tid] = (tid < T) ? 1.0f : 0.0f;
     }
+    // the router rows and slot table were read through the generic proxy;
+    // the next layer's bulk copies (async proxy) overwrite them
+    fence_proxy_async_smem();
     __syncthreads();
     if (p.mode == kModeRoute) continue;
     const int n_routed = M.n_routed;
@@ -685,6 +688,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(s, d[t], acc[r][t]);
           }
         }
+        // the stage is refilled by bulk copies (async proxy): fence this
+        // warp's generic reads of it before handing it back
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&mbar[kBarE0 + sg]);  // this warp is done with the stage
         float v[4 * TT];

@@ -92,6 +92,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   return true;
 }
 
+// Bounded poll for a phase that is known to complete by itself (copies or
+// MMAs already issued), also once the error word is set: used before the
+// CTA exits so that nothing still writes its shared memory or TMEM.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer();
+  while (!mbar_test(bar, parity) && global_timer() - t0 < timeout_ns) {
+  }
+}
+
 // Non-tensor bulk copy global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
@@ -99,18 +108,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Tensor-map gather of 4 rows (box one row high) into consecutive 128-byte
-// rows of shared memory starting at dst; the map's swizzle is applied.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, int col, int r0,
-                                            int r1, int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
       : "memory");
 }
 

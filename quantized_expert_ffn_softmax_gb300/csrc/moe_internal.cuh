@@ -110,9 +110,15 @@ struct Workspace {
 struct moe_layer {
   moe_layer_config cfg;
   moe::LayerDev dev;
-  CUtensorMap tmap_x16;   // x16 rows, box {64, 1}, 128B swizzle (gather4)
-  CUtensorMap tmap_hr;    // hmid_r rows
-  CUtensorMap tmap_hs;    // hmid_s rows
+  CUtensorMap tmap_x16;      // x16 rows, box {64, 128}, 128B swizzle
+  CUtensorMap tmap_hr;       // hmid_r rows, same box
+  CUtensorMap tmap_hs;       // hmid_s rows, same box
+  CUtensorMap tmap_gate;     // packed codes [slots*F][H/2], box {32 B, 128 rows}
+  CUtensorMap tmap_up;       // packed codes [slots*F][H/2]
+  CUtensorMap tmap_down;     // packed codes [slots*H][F/2]
+  CUtensorMap tmap_sh_gate;  // shared expert [Fs][H/2]
+  CUtensorMap tmap_sh_up;    // shared expert [Fs][H/2]
+  CUtensorMap tmap_sh_down;  // shared expert [H][Fs/2]
   int router_shift = 0;               // router weights are scaled by 2^router_shift
   void* weights_block = nullptr;  // one allocation holding all weight copies
   size_t weights_bytes = 0;

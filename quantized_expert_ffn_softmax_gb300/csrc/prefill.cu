@@ -47,30 +47,60 @@ namespace {
 using namespace dev;
 
 constexpr int kNT = 128;           // token tile = largest MMA N used
-constexpr int kStages = 4;
 constexpr int kTileA = 128 * 128;  // bytes: 128 rows x 64 fp16
 constexpr int kTileB = kNT * 128;  // bytes: kNT rows x 64 fp16
+constexpr int kRawTile = 128 * 32; // bytes: 128 rows x 64 packed 4-bit codes
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 4;
 constexpr int kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBWarp0 = 12;
 constexpr int kBucketThreads = 1024;
-constexpr int kPrefetch = 4;       // K steps of weight codes each producer keeps in flight
+constexpr int kScalePrefetch = 8;  // K steps of block scales each producer keeps in flight
 constexpr int kBLag = 2;           // K steps of gathered token rows each B loader keeps in flight
 
 enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 
-// Warp roles after the epilogue and A-producer warps: the gate/up GEMM
-// gathers its token rows with two warps of per-thread async copies; the
-// down and router GEMMs read contiguous rows with one TMA tile per K step.
-// At most 16 warps, so that no SM sub-partition holds more than four and a
-// thread may use 128 registers.
+// Shared-memory rings and warp roles of one GEMM kernel.
+//   stage ring  S stages, each NA dequantised fp16 128x64 tiles (MMA operand
+//               A) and one fp16 kNTx64 token tile (operand B); full_a and
+//               full_b mark the two halves ready, one tcgen05.commit per K
+//               step releases the whole stage
+//   raw ring    SR stages of NA packed-code tiles, filled by TMA; the gate/up
+//               and down GEMMs dequantise from it (the router GEMM reads its
+//               fp32 weights directly and has no raw ring)
+// Warps after the epilogue (0-3) and A producers (4-11): B loaders (gate/up
+// gathers its token rows with two warps of per-thread async copies; down
+// and router load contiguous rows as one TMA tile per K step), the raw
+// loader, and the MMA issuer.  At most 16 warps, so that no SM
+// sub-partition holds more than four and a thread may use 128 registers.
 template <int MODE>
-struct Roles {
+struct Gemm {
+  static constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
+  static constexpr int S = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 5 : 6);
+  static constexpr int SR = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 12 : 0);
+  static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
   static constexpr int kBWarps = (MODE == kSwiglu) ? 2 : 1;
-  static constexpr int kMmaWarp = kBWarp0 + kBWarps;
+  static constexpr int kRawWarp = kBWarp0 + kBWarps;
+  static constexpr int kMmaWarp = kRawWarp + (SR > 0 ? 1 : 0);
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
+  static constexpr int kRawBytes = NA * kRawTile;
+  static constexpr int kStageBytes = NA * kTileA + kTileB;  // A tiles, then the B tile
+  static constexpr int OFF_RAW = S * kStageBytes;
+  static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
+  static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 4) + 4) + 127) & ~127;
+  static constexpr int OFF_META = OFF_BAR + kBarBytes;
+  static constexpr int kSmem = OFF_META + 8 * kNT + 1024;  // + slack for 1 KB alignment
+  static_assert(kThreads <= 16 * 32, "at most 16 warps");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
+};
+
+// Tensor maps of one GEMM launch.
+struct GemmMaps {
+  CUtensorMap a_routed[2];  // packed codes of the routed experts (gate, up | down)
+  CUtensorMap a_shared[2];  // packed codes of the shared expert
+  CUtensorMap b[2];         // B rows: router x16 | down hmid_r, hmid_s
 };
 
 struct GemmParams {
@@ -142,33 +172,37 @@ __device__ __forceinline__ void st_tile_chunk(unsigned char* tile, int r, int j,
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_x,
-                    const __grid_constant__ CUtensorMap tm_hr,
-                    const __grid_constant__ CUtensorMap tm_hs) {
-  constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
-  constexpr int STAGE = NA * kTileA + kTileB;
-  constexpr int kMmaWarp = Roles<MODE>::kMmaWarp;
+__global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ GemmMaps maps) {
+  using G = Gemm<MODE>;
+  constexpr int NA = G::NA, S = G::S, SR = G::SR;
+  constexpr int kMmaWarp = G::kMmaWarp;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE);
-  uint64_t* full_a = bars;
-  uint64_t* full_b = bars + kStages;
-  uint64_t* empty = bars + 2 * kStages;
-  uint64_t* tfull = bars + 3 * kStages;
+  unsigned char* sR = smem + G::OFF_RAW;   // SR stages x NA raw code tiles
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
+  uint64_t* full_b = full_a + S;
+  uint64_t* empty = full_b + S;
+  uint64_t* raw_full = empty + S;
+  uint64_t* raw_empty = raw_full + G::SRb;
+  uint64_t* tfull = raw_empty + G::SRb;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   // per-unit token metadata of the epilogue: two words per token column
-  int* meta_i = reinterpret_cast<int*>(smem + kStages * STAGE + 256);
+  int* meta_i = reinterpret_cast<int*>(smem + G::OFF_META);
   float* meta_f = reinterpret_cast<float*>(meta_i + kNT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full_a[s], kProdThreads);
-      mbar_init(&full_b[s], MODE == kSwiglu ? Roles<MODE>::kBWarps * 32 : 1);
+      mbar_init(&full_b[s], MODE == kSwiglu ? G::kBWarps * 32 : 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < SR; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kProdWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -205,8 +239,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       if (r < U.n) {
         if (MODE == kSwiglu) {
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
-          const int sx = __ldg(p.xshift + tok);
-          meta_i[r] = sx;  // D * 2^sx = x-scale restored; h stored * 2^-2sx
+          meta_i[r] = __ldg(p.xshift + tok);  // D * 2^sx restores x; h is stored * 2^-2sx
         } else if (MODE == kScatter) {
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
           const float wgt = U.shared ? 1.0f : __ldg(p.perm_w + U.p0 + r);
@@ -226,12 +259,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       tc_fence_after();
       const int neff = (U.n + 15) & ~15;
       const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 256);
-      int q = 0;
       __half* hrow = nullptr;
       size_t hstride = 0;
       if (MODE == kSwiglu) {
         const int f = U.mt * 128 + r;
-        q = (f & ~7) | ((f & 4) ? (((f & 3) << 1) | 1) : ((f & 3) << 1));
+        const int q = (f & ~7) | ((f & 4) ? (((f & 3) << 1) | 1) : ((f & 3) << 1));
         hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
         hrow = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + q;
       }
@@ -267,121 +299,114 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   } else if (warp < kProdWarp0 + kProdWarps) {
     // ------------------------------------------------------------ A producers
     const int pi = threadIdx.x - kProdWarp0 * 32;  // 0..255
-    const int r = pi & 127;
-    const int part = pi >> 7;  // gate/up: matrix; down/router: which half of the K step
     const LayerDev& Wd = p.W;
     uint32_t it = 0;
     bool alive = true;
     for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
       const UnitInfo U = unit_info<MODE>(p, u);
       const int nks = U.K / 64;
-      if (MODE == kSwiglu) {
-        const int f = U.mt * 128 + r;
-        const int H = p.H;
-        const uint8_t* q;
-        const uint16_t* sc;
-        if (U.shared) {
-          q = (part ? Wd.sh_up_q : Wd.sh_gate_q) + (size_t)f * (H / 2);
-          sc = (part ? Wd.sh_up_s : Wd.sh_gate_s) + (size_t)f * (H / 32);
+      if constexpr (MODE != kRouter) {
+        // Codes come from the raw ring (one TMA tile per matrix per K step);
+        // scales (4 bytes per row and K step) ride in a register ring.
+        //   gate/up: thread = (matrix part, row r), all 64 K of the step
+        //   down:    thread = (K half part, row r); lanes 8i..8i+7 read four
+        //            whole 32-byte rows, so the shared reads do not conflict
+        int r, part;
+        if (MODE == kSwiglu) {
+          r = pi & 127;
+          part = pi >> 7;
         } else {
-          const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
-          q = (part ? Wd.up_q : Wd.gate_q) + (slot * p.F + f) * (H / 2);
-          sc = (part ? Wd.up_s : Wd.gate_s) + (slot * p.F + f) * (H / 32);
+          r = ((pi >> 3) << 2) | (pi & 3);
+          part = (pi >> 2) & 1;
         }
-        // a ring of kPrefetch K steps of codes and scales in registers keeps
-        // that many global loads in flight per thread
-        uint4 ca[kPrefetch], cb[kPrefetch];
-        uint32_t cs[kPrefetch];
-#pragma unroll
-        for (int i = 0; i < kPrefetch; ++i) {
-          if (i < nks) {
-            ca[i] = ld_stream(q + i * 32);
-            cb[i] = ld_stream(q + i * 32 + 16);
-            cs[i] = __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * i));
+        const uint16_t* sc;
+        int sstride;  // scale entries per row
+        if (MODE == kSwiglu) {
+          const int f = U.mt * 128 + r;
+          sstride = p.H / 32;
+          if (U.shared) {
+            sc = (part ? Wd.sh_up_s : Wd.sh_gate_s) + (size_t)f * sstride;
+          } else {
+            const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
+            sc = (part ? Wd.up_s : Wd.gate_s) + (slot * p.F + f) * sstride;
+          }
+        } else {
+          const int i = U.mt * 128 + r;  // output row of H
+          sstride = U.K / 32;
+          if (U.shared) {
+            sc = Wd.sh_down_s + (size_t)i * sstride;
+          } else {
+            const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
+            sc = Wd.down_s + (slot * p.H + i) * sstride;
           }
         }
-        for (int ks0 = 0; ks0 < nks && alive; ks0 += kPrefetch) {
+        uint32_t cs[kScalePrefetch];
 #pragma unroll
-          for (int i = 0; i < kPrefetch; ++i) {
+        for (int i = 0; i < kScalePrefetch; ++i)
+          if (i < nks)
+            cs[i] = (MODE == kSwiglu) ? __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * i))
+                                      : (uint32_t)__ldg(sc + 2 * i + part);
+        const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
+        for (int ks0 = 0; ks0 < nks && alive; ks0 += kScalePrefetch) {
+#pragma unroll
+          for (int i = 0; i < kScalePrefetch; ++i) {
             const int ks = ks0 + i;
             if (ks < nks && alive) {
-              const int s = it % kStages;
+              const int sr = it % SR, st = it % S;
               bool ok = true;
-              if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+              if (lane == 0) ok = mbar_wait(&raw_full[sr], (it / SR) & 1, p.err, tmo);
               ok = __shfl_sync(0xffffffffu, ok, 0);
-              if (!ok) {
-                alive = false;
-              } else {
-                unsigned char* tile = smem + s * STAGE + part * kTileA;
-                const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(cs[i] & 0xffffu)));
-                const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(cs[i] >> 16)));
-                st_tile_chunk(tile, r, 0, dequant_word(ca[i].x, slo));
-                st_tile_chunk(tile, r, 1, dequant_word(ca[i].y, slo));
-                st_tile_chunk(tile, r, 2, dequant_word(ca[i].z, slo));
-                st_tile_chunk(tile, r, 3, dequant_word(ca[i].w, slo));
-                st_tile_chunk(tile, r, 4, dequant_word(cb[i].x, shi));
-                st_tile_chunk(tile, r, 5, dequant_word(cb[i].y, shi));
-                st_tile_chunk(tile, r, 6, dequant_word(cb[i].z, shi));
-                st_tile_chunk(tile, r, 7, dequant_word(cb[i].w, shi));
-                fence_proxy_async_smem();
-                mbar_arrive(&full_a[s]);
-                ++it;
-                if (ks + kPrefetch < nks) {
-                  ca[i] = ld_stream(q + (ks + kPrefetch) * 32);
-                  cb[i] = ld_stream(q + (ks + kPrefetch) * 32 + 16);
-                  cs[i] = __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * (ks + kPrefetch)));
+              if (ok) (void)mbar_test(&raw_full[sr], (it / SR) & 1);  // every lane acquires
+              uint4 ca, cb;
+              if (ok) {
+                const unsigned char* rs = sR + sr * G::kRawBytes;
+                if (MODE == kSwiglu) {
+                  const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
+                  const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
+                  ca = h ? q1 : q0;
+                  cb = h ? q0 : q1;
+                } else {
+                  ca = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
+                  cb = ca;
                 }
+                // generic-proxy reads of a buffer that TMA (async proxy) will
+                // overwrite: fence them before the stage is handed back
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[sr]);
+                if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
               }
-            }
-          }
-        }
-      } else if (MODE == kScatter) {
-        const int i = U.mt * 128 + r;  // output row of H
-        const int K = U.K;
-        const uint8_t* q;
-        const uint16_t* sc;
-        if (U.shared) {
-          q = Wd.sh_down_q + (size_t)i * (K / 2);
-          sc = Wd.sh_down_s + (size_t)i * (K / 32);
-        } else {
-          const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
-          q = Wd.down_q + (slot * p.H + i) * (K / 2);
-          sc = Wd.down_s + (slot * p.H + i) * (K / 32);
-        }
-        uint4 cc[kPrefetch];
-        uint16_t cv[kPrefetch];
-#pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-          if (j < nks) {
-            cc[j] = ld_stream(q + j * 32 + part * 16);
-            cv[j] = __ldg(sc + 2 * j + part);
-          }
-        }
-        for (int ks0 = 0; ks0 < nks && alive; ks0 += kPrefetch) {
-#pragma unroll
-          for (int j = 0; j < kPrefetch; ++j) {
-            const int ks = ks0 + j;
-            if (ks < nks && alive) {
-              const int s = it % kStages;
-              bool ok = true;
-              if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) {
                 alive = false;
               } else {
-                unsigned char* tile = smem + s * STAGE;
-                const __half2 s2 = __half2half2(__ushort_as_half(cv[j]));
-                st_tile_chunk(tile, r, part * 4 + 0, dequant_word(cc[j].x, s2));
-                st_tile_chunk(tile, r, part * 4 + 1, dequant_word(cc[j].y, s2));
-                st_tile_chunk(tile, r, part * 4 + 2, dequant_word(cc[j].z, s2));
-                st_tile_chunk(tile, r, part * 4 + 3, dequant_word(cc[j].w, s2));
-                fence_proxy_async_smem();
-                mbar_arrive(&full_a[s]);
-                ++it;
-                if (ks + kPrefetch < nks) {
-                  cc[j] = ld_stream(q + (ks + kPrefetch) * 32 + part * 16);
-                  cv[j] = __ldg(sc + 2 * (ks + kPrefetch) + part);
+                unsigned char* tile = smem + st * G::kStageBytes;
+                if (MODE == kSwiglu) {
+                  tile += part * kTileA;
+                  const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(cs[i] & 0xffffu)));
+                  const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(cs[i] >> 16)));
+                  st_tile_chunk(tile, r, 0, dequant_word(ca.x, slo));
+                  st_tile_chunk(tile, r, 1, dequant_word(ca.y, slo));
+                  st_tile_chunk(tile, r, 2, dequant_word(ca.z, slo));
+                  st_tile_chunk(tile, r, 3, dequant_word(ca.w, slo));
+                  st_tile_chunk(tile, r, 4, dequant_word(cb.x, shi));
+                  st_tile_chunk(tile, r, 5, dequant_word(cb.y, shi));
+                  st_tile_chunk(tile, r, 6, dequant_word(cb.z, shi));
+                  st_tile_chunk(tile, r, 7, dequant_word(cb.w, shi));
+                } else {
+                  const __half2 s2 = __half2half2(__ushort_as_half((uint16_t)cs[i]));
+                  st_tile_chunk(tile, r, part * 4 + 0, dequant_word(ca.x, s2));
+                  st_tile_chunk(tile, r, part * 4 + 1, dequant_word(ca.y, s2));
+                  st_tile_chunk(tile, r, part * 4 + 2, dequant_word(ca.z, s2));
+                  st_tile_chunk(tile, r, part * 4 + 3, dequant_word(ca.w, s2));
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(&full_a[st]);
+                ++it;
+                const int kn = ks + kScalePrefetch;
+                if (kn < nks)
+                  cs[i] = (MODE == kSwiglu) ? __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * kn))
+                                            : (uint32_t)__ldg(sc + 2 * kn + part);
               }
             }
           }
@@ -389,6 +414,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       } else {
         // router: rows are experts; K' = 2H; step ks < H/64 writes the fp16
         // "hi" term of w * 2^router_shift, later steps the "mid" remainder
+        const int r = pi & 127;
+        const int part = pi >> 7;  // which half of the K step
         const int e = U.mt * 128 + r;
         const bool valid = e < p.E;
         const float* wrow = Wd.router_w + (size_t)(valid ? e : 0) * p.H;
@@ -400,15 +427,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           const float4* src = reinterpret_cast<const float4*>(wrow + kk * 64 + part * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[i] = valid ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const int s = it % kStages;
+          const int st = it % S;
           bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             alive = false;
             break;
           }
-          unsigned char* tile = smem + s * STAGE;
+          unsigned char* tile = smem + st * G::kStageBytes;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {  // 8-element group g of this half
             const float a[8] = {v[2 * g].x, v[2 * g].y, v[2 * g].z, v[2 * g].w,
@@ -429,11 +456,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             st_tile_chunk(tile, r, part * 4 + g, make_uint4(o[0], o[1], o[2], o[3]));
           }
           fence_proxy_async_smem();
-          mbar_arrive(&full_a[s]);
+          mbar_arrive(&full_a[st]);
         }
       }
     }
-  } else if (warp < kMmaWarp) {
+  } else if (warp < G::kRawWarp) {
     // ------------------------------------------------------------ B loaders
     uint32_t it = 0;
     bool alive = true;
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       // bw*RW + 4i + (l >> 3), i < RW/4: every warp instruction moves four
       // whole 128-byte rows.  A thread's copies of K step j form one async
       // group; it retires step j (wait, proxy fence, arrive) kBLag steps later.
-      constexpr int RW = kNT / Roles<MODE>::kBWarps;  // rows per warp
+      constexpr int RW = kNT / G::kBWarps;  // rows per warp
       const int bw = warp - kBWarp0;
       const int c = lane & 7;
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
@@ -460,15 +487,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         }
         const int nks = U.K / 64;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % kStages;
+          const int st = it % S;
           bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo);
+          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             alive = false;
             break;
           }
-          const uint32_t tile = smem_u32(smem + s * STAGE + NA * kTileA);
+          const uint32_t tile = smem_u32(smem + st * G::kStageBytes + NA * kTileA);
 #pragma unroll
           for (int i = 0; i < RW / 4; ++i)
             if (dst[i] != 0xffffffffu) cp_async_16(tile + dst[i], p.x16 + src[i] + ks * 64);
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if (it >= (uint32_t)kBLag) {
             cp_async_wait<kBLag>();
             fence_proxy_async_smem();
-            mbar_arrive(&full_b[(it - kBLag) % kStages]);
+            mbar_arrive(&full_b[(it - kBLag) % S]);
           }
         }
       }
@@ -485,33 +512,62 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       if (alive) {
         fence_proxy_async_smem();
         for (uint32_t q = it > (uint32_t)kBLag ? it - kBLag : 0u; q < it; ++q)
-          mbar_arrive(&full_b[q % kStages]);
+          mbar_arrive(&full_b[q % S]);
       }
     } else {
       if (lane == 0) {
         const int kpp = p.H / 64;
         for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
           const UnitInfo U = unit_info<MODE>(p, u);
-          const CUtensorMap* tm = (MODE == kScatter) ? (U.shared ? &tm_hs : &tm_hr) : &tm_x;
+          const CUtensorMap* tm = (MODE == kScatter) ? &maps.b[U.shared ? 1 : 0] : &maps.b[0];
           const int nks = U.K / 64;
           for (int ks = 0; ks < nks; ++ks, ++it) {
-            const int s = it % kStages;
-            if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, tmo)) {
+            const int st = it % S;
+            if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo)) {
               alive = false;
               break;
             }
-            mbar_expect_tx(&full_b[s], (uint32_t)kTileB);
+            mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
             const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-            tma_load_2d(smem + s * STAGE + NA * kTileA, tm, col, U.p0, &full_b[s]);
+            tma_load_2d(smem + st * G::kStageBytes + NA * kTileA, tm, col, U.p0, &full_b[st]);
           }
         }
         // let every copy this thread issued land before the CTA can exit
-        const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
-        for (uint32_t q = first; q < it; ++q)
-          mbar_wait(&full_b[q % kStages], (q / kStages) & 1, p.err, tmo);
+        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+        for (uint32_t q = first; q < it; ++q) drain_wait(&full_b[q % S], (q / S) & 1, tmo);
       }
       __syncwarp();
     }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ raw code loader
+    // One TMA tile (128 rows x 32 bytes of packed codes) per matrix and K step.
+    if constexpr (SR > 0) if (lane == 0) {
+      uint32_t it = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        const int slot = U.shared ? 0 : __ldg(p.W.slot_of + U.e);
+        const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
+        const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * 128;
+        const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
+        const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
+        const int nks = U.K / 64;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int sr = it % SR;
+          if (!mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo)) {
+            alive = false;
+            break;
+          }
+          mbar_expect_tx(&raw_full[sr], (uint32_t)G::kRawBytes);
+          unsigned char* dst = sR + sr * G::kRawBytes;
+          tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
+          if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
+        }
+      }
+      const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
+      for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -528,24 +584,24 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         const int nks = U.K / 64;
         bool ok = true;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&full_a[s], ph, p.err, tmo) || !mbar_wait(&full_b[s], ph, p.err, tmo)) {
+          const int st = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(&full_a[st], ph, p.err, tmo) || !mbar_wait(&full_b[st], ph, p.err, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * STAGE);
-          const uint64_t da0 = smem_desc_sw128(sa);
-          const uint64_t da1 = smem_desc_sw128(sa + kTileA);
-          const uint64_t db = smem_desc_sw128(sa + NA * kTileA);
+          const uint32_t a_addr = smem_u32(smem + st * G::kStageBytes);
+          const uint64_t da0 = smem_desc_sw128(a_addr);
+          const uint64_t da1 = smem_desc_sw128(a_addr + kTileA);
+          const uint64_t db = smem_desc_sw128(a_addr + NA * kTileA);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (ks | kk) ? 1u : 0u;
             umma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
             if (NA == 2) umma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
-          umma_commit(&empty[s]);
+          umma_commit(&empty[st]);
         }
         if (!ok) break;
         umma_commit(&tfull[b]);
@@ -554,13 +610,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       // Normally the epilogue has consumed every committed accumulator.  On
       // an error path, wait (bounded) for the last commit so that no MMA is
       // still writing TMEM when it is released.
-      if (committed >= 0 && ld_relaxed_i32(p.err) != 0) {
-        // the sticky error makes mbar_wait return at once: poll directly
-        const uint64_t t0 = global_timer();
-        while (!mbar_test(&tfull[committed & 1], (committed >> 1) & 1) &&
-               global_timer() - t0 < tmo) {
-        }
-      }
+      if (committed >= 0 && ld_relaxed_i32(p.err) != 0)
+        drain_wait(&tfull[committed & 1], (committed >> 1) & 1, tmo);
     }
     __syncwarp();
   }
@@ -846,23 +897,36 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2-D fp16 map [rows][cols], box {64, 128} (128 rows of 128 bytes: one
 // K step of a B tile), 128B swizzle; rows past the end read as zero.
-bool encode_rows(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kNT};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over packed 4-bit codes [rows][bytes_per_row], box {32, 128}:
+// one K step (64 codes) of 128 weight rows, stored densely (32-byte rows).
+bool encode_codes(CUtensorMap* m, const void* base, uint64_t bytes_per_row, uint64_t rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {bytes_per_row, rows};
+  cuuint64_t strides[1] = {bytes_per_row};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE>
 moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_t s,
                        const char** why) {
-  constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
-  const size_t smem = (size_t)kStages * (NA * kTileA + kTileB) + 1024 + 256 + 8 * kNT;
+  const size_t smem = (size_t)Gemm<MODE>::kSmem;
   auto kern = moe_gemm_kernel<MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
@@ -872,7 +936,23 @@ moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_
   static const char* const names[3] = {"moe_gemm_gateup_swiglu", "moe_gemm_down_scatter",
                                        "moe_gemm_router"};
   prof::Scope scope(names[MODE], s);
-  kern<<<grid, Roles<MODE>::kThreads, smem, s>>>(gp, L->tmap_x16, L->tmap_hr, L->tmap_hs);
+  GemmMaps maps;
+  if (MODE == kSwiglu) {
+    maps.a_routed[0] = L->tmap_gate;
+    maps.a_routed[1] = L->tmap_up;
+    maps.a_shared[0] = L->tmap_sh_gate;
+    maps.a_shared[1] = L->tmap_sh_up;
+    maps.b[0] = maps.b[1] = L->tmap_x16;  // unused: gate/up gathers with cp.async
+  } else if (MODE == kScatter) {
+    maps.a_routed[0] = maps.a_routed[1] = L->tmap_down;
+    maps.a_shared[0] = maps.a_shared[1] = L->tmap_sh_down;
+    maps.b[0] = L->tmap_hr;
+    maps.b[1] = L->tmap_hs;
+  } else {
+    maps.a_routed[0] = maps.a_routed[1] = maps.a_shared[0] = maps.a_shared[1] = L->tmap_gate;
+    maps.b[0] = maps.b[1] = L->tmap_x16;
+  }
+  kern<<<grid, Gemm<MODE>::kThreads, smem, s>>>(gp, maps);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = cudaGetErrorString(e);
@@ -913,9 +993,19 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   w.max_dn_units = z.max_dn;
   const uint64_t Tm = c.max_tokens;
   const uint64_t Fs = c.shared_ffn ? c.shared_ffn : 128;
+  // packed-code maps; without a shared expert its maps alias the routed ones
+  const LayerDev& d = L->dev;
+  const uint64_t S = c.n_slots, H = c.hidden, F = c.ffn;
+  const bool sh = c.shared_ffn > 0;
   if (!encode_rows(&L->tmap_x16, w.x16, c.hidden, Tm) ||
       !encode_rows(&L->tmap_hr, w.hmid_r, c.ffn, Tm * c.top_k) ||
-      !encode_rows(&L->tmap_hs, w.hmid_s, Fs, Tm)) {
+      !encode_rows(&L->tmap_hs, w.hmid_s, Fs, Tm) ||
+      !encode_codes(&L->tmap_gate, d.gate_q, H / 2, S * F) ||
+      !encode_codes(&L->tmap_up, d.up_q, H / 2, S * F) ||
+      !encode_codes(&L->tmap_down, d.down_q, F / 2, S * H) ||
+      !encode_codes(&L->tmap_sh_gate, sh ? d.sh_gate_q : d.gate_q, H / 2, sh ? Fs : F) ||
+      !encode_codes(&L->tmap_sh_up, sh ? d.sh_up_q : d.up_q, H / 2, sh ? Fs : F) ||
+      !encode_codes(&L->tmap_sh_down, sh ? d.sh_down_q : d.down_q, sh ? Fs / 2 : F / 2, H)) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable?)";
     return MOE_ERR_CUDA;
   }
