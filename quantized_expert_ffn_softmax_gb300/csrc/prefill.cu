@@ -56,7 +56,7 @@ constexpr int kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBWarp0 = 12;
 constexpr int kBucketThreads = 1024;
-constexpr int kScalePrefetch = 8;  // K steps of block scales each producer keeps in flight
+constexpr int kScaleLead = 3;      // K steps of block scales the raw loader loads ahead
 constexpr int kBLag = 2;           // K steps of gathered token rows each B loader keeps in flight
 
 enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
@@ -78,13 +78,13 @@ template <int MODE>
 struct Gemm {
   static constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
   static constexpr int S = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 5 : 6);
-  static constexpr int SR = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 12 : 0);
+  static constexpr int SR = (MODE == kSwiglu) ? 3 : (MODE == kScatter ? 12 : 0);
   static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
   static constexpr int kBWarps = (MODE == kSwiglu) ? 2 : 1;
   static constexpr int kRawWarp = kBWarp0 + kBWarps;
   static constexpr int kMmaWarp = kRawWarp + (SR > 0 ? 1 : 0);
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
-  static constexpr int kRawBytes = NA * kRawTile;
+  static constexpr int kRawBytes = NA * (kRawTile + 128 * 4);  // codes, then scales
   static constexpr int kStageBytes = NA * kTileA + kTileB;  // A tiles, then the B tile
   static constexpr int OFF_RAW = S * kStageBytes;
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
@@ -94,6 +94,10 @@ struct Gemm {
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
+  // A producers take K steps in groups of kGroup (a divisor of every K/64);
+  // pairs halve the per-step overhead where the raw ring is deep enough
+  static constexpr int kGroup = (MODE == kScatter) ? 2 : 1;
+  static_assert(MODE == kRouter || (S >= 2 * kGroup && SR >= 2 * kGroup), "ring depth per group");
 };
 
 // Tensor maps of one GEMM launch.
@@ -306,8 +310,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       const UnitInfo U = unit_info<MODE>(p, u);
       const int nks = U.K / 64;
       if constexpr (MODE != kRouter) {
-        // Codes come from the raw ring (one TMA tile per matrix per K step);
-        // scales (4 bytes per row and K step) ride in a register ring.
+        // Codes and block scales come from the raw ring, filled by the raw
+        // loader warp (codes: one TMA tile per matrix; scales: one 32-bit
+        // word per row holding the step's two fp16 block scales).
         //   gate/up: thread = (matrix part, row r), all 64 K of the step
         //   down:    thread = (K half part, row r); lanes 8i..8i+7 read four
         //            whole 32-byte rows, so the shared reads do not conflict
@@ -319,97 +324,80 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           r = ((pi >> 3) << 2) | (pi & 3);
           part = (pi >> 2) & 1;
         }
-        const uint16_t* sc;
-        int sstride;  // scale entries per row
-        if (MODE == kSwiglu) {
-          const int f = U.mt * 128 + r;
-          sstride = p.H / 32;
-          if (U.shared) {
-            sc = (part ? Wd.sh_up_s : Wd.sh_gate_s) + (size_t)f * sstride;
-          } else {
-            const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
-            sc = (part ? Wd.up_s : Wd.gate_s) + (slot * p.F + f) * sstride;
-          }
-        } else {
-          const int i = U.mt * 128 + r;  // output row of H
-          sstride = U.K / 32;
-          if (U.shared) {
-            sc = Wd.sh_down_s + (size_t)i * sstride;
-          } else {
-            const size_t slot = (size_t)__ldg(Wd.slot_of + U.e);
-            sc = Wd.down_s + (slot * p.H + i) * sstride;
-          }
-        }
-        uint32_t cs[kScalePrefetch];
-#pragma unroll
-        for (int i = 0; i < kScalePrefetch; ++i)
-          if (i < nks)
-            cs[i] = (MODE == kSwiglu) ? __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * i))
-                                      : (uint32_t)__ldg(sc + 2 * i + part);
         const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
-        for (int ks0 = 0; ks0 < nks && alive; ks0 += kScalePrefetch) {
+        // K steps go in groups of P (nks is even): one set of waits, one
+        // proxy fence and one round of hand-backs per group
+        constexpr int P = G::kGroup;
+        for (int ks = 0; ks < nks && alive; ks += P) {
+          bool ok = true;
+          uint4 ca[P], cb[P];
+          uint32_t sw[P];  // each step's two block scales of this row
 #pragma unroll
-          for (int i = 0; i < kScalePrefetch; ++i) {
-            const int ks = ks0 + i;
-            if (ks < nks && alive) {
-              const int sr = it % SR, st = it % S;
-              bool ok = true;
-              if (lane == 0) ok = mbar_wait(&raw_full[sr], (it / SR) & 1, p.err, tmo);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
-              if (ok) (void)mbar_test(&raw_full[sr], (it / SR) & 1);  // every lane acquires
-              uint4 ca, cb;
-              if (ok) {
-                const unsigned char* rs = sR + sr * G::kRawBytes;
-                if (MODE == kSwiglu) {
-                  const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
-                  const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
-                  ca = h ? q1 : q0;
-                  cb = h ? q0 : q1;
-                } else {
-                  ca = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
-                  cb = ca;
-                }
-                // generic-proxy reads of a buffer that TMA (async proxy) will
-                // overwrite: fence them before the stage is handed back
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[sr]);
-                if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-              }
-              if (!ok) {
-                alive = false;
+          for (int q = 0; q < P; ++q) {
+            const uint32_t iq = it + q;
+            const int sr = iq % SR;
+            if (lane == 0 && ok) ok = mbar_wait(&raw_full[sr], (iq / SR) & 1, p.err, tmo);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) {
+              (void)mbar_test(&raw_full[sr], (iq / SR) & 1);  // every lane acquires
+              const unsigned char* rs = sR + sr * G::kRawBytes;
+              sw[q] = reinterpret_cast<const uint32_t*>(rs + NA * kRawTile)[(MODE == kSwiglu ? part * 128 : 0) + r];
+              if (MODE == kSwiglu) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
+                ca[q] = h ? q1 : q0;
+                cb[q] = h ? q0 : q1;
               } else {
-                unsigned char* tile = smem + st * G::kStageBytes;
-                if (MODE == kSwiglu) {
-                  tile += part * kTileA;
-                  const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(cs[i] & 0xffffu)));
-                  const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(cs[i] >> 16)));
-                  st_tile_chunk(tile, r, 0, dequant_word(ca.x, slo));
-                  st_tile_chunk(tile, r, 1, dequant_word(ca.y, slo));
-                  st_tile_chunk(tile, r, 2, dequant_word(ca.z, slo));
-                  st_tile_chunk(tile, r, 3, dequant_word(ca.w, slo));
-                  st_tile_chunk(tile, r, 4, dequant_word(cb.x, shi));
-                  st_tile_chunk(tile, r, 5, dequant_word(cb.y, shi));
-                  st_tile_chunk(tile, r, 6, dequant_word(cb.z, shi));
-                  st_tile_chunk(tile, r, 7, dequant_word(cb.w, shi));
-                } else {
-                  const __half2 s2 = __half2half2(__ushort_as_half((uint16_t)cs[i]));
-                  st_tile_chunk(tile, r, part * 4 + 0, dequant_word(ca.x, s2));
-                  st_tile_chunk(tile, r, part * 4 + 1, dequant_word(ca.y, s2));
-                  st_tile_chunk(tile, r, part * 4 + 2, dequant_word(ca.z, s2));
-                  st_tile_chunk(tile, r, part * 4 + 3, dequant_word(ca.w, s2));
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&full_a[st]);
-                ++it;
-                const int kn = ks + kScalePrefetch;
-                if (kn < nks)
-                  cs[i] = (MODE == kSwiglu) ? __ldg(reinterpret_cast<const uint32_t*>(sc + 2 * kn))
-                                            : (uint32_t)__ldg(sc + 2 * kn + part);
+                ca[q] = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
+                cb[q] = ca[q];
               }
             }
           }
+#pragma unroll
+          for (int q = 0; q < P; ++q) {
+            const uint32_t iq = it + q;
+            if (lane == 0 && ok) ok = mbar_wait(&empty[iq % S], ((iq / S) & 1) ^ 1, p.err, tmo);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
+          if (!ok) {
+            alive = false;
+            break;
+          }
+#pragma unroll
+          for (int q = 0; q < P; ++q) {
+            unsigned char* tile = smem + ((it + q) % S) * G::kStageBytes;
+            if (MODE == kSwiglu) {
+              tile += part * kTileA;
+              const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sw[q] & 0xffffu)));
+              const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sw[q] >> 16)));
+              st_tile_chunk(tile, r, 0, dequant_word(ca[q].x, slo));
+              st_tile_chunk(tile, r, 1, dequant_word(ca[q].y, slo));
+              st_tile_chunk(tile, r, 2, dequant_word(ca[q].z, slo));
+              st_tile_chunk(tile, r, 3, dequant_word(ca[q].w, slo));
+              st_tile_chunk(tile, r, 4, dequant_word(cb[q].x, shi));
+              st_tile_chunk(tile, r, 5, dequant_word(cb[q].y, shi));
+              st_tile_chunk(tile, r, 6, dequant_word(cb[q].z, shi));
+              st_tile_chunk(tile, r, 7, dequant_word(cb[q].w, shi));
+            } else {
+              const __half2 s2 =
+                  __half2half2(__ushort_as_half((uint16_t)(part ? sw[q] >> 16 : sw[q] & 0xffffu)));
+              st_tile_chunk(tile, r, part * 4 + 0, dequant_word(ca[q].x, s2));
+              st_tile_chunk(tile, r, part * 4 + 1, dequant_word(ca[q].y, s2));
+              st_tile_chunk(tile, r, part * 4 + 2, dequant_word(ca[q].z, s2));
+              st_tile_chunk(tile, r, part * 4 + 3, dequant_word(ca[q].w, s2));
+            }
+          }
+          // one proxy fence orders both this thread's tile writes (read next
+          // by the tensor core) and its reads of the raw stages (overwritten
+          // next by TMA) before the hand-backs
+          fence_proxy_async_smem();
+#pragma unroll
+          for (int q = 0; q < P; ++q) mbar_arrive(&full_a[(it + q) % S]);
+          __syncwarp();
+          if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < P; ++q) mbar_arrive(&raw_empty[(it + q) % SR]);
+          it += P;
         }
       } else {
         // router: rows are experts; K' = 2H; step ks < H/64 writes the fp16
@@ -539,33 +527,83 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       __syncwarp();
     }
   } else if (warp < kMmaWarp) {
-    // ------------------------------------------------------------ raw code loader
-    // One TMA tile (128 rows x 32 bytes of packed codes) per matrix and K step.
-    if constexpr (SR > 0) if (lane == 0) {
+    // ------------------------------------------------------------ raw loader
+    // Per K step and matrix: lane 0 issues one TMA tile of packed codes (128
+    // rows x 32 bytes); every lane stages the block scales of four rows (one
+    // 32-bit word per row: the step's two fp16 scales) from a register ring
+    // loaded kScaleLead steps ahead.  The scale stores precede lane 0's
+    // arrive on raw_full, which publishes them together with the codes.
+    if constexpr (SR > 0) {
       uint32_t it = 0;
       bool alive = true;
+      const LayerDev& Wd = p.W;
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
         const UnitInfo U = unit_info<MODE>(p, u);
-        const int slot = U.shared ? 0 : __ldg(p.W.slot_of + U.e);
+        const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
         const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
         const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * 128;
         const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
         const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
+        const int C = U.K / 32;  // scales per weight row
+        const uint16_t* sb[NA];  // this lane's first row of scales, per matrix
+        if (MODE == kSwiglu) {
+          sb[0] = (U.shared ? Wd.sh_gate_s : Wd.gate_s) + ((size_t)row + lane) * C;
+          if (NA == 2) sb[NA - 1] = (U.shared ? Wd.sh_up_s : Wd.up_s) + ((size_t)row + lane) * C;
+        } else {
+          sb[0] = (U.shared ? Wd.sh_down_s : Wd.down_s) + ((size_t)row + lane) * C;
+        }
+        const size_t rstep = (size_t)32 * C;  // 32 rows further
         const int nks = U.K / 64;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int sr = it % SR;
-          if (!mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo)) {
-            alive = false;
-            break;
+        uint32_t sv[kScaleLead][NA * 4];
+#pragma unroll
+        for (int d = 0; d < kScaleLead; ++d)
+          if (d < nks)
+#pragma unroll
+            for (int m = 0; m < NA; ++m)
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                sv[d][m * 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(sb[m] + j * rstep + 2 * d));
+        for (int ks0 = 0; ks0 < nks && alive; ks0 += kScaleLead) {
+#pragma unroll
+          for (int d = 0; d < kScaleLead; ++d) {
+            const int ks = ks0 + d;
+            if (ks < nks && alive) {
+              const int sr = it % SR;
+              bool ok = true;
+              if (lane == 0) ok = mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) {
+                alive = false;
+              } else {
+                unsigned char* dst = sR + sr * G::kRawBytes;
+                uint32_t* sdst = reinterpret_cast<uint32_t*>(dst + NA * kRawTile);
+#pragma unroll
+                for (int m = 0; m < NA; ++m)
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) sdst[m * 128 + j * 32 + lane] = sv[d][m * 4 + j];
+                __syncwarp();
+                if (lane == 0) {
+                  mbar_expect_tx(&raw_full[sr], (uint32_t)(NA * kRawTile));
+                  tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
+                  if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
+                }
+                ++it;
+                const int kn = ks + kScaleLead;
+                if (kn < nks)
+#pragma unroll
+                  for (int m = 0; m < NA; ++m)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                      sv[d][m * 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(sb[m] + j * rstep + 2 * kn));
+              }
+            }
           }
-          mbar_expect_tx(&raw_full[sr], (uint32_t)G::kRawBytes);
-          unsigned char* dst = sR + sr * G::kRawBytes;
-          tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
-          if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
         }
       }
-      const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
-      for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
+      if (lane == 0) {
+        const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
+        for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
+      }
     }
     __syncwarp();
   } else {
