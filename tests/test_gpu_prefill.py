@@ -123,6 +123,16 @@ def test_prefill125b_chunk_sampled_parity(cuda_device):
         xd = to_dev(x)
         y = to_host_bits(layer.forward(xd))
         assert moe.moe_status_sync(layer.handle) == moe.MOE_OK
+        # repeated runs agree up to the order of the fp32 combine reductions
+        # (one bf16 rounding of each element, plus reordering noise): a
+        # pipeline race that hands a buffer back early shows up here as
+        # whole rows that differ
+        y0 = bf16_f64(y)
+        for _ in range(2):
+            yr = bf16_f64(to_host_bits(layer.forward(xd)))
+            assert moe.moe_status_sync(layer.handle) == moe.MOE_OK
+            bound = 2.0 ** -7 * np.abs(y0) + 1e-5 * np.abs(y0).max()
+            assert np.all(np.abs(yr - y0) <= bound), float(np.max(np.abs(yr - y0)))
         ids, w = layer.route(xd)
         ids, w = ids.cpu().numpy(), w.cpu().numpy()
         offs = np.zeros(cfg.n_experts + 1, np.int32)
