@@ -5,10 +5,10 @@
 //            router GEMV (fp32) over this CTA's experts, whose W_r rows
 //            were prefetched into shared memory during the previous layer
 //   barrier
-//   top-k    two levels: every warp selects the top-k of one slice of the
-//            experts, one warp per token merges the slices; softmax over
-//            the selection; the expert-unit list.  Computed redundantly by
-//            every CTA.  Then the CTA starts the bulk copies (TMA) of the
+//   top-k    ranking, not serial selection: every warp ranks its slice of
+//            the logits with warp shuffles, the slices' top-k candidates
+//            rank each other in shared memory; softmax over the selection;
+//            the expert-unit list.  Computed redundantly by every CTA.  Then the CTA starts the bulk copies (TMA) of the
 //            expert weights it reads in this layer: the gate/up rows of its
 //            first items and the down rows of its output rows, with their
 //            block-scale tiles
@@ -146,59 +146,67 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
   return v[0];
 }
 
-// Monotonic 32-bit key of a float (larger float -> larger key, > 0); NaN -> 0.
+// Monotonic 32-bit key of a float (larger float -> larger key, > 0); NaN -> 0;
+// -0 and +0 get the same key (they compare equal).
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f != f) return 0u;
-  const uint32_t b = __float_as_uint(f);
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// k rounds of selection over NJ candidates per lane (keys, ids), descending
-// by key, ties to the lower id; key 0 marks an empty candidate.  Lane r < k
-// receives the r-th (key, id); (0, -1) when fewer than k candidates exist.
-template <int NJ>
-__device__ __forceinline__ void warp_select(uint32_t (&key)[NJ], const int (&id)[NJ], int k,
-                                            uint32_t* out_key, int* out_id) {
-  const int lane = threadIdx.x & 31;
-  uint32_t bk = 0u;
-  int bi = 0x7fffffff, bj = 0;
+// Top-k of T tokens' logits by the whole CTA, by ranking instead of serial
+// selection rounds.  Level 1: thread (warp w, lane) holds the logits
+// e = 32w + lane + 256j, j < NPL, of each token and counts, with 32 warp
+// shuffles per j, how many logits of its warp beat each of them (larger
+// value, or equal value and lower expert id); a logit of warp rank r < k
+// becomes candidate w*k + r.  Level 2: each of the 8k candidates of a token
+// counts the candidates that beat it (2 or 4 adjacent lanes share one
+// candidate, each scanning a quarter or half of the list); rank r < k is the
+// r-th selection.
+// A candidate is the 64-bit key (order_key(z) << 32) | ~e (0 = empty), so
+// candidates compare as plain integers and never tie.
+template <int NPL>
+__device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
+                                            uint64_t (*cand)[kWarps * kMaxTopK]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t key[kMaxDecodeTokens][NPL];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
-      bk = key[j];
-      bi = id[j];
-      bj = j;
+  for (int t = 0; t < kMaxDecodeTokens; ++t)
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = 32 * warp + lane + 256 * j;
+      key[t][j] = (t < T && e < E) ? order_key(__ldcg(z + (size_t)t * E + e)) : 0u;
     }
-  uint32_t mk = 0u;
-  int mi = -1;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = (bk == gk && gk != 0u) ? (uint32_t)bi : 0xffffffffu;
-    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-    if (lane == r) {
-      mk = gk;
-      mi = (win == 0xffffffffu) ? -1 : (int)win;
-    }
-    if (gk != 0u && cand == win) {  // this lane holds the winner: take it, find its next best
 #pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (j == bj) key[j] = 0u;
-      bk = 0u;
-      bi = 0x7fffffff;
+  for (int t = 0; t < kMaxDecodeTokens; ++t) {
+    if (t >= T) break;
+    int rank[NPL];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
-          bk = key[j];
-          bi = id[j];
-          bj = j;
+    for (int j = 0; j < NPL; ++j) rank[j] = 0;
+#pragma unroll 8
+    for (int src = 0; src < 32; ++src) {
+#pragma unroll
+      for (int jj = 0; jj < NPL; ++jj) {
+        const uint32_t ks = __shfl_sync(0xffffffffu, key[t][jj], src);
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+          // logit (src, jj) has the lower expert id iff jj < j, or jj == j and src < lane
+          const bool lower_id = (jj < j) || (jj == j && src < lane);
+          rank[j] += (ks > key[t][j] || (ks == key[t][j] && lower_id)) ? 1 : 0;
         }
+      }
     }
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (rank[j] < k) {
+        const uint32_t e = (uint32_t)(32 * warp + lane + 256 * j);
+        cand[t][warp * k + rank[j]] = key[t][j] ? (((uint64_t)key[t][j] << 32) | (uint64_t)(~e)) : 0ull;
+      }
   }
-  *out_key = mk;
-  *out_id = mi;
 }
 
 }  // namespace
@@ -258,6 +266,8 @@ struct DecodeMisc {
   int pad0[2];
   int sel_id[kMaxDecodeTokens][kMaxTopK];
   float sel_w[kMaxDecodeTokens][kMaxTopK];
+  uint64_t cand[kMaxDecodeTokens][kWarps * kMaxTopK];  // top-k level-1 candidates, w*k + r
+  uint64_t sel_key[kMaxDecodeTokens][kMaxTopK];       // top-k level-2 result
   int unit_expert[kMaxUnits];
   int unit_slot[kMaxUnits];
   float unit_w[kMaxUnits][kMaxDecodeTokens];
@@ -265,8 +275,7 @@ struct DecodeMisc {
   int prefix[kMaxExperts / 32 + 1];
   float red_ss[kWarps][4];
   float red_mx[kWarps][4];
-  uint32_t cand_key[kWarps][kMaxTopK];  // top-k level 1: per-warp selections
-  int cand_id[kWarps][kMaxTopK];
+  float red_z[kWarps][4];
 };
 static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 
@@ -339,26 +348,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint16_t* xsrc = (l == 0) ? p.x_in : (p.xbuf + (size_t)(l & 1) * kMaxDecodeTokens * H);
 
     // ------------------------------------------------ phase R: stage x, router
+    // pass 1: stage x (8 bf16 per thread and step) and take its sum of
+    // squares (stacks) and max |x| from the registers
     uint16_t* stage_dst = stack ? hres : xb;
-    for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
-      const int t = i / (H / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = __ldcg(reinterpret_cast<const uint4*>(xsrc + (size_t)t * H) + (i - t * (H / 8)));
-      reinterpret_cast<uint4*>(stage_dst)[i] = v;
-    }
-    __syncthreads();
     {
-      // one pass: sum of squares (stacks) and max |x| of the staged rows
       float ss[TT], mx[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) ss[t] = mx[t] = 0.0f;
-      for (int i = tid; i < H; i += kDecodeThreads) {
+      for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
+        const int t = i / (H / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < T) v = __ldcg(reinterpret_cast<const uint4*>(xsrc + (size_t)t * H) + (i - t * (H / 8)));
+        reinterpret_cast<uint4*>(stage_dst)[i] = v;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float a = 0.0f, m = 0.0f;
 #pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          const float v = __bfloat162float(__ushort_as_bfloat16(stage_dst[t * H + i]));
-          ss[t] = fmaf(v, v, ss[t]);
-          mx[t] = fmaxf(mx[t], fabsf(v));
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+          a = fmaf(lo, lo, fmaf(hi, hi, a));
+          m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
         }
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt)
+          if (tt == t) {
+            ss[tt] += a;
+            mx[tt] = fmaxf(mx[tt], m);
+          }
       }
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
@@ -385,54 +400,71 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         sc[t] = pow2f(-s);
         if (tid == 0) M.x_shift[t] = s;
       }
-      if (stack) {
-        for (int i = tid; i < TT * H; i += kDecodeThreads) {
-          const int t = i / H;
-          float v = __bfloat162float(__ushort_as_bfloat16(hres[i]));
-#pragma unroll
-          for (int tt = 0; tt < TT; ++tt)
-            if (tt == t) v *= inv[tt];
-          xb[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-        }
-        __syncthreads();
-        if (blockIdx.x == 0 && p.in_trace)
-          for (int i = tid; i < T * H; i += kDecodeThreads) p.in_trace[(size_t)l * T * H + i] = xb[i];
-      }
-      // fp16 pair planes: xp[(t*4 + q)*C + c] = pairs (x[32c+8q+j], x[32c+8q+j+4]), j < 4
-      for (int i = tid; i < TT * C * 4; i += kDecodeThreads) {
-        const int t = i / (4 * C);
-        const int rem = i - t * 4 * C;
-        const int q = rem / C;
-        const int c = rem - q * C;
-        float sc_t = 1.0f;
+      // pass 2, one 8-group (32c + 8q .. +7) per step: u (stacks) and the
+      // fp16 pair planes xp[(t*4 + q)*C + c] = pairs (x[32c+8q+j], x[32c+8q+j+4])
+      for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
+        const int t = i / (H / 8), g = i - t * (H / 8);
+        float inv_t = 1.0f, sc_t = 1.0f;
 #pragma unroll
         for (int tt = 0; tt < TT; ++tt)
-          if (tt == t) sc_t = sc[tt];
-        const uint16_t* src = xb + t * H + 32 * c + 8 * q;
+          if (tt == t) {
+            inv_t = inv[tt];
+            sc_t = sc[tt];
+          }
+        const uint4 v = reinterpret_cast<const uint4*>(stage_dst)[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float e[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          e[2 * q] = __uint_as_float(w[q] << 16);
+          e[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+        }
+        if (stack) {
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat16 lo = __float2bfloat16_rn(e[2 * q] * inv_t);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(e[2 * q + 1] * inv_t);
+            e[2 * q] = __bfloat162float(lo);
+            e[2 * q + 1] = __bfloat162float(hi);
+            o[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+          }
+          const uint4 u = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(xb)[i] = u;
+          if (blockIdx.x == 0 && p.in_trace && t < T)
+            reinterpret_cast<uint4*>(p.in_trace + ((size_t)l * T + t) * H)[g] = u;
+        }
         uint32_t out[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float a = __bfloat162float(__ushort_as_bfloat16(src[j])) * sc_t;
-          float b = __bfloat162float(__ushort_as_bfloat16(src[j + 4])) * sc_t;
-          __half2 hh = __floats2half2_rn(a, b);
+          __half2 hh = __floats2half2_rn(e[j] * sc_t, e[j + 4] * sc_t);
           out[j] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        xp[(t * 4 + q) * C + c] = make_uint4(out[0], out[1], out[2], out[3]);
+        xp[(t * 4 + (g & 3)) * C + (g >> 2)] = make_uint4(out[0], out[1], out[2], out[3]);
       }
+      __syncthreads();
     }
-    // router: warp j computes the logits of this CTA's j-th expert from the
-    // prefetched W_r row
+    // router: this CTA's expert rows e = blockIdx + j*grid (prefetched W_r
+    // rows); row j is split over the warps w with w % my_rows == j, each
+    // summing one slice of H; the slices meet in shared memory
+    // this thread's router bias (read before the row wait, off the critical path)
+    const float bias_mine = (tid < min(my_rows, kWarps) * T)
+                                ? __ldg(W.router_b + blockIdx.x + (tid / T) * grid) : 0.0f;
     if (my_rows > 0 || slots_bulk_of(l)) {  // the R barrier was armed for this layer
       mbar_wait(&mbar[kBarR], ph_r, p.err, tmo);
       ph_r ^= 1u;
     }
-    for (int j = warp; j < my_rows; j += kWarps) {
-      const int e = blockIdx.x + j * grid;
-      const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)j * H);
+    for (int j0 = 0; j0 < my_rows; j0 += kWarps) {  // batches of at most kWarps rows
+      const int nr = min(kWarps, my_rows - j0);
+      const int j = warp % nr, part = warp / nr;
+      const int nparts = (kWarps - j + nr - 1) / nr;
+      const int n4 = H / 4, chunk = (n4 + nparts - 1) / nparts;
+      const int i0 = part * chunk, i1 = min(n4, i0 + chunk);
+      const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)(j0 + j) * H);
       float acc[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-      for (int idx = lane; idx < H / 4; idx += 32) {
+      for (int idx = i0 + lane; idx < i1; idx += 32) {
         const float4 wv = wrow[idx];
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
@@ -446,54 +478,53 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         const float s = warp_sum(acc[t]);
-        if (lane == 0 && t < T) p.z[(size_t)t * E + e] = s + __ldg(W.router_b + e);
+        if (lane == 0) M.red_z[warp][t] = s;
       }
+      __syncthreads();
+      if (tid < nr * T) {
+        const int jr = tid / T, t = tid - (tid / T) * T;
+        float z = 0.0f;
+        for (int w = jr; w < kWarps; w += nr) z += M.red_z[w][t];
+        const int e = blockIdx.x + (j0 + jr) * grid;
+        p.z[(size_t)t * E + e] = z + (j0 == 0 ? bias_mine : __ldg(W.router_b + e));
+      }
+      __syncthreads();  // red_z is reused by the next batch
     }
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
 
     // ------------------------------------------------ top-k + softmax + units
+    // (every CTA computes it redundantly from the logits in L2)
+    if (tid < kMaxDecodeTokens * kMaxTopK) (&M.sel_key[0][0])[tid] = 0ull;
+    if (E <= 256) topk_level1<1>(p.z, T, E, k, M.cand);
+    else if (E <= 512) topk_level1<2>(p.z, T, E, k, M.cand);
+    else topk_level1<4>(p.z, T, E, k, M.cand);
+    __syncthreads();
     {
-      // level 1: the warps of token t each select the top-k of one slice
-      constexpr int G = kWarps / TT;  // warps per token
-      constexpr int NJ1 = 4 * TT;     // logits per lane, E <= 1024
-      const int t = warp / G, g = warp - (warp / G) * G;
-      const int seg = (E + G - 1) / G;
-      const int e0 = g * seg;
-      uint32_t key[NJ1];
-      int id[NJ1];
-#pragma unroll
-      for (int j = 0; j < NJ1; ++j) {
-        const int e = e0 + lane + 32 * j;
-        const bool in = t < T && lane + 32 * j < seg && e < E;
-        key[j] = in ? order_key(__ldcg(p.z + (size_t)t * E + e)) : 0u;
-        id[j] = e;
-      }
-      uint32_t ok1;
-      int oi1;
-      warp_select<NJ1>(key, id, k, &ok1, &oi1);
-      if (lane < k) {
-        M.cand_key[warp][lane] = ok1;
-        M.cand_id[warp][lane] = oi1;
+      const int nc = kWarps * k;                // candidates per token
+      const int ncp = nc <= 64 ? 64 : 128;      // padded with empty entries
+      const int P = kDecodeThreads / ncp;       // lanes per candidate: 4 or 2
+      const int c = tid / P, part = tid - (tid / P) * P;
+      const int per = ncp / P;                  // entries each lane scans: 16 or 64
+      for (int t = 0; t < T; ++t) {
+        const uint64_t mine = (c < nc) ? M.cand[t][c] : 0ull;
+        int r = 0;
+        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(&M.cand[t][part * per]);
+#pragma unroll 4
+        for (int q = 0; q < per / 2; ++q) {
+          const ulonglong2 o = src[q];
+          r += (part * per + 2 * q < nc && o.x > mine) ? 1 : 0;
+          r += (part * per + 2 * q + 1 < nc && o.y > mine) ? 1 : 0;
+        }
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        if (P == 4) r += __shfl_xor_sync(0xffffffffu, r, 2);
+        if (part == 0 && c < nc && r < k && mine != 0ull) M.sel_key[t][r] = mine;
       }
     }
     __syncthreads();
     if (warp < T) {
-      // level 2: warp t merges the G slices of token t
-      constexpr int G = kWarps / TT;
-      constexpr int NJ2 = (G * kMaxTopK + 31) / 32;
-      uint32_t key[NJ2];
-      int id[NJ2];
-#pragma unroll
-      for (int j = 0; j < NJ2; ++j) {
-        const int c = lane + 32 * j;  // candidate c = (slice c / k, rank c % k)
-        const bool in = c < G * k;
-        const int wsrc = warp * G + (in ? c / k : 0), r = in ? c - (c / k) * k : 0;
-        key[j] = in ? M.cand_key[wsrc][r] : 0u;
-        id[j] = in ? M.cand_id[wsrc][r] : 0x7fffffff;
-      }
-      uint32_t ok2;
-      int oi2;
-      warp_select<NJ2>(key, id, k, &ok2, &oi2);
+      const uint64_t sk = (lane < k) ? M.sel_key[warp][lane] : 0ull;
+      uint32_t ok2 = (uint32_t)(sk >> 32);
+      int oi2 = (sk != 0ull) ? (int)(~(uint32_t)sk) : -1;
       const bool bad = (lane < k) && (ok2 == 0u || oi2 < 0 || oi2 >= E);
       if (__any_sync(0xffffffffu, bad)) {  // only reachable with non-finite logits
         if (lane == 0) atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
