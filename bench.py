@@ -26,6 +26,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -71,7 +72,12 @@ def prefill_flops(cfg, T) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """nvidia-smi sampling (every 50 ms) of SM clocks and throttle reasons.
+
+    Started before the warm-up so that it is running when the timed region
+    begins; each sample is stamped with the host time it arrived, and the
+    summary keeps only the samples taken between mark_start() and
+    mark_stop() (the timed region)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -80,29 +86,53 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.rows = []
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
+            t_end = time.time() + 5.0
+            while not self.rows and time.time() < t_end:  # running before timing starts
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                self.out = ""
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
     def summary(self):
-        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        rows = []
+        for t, line in self.rows:
+            if self.t0 is not None and self.t1 is not None and not (self.t0 <= t <= self.t1 + 0.06):
+                continue
+            r = next(csv.reader(io.StringIO(line)), [])
+            if len(r) >= 9:
+                rows.append(r)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -197,7 +227,7 @@ def build_stack(cfg, max_tokens):
     return layers
 
 
-def time_steps(fn, steps, warmup, dist, ring_len):
+def time_steps(fn, steps, warmup, dist, ring_len, clk=None):
     import torch
 
     for i in range(warmup):
@@ -206,11 +236,15 @@ def time_steps(fn, steps, warmup, dist, ring_len):
     dist.barrier()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.mark_start()
     s.record()
     for i in range(steps):
         fn((warmup + i) % ring_len)
     e.record()
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark_stop()
     dist.barrier()
     torch.cuda.synchronize()
     return dist.max(s.elapsed_time(e) / steps)
@@ -259,7 +293,7 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
         moe.moe_stack_forward(hs, L, ring[i], T, y)
 
     with ClockSampler(dist.local) as clk:
-        ms = time_steps(step, steps, warmup, dist, len(ring))
+        ms = time_steps(step, steps, warmup, dist, len(ring), clk)
     prof = kernel_profile(step, min(steps, 50), len(ring))
     assert moe.moe_status_sync(hs[0]) == moe.MOE_OK
     kcount, kms = prof.get("moe_decode_kernel", (0, 0.0))
@@ -311,7 +345,8 @@ def bench_prefill(name, steps, warmup, dist):
     def step(i):
         moe.moe_forward(layer.handle, xs[i], T, y)
 
-    ms = time_steps(step, steps, warmup, dist, 2)
+    with ClockSampler(dist.local) as clk:
+        ms = time_steps(step, steps, warmup, dist, 2, clk)
     prof = kernel_profile(step, min(steps, 20), 2)
     assert moe.moe_status_sync(layer.handle) == moe.MOE_OK
     # algorithmic FLOPs per GEMM kernel
@@ -337,7 +372,8 @@ def bench_prefill(name, steps, warmup, dist):
            "tflops_step": prefill_flops(cfg, T) / (ms / 1e3) / 1e12,
            "grouped_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
            "kernels": kern,
-           "launches_per_step": sum(v["launches"] for v in kern.values()) / max(1, min(steps, 20))}
+           "launches_per_step": sum(v["launches"] for v in kern.values()) / max(1, min(steps, 20)),
+           "clocks": clk.summary()}
     layer.close()
     torch.cuda.empty_cache()
     return out
@@ -411,7 +447,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
