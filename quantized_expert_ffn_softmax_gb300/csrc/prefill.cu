@@ -76,26 +76,41 @@ enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 // sub-partition holds more than four and a thread may use 128 registers.
 template <int MODE>
 struct Gemm {
+  // gate/up and down stage their dequantised A tiles in tensor memory (the
+  // MMA reads A from TMEM, B from shared memory); the router keeps A in
+  // shared memory.  TMEM columns: accumulators from 0, A stages from kACol0.
+  static constexpr bool kTmemA = (MODE != kRouter);
   static constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
-  static constexpr int S = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 5 : 6);
-  static constexpr int SR = (MODE == kSwiglu) ? 3 : (MODE == kScatter ? 12 : 0);
+  static constexpr int S = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 8 : 6);
+  static constexpr int SR = (MODE == kSwiglu) ? 12 : (MODE == kScatter ? 12 : 0);
   static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
+  static constexpr int kAccBufs = (MODE == kSwiglu) ? 1 : 2;
+  static constexpr int kAccCols = NA * 128;  // gate | up, or one accumulator
+  static constexpr int kACol0 = 256;
+  static constexpr int kACols = NA * 32;     // 64 fp16 of K per matrix = 32 columns
+  static_assert(kAccBufs * kAccCols <= kACol0, "accumulators below the A stages");
+  static_assert(!kTmemA || kACol0 + S * kACols <= 512, "A stages fit in TMEM");
   static constexpr int kBWarps = (MODE == kSwiglu) ? 2 : 1;
   static constexpr int kRawWarp = kBWarp0 + kBWarps;
   static constexpr int kMmaWarp = kRawWarp + (SR > 0 ? 1 : 0);
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kRawBytes = NA * (kRawTile + 128 * 4);  // codes, then scales
-  static constexpr int kStageBytes = NA * kTileA + kTileB;  // A tiles, then the B tile
+  static constexpr int kBOff = kTmemA ? 0 : NA * kTileA;       // B tile offset in a stage
+  static constexpr int kStageBytes = kBOff + kTileB;
   static constexpr int OFF_RAW = S * kStageBytes;
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
   static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 4) + 4) + 127) & ~127;
   static constexpr int OFF_META = OFF_BAR + kBarBytes;
-  static constexpr int kSmem = OFF_META + 8 * kNT + 1024;  // + slack for 1 KB alignment
+  // gate/up: the unit's SwiGLU rows staged as fp16 [128 tokens][128 f] so the
+  // accumulator is released before the rows are written out
+  static constexpr int kHStage = (MODE == kSwiglu) ? kNT * 128 * 2 : 0;
+  static constexpr int OFF_HST = OFF_META + 8 * kNT;
+  static constexpr int kSmem = OFF_HST + kHStage + 1024;  // + slack for 1 KB alignment
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
   // A producers take K steps in groups of kGroup (a divisor of every K/64);
-  // pairs halve the per-step overhead where the raw ring is deep enough
+  // pairs halve the per-step overhead where the rings are deep enough
   static constexpr int kGroup = (MODE == kScatter) ? 2 : 1;
   static_assert(MODE == kRouter || (S >= 2 * kGroup && SR >= 2 * kGroup), "ring depth per group");
 };
@@ -196,6 +211,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
   // per-unit token metadata of the epilogue: two words per token column
   int* meta_i = reinterpret_cast<int*>(smem + G::OFF_META);
   float* meta_f = reinterpret_cast<float*>(meta_i + kNT);
+  __half* hst = reinterpret_cast<__half*>(smem + G::OFF_HST);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -253,24 +269,20 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           meta_f[r] = pow2f(__ldg(p.xshift + U.p0 + r) - p.router_shift);
         }
       }
-      const int b = j & 1;
+      const int b = (G::kAccBufs == 2) ? (j & 1) : 0;
+      const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&tfull[b], (j >> 1) & 1, p.err, tmo);
+      if (lane == 0) ok = mbar_wait(&tfull[b], tpar, p.err, tmo);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       // meta is ready, and the four warps agree on whether to go on (the
       // break must be uniform: the named barriers wait for all of them)
       if (!named_bar_and(1, kEpiWarps * 32, ok)) break;
       tc_fence_after();
       const int neff = (U.n + 15) & ~15;
-      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 256);
-      __half* hrow = nullptr;
-      size_t hstride = 0;
-      if (MODE == kSwiglu) {
-        const int f = U.mt * 128 + r;
-        const int q = (f & ~7) | ((f & 4) ? (((f & 3) << 1) | 1) : ((f & 3) << 1));
-        hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
-        hrow = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + q;
-      }
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * G::kAccCols);
+      // gate/up: column of row r inside the tile's 128 (8-groups in the
+      // unpack order 0,4,1,5,2,6,3,7, as the down GEMM's K expects)
+      const int qloc = (r & ~7) | ((r & 4) ? (((r & 3) << 1) | 1) : ((r & 3) << 1));
       constexpr int CW = (NA == 2) ? 16 : 32;  // columns per TMEM load
       for (int c0 = 0; c0 < neff; c0 += CW) {
         uint32_t v0[CW], v1[CW];
@@ -285,8 +297,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             const int sx = meta_i[t];
             const float g = __uint_as_float(v0[jj]) * pow2f(sx);
             const float uu = __uint_as_float(v1[jj]) * pow2f(sx);
-            const float h = __fdividef(g, 1.0f + __expf(-g)) * uu;
-            hrow[(size_t)t * hstride] = __float2half_rn(h * pow2f(-2 * sx));
+            const float h = silu_fast(g) * uu;
+            hst[t * 128 + qloc] = __float2half_rn(h * pow2f(-2 * sx));
           } else if (MODE == kScatter) {
             atomicAdd(p.yacc + (size_t)meta_i[t] * p.H + U.mt * 128 + r,
                       __uint_as_float(v0[jj]) * meta_f[t]);
@@ -299,6 +311,18 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[b]);
+      if (MODE == kSwiglu) {
+        // write the staged rows out (16-byte stores) while the MMAs of the
+        // next unit already run in the released accumulator
+        named_bar_sync(2, kEpiWarps * 32);
+        const size_t hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
+        __half* hbase = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + U.mt * 128;
+        for (int idx = r; idx < U.n * 16; idx += kEpiWarps * 32) {
+          const int t = idx >> 4, c = idx & 15;
+          *reinterpret_cast<uint4*>(hbase + (size_t)t * hstride + c * 8) =
+              *reinterpret_cast<const uint4*>(hst + t * 128 + c * 8);
+        }
+      }
     }
   } else if (warp < kProdWarp0 + kProdWarps) {
     // ------------------------------------------------------------ A producers
@@ -313,17 +337,12 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         // Codes and block scales come from the raw ring, filled by the raw
         // loader warp (codes: one TMA tile per matrix; scales: one 32-bit
         // word per row holding the step's two fp16 block scales).
-        //   gate/up: thread = (matrix part, row r), all 64 K of the step
-        //   down:    thread = (K half part, row r); lanes 8i..8i+7 read four
-        //            whole 32-byte rows, so the shared reads do not conflict
-        int r, part;
-        if (MODE == kSwiglu) {
-          r = pi & 127;
-          part = pi >> 7;
-        } else {
-          r = ((pi >> 3) << 2) | (pi & 3);
-          part = (pi >> 2) & 1;
-        }
+        //   gate/up: part = matrix, all 64 K of the step
+        //   down:    part = which 32-element half of the step
+        // thread = (part, row r), r = 32*(warp%4) + lane: the TMEM lane it
+        // writes (a warp reaches only its own quarter of the 128 lanes)
+        const int r = 32 * (warp & 3) + lane;
+        const int part = pi >> 7;
         const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
         // K steps go in groups of P (nks is even): one set of waits, one
         // proxy fence and one round of hand-backs per group
@@ -363,36 +382,49 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             alive = false;
             break;
           }
+          tc_fence_after();  // the MMAs that read these A stages are complete
+          const uint32_t arow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)G::kACol0;
 #pragma unroll
           for (int q = 0; q < P; ++q) {
-            unsigned char* tile = smem + ((it + q) % S) * G::kStageBytes;
+            const uint32_t acol = arow + (uint32_t)(((it + q) % S) * G::kACols);
             if (MODE == kSwiglu) {
-              tile += part * kTileA;
               const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sw[q] & 0xffffu)));
               const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sw[q] >> 16)));
-              st_tile_chunk(tile, r, 0, dequant_word(ca[q].x, slo));
-              st_tile_chunk(tile, r, 1, dequant_word(ca[q].y, slo));
-              st_tile_chunk(tile, r, 2, dequant_word(ca[q].z, slo));
-              st_tile_chunk(tile, r, 3, dequant_word(ca[q].w, slo));
-              st_tile_chunk(tile, r, 4, dequant_word(cb[q].x, shi));
-              st_tile_chunk(tile, r, 5, dequant_word(cb[q].y, shi));
-              st_tile_chunk(tile, r, 6, dequant_word(cb[q].z, shi));
-              st_tile_chunk(tile, r, 7, dequant_word(cb[q].w, shi));
+              const uint32_t wds[8] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w,
+                                       cb[q].x, cb[q].y, cb[q].z, cb[q].w};
+              uint32_t o[32];
+#pragma unroll
+              for (int w = 0; w < 8; ++w) {
+                const uint4 d = dequant_word(wds[w], w < 4 ? slo : shi);
+                o[4 * w] = d.x;
+                o[4 * w + 1] = d.y;
+                o[4 * w + 2] = d.z;
+                o[4 * w + 3] = d.w;
+              }
+              tmem_st32(acol + (uint32_t)(part * 32), o);
             } else {
               const __half2 s2 =
                   __half2half2(__ushort_as_half((uint16_t)(part ? sw[q] >> 16 : sw[q] & 0xffffu)));
-              st_tile_chunk(tile, r, part * 4 + 0, dequant_word(ca[q].x, s2));
-              st_tile_chunk(tile, r, part * 4 + 1, dequant_word(ca[q].y, s2));
-              st_tile_chunk(tile, r, part * 4 + 2, dequant_word(ca[q].z, s2));
-              st_tile_chunk(tile, r, part * 4 + 3, dequant_word(ca[q].w, s2));
+              const uint32_t wds[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
+              uint32_t o[16];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint4 d = dequant_word(wds[w], s2);
+                o[4 * w] = d.x;
+                o[4 * w + 1] = d.y;
+                o[4 * w + 2] = d.z;
+                o[4 * w + 3] = d.w;
+              }
+              tmem_st16(acol + (uint32_t)(part * 16), o);
             }
           }
-          // one proxy fence orders both this thread's tile writes (read next
-          // by the tensor core) and its reads of the raw stages (overwritten
-          // next by TMA) before the hand-backs
-          fence_proxy_async_smem();
+          tmem_wait_st();
+          tc_fence_before();
 #pragma unroll
           for (int q = 0; q < P; ++q) mbar_arrive(&full_a[(it + q) % S]);
+          // the raw stages were read through the generic proxy and are
+          // refilled by TMA (async proxy): fence before handing them back
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0)
 #pragma unroll
@@ -423,7 +455,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             alive = false;
             break;
           }
-          unsigned char* tile = smem + st * G::kStageBytes;
+          unsigned char* tile = smem + st * G::kStageBytes;  // router: A tile at the stage start
 #pragma unroll
           for (int g = 0; g < 4; ++g) {  // 8-element group g of this half
             const float a[8] = {v[2 * g].x, v[2 * g].y, v[2 * g].z, v[2 * g].w,
@@ -483,7 +515,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             alive = false;
             break;
           }
-          const uint32_t tile = smem_u32(smem + st * G::kStageBytes + NA * kTileA);
+          const uint32_t tile = smem_u32(smem + st * G::kStageBytes + G::kBOff);
 #pragma unroll
           for (int i = 0; i < RW / 4; ++i)
             if (dst[i] != 0xffffffffu) cp_async_16(tile + dst[i], p.x16 + src[i] + ks * 64);
@@ -517,7 +549,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             }
             mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
             const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-            tma_load_2d(smem + st * G::kStageBytes + NA * kTileA, tm, col, U.p0, &full_b[st]);
+            tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, &full_b[st]);
           }
         }
         // let every copy this thread issued land before the CTA can exit
@@ -614,10 +646,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
         const UnitInfo U = unit_info<MODE>(p, u);
         const int neff = (U.n + 15) & ~15;
-        const int b = j & 1;
-        if (!mbar_wait(&tempty[b], ((j >> 1) & 1) ^ 1, p.err, tmo)) break;
+        const int b = (G::kAccBufs == 2) ? (j & 1) : 0;
+        const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
+        if (!mbar_wait(&tempty[b], tpar ^ 1, p.err, tmo)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(b * 256), d1 = d0 + 128;
+        const uint32_t d0 = tmem + (uint32_t)(b * G::kAccCols), d1 = d0 + 128;
         const uint32_t idesc = idesc_f16_m128(neff);
         const int nks = U.K / 64;
         bool ok = true;
@@ -629,15 +662,23 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + st * G::kStageBytes);
-          const uint64_t da0 = smem_desc_sw128(a_addr);
-          const uint64_t da1 = smem_desc_sw128(a_addr + kTileA);
-          const uint64_t db = smem_desc_sw128(a_addr + NA * kTileA);
+          const uint32_t s_addr = smem_u32(smem + st * G::kStageBytes);
+          const uint64_t db = smem_desc_sw128(s_addr + G::kBOff);
+          if constexpr (G::kTmemA) {
+            const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (ks | kk) ? 1u : 0u;
-            umma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (NA == 2) umma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            for (int kk = 0; kk < 4; ++kk) {  // 16 K = 8 TMEM columns per MMA
+              const uint32_t acc = (ks | kk) ? 1u : 0u;
+              umma_f16_ts(d0, a0 + 8 * kk, db + 2 * kk, idesc, acc);
+              if (NA == 2) umma_f16_ts(d1, a0 + 32 + 8 * kk, db + 2 * kk, idesc, acc);
+            }
+          } else {
+            const uint64_t da0 = smem_desc_sw128(s_addr);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (ks | kk) ? 1u : 0u;
+              umma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            }
           }
           umma_commit(&empty[st]);
         }
@@ -648,8 +689,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       // Normally the epilogue has consumed every committed accumulator.  On
       // an error path, wait (bounded) for the last commit so that no MMA is
       // still writing TMEM when it is released.
-      if (committed >= 0 && ld_relaxed_i32(p.err) != 0)
-        drain_wait(&tfull[committed & 1], (committed >> 1) & 1, tmo);
+      if (committed >= 0 && ld_relaxed_i32(p.err) != 0) {
+        const int cb = (G::kAccBufs == 2) ? (committed & 1) : 0;
+        const uint32_t cp = (G::kAccBufs == 2) ? ((committed >> 1) & 1) : (committed & 1);
+        drain_wait(&tfull[cb], cp, tmo);
+      }
     }
     __syncwarp();
   }
