@@ -273,6 +273,13 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     int sh = 5 - ex;                             // m * 2^sh in [16, 32)
     L->router_shift = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
   }
+  {
+    const char* why = "";
+    if ((st = moe::prefill_prepare_router(L, &why)) != MOE_OK) {
+      moe_layer_destroy(L);
+      return fail(st, "prefill router weights: %s", why);
+    }
+  }
   *out = L;
   return MOE_OK;
 }

@@ -100,6 +100,7 @@ struct Workspace {
   __half* hmid_r = nullptr;     // [max_tokens*k][F] routed SwiGLU output (bucket order)
   __half* hmid_s = nullptr;     // [max_tokens][Fs] shared-expert SwiGLU output
   float* yacc = nullptr;        // [max_tokens][H] fp32 combine accumulator
+  __half* wr16 = nullptr;       // [E][2H] router weights * 2^shift as fp16 hi | mid terms
   int max_gu_units = 0, max_dn_units = 0;
   void* scratch = nullptr;
   size_t bytes = 0;
@@ -113,6 +114,7 @@ struct moe_layer {
   CUtensorMap tmap_x16;      // x16 rows, box {64, 128}, 128B swizzle
   CUtensorMap tmap_hr;       // hmid_r rows, same box
   CUtensorMap tmap_hs;       // hmid_s rows, same box
+  CUtensorMap tmap_wr16;     // wr16 rows [E][2H], box {64, 128}, 128B swizzle
   CUtensorMap tmap_gate;     // packed codes [slots*F][H/2], box {32 B, 128 rows}
   CUtensorMap tmap_up;       // packed codes [slots*F][H/2]
   CUtensorMap tmap_down;     // packed codes [slots*H][F/2]
@@ -141,4 +143,6 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
 size_t prefill_workspace_bytes(const moe_layer_config& c);
 // Carves the prefill workspace out of `scratch` and encodes the tensor maps.
 moe_status prefill_init(moe_layer* L, void* scratch, const char** why);
+// after router_shift is known: the fp16 hi/mid split of the router weights
+moe_status prefill_prepare_router(moe_layer* L, const char** why);
 }  // namespace moe

@@ -184,12 +184,6 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Store chunk j (16 B, K elements 8j..8j+7) of row r into a 128-byte
-// swizzled K-major tile.
-__device__ __forceinline__ void st_tile_chunk(unsigned char* tile, int r, int j, uint4 v) {
-  *reinterpret_cast<uint4*>(tile + r * 128 + ((j ^ (r & 7)) << 4)) = v;
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ GemmMaps maps) {
@@ -327,10 +321,10 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
   } else if (warp < kProdWarp0 + kProdWarps) {
     // ------------------------------------------------------------ A producers
     const int pi = threadIdx.x - kProdWarp0 * 32;  // 0..255
-    const LayerDev& Wd = p.W;
     uint32_t it = 0;
     bool alive = true;
-    for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+    // (the router GEMM has no A producers: its A tiles arrive by TMA)
+    for (int u = blockIdx.x; u < n_units && alive && MODE != kRouter; u += gridDim.x) {
       const UnitInfo U = unit_info<MODE>(p, u);
       const int nks = U.K / 64;
       if constexpr (MODE != kRouter) {
@@ -431,53 +425,6 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             for (int q = 0; q < P; ++q) mbar_arrive(&raw_empty[(it + q) % SR]);
           it += P;
         }
-      } else {
-        // router: rows are experts; K' = 2H; step ks < H/64 writes the fp16
-        // "hi" term of w * 2^router_shift, later steps the "mid" remainder
-        const int r = pi & 127;
-        const int part = pi >> 7;  // which half of the K step
-        const int e = U.mt * 128 + r;
-        const bool valid = e < p.E;
-        const float* wrow = Wd.router_w + (size_t)(valid ? e : 0) * p.H;
-        const float scale = pow2f(p.router_shift);
-        const int kpp = p.H / 64;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int pass = ks / kpp, kk = ks - pass * kpp;
-          float4 v[8];
-          const float4* src = reinterpret_cast<const float4*>(wrow + kk * 64 + part * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = valid ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const int st = it % S;
-          bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            alive = false;
-            break;
-          }
-          unsigned char* tile = smem + st * G::kStageBytes;  // router: A tile at the stage start
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {  // 8-element group g of this half
-            const float a[8] = {v[2 * g].x, v[2 * g].y, v[2 * g].z, v[2 * g].w,
-                                v[2 * g + 1].x, v[2 * g + 1].y, v[2 * g + 1].z, v[2 * g + 1].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {  // pair jj = (element jj, element jj + 4)
-              const float w0 = a[jj] * scale, w1 = a[jj + 4] * scale;
-              const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
-              __half2 hv;
-              if (pass == 0)
-                hv = __halves2half2(h0, h1);
-              else
-                hv = __halves2half2(__float2half_rn(w0 - __half2float(h0)),
-                                    __float2half_rn(w1 - __half2float(h1)));
-              o[jj] = *reinterpret_cast<uint32_t*>(&hv);
-            }
-            st_tile_chunk(tile, r, part * 4 + g, make_uint4(o[0], o[1], o[2], o[3]));
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(&full_a[st]);
-        }
       }
     }
   } else if (warp < G::kRawWarp) {
@@ -547,7 +494,13 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
               alive = false;
               break;
             }
-            mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
+            if (MODE == kRouter) {
+              // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
+              mbar_expect_tx(&full_b[st], (uint32_t)(kTileA + kTileB));
+              tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, &full_b[st]);
+            } else {
+              mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
+            }
             const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
             tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, &full_b[st]);
           }
@@ -657,7 +610,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int st = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(&full_a[st], ph, p.err, tmo) || !mbar_wait(&full_b[st], ph, p.err, tmo)) {
+          if ((MODE != kRouter && !mbar_wait(&full_a[st], ph, p.err, tmo)) ||
+              !mbar_wait(&full_b[st], ph, p.err, tmo)) {
             ok = false;
             break;
           }
@@ -920,15 +874,60 @@ __global__ void __launch_bounds__(kBucketThreads, 1) bucket_kernel(const BucketP
   }
 }
 
-__global__ void finalize_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
+// y (bf16) = yacc (fp32): scalar version for a y that is not 16-byte aligned.
+__global__ void finalize_scalar_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(yacc[i]));
+}
+
+// y (bf16) = yacc (fp32), 8 elements per step (n is a multiple of 8, y
+// 16-byte aligned).
+__global__ void finalize_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
+  const size_t n8 = n / 8;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j])) |
+             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j + 1])) << 16);
+    reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Router weights for the prefill router GEMM: row e of `out` is the fp16
+// "hi" term of W_r[e] * 2^shift (K < H), then the fp16 remainder "mid" of
+// the same products (K >= H), each 8-group of K reordered to the unpack
+// order 0,4,1,5,2,6,3,7 that the fp16 activations use.
+__global__ void router_split_kernel(const float* __restrict__ wr, int E, int H, int shift,
+                                    __half* __restrict__ out) {
+  const size_t n8 = (size_t)E * H / 8;
+  const float sc = pow2f(shift);
+  for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < n8; g += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = g / (H / 8), c = g - e * (H / 8);
+    const float* src = wr + e * H + 8 * c;
+    uint32_t hi[4], mid[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {  // pair jj = (element jj, element jj + 4)
+      const float w0 = src[jj] * sc, w1 = src[jj + 4] * sc;
+      const __half h0 = __float2half_rn(w0), h1 = __float2half_rn(w1);
+      __half2 a = __halves2half2(h0, h1);
+      __half2 b = __halves2half2(__float2half_rn(w0 - __half2float(h0)),
+                                 __float2half_rn(w1 - __half2float(h1)));
+      hi[jj] = *reinterpret_cast<uint32_t*>(&a);
+      mid[jj] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(out + e * 2 * H)[c] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    reinterpret_cast<uint4*>(out + e * 2 * H + H)[c] = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+  }
 }
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillSizes {
-  size_t x16, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc;
+  size_t x16, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16;
   int max_gu, max_dn;
   static PrefillSizes make(const moe_layer_config& c) {
     PrefillSizes s;
@@ -953,12 +952,13 @@ struct PrefillSizes {
     s.hmid_r = Tk * F * 2;
     s.hmid_s = Tm * (Fs ? Fs : 128) * 2;
     s.yacc = Tm * H * 4;
+    s.wr16 = E * 2 * H * 2;
     return s;
   }
   size_t total() const {
     return align256(x16) + align256(xshift) + align256(zf) + align256(ids) + align256(w) +
            align256(offsets) + align256(perm_tok) + align256(perm_w) + align256(gu) + align256(dn) +
-           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc);
+           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc) + align256(wr16);
   }
 };
 
@@ -1031,7 +1031,7 @@ moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_
     maps.b[0] = L->tmap_hr;
     maps.b[1] = L->tmap_hs;
   } else {
-    maps.a_routed[0] = maps.a_routed[1] = maps.a_shared[0] = maps.a_shared[1] = L->tmap_gate;
+    maps.a_routed[0] = maps.a_routed[1] = maps.a_shared[0] = maps.a_shared[1] = L->tmap_wr16;
     maps.b[0] = maps.b[1] = L->tmap_x16;
   }
   kern<<<grid, Gemm<MODE>::kThreads, smem, s>>>(gp, maps);
@@ -1071,6 +1071,7 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   w.hmid_r = (__half*)take(z.hmid_r);
   w.hmid_s = (__half*)take(z.hmid_s);
   w.yacc = (float*)take(z.yacc);
+  w.wr16 = (__half*)take(z.wr16);
   w.max_gu_units = z.max_gu;
   w.max_dn_units = z.max_dn;
   const uint64_t Tm = c.max_tokens;
@@ -1089,6 +1090,23 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
       !encode_codes(&L->tmap_sh_up, sh ? d.sh_up_q : d.up_q, H / 2, sh ? Fs : F) ||
       !encode_codes(&L->tmap_sh_down, sh ? d.sh_down_q : d.down_q, sh ? Fs / 2 : F / 2, H)) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable?)";
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status prefill_prepare_router(moe_layer* L, const char** why) {
+  const moe_layer_config& c = L->cfg;
+  router_split_kernel<<<4 * L->num_sms, 256>>>(L->dev.router_w, c.n_experts, c.hidden, L->router_shift,
+                                               L->ws.wr16);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    *why = cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+  }
+  if (!encode_rows(&L->tmap_wr16, L->ws.wr16, 2 * (uint64_t)c.hidden, (uint64_t)c.n_experts)) {
+    *why = "cuTensorMapEncodeTiled failed (router weights)";
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -1193,7 +1211,10 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   if ((st = launch_gemm<kScatter>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;
   {
     prof::Scope sc("moe_finalize", s);
-    finalize_kernel<<<2 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
+    if ((reinterpret_cast<uintptr_t>(y) & 15u) == 0)
+      finalize_kernel<<<4 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
+    else
+      finalize_scalar_kernel<<<2 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) {
     *why = cudaGetErrorString(e);
