@@ -101,6 +101,7 @@ struct Workspace {
   __half* hmid_s = nullptr;     // [max_tokens][Fs] shared-expert SwiGLU output
   float* yacc = nullptr;        // [max_tokens][H] fp32 combine accumulator
   __half* wr16 = nullptr;       // [E][2H] router weights * 2^shift as fp16 hi | mid terms
+  int32_t* ccount = nullptr;    // [chunks][E] bucketing counts / chunk bases
   int max_gu_units = 0, max_dn_units = 0;
   void* scratch = nullptr;
   size_t bytes = 0;

@@ -56,6 +56,7 @@ constexpr int kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBWarp0 = 12;
 constexpr int kBucketThreads = 1024;
+constexpr int kMaxBucketChunks = 256;  // chunks of assignments in the bucketing
 constexpr int kScaleLead = 3;      // K steps of block scales the raw loader loads ahead
 constexpr int kBLag = 2;           // K steps of gathered token rows each B loader keeps in flight
 
@@ -721,6 +722,8 @@ struct BucketParams {
   const int32_t* ids;
   const float* w;
   int T, k, E, F, Fs, H;
+  int nc;            // chunks of the (token, slot) assignments, in order
+  int32_t* ccount;   // [nc][E] per-chunk counts, then per-chunk bases (before offsets)
   int32_t* offsets;
   int32_t* perm_tok;
   float* perm_w;
@@ -758,44 +761,81 @@ __device__ __forceinline__ int block_scan_1024(int v, int* scratch, int* total) 
   return before;
 }
 
-// Stable counting sort of the T*k assignments by expert (then token), and
-// the work-unit lists of the gate/up and down GEMMs.  One CTA of 1024
-// threads; warp w owns a contiguous range of tokens.
-__global__ void __launch_bounds__(kBucketThreads, 1) bucket_kernel(const BucketParams p) {
+// Stable counting sort of the T*k assignments (t, j), taken in the order
+// t*k + j, by expert; and the work-unit lists of the two GEMMs.  Three
+// launches: per-chunk counts (one warp per chunk of consecutive
+// assignments), one CTA for the scans and the unit lists, and the stable
+// scatter (one warp per chunk; equal experts within a 32-assignment step
+// take consecutive positions in lane order).
+__device__ __forceinline__ void chunk_range(const BucketParams& p, int c, int* a_begin, int* a_end) {
+  const long long n = (long long)p.T * p.k;
+  *a_begin = (int)(n * c / p.nc);
+  *a_end = (int)(n * (c + 1) / p.nc);
+}
+
+__global__ void __launch_bounds__(32) bucket_count_kernel(const BucketParams p) {
+  extern __shared__ int h[];  // [E]
+  const int E = p.E, lane = threadIdx.x, c = blockIdx.x;
+  for (int i = lane; i < E; i += 32) h[i] = 0;
+  __syncwarp();
+  int a_begin, a_end;
+  chunk_range(p, c, &a_begin, &a_end);
+  for (int a = a_begin + lane; a < a_end; a += 32) {
+    const int e = __ldg(p.ids + a);
+    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+    else atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+  }
+  __syncwarp();
+  for (int i = lane; i < E; i += 32) p.ccount[(size_t)c * E + i] = h[i];
+}
+
+__global__ void __launch_bounds__(32) bucket_scatter_kernel(const BucketParams p) {
+  extern __shared__ int cur[];  // [E]: next position of each expert in this chunk
+  const int E = p.E, k = p.k, lane = threadIdx.x, c = blockIdx.x;
+  for (int i = lane; i < E; i += 32) cur[i] = p.ccount[(size_t)c * E + i] + p.offsets[i];
+  __syncwarp();
+  int a_begin, a_end;
+  chunk_range(p, c, &a_begin, &a_end);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int a0 = a_begin; a0 < a_end; a0 += 32) {
+    const int a = a0 + lane;
+    int e = (a < a_end) ? __ldg(p.ids + a) : -1;
+    const float wv = (a < a_end) ? __ldg(p.w + a) : 0.0f;
+    if (e >= E) e = -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    int base = 0;
+    if (e >= 0) base = cur[e];
+    __syncwarp();
+    if (e >= 0) {
+      const int pos = base + __popc(same & lt_mask);
+      p.perm_tok[pos] = a / k;
+      p.perm_w[pos] = wv;
+      if ((same & lt_mask) == 0) cur[e] = base + __popc(same);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kBucketThreads, 1) bucket_scan_kernel(const BucketParams p) {
   extern __shared__ int sm[];
-  const int E = p.E, k = p.k, T = p.T;
-  int* hist = sm;                  // [32][E]: per-warp counts, then cursors
-  int* tot = hist + 32 * E;        // [E]
+  const int E = p.E, T = p.T;
+  int* tot = sm;                   // [E]
   int* offs = tot + E;             // [E]
   int* tbase = offs + E;           // [E + 1]
   int* scratch = tbase + E + 1;    // [64]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (T + 31) / 32;
-  const int t_begin = warp * per, t_end = min(T, t_begin + per);
-
-  for (int i = tid; i < 32 * E; i += kBucketThreads) hist[i] = 0;
-  __syncthreads();
-  // per-warp histograms (a token's k ids are distinct: no lane conflicts)
-  for (int t0 = t_begin; t0 < t_end; t0 += 16) {
-    int col[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      col[i] = (lane < k && t0 + i < t_end) ? __ldg(p.ids + (size_t)(t0 + i) * k + lane) : -1;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = col[i];
-      if (e >= 0 && e < E) hist[warp * E + e] += 1;
-      else if (lane < k && t0 + i < t_end) atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-      __syncwarp();
-    }
-  }
-  __syncthreads();
+  const int tid = threadIdx.x;
+  // per expert: exclusive scan over the chunks (chunk bases) and the total
   for (int e = tid; e < E; e += kBucketThreads) {
     int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int c = hist[w * E + e];
-      hist[w * E + e] = run;
-      run += c;
+    for (int c0 = 0; c0 < p.nc; c0 += 8) {  // 8 loads in flight per step
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (c0 + i < p.nc) ? p.ccount[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c0 + i < p.nc) p.ccount[(size_t)(c0 + i) * E + e] = run;
+        run += v[i];
+      }
     }
     tot[e] = run;
   }
@@ -819,30 +859,6 @@ __global__ void __launch_bounds__(kBucketThreads, 1) bucket_kernel(const BucketP
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kBucketThreads)
-    for (int w = 0; w < 32; ++w) hist[w * E + e] += offs[e];
-  __syncthreads();
-  // stable scatter: each warp walks its tokens in order
-  for (int t0 = t_begin; t0 < t_end; t0 += 16) {
-    int col[16];
-    float wc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const bool in = lane < k && t0 + i < t_end;
-      col[i] = in ? __ldg(p.ids + (size_t)(t0 + i) * k + lane) : -1;
-      wc[i] = in ? __ldg(p.w + (size_t)(t0 + i) * k + lane) : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = col[i];
-      if (e >= 0 && e < E) {
-        const int pos = hist[warp * E + e]++;
-        p.perm_tok[pos] = t0 + i;
-        p.perm_w[pos] = wc[i];
-      }
-      __syncwarp();
-    }
-  }
   // work units: routed tiles g -> (expert, tile) by binary search on tbase
   const int ntiles = tbase[E];
   const int mF = p.F / 128, mH = p.H / 128, mS = p.Fs / 128;
@@ -927,7 +943,8 @@ __global__ void router_split_kernel(const float* __restrict__ wr, int E, int H, 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillSizes {
-  size_t x16, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16;
+  size_t x16, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16,
+      ccount;
   int max_gu, max_dn;
   static PrefillSizes make(const moe_layer_config& c) {
     PrefillSizes s;
@@ -953,12 +970,14 @@ struct PrefillSizes {
     s.hmid_s = Tm * (Fs ? Fs : 128) * 2;
     s.yacc = Tm * H * 4;
     s.wr16 = E * 2 * H * 2;
+    s.ccount = (size_t)kMaxBucketChunks * E * 4;
     return s;
   }
   size_t total() const {
     return align256(x16) + align256(xshift) + align256(zf) + align256(ids) + align256(w) +
            align256(offsets) + align256(perm_tok) + align256(perm_w) + align256(gu) + align256(dn) +
-           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc) + align256(wr16);
+           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc) + align256(wr16) +
+           align256(ccount);
   }
 };
 
@@ -1072,6 +1091,7 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   w.hmid_s = (__half*)take(z.hmid_s);
   w.yacc = (float*)take(z.yacc);
   w.wr16 = (__half*)take(z.wr16);
+  w.ccount = (int32_t*)take(z.ccount);
   w.max_gu_units = z.max_gu;
   w.max_dn_units = z.max_dn;
   const uint64_t Tm = c.max_tokens;
@@ -1188,15 +1208,14 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   bp.dn_units = ws.dn_units;
   bp.n_units = ws.n_units;
   bp.err = ws.err;
-  const size_t bsmem = sizeof(int) * (32 * (size_t)E + 3 * (size_t)E + 1 + 64);
-  if (cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem) !=
-      cudaSuccess) {
-    *why = "cudaFuncSetAttribute(bucket smem)";
-    return MOE_ERR_CUDA;
-  }
+  bp.nc = std::max(1, std::min(kMaxBucketChunks, (T * k + 1023) / 1024));  // ~1024 per chunk
+  bp.ccount = ws.ccount;
+  const size_t bsmem = sizeof(int) * (3 * (size_t)E + 1 + 64);
   {
     prof::Scope sc("moe_bucket", s);
-    bucket_kernel<<<1, kBucketThreads, bsmem, s>>>(bp);
+    bucket_count_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
+    bucket_scan_kernel<<<1, kBucketThreads, bsmem, s>>>(bp);
+    bucket_scatter_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
   }
 
   gp.units = ws.gu_units;
