@@ -253,8 +253,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       named_bar_sync(1, kEpiWarps * 32);  // the previous unit is done with meta
       if (r < U.n) {
         if (MODE == kSwiglu) {
+          // D * 2^sx restores x; h is stored * 2^-2sx, i.e. silu(g) * D_u * 2^-sx
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
-          meta_i[r] = __ldg(p.xshift + tok);  // D * 2^sx restores x; h is stored * 2^-2sx
+          const int sx = __ldg(p.xshift + tok);
+          meta_f[r] = pow2f(sx);
+          reinterpret_cast<float*>(meta_i)[r] = pow2f(-sx);
         } else if (MODE == kScatter) {
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
           const float wgt = U.shared ? 1.0f : __ldg(p.perm_w + U.p0 + r);
@@ -279,28 +282,59 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       // unpack order 0,4,1,5,2,6,3,7, as the down GEMM's K expects)
       const int qloc = (r & ~7) | ((r & 4) ? (((r & 3) << 1) | 1) : ((r & 3) << 1));
       constexpr int CW = (NA == 2) ? 16 : 32;  // columns per TMEM load
-      for (int c0 = 0; c0 < neff; c0 += CW) {
-        uint32_t v0[CW], v1[CW];
-        tmem_ld(tbase + c0, v0);
-        if (NA == 2) tmem_ld(tbase + 128 + c0, v1);
+      if (MODE == kSwiglu) {
+        // drain: the next chunk's TMEM loads are issued before this chunk is
+        // processed; per element one scale, SiLU, one product, one store
+        const float* sA = meta_f;
+        const float* sB = reinterpret_cast<const float*>(meta_i);
+        uint32_t g0[CW], u0[CW];
+        tmem_ld(tbase, g0);
+        tmem_ld(tbase + 128, u0);
         tmem_wait_ld();
+        for (int c0 = 0; c0 < neff; c0 += CW) {
+          uint32_t g1[CW], u1[CW];
+          const bool more = c0 + CW < neff;
+          if (more) {
+            tmem_ld(tbase + c0 + CW, g1);
+            tmem_ld(tbase + 128 + c0 + CW, u1);
+          }
 #pragma unroll
-        for (int jj = 0; jj < CW; ++jj) {
-          const int t = c0 + jj;
-          if (t >= U.n) continue;
-          if (MODE == kSwiglu) {
-            const int sx = meta_i[t];
-            const float g = __uint_as_float(v0[jj]) * pow2f(sx);
-            const float uu = __uint_as_float(v1[jj]) * pow2f(sx);
-            const float h = silu_fast(g) * uu;
-            hst[t * 128 + qloc] = __float2half_rn(h * pow2f(-2 * sx));
-          } else if (MODE == kScatter) {
-            atomicAdd(p.yacc + (size_t)meta_i[t] * p.H + U.mt * 128 + r,
-                      __uint_as_float(v0[jj]) * meta_f[t]);
-          } else {
-            const int e = U.mt * 128 + r;
-            if (e < p.E)
-              p.z[(size_t)(U.p0 + t) * p.E + e] = __uint_as_float(v0[jj]) * meta_f[t] + bias_r;
+          for (int jj = 0; jj < CW; jj += 2) {  // tokens t, t+1 as one half2
+            const int t = c0 + jj;
+            const __half2 g = __floats2half2_rn(__uint_as_float(g0[jj]) * sA[t],
+                                                __uint_as_float(g0[jj + 1]) * sA[t + 1]);
+            const __half2 u = __floats2half2_rn(__uint_as_float(u0[jj]) * sB[t],
+                                                __uint_as_float(u0[jj + 1]) * sB[t + 1]);
+            const __half2 h = __hmul2(silu_fast2(g), u);
+            hst[t * 128 + qloc] = __low2half(h);
+            hst[(t + 1) * 128 + qloc] = __high2half(h);
+          }
+          if (more) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+              g0[jj] = g1[jj];
+              u0[jj] = u1[jj];
+            }
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < neff; c0 += CW) {
+          uint32_t v0[CW];
+          tmem_ld(tbase + c0, v0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < CW; ++jj) {
+            const int t = c0 + jj;
+            if (t >= U.n) continue;
+            if (MODE == kScatter) {
+              atomicAdd(p.yacc + (size_t)meta_i[t] * p.H + U.mt * 128 + r,
+                        __uint_as_float(v0[jj]) * meta_f[t]);
+            } else {
+              const int e = U.mt * 128 + r;
+              if (e < p.E)
+                p.z[(size_t)(U.p0 + t) * p.E + e] = __uint_as_float(v0[jj]) * meta_f[t] + bias_r;
+            }
           }
         }
       }
