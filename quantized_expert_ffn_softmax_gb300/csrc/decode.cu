@@ -92,6 +92,41 @@ __device__ __forceinline__ void unpack_codes(uint32_t w, __half2 (&h)[4]) {
   }
 }
 
+// As dot_block, but the two 16-element halves of the block are returned
+// separately (their activations carry different power-of-two scales).
+template <int TT>
+__device__ __forceinline__ void dot_block_halves(const uint4 w, const uint4 (&act)[TT][4],
+                                                 float (&lo)[TT], float (&hi)[TT]) {
+  __half2 c[4][4];
+  unpack_codes(w.x, c[0]);
+  unpack_codes(w.y, c[1]);
+  unpack_codes(w.z, c[2]);
+  unpack_codes(w.w, c[3]);
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    const __half2* a0 = reinterpret_cast<const __half2*>(&act[t][0]);
+    const __half2* a1 = reinterpret_cast<const __half2*>(&act[t][1]);
+    const __half2* a2 = reinterpret_cast<const __half2*>(&act[t][2]);
+    const __half2* a3 = reinterpret_cast<const __half2*>(&act[t][3]);
+    __half2 s0 = __hmul2(c[0][0], a0[0]);
+    __half2 s1 = __hmul2(c[2][0], a2[0]);
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+      s0 = __hfma2(c[0][j], a0[j], s0);
+      s1 = __hfma2(c[2][j], a2[j], s1);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s0 = __hfma2(c[1][j], a1[j], s0);
+      s1 = __hfma2(c[3][j], a3[j], s1);
+    }
+    const float2 f0 = __half22float2(s0);
+    const float2 f1 = __half22float2(s1);
+    lo[t] = f0.x + f0.y;
+    hi[t] = f1.x + f1.y;
+  }
+}
+
 template <int TT>
 __device__ __forceinline__ void dot_block(const uint4 w, const uint4 (&act)[TT][4],
                                           float (&out)[TT]) {
@@ -213,7 +248,7 @@ __device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
 struct DecodeSmem {
-  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dbuf, hp, total;
+  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dbuf, hp, hsh, total;
   size_t g_stage, d_item;
   int nmy, nd_items;
   bool dprefetch;
@@ -247,7 +282,8 @@ struct DecodeSmem {
     s.gbuf = (region + (size_t)TT * H * 2 + 127) & ~(size_t)127;
     const size_t g_end = s.gbuf + (size_t)g_stages * s.g_stage;
     s.hp = region;
-    const size_t h_end = region + ((size_t)n_routed_max * F + Fs) * TT * 2;
+    s.hsh = region + ((size_t)n_routed_max * F + Fs) * TT * 2;  // int8 half-block shifts
+    const size_t h_end = s.hsh + (((size_t)n_routed_max * F + Fs) / 32 * TT * 2 + 15) / 16 * 16;
     o = g_end > h_end ? g_end : h_end;
     o = (o + 127) & ~(size_t)127;
     s.dbuf = o;
@@ -276,6 +312,7 @@ struct DecodeMisc {
   float red_ss[kWarps][4];
   float red_mx[kWarps][4];
   float red_z[kWarps][4];
+  float hst[2][16][4];  // w*h of a gate/up item's 16 rows (double-buffered by item)
 };
 static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 
@@ -305,7 +342,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   unsigned char* gbuf = smem + L.gbuf;
   unsigned char* dbuf = smem + L.dbuf;
   uint4* hp = reinterpret_cast<uint4*>(smem + L.hp);
-  float* amax_g = reinterpret_cast<float*>(p.bar->pad);  // [2][4], zeroed with the counter
+  // w*h of the layer in global scratch, as fp16 pair planes laid out like the
+  // down phase's staging (unit u at u*TT*4*CF uint4s, the shared unit after
+  // the routed ones), followed by the int8 shift of each 16-element half-block
+  uint4* hp16 = reinterpret_cast<uint4*>(p.hbuf);
+  int8_t* hsh_g = reinterpret_cast<int8_t*>(hp16 + (size_t)TT * 4 * ((p.max_units - 1) * CF + CS));
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1) ? kWarps : 1);
@@ -674,21 +715,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // ------------------------------------------------ phase G: gate/up + SwiGLU
     {
       // warp w owns row pairs 2w, 2w+1 of every item (gate and up rows)
-      float* amax_l = amax_g + (l & 1) * 4;
       for (int q = 0; (int)blockIdx.x + q * grid < n_gitems; ++q) {
         const int it = blockIdx.x + q * grid;
-        int Fu, u, f0;
-        size_t hoff;
+        int u, f0;
         if (it < n_routed * ipu) {
           u = it / ipu;
           f0 = (it - u * ipu) * 16;
-          Fu = F;
-          hoff = (size_t)u * kMaxDecodeTokens * F;
         } else {
           u = n_routed;
           f0 = (it - n_routed * ipu) * 16;
-          Fu = Fs;
-          hoff = (size_t)(p.max_units - 1) * kMaxDecodeTokens * F;
         }
         const int sg = q % NG;
         const uint32_t par = gcount[sg] & 1u;
@@ -740,10 +775,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const float xs = pow2f(M.x_shift[t]);
           const float g = s * xs, uu = up * xs;
           const float h = g / (1.0f + __expf(-g)) * uu;
-          p.hbuf[hoff + (size_t)t * Fu + f0 + 2 * warp + rp] = h;
-          // per-token max |w h| over the layer, for the down phase's fp16 range
-          const float a = fabsf(h * M.unit_w[u][t]);
-          if (a > 0.0f && isfinite(a)) atomicMax(reinterpret_cast<int*>(amax_l + t), __float_as_int(a));
+          M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
+        }
+        __syncthreads();  // the item's 16 rows of w*h are staged
+        if (tid < TT * 2) {
+          // the item's rows as fp16 pair planes in the down phase's layout,
+          // scaled by a power of two that puts this token's max |w h| over
+          // the 16 rows in [32, 64) (the shift goes beside them)
+          const int t = tid >> 1, g8 = tid & 1;
+          float m = 0.0f;
+#pragma unroll
+          for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(M.hst[q & 1][r][t]));
+          const int sh = range_shift(m);
+          const float sc = pow2f(-sh);
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __half2 hh = __floats2half2_rn(M.hst[q & 1][8 * g8 + j][t] * sc, M.hst[q & 1][8 * g8 + j + 4][t] * sc);
+            o[j] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          const int Cu = (u < n_routed) ? CF : CS;
+          const int c = f0 >> 5, half = (f0 >> 4) & 1;
+          hp16[(size_t)u * TT * 4 * CF + (size_t)t * 4 * Cu + (size_t)(2 * half + g8) * Cu + c] =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          if (g8 == 0) hsh_g[(size_t)u * TT * 2 * CF + (size_t)t * 2 * Cu + (size_t)half * Cu + c] = (int8_t)sh;
         }
         // refill this stage with item q + NG once every warp has read it
         if (warp == 0 && lane == 0 && (int)blockIdx.x + (q + NG) * grid < n_gitems) {
@@ -757,58 +812,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     // ------------------------------------------------ phase D: down + combine
     {
-      const size_t sh_hoff = (size_t)(p.max_units - 1) * kMaxDecodeTokens * F;
-      if (blockIdx.x == 0 && tid < 4) amax_g[((l + 1) & 1) * 4 + tid] = 0.0f;  // next layer's
-      int dsh[TT];
-#pragma unroll
-      for (int t = 0; t < TT; ++t) dsh[t] = range_shift(__ldcg(amax_g + (l & 1) * 4 + t));
-      // stage w*h as fp16 pair planes: unit u base = u*TT*4*CF (shared: n_routed*TT*4*CF)
+      // stage the layer's fp16 w*h planes and their half-block shifts (plain
+      // copies: the gate/up phase of every CTA wrote them before the barrier)
+      int8_t* hsh = reinterpret_cast<int8_t*>(smem + L.hsh);
       {
-        const int n_chunks = n_routed * CF + CS;
-#pragma unroll 2
-        for (int i = tid; i < n_chunks * TT; i += kDecodeThreads) {
-          const int t = i / n_chunks;
-          const int pc = i - t * n_chunks;
-          int u, c, Cu;
-          size_t ho;
-          if (pc < n_routed * CF) {
-            u = pc / CF;
-            c = pc - u * CF;
-            Cu = CF;
-            ho = (size_t)u * kMaxDecodeTokens * F;
-          } else {
-            u = n_routed;
-            c = pc - n_routed * CF;
-            Cu = CS;
-            ho = sh_hoff;
-          }
-          int sh = 0;
-#pragma unroll
-          for (int tt = 0; tt < TT; ++tt)
-            if (tt == t) sh = dsh[tt];
-          const float wt = M.unit_w[u][t] * pow2f(-sh);
-          const float4* src = reinterpret_cast<const float4*>(p.hbuf + ho + (size_t)t * (Cu * 32) + c * 32);
-          float vv[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 f4 = __ldcg(src + j);
-            vv[4 * j] = f4.x * wt;
-            vv[4 * j + 1] = f4.y * wt;
-            vv[4 * j + 2] = f4.z * wt;
-            vv[4 * j + 3] = f4.w * wt;
-          }
-          uint4* dst = hp + (size_t)u * TT * 4 * CF + (size_t)t * 4 * Cu + c;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              __half2 hh = __floats2half2_rn(vv[8 * qq + j], vv[8 * qq + j + 4]);
-              o[j] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-            dst[qq * Cu] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
+        const int n16 = (n_routed * CF + CS) * TT * 4;
+        for (int i = tid; i < n16; i += kDecodeThreads) hp[i] = __ldcg(hp16 + i);
+        const int nsh = (n_routed * CF + CS) * TT * 2;
+        for (int i = tid; i < nsh; i += kDecodeThreads) hsh[i] = __ldcg(hsh_g + i);
       }
       __syncthreads();
       const int P = n_routed * CF + CS;
@@ -842,6 +853,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           for (int t = 0; t < TT; ++t)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) act[t][qq] = ap[(t * 4 + qq) * Cu];
+          float slo[TT], shi[TT];  // 2^shift of the two half-blocks, per token
+          {
+            const int8_t* sp = hsh + (size_t)u * TT * 2 * CF + c;
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+              slo[t] = pow2f(sp[(t * 2) * Cu]);
+              shi[t] = pow2f(sp[(t * 2 + 1) * Cu]);
+            }
+          }
 #pragma unroll
           for (int q = 0; q < kMaxRowsPerWarp; ++q) {
             if (q < nq) {
@@ -859,10 +879,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 wv = ld_stream(base + (size_t)i * (Cu * 16) + c * 16);
                 s = __half2float(__ushort_as_half(__ldg(sbase + (size_t)i * Cu + c)));
               }
-              float d[TT];
-              dot_block<TT>(wv, act, d);
+              float dlo[TT], dhi[TT];
+              dot_block_halves<TT>(wv, act, dlo, dhi);
 #pragma unroll
-              for (int t = 0; t < TT; ++t) acc[q][t] = fmaf(s, d[t], acc[q][t]);
+              for (int t = 0; t < TT; ++t)
+                acc[q][t] = fmaf(s, fmaf(dlo[t], slo[t], dhi[t] * shi[t]), acc[q][t]);
             }
           }
         }
@@ -877,11 +898,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int idx = lane / REP;
           const int q = idx / TT, t = idx - (idx / TT) * TT;
           if (q < nq && t < T) {
-            int sh = 0;
-#pragma unroll
-            for (int tt = 0; tt < TT; ++tt)
-              if (tt == t) sh = dsh[tt];
-            const float y = y0 * pow2f(sh);
+            const float y = y0;
             const int i = ((int)blockIdx.x + (q0 + q) * grid) * 8 + warp;
             const __nv_bfloat16 yb = __float2bfloat16_rn(y);
             if (p.mode == kModeForward) {
