@@ -836,17 +836,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         for (int q = 0; q < kMaxRowsPerWarp; ++q)
 #pragma unroll
           for (int t = 0; t < TT; ++t) acc[q][t] = 0.0f;
+        // (unit, chunk) of pp advance by 32 chunks per step, without a division
+        int u = 0, c = lane;
+        while (u < n_routed && c >= CF) {
+          c -= CF;
+          ++u;
+        }
         for (int pp = lane; pp < P; pp += 32) {
-          int u, c, Cu;
-          if (pp < n_routed * CF) {
-            u = pp / CF;
-            c = pp - u * CF;
-            Cu = CF;
-          } else {
-            u = n_routed;
-            c = pp - n_routed * CF;
-            Cu = CS;
-          }
+          const int Cu = (u < n_routed) ? CF : CS;
           uint4 act[TT][4];
           const uint4* ap = hp + (size_t)u * TT * 4 * CF + c;
 #pragma unroll
@@ -885,6 +882,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               for (int t = 0; t < TT; ++t)
                 acc[q][t] = fmaf(s, fmaf(dlo[t], slo[t], dhi[t] * shi[t]), acc[q][t]);
             }
+          }
+          c += 32;
+          while (u < n_routed && c >= CF) {
+            c -= CF;
+            ++u;
           }
         }
         float v[kMaxRowsPerWarp * TT];
