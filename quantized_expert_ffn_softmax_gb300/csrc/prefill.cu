@@ -110,8 +110,9 @@ struct Gemm {
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
-  // A producers take K steps in groups of kGroup (a divisor of every K/64);
-  // pairs halve the per-step overhead where the rings are deep enough
+  // down producers take K steps in pairs (every K/64 is even: K is a
+  // multiple of 128), halving the per-step waits and fences; gate/up does
+  // more work per step and is faster one step at a time
   static constexpr int kGroup = (MODE == kScatter) ? 2 : 1;
   static_assert(MODE == kRouter || (S >= 2 * kGroup && SR >= 2 * kGroup), "ring depth per group");
 };
