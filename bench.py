@@ -173,7 +173,11 @@ def ncu_traffic(kernel_key: str, src_hash: str):
 # --------------------------------------------------------------------------- GPU arm
 
 class Dist:
-    def __init__(self, n_gpus: int):
+    """One process per GPU (replicas: no collective on the data path); the
+    process group only carries the barrier and the max over ranks of the
+    step time.  backend "gloo" runs it on CPU tensors (tests)."""
+
+    def __init__(self, n_gpus: int, backend: str = "nccl"):
         import torch
 
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -181,11 +185,16 @@ class Dist:
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.n = max(n_gpus, self.world)
         self.pg = None
-        torch.cuda.set_device(self.local)
+        self.device = "cuda" if backend == "nccl" else "cpu"
+        if self.device == "cuda":
+            torch.cuda.set_device(self.local)
         if self.world > 1:
             import torch.distributed as dist
 
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            if self.device == "cuda":
+                dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            else:
+                dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -197,13 +206,19 @@ class Dist:
             return v
         import torch
 
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def job_tokens_per_s(n_ranks: int, tokens_per_rank_step: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: every rank processes its own tokens each step
+    (weak scaling); the job's step time is the slowest rank's."""
+    return n_ranks * tokens_per_rank_step / (ms_per_step_max / 1e3)
 
 
 def build_stack(cfg, max_tokens):
@@ -301,7 +316,7 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
     launches_per_step = kcount / max(1, min(steps, 50))
     out = {
         "ms_per_step": ms,
-        "tok_s": dist.n * T / (ms / 1e3),
+        "tok_s": job_tokens_per_s(dist.n, T, ms),
         "bytes_per_step": bytes_per_step,
         "gbs_step": bytes_per_step / (ms / 1e3) / 1e9,
         "kernel_ms": k_avg,
