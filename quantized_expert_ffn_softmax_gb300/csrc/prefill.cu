@@ -109,6 +109,7 @@ struct Gemm {
   static constexpr int kSmem = OFF_HST + kHStage + 1024;  // + slack for 1 KB alignment
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
   static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(OFF_META % 16 == 0, "token factors are read as 16-byte vectors");
   static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
   // down producers take K steps in pairs (every K/64 is even: K is a
   // multiple of 128), halving the per-step waits and fences; gate/up does
@@ -299,16 +300,31 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             tmem_ld(tbase + c0 + CW, g1);
             tmem_ld(tbase + 128 + c0 + CW, u1);
           }
+          // the chunk's token factors are read into registers before its
+          // first store: loads placed between the stores would each wait
+          // for the stores before them (the compiler cannot rule out aliasing)
+          float fa[CW], fb[CW];
+#pragma unroll
+          for (int q = 0; q < CW; q += 4) {
+            const float4 va = *reinterpret_cast<const float4*>(sA + c0 + q);
+            const float4 vb = *reinterpret_cast<const float4*>(sB + c0 + q);
+            fa[q] = va.x, fa[q + 1] = va.y, fa[q + 2] = va.z, fa[q + 3] = va.w;
+            fb[q] = vb.x, fb[q + 1] = vb.y, fb[q + 2] = vb.z, fb[q + 3] = vb.w;
+          }
+          __half2 hv[CW / 2];
 #pragma unroll
           for (int jj = 0; jj < CW; jj += 2) {  // tokens t, t+1 as one half2
+            const __half2 g = __floats2half2_rn(__uint_as_float(g0[jj]) * fa[jj],
+                                                __uint_as_float(g0[jj + 1]) * fa[jj + 1]);
+            const __half2 u = __floats2half2_rn(__uint_as_float(u0[jj]) * fb[jj],
+                                                __uint_as_float(u0[jj + 1]) * fb[jj + 1]);
+            hv[jj / 2] = __hmul2(silu_fast2(g), u);
+          }
+#pragma unroll
+          for (int jj = 0; jj < CW; jj += 2) {
             const int t = c0 + jj;
-            const __half2 g = __floats2half2_rn(__uint_as_float(g0[jj]) * sA[t],
-                                                __uint_as_float(g0[jj + 1]) * sA[t + 1]);
-            const __half2 u = __floats2half2_rn(__uint_as_float(u0[jj]) * sB[t],
-                                                __uint_as_float(u0[jj + 1]) * sB[t + 1]);
-            const __half2 h = __hmul2(silu_fast2(g), u);
-            hst[t * 128 + qloc] = __low2half(h);
-            hst[(t + 1) * 128 + qloc] = __high2half(h);
+            hst[t * 128 + qloc] = __low2half(hv[jj / 2]);
+            hst[(t + 1) * 128 + qloc] = __high2half(hv[jj / 2]);
           }
           if (more) {
             tmem_wait_ld();
@@ -324,17 +340,33 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           uint32_t v0[CW];
           tmem_ld(tbase + c0, v0);
           tmem_wait_ld();
+          // per 16 tokens: factors into registers first, then the stores or
+          // reductions (a shared load after a global store through a generic
+          // pointer would have to wait for it)
 #pragma unroll
-          for (int jj = 0; jj < CW; ++jj) {
-            const int t = c0 + jj;
-            if (t >= U.n) continue;
-            if (MODE == kScatter) {
-              atomicAdd(p.yacc + (size_t)meta_i[t] * p.H + U.mt * 128 + r,
-                        __uint_as_float(v0[jj]) * meta_f[t]);
-            } else {
-              const int e = U.mt * 128 + r;
-              if (e < p.E)
-                p.z[(size_t)(U.p0 + t) * p.E + e] = __uint_as_float(v0[jj]) * meta_f[t] + bias_r;
+          for (int hq = 0; hq < CW; hq += 16) {
+            float tf[16];
+            int ti[16];
+#pragma unroll
+            for (int q = 0; q < 16; q += 4) {
+              const float4 vf = *reinterpret_cast<const float4*>(meta_f + c0 + hq + q);
+              tf[q] = vf.x, tf[q + 1] = vf.y, tf[q + 2] = vf.z, tf[q + 3] = vf.w;
+              if (MODE == kScatter) {
+                const int4 vi = *reinterpret_cast<const int4*>(meta_i + c0 + hq + q);
+                ti[q] = vi.x, ti[q + 1] = vi.y, ti[q + 2] = vi.z, ti[q + 3] = vi.w;
+              }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int t = c0 + hq + jj;
+              if (t >= U.n) continue;
+              const float v = __uint_as_float(v0[hq + jj]) * tf[jj];
+              if (MODE == kScatter) {
+                atomicAdd(p.yacc + (size_t)ti[jj] * p.H + U.mt * 128 + r, v);
+              } else {
+                const int e = U.mt * 128 + r;
+                if (e < p.E) p.z[(size_t)(U.p0 + t) * p.E + e] = v + bias_r;
+              }
             }
           }
         }
