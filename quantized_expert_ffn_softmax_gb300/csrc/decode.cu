@@ -24,7 +24,8 @@
 // Only the router logits, h and h_{l+1} cross between CTAs (through L2);
 // every weight byte is read from HBM once, by a bulk copy issued as soon as
 // its address is known.  Packed 4-bit codes become fp16 pairs with a
-// magic-exponent OR (0x6400 | n = 1024 + n, minus 1032 = n - 8, exact);
+// magic-exponent OR (0x6400 | n = 1024 + n, minus 1032 = n - 8, exact; a
+// nibble one position higher goes into 0x5400 = 64.0 instead);
 // products with the fp16 activations are exact and summed within a
 // 32-weight block in fp16, then scaled by the block scale and summed in
 // fp32.  Activations are rescaled by a per-token power of two before the
@@ -83,13 +84,23 @@ __device__ __forceinline__ int range_shift(float amax) {
 // activations, held as 4 x (4 fp16 pairs) in the order the codes unpack:
 // word q of the block covers elements 8q..8q+7; pair j of word q is
 // (element 8q+j, element 8q+j+4).
+// Nibbles in bits 0-3 of a half word are ORed into the mantissa of 1024.0
+// (0x6400: unit step), nibbles in bits 4-7 into that of 64.0 (0x5400: step
+// 1/16, so n * 16 adds n); one shift by 8 brings nibbles 2 and 3 into those
+// positions.  Subtracting 1032 or 72 leaves n - 8 exactly.
 __device__ __forceinline__ void unpack_codes(uint32_t w, __half2 (&h)[4]) {
   const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // (1024+n_lo, 1024+n_hi)
-    h[j] = __hsub2(*reinterpret_cast<__half2*>(&v), k1032);     // exact n - 8
-  }
+  const __half2 k72 = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));
+  const uint32_t w8 = w >> 8;
+  uint32_t v[4];
+  v[0] = (w & 0x000F000Fu) | 0x64006400u;   // (1024 + n0, 1024 + n4)
+  v[1] = (w & 0x00F000F0u) | 0x54005400u;   // (64 + n1, 64 + n5)
+  v[2] = (w8 & 0x000F000Fu) | 0x64006400u;  // (1024 + n2, 1024 + n6)
+  v[3] = (w8 & 0x00F000F0u) | 0x54005400u;  // (64 + n3, 64 + n7)
+  h[0] = __hsub2(*reinterpret_cast<__half2*>(&v[0]), k1032);
+  h[1] = __hsub2(*reinterpret_cast<__half2*>(&v[1]), k72);
+  h[2] = __hsub2(*reinterpret_cast<__half2*>(&v[2]), k1032);
+  h[3] = __hsub2(*reinterpret_cast<__half2*>(&v[3]), k72);
 }
 
 // As dot_block, but the two 16-element halves of the block are returned

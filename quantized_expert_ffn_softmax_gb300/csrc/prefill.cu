@@ -174,14 +174,20 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmParams& p, int u) {
 }
 
 // 8 packed 4-bit codes (one 32-bit word, elements 8j..8j+7) -> 8 fp16
-// weights (code - 8) * scale, in the unpack order 0,4,1,5,2,6,3,7.
+// weights (code - 8) * scale, in the unpack order 0,4,1,5,2,6,3,7.  A nibble
+// in bits 0-3 of a half word ORed into 1024.0 (0x6400) reads 1024 + n; one
+// in bits 4-7 ORed into 64.0 (0x5400, mantissa step 1/16) reads 64 + n; a
+// single shift by 8 brings the other two nibbles into those positions.
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
   const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 k72 = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));
+  const uint32_t w8 = w >> 8;
+  uint32_t v[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                   (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x54005400u};
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-    __half2 h = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&v), k1032), s2);
+    __half2 h = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&v[j]), (j & 1) ? k72 : k1032), s2);
     o[j] = *reinterpret_cast<uint32_t*>(&h);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
