@@ -1285,9 +1285,15 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   bp.ccount = ws.ccount;
   const size_t bsmem = sizeof(int) * (3 * (size_t)E + 1 + 64);
   {
-    prof::Scope sc("moe_bucket", s);
+    prof::Scope sc("moe_bucket_count", s);
     bucket_count_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
+  }
+  {
+    prof::Scope sc("moe_bucket_scan", s);
     bucket_scan_kernel<<<1, kBucketThreads, bsmem, s>>>(bp);
+  }
+  {
+    prof::Scope sc("moe_bucket_scatter", s);
     bucket_scatter_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
   }
 
