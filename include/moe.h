@@ -11,6 +11,14 @@
  *   w   = softmax of z over S             routing weights, sum to 1
  *   y   = sum_{e in S} w_e FFN_{slot(e)}(x) + FFN_shared(x)
  *   FFN(x) = W_d (silu(W_g x) * (W_u x))  SwiGLU expert
+ * Routing variants (moe_layer_config.routing_flags, all off by default):
+ *   MOE_ROUTING_NO_RENORM       w_e = softmax over all E logits, taken at
+ *                               the selected experts (sums to less than 1)
+ *   MOE_ROUTING_BIAS_SELECT_ONLY the bias b enters the selection only: S is
+ *                               the top-k of W_r x + b, the weights use the
+ *                               logits W_r x without b
+ *   MOE_ROUTING_SHARED_GATE     the shared expert is scaled per token by
+ *                               sigmoid(g . x), g = sh_gate_w [H] fp32
  * Every expert is reached through a resident slot table (the pages' VRAM
  * expert cache, here sized to hold all experts in HBM).  Expert weights are
  * symmetric 4-bit codes in blocks of 32 along the reduction dimension with
@@ -52,11 +60,20 @@ typedef enum {
   MOE_ERR_TIMEOUT = -6   /* a bounded device-side wait ran out */
 } moe_status;
 
+/* Routing variant bits for moe_layer_config.routing_flags; combinations are
+ * allowed (MOE_ROUTING_SHARED_GATE needs shared_ffn > 0). */
+enum {
+  MOE_ROUTING_NO_RENORM = 1,
+  MOE_ROUTING_BIAS_SELECT_ONLY = 2,
+  MOE_ROUTING_SHARED_GATE = 4
+};
+
 /* Layer shape.  Limits: hidden % 128 == 0 and 128 <= hidden <= 8192;
  * 1 <= n_experts <= 1024; 1 <= top_k <= min(16, n_experts);
  * ffn % 128 == 0 and 128 <= ffn <= 4096; shared_ffn == 0 or a multiple of
  * 128 up to 4096; n_slots == n_experts (the slot table holds every expert);
- * 1 <= max_tokens <= 65536 (sizes the workspaces). */
+ * 1 <= max_tokens <= 65536 (sizes the workspaces); routing_flags a
+ * combination of the MOE_ROUTING_* bits (0: the default routing above). */
 typedef struct {
   int32_t hidden;     /* H */
   int32_t n_experts;  /* E */
@@ -65,6 +82,7 @@ typedef struct {
   int32_t shared_ffn; /* Fs: shared expert intermediate size, 0 = none */
   int32_t n_slots;    /* S: expert-cache slots */
   int32_t max_tokens; /* largest n_tokens any call will pass */
+  int32_t routing_flags; /* MOE_ROUTING_* bits */
 } moe_layer_config;
 
 /* Packed weights, all row-major with the reduction dimension contiguous.
@@ -76,7 +94,9 @@ typedef struct {
  *   sh_gate_q, sh_up_q [Fs][H/2], sh_*_s [Fs][H/32]
  *   sh_down_q [H][Fs/2], sh_down_s [H][Fs/32]        (NULL when Fs == 0)
  *   router_w [E][H] fp32, router_bias [E] fp32 or NULL (zero bias)
- *   slot_of_expert [E]: a permutation of 0..S-1 (validated at create). */
+ *   slot_of_expert [E]: a permutation of 0..S-1 (validated at create)
+ *   sh_gate_w [H] fp32: shared-expert gate vector, read only with
+ *   MOE_ROUTING_SHARED_GATE (NULL otherwise). */
 typedef struct {
   const float* router_w;
   const float* router_bias;
@@ -93,6 +113,7 @@ typedef struct {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
+  const float* sh_gate_w;
 } moe_layer_weights;
 
 /* Creates a layer: validates cfg and the slot table, allocates the layer's
@@ -108,8 +129,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
 void moe_layer_destroy(moe_layer* layer);
 
 /* Router + top-k only.  x_bf16 [T][H] (bf16 bits); outputs topk_ids [T][k]
- * (logical expert ids, descending logit, ties to the lower id) and topk_w
- * [T][k] (softmax over the selected logits). */
+ * (logical expert ids, descending selection logit, ties to the lower id) and
+ * topk_w [T][k] (softmax over the selected logits, or as routing_flags
+ * say). */
 moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t* topk_ids,
                      float* topk_w, void* stream);
 

@@ -58,7 +58,7 @@ class OracleLayer(ctypes.Structure):
         (n, ctypes.c_void_p) for n in (
             "router_w", "router_b", "slot_of_expert", "gate_q", "gate_s", "up_q", "up_s",
             "down_q", "down_s", "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q",
-            "sh_down_s")]
+            "sh_down_s")] + [("routing_flags", ctypes.c_int), ("sh_gate_w", ctypes.c_void_p)]
 
 
 def lib():
@@ -79,6 +79,9 @@ def lib():
         L.oracle_router_logits.argtypes = [i32, i32, i32, vp, vp, vp, vp]
         L.oracle_topk_softmax.argtypes = [i32, i32, i32, vp, vp, vp, vp]
         L.oracle_topk_softmax_full.argtypes = [i32, i32, i32, vp, vp, vp]
+        L.oracle_route_weights.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
+        L.oracle_shared_gate.argtypes = [i32, vp, vp]
+        L.oracle_shared_gate.restype = d
         L.oracle_bucket.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp]
         L.oracle_expert_ffn.argtypes = [i32, i32] + [vp] * 8
         L.oracle_combine_token.argtypes = [i32, i32, i32, i32] + [vp] * 15
@@ -167,6 +170,26 @@ def topk_softmax_full(z, k):
     return ids, w
 
 
+def route_weights(zsel, b, ids, flags: int) -> np.ndarray:
+    """Routing weights [T][k] of the selection ids under the variant flags
+    (1: no renormalisation, 2: bias for selection only); zsel = W_r x + b."""
+    zsel = _c(zsel, np.float64)
+    T, E = zsel.shape
+    ids = _c(ids, np.int32)
+    k = ids.shape[1]
+    bb = None if b is None else _c(b, np.float32)
+    w = np.empty((T, k), np.float64)
+    lib().oracle_route_weights(T, E, k, int(flags), _p(zsel), _p(bb), _p(ids), _p(w))
+    return w
+
+
+def shared_gate(g, x_bf16) -> float:
+    """sigmoid(g . x) for one token (g fp32 [H], x bf16 bits [H])."""
+    g = _c(g, np.float32)
+    x = _c(x_bf16, np.uint16).reshape(-1)
+    return float(lib().oracle_shared_gate(x.size, _p(g), _p(x)))
+
+
 def bucket(ids, E):
     ids = _c(ids, np.int32)
     T, k = ids.shape
@@ -240,7 +263,8 @@ def _layer_struct(Ld: dict, top_k: int):
                      g("gate_q", np.uint8), g("gate_s", np.uint16), g("up_q", np.uint8),
                      g("up_s", np.uint16), g("down_q", np.uint8), g("down_s", np.uint16),
                      g("sh_gate_q", np.uint8), g("sh_gate_s", np.uint16), g("sh_up_q", np.uint8),
-                     g("sh_up_s", np.uint16), g("sh_down_q", np.uint8), g("sh_down_s", np.uint16))
+                     g("sh_up_s", np.uint16), g("sh_down_q", np.uint8), g("sh_down_s", np.uint16),
+                     int(Ld.get("routing_flags", 0)), g("sh_gate_w", np.float32))
     return st, keep
 
 

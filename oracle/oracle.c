@@ -25,6 +25,15 @@
  *    scale; byte i of a row holds element 2i (low nibble), 2i+1 (high);
  *  - layer output y = sum_j w_j y_{e_j} + y_shared, shared weight 1,
  *    rounded to bf16 only at the output;
+ *  - routing variants, each off unless its flag is set (the pages give no
+ *    routing formulas, so these follow the common MoE conventions):
+ *      no renormalisation (1): w_j = softmax over all E logits, read at
+ *        the selected experts (the weights sum to less than 1);
+ *      bias for selection only (2): the selection ranks z = W_r x + b, the
+ *        weights use W_r x without b (over the selection, or over all E
+ *        with flag 1);
+ *      gated shared expert (4): the shared term is scaled per token by
+ *        sigmoid(g . x) for a gate vector g [H];
  *  - stack (pre-norm residual, RMSNorm with unit gain; a plain residual
  *    stack of these layers diverges -- the SwiGLU output grows with the
  *    square of its input): u_l = bf16(h_l / sqrt(mean(h_l^2) + 1e-6)),
@@ -162,6 +171,39 @@ void oracle_topk_softmax(int T, int E, int k, const double* z, int32_t* ids, dou
   free(buf);
 }
 
+/* Routing weights of a given selection ids [T][k] under the variant flags
+ * (1: no renormalisation, 2: bias for selection only).  zsel [T][E] are the
+ * selection logits W_r x + b; b [E] (may be NULL = 0) is removed from the
+ * weights' logits with flag 2.  Without flag 1: softmax over the k selected
+ * weight logits; with it: softmax over all E weight logits, taken at the
+ * selection. */
+void oracle_route_weights(int T, int E, int k, int flags, const double* zsel, const float* b,
+                          const int32_t* ids, double* w) {
+  for (int t = 0; t < T; ++t) {
+    const double* zt = zsel + (size_t)t * E;
+    const int32_t* it = ids + (size_t)t * k;
+    double* wt = w + (size_t)t * k;
+    const int strip = (flags & 2) && b;
+    if (flags & 1) {
+      double m = -INFINITY, den = 0.0;
+      for (int e = 0; e < E; ++e) {
+        double v = zt[e] - (strip ? (double)b[e] : 0.0);
+        m = v > m ? v : m;
+      }
+      for (int e = 0; e < E; ++e) den += exp(zt[e] - (strip ? (double)b[e] : 0.0) - m);
+      for (int j = 0; j < k; ++j) wt[j] = exp(zt[it[j]] - (strip ? (double)b[it[j]] : 0.0) - m) / den;
+    } else {
+      double m = -INFINITY, den = 0.0;
+      for (int j = 0; j < k; ++j) {
+        double v = zt[it[j]] - (strip ? (double)b[it[j]] : 0.0);
+        m = v > m ? v : m;
+      }
+      for (int j = 0; j < k; ++j) den += exp(zt[it[j]] - (strip ? (double)b[it[j]] : 0.0) - m);
+      for (int j = 0; j < k; ++j) wt[j] = exp(zt[it[j]] - (strip ? (double)b[it[j]] : 0.0) - m) / den;
+    }
+  }
+}
+
 /* The other order of the same reading: softmax over all E logits, then the
  * same selection, then renormalise the k selected probabilities. */
 void oracle_topk_softmax_full(int T, int E, int k, const double* z, int32_t* ids, double* w) {
@@ -222,15 +264,15 @@ void oracle_expert_ffn(int H, int F, const uint8_t* gq, const uint16_t* gs, cons
 }
 
 /* One token through the layer, given the selected experts' weights:
- * y = sum_j w[j] FFN(expert j) + FFN(shared).  Pointer arrays hold the k
- * selected experts' tensors; sh_* may be NULL (no shared expert). */
-void oracle_combine_token(int H, int F, int Fs, int k, const double* w,
-                          const uint8_t* const* gq, const uint16_t* const* gs,
-                          const uint8_t* const* uq, const uint16_t* const* us,
-                          const uint8_t* const* dq, const uint16_t* const* ds,
-                          const uint8_t* sh_gq, const uint16_t* sh_gs, const uint8_t* sh_uq,
-                          const uint16_t* sh_us, const uint8_t* sh_dq, const uint16_t* sh_ds,
-                          const uint16_t* x_bf16, double* y) {
+ * y = sum_j w[j] FFN(expert j) + sh_w FFN(shared).  Pointer arrays hold the
+ * k selected experts' tensors; sh_* may be NULL (no shared expert). */
+static void combine_token_w(int H, int F, int Fs, int k, const double* w,
+                            const uint8_t* const* gq, const uint16_t* const* gs,
+                            const uint8_t* const* uq, const uint16_t* const* us,
+                            const uint8_t* const* dq, const uint16_t* const* ds,
+                            const uint8_t* sh_gq, const uint16_t* sh_gs, const uint8_t* sh_uq,
+                            const uint16_t* sh_us, const uint8_t* sh_dq, const uint16_t* sh_ds,
+                            double sh_w, const uint16_t* x_bf16, double* y) {
   double* x = (double*)malloc(sizeof(double) * (size_t)H);
   double* ye = (double*)malloc(sizeof(double) * (size_t)H);
   for (int h = 0; h < H; ++h) {
@@ -243,10 +285,29 @@ void oracle_combine_token(int H, int F, int Fs, int k, const double* w,
   }
   if (Fs > 0 && sh_gq) {
     oracle_expert_ffn(H, Fs, sh_gq, sh_gs, sh_uq, sh_us, sh_dq, sh_ds, x, ye);
-    for (int h = 0; h < H; ++h) y[h] += ye[h];
+    for (int h = 0; h < H; ++h) y[h] += sh_w * ye[h];
   }
   free(x);
   free(ye);
+}
+
+/* The same with the shared expert's weight 1 (the default routing). */
+void oracle_combine_token(int H, int F, int Fs, int k, const double* w,
+                          const uint8_t* const* gq, const uint16_t* const* gs,
+                          const uint8_t* const* uq, const uint16_t* const* us,
+                          const uint8_t* const* dq, const uint16_t* const* ds,
+                          const uint8_t* sh_gq, const uint16_t* sh_gs, const uint8_t* sh_uq,
+                          const uint16_t* sh_us, const uint8_t* sh_dq, const uint16_t* sh_ds,
+                          const uint16_t* x_bf16, double* y) {
+  combine_token_w(H, F, Fs, k, w, gq, gs, uq, us, dq, ds, sh_gq, sh_gs, sh_uq, sh_us, sh_dq, sh_ds,
+                  1.0, x_bf16, y);
+}
+
+/* Gate of a gated shared expert for one token: sigmoid(sum_h g[h] x[h]). */
+double oracle_shared_gate(int H, const float* g, const uint16_t* x_bf16) {
+  double acc = 0.0;
+  for (int h = 0; h < H; ++h) acc += (double)g[h] * oracle_bf16_to_double(x_bf16[h]);
+  return 1.0 / (1.0 + exp(-acc));
 }
 
 /* ------------------------------------------------------------ whole layer */
@@ -268,6 +329,8 @@ typedef struct {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;       /* [H][Fs/2] */
   const uint16_t* sh_down_s;
+  int routing_flags;              /* 1 no renormalisation, 2 bias selects only, 4 gated shared */
+  const float* sh_gate_w;         /* [H], read with flag 4 */
 } oracle_layer;
 
 /* T tokens through one layer.  Outputs: y [T][H] fp64, and optionally the
@@ -283,25 +346,25 @@ int oracle_moe_forward(const oracle_layer* L, int T, const uint16_t* x_bf16,
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
   double* margin = (double*)malloc(sizeof(double) * (size_t)T);
+  const int flags = L->routing_flags;
+  if ((flags & ~7) || ((flags & 4) && (Fs == 0 || !L->sh_gate_w))) {
+    free(z); free(ids); free(w); free(margin);
+    return -1;
+  }
   oracle_router_logits(T, H, E, L->router_w, L->router_b, x_bf16, z);
   oracle_topk_softmax(T, E, k, z, ids, w, margin);
   if (forced_ids) {
-    for (int t = 0; t < T; ++t) {
-      double zmax = -INFINITY, den = 0.0;
-      for (int j = 0; j < k; ++j) {
-        int e = forced_ids[t * k + j];
-        if (e < 0 || e >= E) {
-          free(z); free(ids); free(w); free(margin);
-          return -2;
-        }
-        ids[t * k + j] = e;
-        double v = z[(size_t)t * E + e];
-        zmax = v > zmax ? v : zmax;
+    for (int i = 0; i < T * k; ++i) {
+      if (forced_ids[i] < 0 || forced_ids[i] >= E) {
+        free(z); free(ids); free(w); free(margin);
+        return -2;
       }
-      for (int j = 0; j < k; ++j) den += exp(z[(size_t)t * E + ids[t * k + j]] - zmax);
-      for (int j = 0; j < k; ++j) w[t * k + j] = exp(z[(size_t)t * E + ids[t * k + j]] - zmax) / den;
+      ids[i] = forced_ids[i];
     }
   }
+  /* the default weights (softmax over the selection) came with the top-k;
+     the variants and forced selections recompute them */
+  if (flags || forced_ids) oracle_route_weights(T, E, k, flags, z, L->router_b, ids, w);
   const size_t gsz = (size_t)F * (H / 2), gss = (size_t)F * (H / 32);
   const size_t dsz = (size_t)H * (F / 2), dss = (size_t)H * (F / 32);
   const uint8_t** pg = (const uint8_t**)malloc(sizeof(void*) * k);
@@ -326,9 +389,10 @@ int oracle_moe_forward(const oracle_layer* L, int T, const uint16_t* x_bf16,
       pds[j] = L->down_s + slot * dss;
     }
     if (rc) break;
-    oracle_combine_token(H, F, Fs, k, w + (size_t)t * k, pg, pgs, pu, pus, pd, pds, L->sh_gate_q,
-                         L->sh_gate_s, L->sh_up_q, L->sh_up_s, L->sh_down_q, L->sh_down_s,
-                         x_bf16 + (size_t)t * H, y + (size_t)t * H);
+    const double sh_w = (flags & 4) ? oracle_shared_gate(H, L->sh_gate_w, x_bf16 + (size_t)t * H) : 1.0;
+    combine_token_w(H, F, Fs, k, w + (size_t)t * k, pg, pgs, pu, pus, pd, pds, L->sh_gate_q,
+                    L->sh_gate_s, L->sh_up_q, L->sh_up_s, L->sh_down_q, L->sh_down_s, sh_w,
+                    x_bf16 + (size_t)t * H, y + (size_t)t * H);
   }
   if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);
   if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * k);

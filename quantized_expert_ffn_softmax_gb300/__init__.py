@@ -39,12 +39,18 @@ class moe_layer_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("ffn", ctypes.c_int32),
                 ("shared_ffn", ctypes.c_int32), ("n_slots", ctypes.c_int32),
-                ("max_tokens", ctypes.c_int32)]
+                ("max_tokens", ctypes.c_int32), ("routing_flags", ctypes.c_int32)]
+
+
+# routing variant bits of moe_layer_config.routing_flags (moe.h)
+ROUTING_NO_RENORM = 1
+ROUTING_BIAS_SELECT_ONLY = 2
+ROUTING_SHARED_GATE = 4
 
 
 WEIGHT_FIELDS = ("router_w", "router_bias", "slot_of_expert", "gate_q", "gate_s", "up_q", "up_s",
                  "down_q", "down_s", "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q",
-                 "sh_down_s")
+                 "sh_down_s", "sh_gate_w")
 
 
 class moe_layer_weights(ctypes.Structure):
@@ -143,7 +149,8 @@ def moe_layer_create(config: dict, weights: dict, weights_on_device: bool) -> in
     """Creates a layer; returns its opaque handle (an integer address)."""
     cfg = moe_layer_config(config["hidden"], config["n_experts"], config["top_k"],
                            config["ffn"], config.get("shared_ffn", 0),
-                           config.get("n_slots", config["n_experts"]), config["max_tokens"])
+                           config.get("n_slots", config["n_experts"]), config["max_tokens"],
+                           config.get("routing_flags", 0))
     w = moe_layer_weights(*[_ptr(weights.get(n)) for n in WEIGHT_FIELDS])
     out = ctypes.c_void_p()
     _check(lib().moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), int(bool(weights_on_device)),
@@ -155,7 +162,7 @@ def _cfg_struct(config: dict) -> moe_layer_config:
     return moe_layer_config(config["hidden"], config["n_experts"], config["top_k"],
                             config["ffn"], config.get("shared_ffn", 0),
                             config.get("n_slots", config["n_experts"]),
-                            config.get("max_tokens", 4))
+                            config.get("max_tokens", 4), config.get("routing_flags", 0))
 
 
 def moe_forward_noalloc(config: dict, weights: dict, x, n_tokens: int, y, status_out=None,

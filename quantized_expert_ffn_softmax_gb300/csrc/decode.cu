@@ -268,7 +268,7 @@ struct DecodeSmem {
     DecodeSmem s;
     const int C = H / 32;
     const int n_routed_max = max_units - 1;
-    s.nmy = (E + grid - 1) / grid;
+    s.nmy = (E + 1 + grid - 1) / grid;  // router rows per CTA, with room for the gate row
     s.nd_items = (H / 8 + grid - 1) / grid;
     s.g_stage = (size_t)16 * H + (size_t)64 * C;  // gate+up rows (2 x 16 x H/2) + scales
     s.d_item = (size_t)9 * ((size_t)n_routed_max * F + Fs) / 2;  // per unit: codes 4F_u, scales F_u/2
@@ -369,8 +369,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   unsigned nbar = 0;
   const uint64_t tmo = p.timeout_ns;
   const bool stack = (p.mode == kModeStack);
-  // experts of this CTA: e = blockIdx.x + j * grid, j < my_rows
-  const int my_rows = ((int)blockIdx.x < E) ? (E - (int)blockIdx.x + grid - 1) / grid : 0;
+  // Router rows of this CTA in layer l: e = blockIdx.x + j * grid, j < rows;
+  // with a gated shared expert, row E is the gate vector (its logit g . u
+  // goes to p.gz instead of the logits).
+  auto router_rows = [&](int l) {
+    const int Er = E + ((p.layers[l].routing_flags & MOE_ROUTING_SHARED_GATE) ? 1 : 0);
+    return ((int)blockIdx.x < Er) ? (Er - (int)blockIdx.x + grid - 1) / grid : 0;
+  };
 
   // Router rows of this CTA's experts for layer l (and the slot table when
   // its size and alignment allow a bulk copy), into shared memory on the R
@@ -381,13 +386,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   auto prefetch_router = [&](int l) {
     const LayerDev& W = p.layers[l];
     const bool slots_bulk = slots_bulk_of(l);
+    const int rows = router_rows(l);
     if (warp == kWarps - 1) {
-      const uint32_t bytes = (uint32_t)my_rows * H * 4u + (slots_bulk ? (uint32_t)E * 4u : 0u);
+      const uint32_t bytes = (uint32_t)rows * H * 4u + (slots_bulk ? (uint32_t)E * 4u : 0u);
       if (lane == 0 && bytes) mbar_expect_tx(&mbar[kBarR], bytes);
       __syncwarp();
-      for (int j = lane; j < my_rows; j += 32)
-        bulk_g2s(wr + (size_t)j * H, W.router_w + (size_t)(blockIdx.x + j * grid) * H, H * 4u,
+      for (int j = lane; j < rows; j += 32) {
+        const int e = blockIdx.x + j * grid;
+        bulk_g2s(wr + (size_t)j * H, (e < E) ? W.router_w + (size_t)e * H : W.sh_gate_w, H * 4u,
                  &mbar[kBarR]);
+      }
       if (slots_bulk && lane == 31) bulk_g2s(slots, W.slot_of, (uint32_t)E * 4u, &mbar[kBarR]);
     }
     if (!slots_bulk)
@@ -499,9 +507,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // router: this CTA's expert rows e = blockIdx + j*grid (prefetched W_r
     // rows); row j is split over the warps w with w % my_rows == j, each
     // summing one slice of H; the slices meet in shared memory
+    const int my_rows = router_rows(l);
     // this thread's router bias (read before the row wait, off the critical path)
-    const float bias_mine = (tid < min(my_rows, kWarps) * T)
-                                ? __ldg(W.router_b + blockIdx.x + (tid / T) * grid) : 0.0f;
+    const int e_mine = blockIdx.x + (tid / T) * grid;
+    const float bias_mine = (tid < min(my_rows, kWarps) * T && e_mine < E) ? __ldg(W.router_b + e_mine) : 0.0f;
     if (my_rows > 0 || slots_bulk_of(l)) {  // the R barrier was armed for this layer
       mbar_wait(&mbar[kBarR], ph_r, p.err, tmo);
       ph_r ^= 1u;
@@ -538,7 +547,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         float z = 0.0f;
         for (int w = jr; w < kWarps; w += nr) z += M.red_z[w][t];
         const int e = blockIdx.x + (j0 + jr) * grid;
-        p.z[(size_t)t * E + e] = z + (j0 == 0 ? bias_mine : __ldg(W.router_b + e));
+        if (e < E)
+          p.z[(size_t)t * E + e] = z + (j0 == 0 ? bias_mine : __ldg(W.router_b + e));
+        else
+          p.gz[t] = z;  // the shared-expert gate logit
       }
       __syncthreads();  // red_z is reused by the next batch
     }
@@ -586,9 +598,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
       const float zv = key_value(ok2);
-      const float z0 = __shfl_sync(0xffffffffu, zv, 0);
-      const float ex = (lane < k) ? __expf(zv - z0) : 0.0f;
-      const float den = warp_sum(ex);
+      // the weights' logits: the selection logit, or without the bias when
+      // the bias only selects
+      const int rf = W.routing_flags;
+      const bool sel_only = (rf & MOE_ROUTING_BIAS_SELECT_ONLY) != 0;
+      const float base = (sel_only && lane < k) ? zv - __ldg(W.router_b + oi2) : zv;
+      float m, den;
+      if (rf & MOE_ROUTING_NO_RENORM) {
+        // softmax over all E experts, taken at the selected ones
+        const float* zt = p.z + (size_t)warp * E;
+        m = -INFINITY;
+        for (int e = lane; e < E; e += 32)
+          m = fmaxf(m, __ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f));
+        m = warp_max(m);
+        float acc = 0.0f;
+        for (int e = lane; e < E; e += 32)
+          acc += __expf(__ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f) - m);
+        den = warp_sum(acc);
+      } else {
+        m = warp_max(lane < k ? base : -INFINITY);
+        den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
+      }
+      const float ex = (lane < k) ? __expf(base - m) : 0.0f;
       if (lane < k) {
         M.sel_id[warp][lane] = oi2;
         M.sel_w[warp][lane] = ex / den;
@@ -656,7 +687,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     {
       // the shared expert is the unit after the routed ones, weight 1
       const int nr = (TT == 1) ? k : M.n_routed;
-      if (Fs > 0 && tid < kMaxDecodeTokens) M.unit_w[nr][tid] = (tid < T) ? 1.0f : 0.0f;
+      if (Fs > 0 && tid < kMaxDecodeTokens) {
+        float ws = 1.0f;  // gated: sigmoid of the gate logit a CTA wrote before the barrier
+        if ((W.routing_flags & MOE_ROUTING_SHARED_GATE) && tid < T) ws = 1.0f / (1.0f + __expf(-__ldcg(p.gz + tid)));
+        M.unit_w[nr][tid] = (tid < T) ? ws : 0.0f;
+      }
     }
     // the router rows and slot table were read through the generic proxy;
     // the next layer's bulk copies (async proxy) overwrite them

@@ -328,10 +328,14 @@ __device__ __forceinline__ float silu_fast(float g) {
 // value, ties to the lower id; then softmax over the selected logits.  Lane
 // r < k receives id and weight r.  Returns false if a non-finite logit left
 // no valid candidate.  LDCG: read the logits through L2 only (they were
-// written by other CTAs of the same launch).
+// written by other CTAs of the same launch).  Routing variants: with bsel
+// (the bias, which then only selects) the weights use z_e - bsel[e]; with
+// renorm false they are the softmax over all E such values, taken at the
+// selection, instead of the softmax over the selection.
 template <bool LDCG>
-__device__ __forceinline__ bool warp_topk_softmax_impl(const float* z, int E, int k, int* id_out,
-                                                       float* w_out) {
+__device__ __forceinline__ bool warp_topk_softmax_impl(const float* z, int E, int k,
+                                                       const float* bsel, bool renorm,
+                                                       int* id_out, float* w_out) {
   const int lane = threadIdx.x & 31;
   float v[kMaxExperts / 32];
   const int nj = (E + 31) / 32;
@@ -377,20 +381,36 @@ __device__ __forceinline__ bool warp_topk_softmax_impl(const float* z, int E, in
       my_z = bv;
     }
   }
-  const float ex = (lane < k) ? __expf(my_z - z0) : 0.0f;
-  const float den = warp_sum(ex);
+  const float base = (bsel && lane < k) ? my_z - __ldg(bsel + my_id) : my_z;
+  float m = z0, den;
+  if (renorm) {
+    if (bsel) m = warp_max(lane < k ? base : -INFINITY);
+    den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
+  } else {
+    float mm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (j < nj && e < E) mm = fmaxf(mm, v[j] - (bsel ? __ldg(bsel + e) : 0.0f));
+    }
+    m = warp_max(mm);
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (j < nj && e < E) acc += __expf(v[j] - (bsel ? __ldg(bsel + e) : 0.0f) - m);
+    }
+    den = warp_sum(acc);
+  }
+  const float ex = (lane < k) ? __expf(base - m) : 0.0f;
   *id_out = my_id;
   *w_out = ex / den;
   return ok;
 }
 
-__device__ __forceinline__ bool warp_topk_softmax(const float* z, int E, int k, int* id_out,
-                                                  float* w_out) {
-  return warp_topk_softmax_impl<false>(z, E, k, id_out, w_out);
-}
-__device__ __forceinline__ bool warp_topk_softmax_ldcg(const float* z, int E, int k, int* id_out,
-                                                       float* w_out) {
-  return warp_topk_softmax_impl<true>(z, E, k, id_out, w_out);
+__device__ __forceinline__ bool warp_topk_softmax(const float* z, int E, int k, const float* bsel,
+                                                  bool renorm, int* id_out, float* w_out) {
+  return warp_topk_softmax_impl<false>(z, E, k, bsel, renorm, id_out, w_out);
 }
 
 }  // namespace dev

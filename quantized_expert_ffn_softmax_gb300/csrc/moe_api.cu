@@ -76,6 +76,11 @@ moe_status validate_config(const moe_layer_config* c) {
     return fail(MOE_ERR_INVALID, "n_slots=%d must equal n_experts=%d", c->n_slots, c->n_experts);
   if (c->max_tokens < 1 || c->max_tokens > 65536)
     return fail(MOE_ERR_INVALID, "max_tokens=%d: need 1..65536", c->max_tokens);
+  const int known = MOE_ROUTING_NO_RENORM | MOE_ROUTING_BIAS_SELECT_ONLY | MOE_ROUTING_SHARED_GATE;
+  if (c->routing_flags & ~known)
+    return fail(MOE_ERR_INVALID, "routing_flags=0x%x has unknown bits", c->routing_flags);
+  if ((c->routing_flags & MOE_ROUTING_SHARED_GATE) && c->shared_ffn == 0)
+    return fail(MOE_ERR_INVALID, "MOE_ROUTING_SHARED_GATE needs a shared expert (shared_ffn > 0)");
   return MOE_OK;
 }
 
@@ -93,7 +98,7 @@ void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
 extern "C" {
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 200; }
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
@@ -109,6 +114,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (cfg->shared_ffn > 0 && (!w->sh_gate_q || !w->sh_gate_s || !w->sh_up_q || !w->sh_up_s ||
                               !w->sh_down_q || !w->sh_down_s))
     return fail(MOE_ERR_INVALID, "shared_ffn > 0 but a shared-expert pointer is NULL");
+  if ((cfg->routing_flags & MOE_ROUTING_SHARED_GATE) && !w->sh_gate_w)
+    return fail(MOE_ERR_INVALID, "MOE_ROUTING_SHARED_GATE but sh_gate_w is NULL");
   const char* fault = getenv("MOE_FAULT_ALLOC");
   if (fault && atoi(fault) == 1) return fail(MOE_ERR_OOM, "allocation failure injected by MOE_FAULT_ALLOC");
 
@@ -167,6 +174,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     i_sdq = add(w->sh_down_q, (size_t)H * (Fs / 2));
     i_sds = add(w->sh_down_s, (size_t)H * (Fs / 32) * 2);
   }
+  const bool gated = (cfg->routing_flags & MOE_ROUTING_SHARED_GATE) != 0;
+  size_t i_sgw = 0;
+  if (gated) i_sgw = add(w->sh_gate_w, sizeof(float) * H);
   L->weights_bytes = align_up(off, 256);
   cudaError_t e = cudaMalloc(&L->weights_block, L->weights_bytes);
   if (e != cudaSuccess) {
@@ -202,6 +212,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     L->dev.sh_down_q = (const uint8_t*)at(i_sdq);
     L->dev.sh_down_s = (const uint16_t*)at(i_sds);
   }
+  L->dev.sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
+  L->dev.routing_flags = cfg->routing_flags;
 
   // ---- workspace
   const int Fmax = F > Fs ? F : Fs;
@@ -224,6 +236,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   size_t o_ul = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_is = wadd(sizeof(int32_t) * (size_t)Tm * k);
   size_t o_ws = wadd(sizeof(float) * (size_t)Tm * k);
+  size_t o_gz = wadd(sizeof(float) * moe::kMaxDecodeTokens);
+  size_t o_gw = wadd(sizeof(float) * (size_t)Tm);
   size_t o_pf = wadd(moe::prefill_workspace_bytes(*cfg));
   L->ws.bytes = align_up(wo, 256);
   e = cudaMalloc(&L->ws_block, L->ws.bytes);
@@ -243,6 +257,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->ws.u_layer = (uint16_t*)(wb + o_ul);
   L->ws.ids_stage = (int32_t*)(wb + o_is);
   L->ws.w_stage = (float*)(wb + o_ws);
+  L->ws.gz = (float*)(wb + o_gz);
+  L->ws.gw = (float*)(wb + o_gw);
   L->ws.scratch = wb + o_pf;
   e = cudaMemset(L->ws_block, 0, L->ws.bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -324,6 +340,7 @@ moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
   p.max_units = ((T * c.top_k < c.n_experts) ? T * c.top_k : c.n_experts) + 1;
   p.xbuf = L0->ws.xbuf;
   p.z = L0->ws.z;
+  p.gz = L0->ws.gz;
   p.hbuf = L0->ws.hbuf;
   p.bar = L0->ws.bar;
   p.err = L0->ws.err;

@@ -35,6 +35,8 @@ struct LayerDev {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
+  const float* sh_gate_w;  // [H] shared-expert gate vector (MOE_ROUTING_SHARED_GATE)
+  int routing_flags;       // MOE_ROUTING_* bits
 };
 
 // Generation-counting grid barrier state (one per workspace, 128-B aligned).
@@ -60,6 +62,7 @@ struct DecodeParams {
   float* w_out;          // [L][T][k] or null
   uint16_t* xbuf;        // [2][4][H] residual ping-pong
   float* z;              // [4][E]
+  float* gz;             // [4] shared-expert gate logits g . u (MOE_ROUTING_SHARED_GATE)
   float* hbuf;           // [max_units-ish][4][Fmax] fp32
   GridBarrier* bar;
   int* err;
@@ -85,6 +88,8 @@ struct Workspace {
   uint16_t* u_layer = nullptr;  // [max_tokens][H] per-layer normalised input (same)
   int32_t* ids_stage = nullptr; // [max_tokens][k]
   float* w_stage = nullptr;     // [max_tokens][k]
+  float* gz = nullptr;          // [4] decode: shared-expert gate logits
+  float* gw = nullptr;          // [max_tokens] prefill: shared-expert gate weights
   // prefill
   __half* x16 = nullptr;        // [max_tokens][H] fp16, per-token scaled, K-permuted
   int32_t* xshift = nullptr;    // [max_tokens] per-token power-of-two shift

@@ -57,6 +57,10 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
       k > moe::kMaxTopK || k > E || F < 128 || F > 4096 || F % 128 || Fs < 0 || Fs > 4096 ||
       Fs % 128 || cfg->n_slots != E)
     return fail(MOE_ERR_INVALID, "layer shape outside the library's limits");
+  const int known = MOE_ROUTING_NO_RENORM | MOE_ROUTING_BIAS_SELECT_ONLY | MOE_ROUTING_SHARED_GATE;
+  const bool gated = (cfg->routing_flags & MOE_ROUTING_SHARED_GATE) != 0;
+  if ((cfg->routing_flags & ~known) || (gated && (Fs == 0 || !w->sh_gate_w)))
+    return fail(MOE_ERR_INVALID, "routing_flags unknown, or a shared gate without shared expert or sh_gate_w");
   if (n_tokens < 1 || n_tokens > moe::kMaxDecodeTokens)
     return fail(MOE_ERR_CAPACITY, "n_tokens must be 1..4 for the allocation-free entry point");
   if (!w->router_w || !w->router_bias || !w->slot_of_expert || !w->gate_q || !w->gate_s ||
@@ -76,7 +80,8 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   const size_t o_err = up256(o_bar + sizeof(moe::GridBarrier));
   const size_t o_xbuf = up256(o_err + 16);
   const size_t o_z = up256(o_xbuf + sizeof(uint16_t) * 2 * moe::kMaxDecodeTokens * H);
-  const size_t o_h = up256(o_z + sizeof(float) * moe::kMaxDecodeTokens * E);
+  const size_t o_gz = up256(o_z + sizeof(float) * moe::kMaxDecodeTokens * E);
+  const size_t o_h = up256(o_gz + sizeof(float) * moe::kMaxDecodeTokens);
   const size_t need = o_h + sizeof(float) * moe::kMaxDecodeTokens * ((size_t)routed_max * F + Fs);
   if (need > kNoAllocScratchBytes)
     return fail(MOE_ERR_CAPACITY,
@@ -125,6 +130,7 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   p.y_out = static_cast<uint16_t*>(y_bf16);
   p.xbuf = reinterpret_cast<uint16_t*>(sb + o_xbuf);
   p.z = reinterpret_cast<float*>(sb + o_z);
+  p.gz = reinterpret_cast<float*>(sb + o_gz);
   p.hbuf = reinterpret_cast<float*>(sb + o_h);
   p.bar = reinterpret_cast<moe::GridBarrier*>(sb + o_bar);
   p.err = err;
@@ -144,6 +150,8 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   p.layers[0].sh_up_s = w->sh_up_s;
   p.layers[0].sh_down_q = w->sh_down_q;
   p.layers[0].sh_down_s = w->sh_down_s;
+  p.layers[0].sh_gate_w = gated ? w->sh_gate_w : nullptr;
+  p.layers[0].routing_flags = cfg->routing_flags;
   int num_sms = 0;
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();

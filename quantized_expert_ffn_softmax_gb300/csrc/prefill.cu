@@ -139,6 +139,7 @@ struct GemmParams {
   __half* hmid_s;
   float* yacc;
   float* z;
+  const float* gw;           // [T] shared-expert gate weights, or null (weight 1)
   int router_shift;
   int* err;
   unsigned long long timeout_ns;
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           reinterpret_cast<float*>(meta_i)[r] = pow2f(-sx);
         } else if (MODE == kScatter) {
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
-          const float wgt = U.shared ? 1.0f : __ldg(p.perm_w + U.p0 + r);
+          const float wgt = U.shared ? (p.gw ? __ldg(p.gw + tok) : 1.0f) : __ldg(p.perm_w + U.p0 + r);
           meta_i[r] = tok;
           meta_f[r] = wgt * pow2f(2 * __ldg(p.xshift + tok));
         } else {
@@ -777,17 +778,42 @@ __global__ void prep_x16_kernel(const uint16_t* __restrict__ x, int T, int H,
   }
 }
 
+// One warp per token: top-k and routing weights (with the layer's routing
+// variants: bsel = the bias when it only selects, renorm), and, for a gated
+// shared expert, gw[t] = sigmoid(gate . x_t) over the bf16 input row.
 __global__ void topk_kernel(const float* __restrict__ z, int T, int E, int k,
-                            int32_t* __restrict__ ids, float* __restrict__ w, int* err) {
+                            const float* __restrict__ bsel, int renorm,
+                            const float* __restrict__ gate, const uint16_t* __restrict__ x, int H,
+                            float* __restrict__ gw, int32_t* __restrict__ ids,
+                            float* __restrict__ w, int* err) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   int id;
   float wt;
-  const bool ok = warp_topk_softmax(z + (size_t)t * E, E, k, &id, &wt);
+  const bool ok = warp_topk_softmax(z + (size_t)t * E, E, k, bsel, renorm != 0, &id, &wt);
   if (!ok && lane == 0) atomicCAS(err, 0, (int)MOE_ERR_BOUNDS);
   if (lane < k) {
     ids[(size_t)t * k + lane] = id;
     w[(size_t)t * k + lane] = wt;
+  }
+  if (gate) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const float4* gr = reinterpret_cast<const float4*>(gate);
+    float acc = 0.0f;
+    for (int g = lane; g < H / 8; g += 32) {
+      const uint4 xv = __ldg(xr + g);
+      const float4 g0 = __ldg(gr + 2 * g), g1 = __ldg(gr + 2 * g + 1);
+      acc = fmaf(g0.x, __uint_as_float(xv.x << 16), acc);
+      acc = fmaf(g0.y, __uint_as_float(xv.x & 0xffff0000u), acc);
+      acc = fmaf(g0.z, __uint_as_float(xv.y << 16), acc);
+      acc = fmaf(g0.w, __uint_as_float(xv.y & 0xffff0000u), acc);
+      acc = fmaf(g1.x, __uint_as_float(xv.z << 16), acc);
+      acc = fmaf(g1.y, __uint_as_float(xv.z & 0xffff0000u), acc);
+      acc = fmaf(g1.z, __uint_as_float(xv.w << 16), acc);
+      acc = fmaf(g1.w, __uint_as_float(xv.w & 0xffff0000u), acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) gw[t] = 1.0f / (1.0f + __expf(-acc));
   }
 }
 
@@ -1235,6 +1261,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.hmid_s = ws.hmid_s;
   gp.yacc = ws.yacc;
   gp.z = ws.zf;
+  gp.gw = (c.routing_flags & MOE_ROUTING_SHARED_GATE) ? L->ws.gw : nullptr;
   gp.router_shift = L->router_shift;
   gp.err = ws.err;
   gp.timeout_ns = 1000000000ull;
@@ -1250,7 +1277,11 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   float* wts = (route_only && w_out) ? w_out : ws.topk_w;
   {
     prof::Scope sc("moe_topk", s);
-    topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(ws.zf, T, E, k, ids, wts, ws.err);
+    const int rf = c.routing_flags;
+    topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(
+        ws.zf, T, E, k, (rf & MOE_ROUTING_BIAS_SELECT_ONLY) ? L->dev.router_b : nullptr,
+        (rf & MOE_ROUTING_NO_RENORM) ? 0 : 1, (rf & MOE_ROUTING_SHARED_GATE) ? L->dev.sh_gate_w : nullptr,
+        x, H, L->ws.gw, ids, wts, ws.err);
   }
   if (route_only) {
     if ((e = cudaGetLastError()) != cudaSuccess) {

@@ -33,7 +33,7 @@ def h_tol(y_ref, h_ref) -> float:
 
 def config_dict(cfg: W.MoEConfig, max_tokens: int) -> dict:
     return dict(hidden=cfg.hidden, n_experts=cfg.n_experts, top_k=cfg.top_k, ffn=cfg.ffn,
-                shared_ffn=cfg.shared_ffn, max_tokens=max_tokens)
+                shared_ffn=cfg.shared_ffn, max_tokens=max_tokens, routing_flags=cfg.routing_flags)
 
 
 def host_weights(Ld: dict) -> dict:
@@ -42,6 +42,8 @@ def host_weights(Ld: dict) -> dict:
     if "sh_gate_q" in Ld:
         for n in NAMES:
             w["sh_" + n] = Ld["sh_" + n]
+    if "sh_gate_w" in Ld:
+        w["sh_gate_w"] = Ld["sh_gate_w"]
     return w
 
 
@@ -57,6 +59,8 @@ def make_layer_device(cfg, layer_idx, max_tokens=16):
     if cfg.shared_ffn:
         for n in NAMES:
             w["sh_" + n] = Dd["sh_" + n]
+    if "sh_gate_w" in Dd:
+        w["sh_gate_w"] = Dd["sh_gate_w"]
     torch.cuda.synchronize()
     layer = moe.MoELayer(config_dict(cfg, max_tokens), w, True)
     del Dd, w

@@ -32,6 +32,7 @@ _DEV_SO = os.path.join(_HERE, "_gen_device.so")
 
 T_ROUTER, T_GATE, T_UP, T_DOWN, T_SH_GATE, T_SH_UP, T_SH_DOWN = 1, 2, 3, 4, 5, 6, 7
 T_X, T_BIAS_PERM, T_SLOT_PERM, T_DRAFT = 8, 9, 10, 11
+T_SH_GATE_W = 12  # gate vector of a gated shared expert
 
 
 @dataclasses.dataclass(frozen=True)
@@ -54,6 +55,7 @@ class MoEConfig:
     seed: int = 0
     weight_sigma: float = 0.02
     router_sigma: float = 0.02
+    routing_flags: int = 0  # routing variant bits (1 no renorm, 2 bias selects only, 4 gated shared)
 
     @property
     def n_slots(self) -> int:
@@ -196,6 +198,15 @@ def router(cfg: MoEConfig, layer: int):
     return w, b
 
 
+def shared_gate_vector(cfg: MoEConfig, layer: int) -> np.ndarray:
+    """fp32 [H] gate vector of a gated shared expert, router_sigma * N(0,1)."""
+    g = np.empty((1, cfg.hidden), np.float32)
+    rc = _hostlib().gen_dense_matrix(cfg.seed, cfg.wset, layer, T_SH_GATE_W, 0, 1, cfg.hidden,
+                                     cfg.router_sigma, _ptr(g), None, _nthreads())
+    assert rc == 0
+    return g.reshape(-1)
+
+
 def slot_table(cfg: MoEConfig, layer: int) -> np.ndarray:
     """int32 [E]: slot of each logical expert (identity or seeded permutation)."""
     t = np.arange(cfg.n_experts, dtype=np.int32)
@@ -242,6 +253,9 @@ def layer(cfg: MoEConfig, layer_idx: int) -> dict:
     if sh is not None:
         for k, v in sh.items():
             out["sh_" + k] = v
+    if cfg.routing_flags & 4:
+        out["sh_gate_w"] = shared_gate_vector(cfg, layer_idx)
+    out["routing_flags"] = cfg.routing_flags
     return out
 
 
@@ -333,4 +347,6 @@ def device_layer(cfg: MoEConfig, layer_idx: int, device="cuda", stream=None) -> 
                                            cfg.weight_sigma, q.data_ptr(), s.data_ptr(), st)
             assert rc == 0, rc
             out[name + "_q"], out[name + "_s"] = q, s
+    if cfg.routing_flags & 4:
+        out["sh_gate_w"] = torch.from_numpy(shared_gate_vector(cfg, layer_idx)).to(device)
     return out
