@@ -226,7 +226,8 @@ def build_stack(cfg, max_tokens):
     import torch
 
     config = dict(hidden=cfg.hidden, n_experts=cfg.n_experts, top_k=cfg.top_k, ffn=cfg.ffn,
-                  shared_ffn=cfg.shared_ffn, max_tokens=max_tokens)
+                  shared_ffn=cfg.shared_ffn, max_tokens=max_tokens,
+                  routing_flags=cfg.routing_flags)
     layers = []
     for l in range(cfg.n_layers):
         D = W.device_layer(cfg, l)
@@ -236,6 +237,8 @@ def build_stack(cfg, max_tokens):
         if cfg.shared_ffn:
             for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
                 w["sh_" + n] = D["sh_" + n]
+        if "sh_gate_w" in D:
+            w["sh_gate_w"] = D["sh_gate_w"]
         torch.cuda.synchronize()
         layers.append(moe.MoELayer(config, w, True))
         del D, w
@@ -469,7 +472,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     help="time one workload only (profiling cases): decode35b, mtp35b, "
-                         "decode125b or prefill125b")
+                         "decode125b, decode35b_variants or prefill125b")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only on a decode workload: use the first N layers")
     args = ap.parse_args()
@@ -500,10 +503,14 @@ def main():
     head = bench_decode(HEADLINE, args.steps, args.warmup, dist, with_e2e=True)
     extra = {}
     if not args.no_extra:
-        for nm in ("mtp35b", "decode125b"):
+        for nm in ("mtp35b", "decode125b", "decode35b_variants"):
             r = bench_decode(nm, max(20, args.steps // 2), args.warmup, dist)
             r["frac_of_peak_kernel"] = r["gbs_kernel"] / hbm if r["gbs_kernel"] else None
             extra[nm] = r
+        # routing variants: per-layer time beside the default headline stack
+        v = extra["decode35b_variants"]
+        v["us_per_layer"] = v["ms_per_step"] * 1e3 / W.CONFIGS["decode35b_variants"].n_layers
+        v["default_us_per_layer"] = head["ms_per_step"] * 1e3 / W.CONFIGS[HEADLINE].n_layers
         pf = bench_prefill("prefill125b", max(10, args.steps // 10), args.warmup, dist)
         g = pf["kernels"].get("moe_gemm_gateup_swiglu", {})
         pf["roofline_gateup"] = {"bound": "tensor", "achieved": g.get("tflops"), "peak": bf16,

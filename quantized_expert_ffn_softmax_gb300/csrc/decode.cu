@@ -330,7 +330,9 @@ static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 // mbarrier slots
 enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarD = 4, kBarR = 5 };
 
-template <int TT>
+// kVar: some layer of the launch uses a routing variant (routing_flags != 0);
+// the default instantiation carries none of their code.
+template <int TT, bool kVar>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     moe_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -372,9 +374,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // Router rows of this CTA in layer l: e = blockIdx.x + j * grid, j < rows;
   // with a gated shared expert, row E is the gate vector (its logit g . u
   // goes to p.gz instead of the logits).
+  const int rows_e = ((int)blockIdx.x < E) ? (E - (int)blockIdx.x + grid - 1) / grid : 0;
   auto router_rows = [&](int l) {
-    const int Er = E + ((p.layers[l].routing_flags & MOE_ROUTING_SHARED_GATE) ? 1 : 0);
-    return ((int)blockIdx.x < Er) ? (Er - (int)blockIdx.x + grid - 1) / grid : 0;
+    if constexpr (!kVar) {
+      return rows_e;
+    } else {
+      const int Er = E + ((p.routing_flags[l] & MOE_ROUTING_SHARED_GATE) ? 1 : 0);
+      return ((int)blockIdx.x < Er) ? (Er - (int)blockIdx.x + grid - 1) / grid : 0;
+    }
   };
 
   // Router rows of this CTA's experts for layer l (and the slot table when
@@ -393,8 +400,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       __syncwarp();
       for (int j = lane; j < rows; j += 32) {
         const int e = blockIdx.x + j * grid;
-        bulk_g2s(wr + (size_t)j * H, (e < E) ? W.router_w + (size_t)e * H : W.sh_gate_w, H * 4u,
-                 &mbar[kBarR]);
+        bulk_g2s(wr + (size_t)j * H, (!kVar || e < E) ? W.router_w + (size_t)e * H : p.sh_gate_w[l],
+                 H * 4u, &mbar[kBarR]);
       }
       if (slots_bulk && lane == 31) bulk_g2s(slots, W.slot_of, (uint32_t)E * 4u, &mbar[kBarR]);
     }
@@ -509,8 +516,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // summing one slice of H; the slices meet in shared memory
     const int my_rows = router_rows(l);
     // this thread's router bias (read before the row wait, off the critical path)
-    const int e_mine = blockIdx.x + (tid / T) * grid;
-    const float bias_mine = (tid < min(my_rows, kWarps) * T && e_mine < E) ? __ldg(W.router_b + e_mine) : 0.0f;
+    const float bias_mine =
+        (tid < min(my_rows, kWarps) * T && (!kVar || (int)blockIdx.x + (tid / T) * grid < E))
+            ? __ldg(W.router_b + blockIdx.x + (tid / T) * grid) : 0.0f;
     if (my_rows > 0 || slots_bulk_of(l)) {  // the R barrier was armed for this layer
       mbar_wait(&mbar[kBarR], ph_r, p.err, tmo);
       ph_r ^= 1u;
@@ -547,7 +555,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         float z = 0.0f;
         for (int w = jr; w < kWarps; w += nr) z += M.red_z[w][t];
         const int e = blockIdx.x + (j0 + jr) * grid;
-        if (e < E)
+        if (!kVar || e < E)
           p.z[(size_t)t * E + e] = z + (j0 == 0 ? bias_mine : __ldg(W.router_b + e));
         else
           p.gz[t] = z;  // the shared-expert gate logit
@@ -598,28 +606,37 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
       const float zv = key_value(ok2);
-      // the weights' logits: the selection logit, or without the bias when
-      // the bias only selects
-      const int rf = W.routing_flags;
-      const bool sel_only = (rf & MOE_ROUTING_BIAS_SELECT_ONLY) != 0;
-      const float base = (sel_only && lane < k) ? zv - __ldg(W.router_b + oi2) : zv;
-      float m, den;
-      if (rf & MOE_ROUTING_NO_RENORM) {
-        // softmax over all E experts, taken at the selected ones
-        const float* zt = p.z + (size_t)warp * E;
-        m = -INFINITY;
-        for (int e = lane; e < E; e += 32)
-          m = fmaxf(m, __ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f));
-        m = warp_max(m);
-        float acc = 0.0f;
-        for (int e = lane; e < E; e += 32)
-          acc += __expf(__ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f) - m);
-        den = warp_sum(acc);
+      float ex, den;
+      if constexpr (kVar) {
+        // the weights' logits: the selection logit, or without the bias when
+        // the bias only selects
+        const int rf = p.routing_flags[l];
+        const bool sel_only = (rf & MOE_ROUTING_BIAS_SELECT_ONLY) != 0;
+        const float base = (sel_only && lane < k) ? zv - __ldg(W.router_b + oi2) : zv;
+        float m;
+        if (rf & MOE_ROUTING_NO_RENORM) {
+          // softmax over all E experts, taken at the selected ones
+          const float* zt = p.z + (size_t)warp * E;
+          m = -INFINITY;
+          for (int e = lane; e < E; e += 32)
+            m = fmaxf(m, __ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f));
+          m = warp_max(m);
+          float acc = 0.0f;
+          for (int e = lane; e < E; e += 32)
+            acc += __expf(__ldcg(zt + e) - (sel_only ? __ldg(W.router_b + e) : 0.0f) - m);
+          den = warp_sum(acc);
+        } else {
+          // lane 0 holds the largest selection logit; with the bias removed
+          // the order may change, so take the maximum
+          m = sel_only ? warp_max(lane < k ? base : -INFINITY) : __shfl_sync(0xffffffffu, zv, 0);
+          den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
+        }
+        ex = (lane < k) ? __expf(base - m) : 0.0f;
       } else {
-        m = warp_max(lane < k ? base : -INFINITY);
-        den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
+        const float z0 = __shfl_sync(0xffffffffu, zv, 0);
+        ex = (lane < k) ? __expf(zv - z0) : 0.0f;
+        den = warp_sum(ex);
       }
-      const float ex = (lane < k) ? __expf(base - m) : 0.0f;
       if (lane < k) {
         M.sel_id[warp][lane] = oi2;
         M.sel_w[warp][lane] = ex / den;
@@ -689,7 +706,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int nr = (TT == 1) ? k : M.n_routed;
       if (Fs > 0 && tid < kMaxDecodeTokens) {
         float ws = 1.0f;  // gated: sigmoid of the gate logit a CTA wrote before the barrier
-        if ((W.routing_flags & MOE_ROUTING_SHARED_GATE) && tid < T) ws = 1.0f / (1.0f + __expf(-__ldcg(p.gz + tid)));
+        if (kVar && (p.routing_flags[l] & MOE_ROUTING_SHARED_GATE) && tid < T)
+          ws = 1.0f / (1.0f + __expf(-__ldcg(p.gz + tid)));
         M.unit_w[nr][tid] = (tid < T) ? ws : 0.0f;
       }
     }
@@ -979,7 +997,9 @@ size_t decode_smem_bytes(const DecodeParams& p) {
 template <int TT>
 static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int num_sms,
                             const char** why) {
-  auto kern = moe_decode_kernel<TT>;
+  bool var = false;
+  for (int l = 0; l < p_in.n_layers; ++l) var = var || p_in.routing_flags[l] != 0;
+  auto kern = var ? moe_decode_kernel<TT, true> : moe_decode_kernel<TT, false>;
   DecodeParams p = p_in;
   const int grid = num_sms;  // one CTA per SM
   // most staging that fits: 2 gate/up stages and the down weights in shared

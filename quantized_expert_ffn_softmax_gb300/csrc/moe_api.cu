@@ -212,8 +212,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     L->dev.sh_down_q = (const uint8_t*)at(i_sdq);
     L->dev.sh_down_s = (const uint16_t*)at(i_sds);
   }
-  L->dev.sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
-  L->dev.routing_flags = cfg->routing_flags;
+  L->sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
 
   // ---- workspace
   const int Fmax = F > Fs ? F : Fs;
@@ -368,7 +367,11 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
     p.in_trace = in_trace ? in_trace + (size_t)l0 * T * H : nullptr;
     p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
     p.w_out = w_out;
-    for (int l = 0; l < nl; ++l) p.layers[l] = layers[l0 + l]->dev;
+    for (int l = 0; l < nl; ++l) {
+      p.layers[l] = layers[l0 + l]->dev;
+      p.routing_flags[l] = layers[l0 + l]->cfg.routing_flags;
+      p.sh_gate_w[l] = layers[l0 + l]->sh_gate_w;
+    }
     const char* why = "";
     moe_status st = moe::launch_decode(p, stream, L0->num_sms, &why);
     if (st != MOE_OK) return fail(st, "decode launch: %s", why);

@@ -35,8 +35,6 @@ struct LayerDev {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
-  const float* sh_gate_w;  // [H] shared-expert gate vector (MOE_ROUTING_SHARED_GATE)
-  int routing_flags;       // MOE_ROUTING_* bits
 };
 
 // Generation-counting grid barrier state (one per workspace, 128-B aligned).
@@ -73,6 +71,10 @@ struct DecodeParams {
   int want_dprefetch;  // set by the launcher: stage the down weights in shared memory
   int g_stages;        // set by the launcher: gate/up shared-memory stages (1 or 2)
   LayerDev layers[kMaxLayersPerLaunch];
+  // per layer: MOE_ROUTING_* bits and the shared-expert gate vector [H]
+  // (MOE_ROUTING_SHARED_GATE), kept apart from the weight pointers
+  int routing_flags[kMaxLayersPerLaunch];
+  const float* sh_gate_w[kMaxLayersPerLaunch];
 };
 
 // Workspace of one layer object.
@@ -128,6 +130,7 @@ struct moe_layer {
   CUtensorMap tmap_sh_up;    // shared expert [Fs][H/2]
   CUtensorMap tmap_sh_down;  // shared expert [H][Fs/2]
   int router_shift = 0;               // router weights are scaled by 2^router_shift
+  const float* sh_gate_w = nullptr;   // [H] device copy of the shared-expert gate vector, or null
   void* weights_block = nullptr;  // one allocation holding all weight copies
   size_t weights_bytes = 0;
   void* ws_block = nullptr;       // one allocation holding the workspace

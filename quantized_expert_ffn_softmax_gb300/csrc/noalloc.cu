@@ -150,8 +150,8 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   p.layers[0].sh_up_s = w->sh_up_s;
   p.layers[0].sh_down_q = w->sh_down_q;
   p.layers[0].sh_down_s = w->sh_down_s;
-  p.layers[0].sh_gate_w = gated ? w->sh_gate_w : nullptr;
-  p.layers[0].routing_flags = cfg->routing_flags;
+  p.sh_gate_w[0] = gated ? w->sh_gate_w : nullptr;
+  p.routing_flags[0] = cfg->routing_flags;
   int num_sms = 0;
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();

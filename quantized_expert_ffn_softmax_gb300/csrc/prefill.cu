@@ -1280,7 +1280,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
     const int rf = c.routing_flags;
     topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(
         ws.zf, T, E, k, (rf & MOE_ROUTING_BIAS_SELECT_ONLY) ? L->dev.router_b : nullptr,
-        (rf & MOE_ROUTING_NO_RENORM) ? 0 : 1, (rf & MOE_ROUTING_SHARED_GATE) ? L->dev.sh_gate_w : nullptr,
+        (rf & MOE_ROUTING_NO_RENORM) ? 0 : 1, (rf & MOE_ROUTING_SHARED_GATE) ? L->sh_gate_w : nullptr,
         x, H, L->ws.gw, ids, wts, ws.err);
   }
   if (route_only) {

@@ -86,6 +86,11 @@ CONFIGS = {
                                 2, 3, draft_sigma=0.1),
     "decode125b": MoEConfig("decode125b", 1, 48, 2048, 512, 10, 768, 1536, True, 1.1, 4, 4),
     "prefill125b": MoEConfig("prefill125b", 8192, 1, 2048, 512, 10, 768, 1536, True, 1.1, 4, 5),
+    # the decode35b shape (first 8 layers, same weights and inputs) with every
+    # routing variant on: no renormalisation, bias for selection only, gated
+    # shared expert
+    "decode35b_variants": MoEConfig("decode35b_variants", 1, 8, 2048, 256, 8, 512, 512, False,
+                                    1.1, 2, 2, routing_flags=7),
 }
 
 
