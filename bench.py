@@ -437,6 +437,15 @@ def oracle_decode_sample(cfg, n_tokens: int, n_layers: int):
     return per_token_full, desc
 
 
+def headline_config(n_gpus):
+    """The headline workload's config object, shared by both arms."""
+    return {"workload": HEADLINE, "layers": 40, "hidden": 2048, "experts": 256, "top_k": 8,
+            "ffn": 512, "shared_ffn": 512, "tokens_per_step": 1,
+            "weights": "int4, 32-block, fp16 scale", "input_ring": 64,
+            "l2": "expert bytes per step 637 MB > 129 MB L2; 64-input ring",
+            "parallelism": "replica per GPU" if n_gpus > 1 else "single GPU"}
+
+
 def run_reference(args):
     cfg = W.CONFIGS[HEADLINE]
     import oracle
@@ -454,7 +463,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": HEADLINE},
+            "data": "synthetic", "config": headline_config(args.gpus),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -535,11 +544,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": HEADLINE, "layers": 40, "hidden": 2048, "experts": 256, "top_k": 8,
-                   "ffn": 512, "shared_ffn": 512, "tokens_per_step": 1,
-                   "weights": "int4, 32-block, fp16 scale", "input_ring": 64,
-                   "l2": "expert bytes per step 637 MB > 129 MB L2; 64-input ring",
-                   "parallelism": "replica per GPU" if dist.n > 1 else "single GPU"},
+        "config": headline_config(dist.n),
         "roofline": {"bound": "hbm", "achieved": head["gbs_kernel"], "peak": hbm, "unit": "GB/s",
                      "frac": (head["gbs_kernel"] or 0) / hbm,
                      "traffic": ncu_traffic("moe_decode_kernel:" + HEADLINE, src),
