@@ -73,7 +73,11 @@ enum {
  * ffn % 128 == 0 and 128 <= ffn <= 4096; shared_ffn == 0 or a multiple of
  * 128 up to 4096; n_slots == n_experts (the slot table holds every expert);
  * 1 <= max_tokens <= 65536 (sizes the workspaces); routing_flags a
- * combination of the MOE_ROUTING_* bits (0: the default routing above). */
+ * combination of the MOE_ROUTING_* bits (0: the default routing above).
+ * moe_layer_create also refuses shapes whose single-token decode does not
+ * fit the decode kernel's 227 KB of shared memory (one 16-row gate/up stage
+ * is 18 * hidden bytes, so hidden = 8192 does not fit); a 2..4-token call
+ * whose batch does not fit returns MOE_ERR_INVALID. */
 typedef struct {
   int32_t hidden;     /* H */
   int32_t n_experts;  /* E */

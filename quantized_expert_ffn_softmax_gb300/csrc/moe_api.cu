@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -81,6 +82,26 @@ moe_status validate_config(const moe_layer_config* c) {
     return fail(MOE_ERR_INVALID, "routing_flags=0x%x has unknown bits", c->routing_flags);
   if ((c->routing_flags & MOE_ROUTING_SHARED_GATE) && c->shared_ffn == 0)
     return fail(MOE_ERR_INVALID, "MOE_ROUTING_SHARED_GATE needs a shared expert (shared_ffn > 0)");
+  // single-token decode must fit the decode kernel's smallest shared-memory
+  // layout: one gate/up stage (16 rows of H), the CTA's router rows, the
+  // token planes and the w*h staging of k + 1 units (with routing variants,
+  // also the router bias).  Batches of 2..4 tokens need more; a batch that
+  // does not fit is refused by the call (MOE_ERR_INVALID).
+  {
+    moe::DecodeParams p{};  // host-side sizing only
+    p.H = c->hidden;
+    p.E = c->n_experts;
+    p.F = c->ffn;
+    p.Fs = c->shared_ffn;
+    p.T = 1;
+    p.max_units = std::min(c->top_k, c->n_experts) + 1;
+    const size_t bias = c->routing_flags ? (((size_t)c->n_experts * 4 + 127) & ~(size_t)127) : 0;
+    const size_t need = moe::decode_smem_bytes(p) + bias;
+    if (need > (size_t)227 * 1024)
+      return fail(MOE_ERR_INVALID,
+                  "hidden=%d, n_experts=%d: the decode kernel needs %zu KB of shared memory (> 227 KB)",
+                  c->hidden, c->n_experts, (need + 1023) / 1024);
+  }
   return MOE_OK;
 }
 

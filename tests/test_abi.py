@@ -69,3 +69,18 @@ def test_calls_reject_null_layer(lib):
     arr = (ctypes.c_void_p * 1)(None)
     assert L.moe_stack_forward(arr, 0, None, 1, None, None) == moe.MOE_ERR_INVALID
     L.moe_layer_destroy(None)
+
+
+def test_create_refuses_shapes_whose_single_token_decode_cannot_fit(lib):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_create(_cfg(hidden=8192, n_experts=256, top_k=8, ffn=512, shared_ffn=512), {}, False)
+    assert ei.value.status == moe.MOE_ERR_INVALID
+    assert "shared memory" in moe.moe_last_error()
+    # the benchmarked shapes pass the shape checks (and stop at the missing weights)
+    for shape in (dict(hidden=2048, n_experts=256, top_k=8, ffn=512, shared_ffn=512),
+                  dict(hidden=2048, n_experts=512, top_k=10, ffn=768, shared_ffn=1536),
+                  dict(hidden=2048, n_experts=512, top_k=10, ffn=768, shared_ffn=1536,
+                       routing_flags=7)):
+        with pytest.raises(moe.MoeError):
+            moe.moe_layer_create(_cfg(**shape), {}, False)
+        assert "NULL" in moe.moe_last_error()
