@@ -1,29 +1,30 @@
 // Decode / MTP-verify path (1..4 tokens): one persistent cooperative kernel
 // (one CTA per SM) runs a whole stack of MoE layers.  Per layer:
 //
-//   phase R  (stacks: RMS-normalise the residual stream h -> u)
-//            router GEMV (fp32) over this CTA's experts, whose W_r rows
-//            were prefetched into shared memory during the previous layer
+//   phase R  the layer input: x (first layer) or, in stacks, the residual
+//            h = bf16(h + bf16(y)) of the previous layer's output y (fp32,
+//            reduced in L2); RMS norm -> u; router GEMV (fp32) over this
+//            CTA's experts, whose W_r rows were prefetched into shared
+//            memory during the previous layer
 //   barrier
 //   top-k    ranking, not serial selection: every warp ranks its slice of
 //            the logits with warp shuffles, the slices' top-k candidates
 //            rank each other in shared memory; softmax over the selection;
-//            the expert-unit list.  Computed redundantly by every CTA.  Then the CTA starts the bulk copies (TMA) of the
-//            expert weights it reads in this layer: the gate/up rows of its
-//            first items and the down rows of its output rows, with their
-//            block-scale tiles
-//   phase G  fused dequant + gate/up GEMV + SwiGLU from shared memory -> h;
-//            each warp owns whole rows (no CTA-wide reduction); a stage is
-//            refilled as soon as all warps have read it
-//   barrier
-//   phase D  fused dequant + down GEMV + weighted combine from shared
-//            memory (+ residual h + bf16(y) for stacks) -> y / h_{l+1};
-//            each warp owns whole output rows
+//            the expert-unit list.  Computed redundantly by every CTA.
+//   units    a work unit is (expert unit, 32-row block of its F); CTA c
+//            takes units c, c + grid, ...  Per unit: the block's gate/up
+//            rows (two 16-row items, bulk copies into a 2-deep stage ring),
+//            fused dequant GEMV + SwiGLU -> 32 values of w*h per token; then
+//            the block's 32 columns of the down matrix (copied per thread
+//            with async 16-byte copies, straight from the packed rows)
+//            against all H outputs, added into the layer's fp32 output in
+//            L2 with reductions
 //   barrier
 //
-// Only the router logits, h and h_{l+1} cross between CTAs (through L2);
-// every weight byte is read from HBM once, by a bulk copy issued as soon as
-// its address is known.  Packed 4-bit codes become fp16 pairs with a
+// Only the router logits and the layer output cross between CTAs (through
+// L2); every weight byte is read from HBM once.  The output's fp32 sums
+// arrive in any order, so the last bit may differ between runs.  Packed
+// 4-bit codes become fp16 pairs with a
 // magic-exponent OR (0x6400 | n = 1024 + n, minus 1032 = n - 8, exact; a
 // nibble one position higher goes into 0x5400 = 64.0 instead);
 // products with the fp16 activations are exact and summed within a
@@ -42,7 +43,6 @@ namespace {
 using namespace dev;
 
 constexpr int kWarps = kDecodeThreads / 32;
-constexpr int kMaxRowsPerWarp = 4;  // down-phase output rows one warp keeps in registers
 
 // Grid barrier on a counter zeroed before the launch: barrier number `n`
 // completes when the counter reaches (n + 1) * gridDim.x.  Waits are bounded
@@ -101,41 +101,6 @@ __device__ __forceinline__ void unpack_codes(uint32_t w, __half2 (&h)[4]) {
   h[1] = __hsub2(*reinterpret_cast<__half2*>(&v[1]), k72);
   h[2] = __hsub2(*reinterpret_cast<__half2*>(&v[2]), k1032);
   h[3] = __hsub2(*reinterpret_cast<__half2*>(&v[3]), k72);
-}
-
-// As dot_block, but the two 16-element halves of the block are returned
-// separately (their activations carry different power-of-two scales).
-template <int TT>
-__device__ __forceinline__ void dot_block_halves(const uint4 w, const uint4 (&act)[TT][4],
-                                                 float (&lo)[TT], float (&hi)[TT]) {
-  __half2 c[4][4];
-  unpack_codes(w.x, c[0]);
-  unpack_codes(w.y, c[1]);
-  unpack_codes(w.z, c[2]);
-  unpack_codes(w.w, c[3]);
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    const __half2* a0 = reinterpret_cast<const __half2*>(&act[t][0]);
-    const __half2* a1 = reinterpret_cast<const __half2*>(&act[t][1]);
-    const __half2* a2 = reinterpret_cast<const __half2*>(&act[t][2]);
-    const __half2* a3 = reinterpret_cast<const __half2*>(&act[t][3]);
-    __half2 s0 = __hmul2(c[0][0], a0[0]);
-    __half2 s1 = __hmul2(c[2][0], a2[0]);
-#pragma unroll
-    for (int j = 1; j < 4; ++j) {
-      s0 = __hfma2(c[0][j], a0[j], s0);
-      s1 = __hfma2(c[2][j], a2[j], s1);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      s0 = __hfma2(c[1][j], a1[j], s0);
-      s1 = __hfma2(c[3][j], a3[j], s1);
-    }
-    const float2 f0 = __half22float2(s0);
-    const float2 f1 = __half22float2(s1);
-    lo[t] = f0.x + f0.y;
-    hi[t] = f1.x + f1.y;
-  }
 }
 
 template <int TT>
@@ -259,19 +224,14 @@ __device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
 struct DecodeSmem {
-  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dbuf, hp, hsh, total;
-  size_t g_stage, d_item;
-  int nmy, nd_items;
-  bool dprefetch;
-  __host__ __device__ static DecodeSmem make(int H, int E, int F, int Fs, int TT, int max_units,
-                                             int grid, int g_stages, bool want_dprefetch) {
+  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dst, total;
+  size_t g_stage;
+  int nmy;
+  __host__ __device__ static DecodeSmem make(int H, int E, int TT, int grid, int g_stages) {
     DecodeSmem s;
     const int C = H / 32;
-    const int n_routed_max = max_units - 1;
     s.nmy = (E + 1 + grid - 1) / grid;  // router rows per CTA, with room for the gate row
-    s.nd_items = (H / 8 + grid - 1) / grid;
     s.g_stage = (size_t)16 * H + (size_t)64 * C;  // gate+up rows (2 x 16 x H/2) + scales
-    s.d_item = (size_t)9 * ((size_t)n_routed_max * F + Fs) / 2;  // per unit: codes 4F_u, scales F_u/2
     size_t o = 0;
     s.mbar = o;
     o += 128;
@@ -286,21 +246,12 @@ struct DecodeSmem {
     s.wr = o;
     o += (size_t)s.nmy * H * 4;
     o = (o + 127) & ~(size_t)127;
-    // one region shared by phase G (x pair planes + gate/up stages) and
-    // phase D (w*h pair planes): the two are never live at the same time
-    const size_t region = o;
-    s.xp = region;
-    s.gbuf = (region + (size_t)TT * H * 2 + 127) & ~(size_t)127;
-    const size_t g_end = s.gbuf + (size_t)g_stages * s.g_stage;
-    s.hp = region;
-    s.hsh = region + ((size_t)n_routed_max * F + Fs) * TT * 2;  // int8 half-block shifts
-    const size_t h_end = s.hsh + (((size_t)n_routed_max * F + Fs) / 32 * TT * 2 + 15) / 16 * 16;
-    o = g_end > h_end ? g_end : h_end;
+    s.xp = o;  // x pair planes
+    s.gbuf = (o + (size_t)TT * H * 2 + 127) & ~(size_t)127;
+    o = s.gbuf + (size_t)g_stages * s.g_stage;
     o = (o + 127) & ~(size_t)127;
-    s.dbuf = o;
-    const size_t with_d = o + (size_t)s.nd_items * s.d_item;
-    s.dprefetch = want_dprefetch && with_d <= (size_t)227 * 1024 && s.nd_items <= kMaxRowsPerWarp;
-    if (s.dprefetch) o = with_d;
+    s.dst = o;  // down block of a work unit: 16 code bytes + a 4-byte scale pair per output row
+    o += (size_t)H * 20;
     s.total = (o + 127) & ~(size_t)127;
     return s;
   }
@@ -324,11 +275,18 @@ struct DecodeMisc {
   float red_mx[kWarps][4];
   float red_z[kWarps][4];
   float hst[2][16][4];  // w*h of a gate/up item's 16 rows (double-buffered by item)
+  uint4 actD[kMaxDecodeTokens][4];  // w*h of a work unit's 32 rows as fp16 pair planes
+  int dsh[kMaxDecodeTokens];        // their power-of-two shifts
 };
 static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 
 // mbarrier slots
-enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarD = 4, kBarR = 5 };
+enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarR = 4 };
+
+// 4-byte async copy global -> shared (the .ca form; .cg takes 16 bytes only)
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 
 // kVar: some layer of the launch uses a routing variant (routing_flags != 0);
 // the default instantiation carries none of their code.
@@ -339,11 +297,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int H = p.H, E = p.E, k = p.k, F = p.F, Fs = p.Fs, T = p.T;
   const int C = H / 32;
   const int CF = F / 32;
-  const int CS = Fs / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x;
   const DecodeSmem L =
-      DecodeSmem::make(H, E, F, Fs, TT, p.max_units, grid, p.g_stages, p.want_dprefetch != 0);
+      DecodeSmem::make(H, E, TT, grid, p.g_stages);
   const int NG = p.g_stages;  // 1 or 2
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
   DecodeMisc& M = *reinterpret_cast<DecodeMisc*>(smem + L.misc);
@@ -353,21 +310,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint4* xp = reinterpret_cast<uint4*>(smem + L.xp);
   float* wr = reinterpret_cast<float*>(smem + L.wr);
   unsigned char* gbuf = smem + L.gbuf;
-  unsigned char* dbuf = smem + L.dbuf;
-  uint4* hp = reinterpret_cast<uint4*>(smem + L.hp);
-  // w*h of the layer in global scratch, as fp16 pair planes laid out like the
-  // down phase's staging (unit u at u*TT*4*CF uint4s, the shared unit after
-  // the routed ones), followed by the int8 shift of each 16-element half-block
-  uint4* hp16 = reinterpret_cast<uint4*>(p.hbuf);
-  int8_t* hsh_g = reinterpret_cast<int8_t*>(hp16 + (size_t)TT * 4 * ((p.max_units - 1) * CF + CS));
+  unsigned char* dst_s = smem + L.dst;
 
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1) ? kWarps : 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1) ? kWarps : 1);
     fence_mbar_init();
   }
   __syncthreads();
   uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
-  uint32_t ph_d = 0u, ph_r = 0u;
+  uint32_t ph_r = 0u;
   unsigned nbar = 0;
   const uint64_t tmo = p.timeout_ns;
   const bool stack = (p.mode == kModeStack);
@@ -412,7 +363,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   for (int l = 0; l < p.n_layers; ++l) {
     const LayerDev& W = p.layers[l];
-    const uint16_t* xsrc = (l == 0) ? p.x_in : (p.xbuf + (size_t)(l & 1) * kMaxDecodeTokens * H);
+    // the previous layer's output, reduced in L2 (layers after the first)
+    const float* yprev = p.yacc + (size_t)((l + 1) & 1) * kMaxDecodeTokens * H;
 
     // ------------------------------------------------ phase R: stage x, router
     // pass 1: stage x (8 bf16 per thread and step) and take its sum of
@@ -425,7 +377,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
         const int t = i / (H / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (t < T) v = __ldcg(reinterpret_cast<const uint4*>(xsrc + (size_t)t * H) + (i - t * (H / 8)));
+        if (t < T) {
+          const int g8 = i - t * (H / 8);
+          if (l == 0) {
+            v = __ldcg(reinterpret_cast<const uint4*>(p.x_in + (size_t)t * H) + g8);
+          } else {
+            // residual: h_l = bf16(h_{l-1} + bf16(y_{l-1})); h_{l-1} is still
+            // staged here (stacks only: a single layer has no layer 1)
+            const uint4 hv = reinterpret_cast<const uint4*>(hres)[i];
+            const float4 y0 = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8);
+            const float4 y1 = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8 + 1);
+            const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float lo = __uint_as_float(hw[q] << 16) + __bfloat162float(__float2bfloat16_rn(yy[2 * q]));
+              const float hi = __uint_as_float(hw[q] & 0xffff0000u) +
+                               __bfloat162float(__float2bfloat16_rn(yy[2 * q + 1]));
+              o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                     ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+            }
+            v = make_uint4(o[0], o[1], o[2], o[3]);
+            if (blockIdx.x == 0 && p.h_trace)
+              reinterpret_cast<uint4*>(p.h_trace + ((size_t)(l - 1) * T + t) * H)[g8] = v;
+          }
+        }
         reinterpret_cast<uint4*>(stage_dst)[i] = v;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float a = 0.0f, m = 0.0f;
@@ -717,14 +694,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     __syncthreads();
     if (p.mode == kModeRoute) continue;
     const int n_routed = M.n_routed;
-    const int n_units = M.n_units;
+    // the other accumulator held the previous layer's output, which every
+    // CTA read in phase R: zero it for the next layer (its first reductions
+    // come after the next barrier)
+    {
+      float* ynext = p.yacc + (size_t)((l + 1) & 1) * kMaxDecodeTokens * H;
+      for (int i = blockIdx.x * kDecodeThreads + tid; i < TT * H; i += grid * kDecodeThreads) ynext[i] = 0.0f;
+    }
 
-    // ------------------------------------------------ bulk copies of this layer's weights
+    // ------------------------------------------------ work units and their copies
+    // A work unit is (unit, 32-row block of its F): gate/up rows of the block
+    // (two 16-row items through the stage ring), then the block's columns of
+    // the down matrix against all H outputs.  CTA c takes units c, c + grid, ..
     const int ipu = F / 16;  // gate/up items per routed unit
-    const int n_gitems = n_routed * ipu + Fs / 16;
+    const int bpu = F / 32;  // blocks per routed unit
+    const int n_wu = n_routed * bpu + Fs / 32;
+    const int my_wu = ((int)blockIdx.x < n_wu) ? (n_wu - (int)blockIdx.x + grid - 1) / grid : 0;
+    const int n_my_items = 2 * my_wu;
+    auto item_of = [&](int q) { return 2 * ((int)blockIdx.x + (q >> 1) * grid) + (q & 1); };
     auto issue_g = [&](int q) {  // gate/up item q of this CTA into stage q % NG
-      const int it = blockIdx.x + q * grid;
-      if (it >= n_gitems) return;
+      if (q >= n_my_items) return;
+      const int it = item_of(q);
       const uint8_t* gq;
       const uint16_t* gs;
       const uint8_t* uq;
@@ -752,43 +742,55 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
       bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
     };
-    // down items of this CTA: output rows i0 = (blockIdx.x + q * grid) * 8
-    const int n_ditems = ((int)blockIdx.x < H / 8) ? (H / 8 - (int)blockIdx.x + grid - 1) / grid : 0;
+    // unit and block of this CTA's j-th work unit
+    auto wu_of = [&](int j, int& u, int& b) {
+      const int w = blockIdx.x + j * grid;
+      if (w < n_routed * bpu) {
+        u = w / bpu;
+        b = w - u * bpu;
+      } else {
+        u = n_routed;
+        b = w - n_routed * bpu;
+      }
+    };
+    // Down block of work unit j into the down stage, straight from the packed
+    // rows: every thread copies the block's 16 code bytes of its output rows
+    // and the 4-byte scale pair holding the block's scale (async copies, one
+    // commit group per thread).
+    auto issue_d = [&](int j) {
+      int u, b;
+      wu_of(j, u, b);
+      const uint8_t* cq;
+      const uint16_t* cs;
+      int Fu;
+      if (u < n_routed) {
+        const size_t slot = (size_t)M.unit_slot[u];
+        cq = W.down_q + slot * H * (size_t)(F / 2);
+        cs = W.down_s + slot * H * (size_t)CF;
+        Fu = F;
+      } else {
+        cq = W.sh_down_q;
+        cs = W.sh_down_s;
+        Fu = Fs;
+      }
+      const uint32_t s_codes = smem_u32(dst_s), s_scales = smem_u32(dst_s + (size_t)H * 16);
+      for (int r = tid; r < H; r += kDecodeThreads) {
+        cp_async_16(s_codes + (uint32_t)r * 16u, cq + (size_t)r * (Fu / 2) + 16 * b);
+        cp_async_4(s_scales + (uint32_t)r * 4u, cs + (size_t)r * (Fu / 32) + (b & ~1));
+      }
+      cp_async_commit();
+    };
     if (warp == 0 && lane == 0)
       for (int q = 0; q < NG; ++q) issue_g(q);
-    if (warp == kWarps - 1 && L.dprefetch && n_ditems > 0) {
-      // per item: for each unit, codes (8 x F_u/2 bytes) then scales (8 x F_u/16 bytes)
-      if (lane == 0)
-        mbar_expect_tx(&mbar[kBarD], (uint32_t)((size_t)9 * ((size_t)n_routed * F + Fs) / 2 * n_ditems));
-      __syncwarp();
-      for (int job = lane; job < n_ditems * n_units; job += 32) {
-        const int q = job / n_units, u = job - (job / n_units) * n_units;
-        const int i0 = (blockIdx.x + q * grid) * 8;
-        unsigned char* base = dbuf + (size_t)q * L.d_item + (size_t)u * (9 * (size_t)F / 2);
-        if (u < n_routed) {
-          const size_t slot = (size_t)M.unit_slot[u];
-          bulk_g2s(base, W.down_q + (slot * H + i0) * (F / 2), 8u * (F / 2), &mbar[kBarD]);
-          bulk_g2s(base + 8 * (F / 2), W.down_s + (slot * H + i0) * CF, 8u * CF * 2u, &mbar[kBarD]);
-        } else {
-          bulk_g2s(base, W.sh_down_q + (size_t)i0 * (Fs / 2), 8u * (Fs / 2), &mbar[kBarD]);
-          bulk_g2s(base + 8 * (Fs / 2), W.sh_down_s + (size_t)i0 * CS, 8u * CS * 2u, &mbar[kBarD]);
-        }
-      }
-    }
+    if (my_wu > 0) issue_d(0);
 
-    // ------------------------------------------------ phase G: gate/up + SwiGLU
+    // ------------------------------------------------ gate/up + SwiGLU, then down per block
     {
+      float* ycur = p.yacc + (size_t)(l & 1) * kMaxDecodeTokens * H;
       // warp w owns row pairs 2w, 2w+1 of every item (gate and up rows)
-      for (int q = 0; (int)blockIdx.x + q * grid < n_gitems; ++q) {
-        const int it = blockIdx.x + q * grid;
-        int u, f0;
-        if (it < n_routed * ipu) {
-          u = it / ipu;
-          f0 = (it - u * ipu) * 16;
-        } else {
-          u = n_routed;
-          f0 = (it - n_routed * ipu) * 16;
-        }
+      for (int q = 0; q < n_my_items; ++q) {
+        const int it = item_of(q);
+        const int u = (it < n_routed * ipu) ? it / ipu : n_routed;
         const int sg = q % NG;
         const uint32_t par = gcount[sg] & 1u;
         ++gcount[sg];
@@ -842,156 +844,91 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
         }
         __syncthreads();  // the item's 16 rows of w*h are staged
-        if (tid < TT * 2) {
-          // the item's rows as fp16 pair planes in the down phase's layout,
-          // scaled by a power of two that puts this token's max |w h| over
-          // the 16 rows in [32, 64) (the shift goes beside them)
-          const int t = tid >> 1, g8 = tid & 1;
+        // refill this stage with item q + NG once every warp has read it
+        if (warp == 0 && lane == 0 && q + NG < n_my_items) {
+          mbar_wait(&mbar[kBarE0 + sg], par, p.err, tmo);
+          issue_g(q + NG);
+        }
+        if ((q & 1) == 0) continue;
+        // ---- down block of work unit j: both halves of its 32 rows are staged
+        const int j = q >> 1;
+        int ub, b;
+        wu_of(j, ub, b);
+        if (tid < TT * 4) {
+          // fp16 pair planes of the block's 32 w*h values per token, in the
+          // code unpack order, scaled by a power of two that puts the
+          // token's max |w h| in [32, 64) (the shift goes beside them)
+          const int t = tid >> 2, qw = tid & 3;
           float m = 0.0f;
 #pragma unroll
-          for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(M.hst[q & 1][r][t]));
+          for (int f = 0; f < 32; ++f) m = fmaxf(m, fabsf(M.hst[f >> 4][f & 15][t]));
           const int sh = range_shift(m);
           const float sc = pow2f(-sh);
           uint32_t o[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            __half2 hh = __floats2half2_rn(M.hst[q & 1][8 * g8 + j][t] * sc, M.hst[q & 1][8 * g8 + j + 4][t] * sc);
-            o[j] = *reinterpret_cast<uint32_t*>(&hh);
+          for (int jj = 0; jj < 4; ++jj) {
+            const int e0 = 8 * qw + jj, e1 = e0 + 4;
+            __half2 hh = __floats2half2_rn(M.hst[e0 >> 4][e0 & 15][t] * sc, M.hst[e1 >> 4][e1 & 15][t] * sc);
+            o[jj] = *reinterpret_cast<uint32_t*>(&hh);
           }
-          const int Cu = (u < n_routed) ? CF : CS;
-          const int c = f0 >> 5, half = (f0 >> 4) & 1;
-          hp16[(size_t)u * TT * 4 * CF + (size_t)t * 4 * Cu + (size_t)(2 * half + g8) * Cu + c] =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          if (g8 == 0) hsh_g[(size_t)u * TT * 2 * CF + (size_t)t * 2 * Cu + (size_t)half * Cu + c] = (int8_t)sh;
+          M.actD[t][qw] = make_uint4(o[0], o[1], o[2], o[3]);
+          if (qw == 0) M.dsh[t] = sh;
         }
-        // refill this stage with item q + NG once every warp has read it
-        if (warp == 0 && lane == 0 && (int)blockIdx.x + (q + NG) * grid < n_gitems) {
-          mbar_wait(&mbar[kBarE0 + sg], par, p.err, tmo);
-          issue_g(q + NG);
+        cp_async_wait<0>();
+        __syncthreads();  // the act planes, and every thread's copies of the down block
+        uint4 act[TT][4];
+        float ysc[TT];
+        bool live[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) act[t][qq] = M.actD[t][qq];
+          ysc[t] = pow2f(M.dsh[t]);
+          live[t] = (t < T) && M.unit_w[ub][t] != 0.0f;
         }
+        const unsigned char* dc = dst_s;
+        const unsigned char* dsc = dst_s + (size_t)H * 16;
+        for (int r = tid; r < H; r += kDecodeThreads) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(dc + (size_t)r * 16);
+          const uint32_t sp = *reinterpret_cast<const uint32_t*>(dsc + (size_t)r * 4);
+          const float s = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sp >> 16) : (sp & 0xffffu))));
+          float d[TT];
+          dot_block<TT>(wv, act, d);
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+            if (live[t]) atomicAdd(ycur + (size_t)t * H + r, s * d[t] * ysc[t]);
+        }
+        __syncthreads();  // every thread is done with the down stage and the act planes
+        if (j + 1 < my_wu) issue_d(j + 1);
       }
     }
     if (l + 1 < p.n_layers) prefetch_router(l + 1);
+    // the next layer's bulk copies land in shared memory this layer read
+    // through the generic proxy: order those reads before them
+    fence_proxy_async_smem();
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
+  }
 
-    // ------------------------------------------------ phase D: down + combine
-    {
-      // stage the layer's fp16 w*h planes and their half-block shifts (plain
-      // copies: the gate/up phase of every CTA wrote them before the barrier)
-      int8_t* hsh = reinterpret_cast<int8_t*>(smem + L.hsh);
-      {
-        const int n16 = (n_routed * CF + CS) * TT * 4;
-        for (int i = tid; i < n16; i += kDecodeThreads) hp[i] = __ldcg(hp16 + i);
-        const int nsh = (n_routed * CF + CS) * TT * 2;
-        for (int i = tid; i < nsh; i += kDecodeThreads) hsh[i] = __ldcg(hsh_g + i);
-      }
-      __syncthreads();
-      const int P = n_routed * CF + CS;
-      if (L.dprefetch && n_ditems > 0) {
-        mbar_wait(&mbar[kBarD], ph_d, p.err, tmo);
-        ph_d ^= 1u;
-      }
-      // warp w owns row w of up to kMaxRowsPerWarp items at a time: rows
-      // i = (blockIdx.x + q * grid) * 8 + w
-      for (int q0 = 0; q0 < n_ditems; q0 += kMaxRowsPerWarp) {
-        const int nq = min(kMaxRowsPerWarp, n_ditems - q0);
-        float acc[kMaxRowsPerWarp][TT];
-#pragma unroll
-        for (int q = 0; q < kMaxRowsPerWarp; ++q)
-#pragma unroll
-          for (int t = 0; t < TT; ++t) acc[q][t] = 0.0f;
-        // (unit, chunk) of pp advance by 32 chunks per step, without a division
-        int u = 0, c = lane;
-        while (u < n_routed && c >= CF) {
-          c -= CF;
-          ++u;
-        }
-        for (int pp = lane; pp < P; pp += 32) {
-          const int Cu = (u < n_routed) ? CF : CS;
-          uint4 act[TT][4];
-          const uint4* ap = hp + (size_t)u * TT * 4 * CF + c;
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) act[t][qq] = ap[(t * 4 + qq) * Cu];
-          float slo[TT], shi[TT];  // 2^shift of the two half-blocks, per token
-          {
-            const int8_t* sp = hsh + (size_t)u * TT * 2 * CF + c;
-#pragma unroll
-            for (int t = 0; t < TT; ++t) {
-              slo[t] = pow2f(sp[(t * 2) * Cu]);
-              shi[t] = pow2f(sp[(t * 2 + 1) * Cu]);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < kMaxRowsPerWarp; ++q) {
-            if (q < nq) {
-              uint4 wv;
-              float s;
-              if (L.dprefetch) {
-                const unsigned char* ub = dbuf + (size_t)(q0 + q) * L.d_item + (size_t)u * (9 * (size_t)F / 2);
-                wv = *reinterpret_cast<const uint4*>(ub + (size_t)warp * (Cu * 16) + c * 16);
-                s = __half2float(reinterpret_cast<const __half*>(ub + 8 * (Cu * 16))[warp * Cu + c]);
-              } else {
-                const int i = ((int)blockIdx.x + (q0 + q) * grid) * 8 + warp;
-                const size_t slot = (u < n_routed) ? (size_t)M.unit_slot[u] : 0;
-                const uint8_t* base = (u < n_routed) ? W.down_q + slot * H * (F / 2) : W.sh_down_q;
-                const uint16_t* sbase = (u < n_routed) ? W.down_s + slot * H * CF : W.sh_down_s;
-                wv = ld_stream(base + (size_t)i * (Cu * 16) + c * 16);
-                s = __half2float(__ushort_as_half(__ldg(sbase + (size_t)i * Cu + c)));
-              }
-              float dlo[TT], dhi[TT];
-              dot_block_halves<TT>(wv, act, dlo, dhi);
-#pragma unroll
-              for (int t = 0; t < TT; ++t)
-                acc[q][t] = fmaf(s, fmaf(dlo[t], slo[t], dhi[t] * shi[t]), acc[q][t]);
-            }
-          }
-          c += 32;
-          while (u < n_routed && c >= CF) {
-            c -= CF;
-            ++u;
-          }
-        }
-        float v[kMaxRowsPerWarp * TT];
-#pragma unroll
-        for (int q = 0; q < kMaxRowsPerWarp; ++q)
-#pragma unroll
-          for (int t = 0; t < TT; ++t) v[q * TT + t] = acc[q][t];
-        const float y0 = warp_reduce_scatter<kMaxRowsPerWarp * TT>(v, lane);
-        constexpr int REP = 32 / (kMaxRowsPerWarp * TT);
-        if ((lane & (REP - 1)) == 0) {
-          const int idx = lane / REP;
-          const int q = idx / TT, t = idx - (idx / TT) * TT;
-          if (q < nq && t < T) {
-            const float y = y0;
-            const int i = ((int)blockIdx.x + (q0 + q) * grid) * 8 + warp;
-            const __nv_bfloat16 yb = __float2bfloat16_rn(y);
-            if (p.mode == kModeForward) {
-              p.y_out[(size_t)t * H + i] = __bfloat16_as_ushort(yb);
-            } else {
-              const float xv = __bfloat162float(__ushort_as_bfloat16(hres[t * H + i]));
-              const uint16_t xn = __bfloat16_as_ushort(__float2bfloat16_rn(xv + __bfloat162float(yb)));
-              uint16_t* dst = (l == p.n_layers - 1)
-                                  ? p.y_out
-                                  : p.xbuf + (size_t)((l + 1) & 1) * kMaxDecodeTokens * H;
-              dst[(size_t)t * H + i] = xn;
-              if (p.h_trace) p.h_trace[((size_t)l * T + t) * H + i] = xn;
-            }
-          }
-        }
+  // ------------------------------------------------ output: y, or h_L for stacks
+  if (p.mode != kModeRoute) {
+    const float* yl = p.yacc + (size_t)((p.n_layers - 1) & 1) * kMaxDecodeTokens * H;
+    for (int i = blockIdx.x * kDecodeThreads + tid; i < T * H; i += grid * kDecodeThreads) {
+      const __nv_bfloat16 yb = __float2bfloat16_rn(__ldcg(yl + i));
+      if (stack) {
+        const float xv = __bfloat162float(__ushort_as_bfloat16(hres[i]));
+        const uint16_t xn = __bfloat16_as_ushort(__float2bfloat16_rn(xv + __bfloat162float(yb)));
+        p.y_out[i] = xn;
+        if (p.h_trace) p.h_trace[(size_t)(p.n_layers - 1) * T * H + i] = xn;
+      } else {
+        p.y_out[i] = __bfloat16_as_ushort(yb);
       }
     }
-    // the next layer's bulk copies land in shared memory this phase wrote
-    // through the generic proxy: order those writes before them
-    fence_proxy_async_smem();
-    if (l + 1 < p.n_layers) grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
   }
 }
 
 size_t decode_smem_bytes(const DecodeParams& p) {
   const int TT = p.T == 1 ? 1 : (p.T == 2 ? 2 : 4);
-  return DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, 152, 1, false).total;
+  return DecodeSmem::make(p.H, p.E, TT, 152, 1).total;
 }
 
 template <int TT>
@@ -1002,15 +939,13 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
   auto kern = var ? moe_decode_kernel<TT, true> : moe_decode_kernel<TT, false>;
   DecodeParams p = p_in;
   const int grid = num_sms;  // one CTA per SM
-  // most staging that fits: 2 gate/up stages and the down weights in shared
-  // memory, else without the down weights, else one gate/up stage
+  // two gate/up stages when they fit, else one
   const size_t cap = (size_t)227 * 1024;
   p.g_stages = 2;
-  p.want_dprefetch = 1;
-  DecodeSmem sm = DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, grid, 2, true);
+  DecodeSmem sm = DecodeSmem::make(p.H, p.E, TT, grid, 2);
   if (sm.total > cap) {
     p.g_stages = 1;
-    sm = DecodeSmem::make(p.H, p.E, p.F, p.Fs, TT, p.max_units, grid, 1, true);
+    sm = DecodeSmem::make(p.H, p.E, TT, grid, 1);
   }
   if (sm.total > cap) {
     *why = "decode shared-memory footprint exceeds 227 KB for this shape";
@@ -1029,8 +964,10 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
     *why = "decode kernel cannot be resident (occupancy query)";
     return MOE_ERR_CUDA;
   }
-  if (cudaMemsetAsync(p.bar, 0, sizeof(GridBarrier), stream) != cudaSuccess) {
-    *why = "cudaMemsetAsync(barrier) failed";
+  if (cudaMemsetAsync(p.bar, 0, sizeof(GridBarrier), stream) != cudaSuccess ||
+      // the first layer reduces into accumulator 0; the kernel zeroes the other
+      cudaMemsetAsync(p.yacc, 0, sizeof(float) * kMaxDecodeTokens * p.H, stream) != cudaSuccess) {
+    *why = "cudaMemsetAsync(barrier / accumulator) failed";
     return MOE_ERR_CUDA;
   }
   void* args[] = {&p};

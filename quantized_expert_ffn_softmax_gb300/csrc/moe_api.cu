@@ -257,6 +257,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   size_t o_is = wadd(sizeof(int32_t) * (size_t)Tm * k);
   size_t o_ws = wadd(sizeof(float) * (size_t)Tm * k);
   size_t o_gz = wadd(sizeof(float) * moe::kMaxDecodeTokens);
+  size_t o_ya = wadd(sizeof(float) * 2 * moe::kMaxDecodeTokens * H);
   size_t o_gw = wadd(sizeof(float) * (size_t)Tm);
   size_t o_pf = wadd(moe::prefill_workspace_bytes(*cfg));
   L->ws.bytes = align_up(wo, 256);
@@ -278,6 +279,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->ws.ids_stage = (int32_t*)(wb + o_is);
   L->ws.w_stage = (float*)(wb + o_ws);
   L->ws.gz = (float*)(wb + o_gz);
+  L->ws.dyacc = (float*)(wb + o_ya);
   L->ws.gw = (float*)(wb + o_gw);
   L->ws.scratch = wb + o_pf;
   e = cudaMemset(L->ws_block, 0, L->ws.bytes);
@@ -361,6 +363,7 @@ moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
   p.xbuf = L0->ws.xbuf;
   p.z = L0->ws.z;
   p.gz = L0->ws.gz;
+  p.yacc = L0->ws.dyacc;
   p.hbuf = L0->ws.hbuf;
   p.bar = L0->ws.bar;
   p.err = L0->ws.err;

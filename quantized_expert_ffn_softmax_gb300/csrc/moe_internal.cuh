@@ -61,6 +61,7 @@ struct DecodeParams {
   uint16_t* xbuf;        // [2][4][H] residual ping-pong
   float* z;              // [4][E]
   float* gz;             // [4] shared-expert gate logits g . u (MOE_ROUTING_SHARED_GATE)
+  float* yacc;           // [2][4][H] layer outputs, reduced in L2 (fp32)
   float* hbuf;           // [max_units-ish][4][Fmax] fp32
   GridBarrier* bar;
   int* err;
@@ -91,6 +92,7 @@ struct Workspace {
   int32_t* ids_stage = nullptr; // [max_tokens][k]
   float* w_stage = nullptr;     // [max_tokens][k]
   float* gz = nullptr;          // [4] decode: shared-expert gate logits
+  float* dyacc = nullptr;       // [2][4][H] decode: layer outputs, reduced in L2
   float* gw = nullptr;          // [max_tokens] prefill: shared-expert gate weights
   // prefill
   __half* x16 = nullptr;        // [max_tokens][H] fp16, per-token scaled, K-permuted

@@ -81,7 +81,8 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   const size_t o_xbuf = up256(o_err + 16);
   const size_t o_z = up256(o_xbuf + sizeof(uint16_t) * 2 * moe::kMaxDecodeTokens * H);
   const size_t o_gz = up256(o_z + sizeof(float) * moe::kMaxDecodeTokens * E);
-  const size_t o_h = up256(o_gz + sizeof(float) * moe::kMaxDecodeTokens);
+  const size_t o_ya = up256(o_gz + sizeof(float) * moe::kMaxDecodeTokens);
+  const size_t o_h = up256(o_ya + sizeof(float) * 2 * moe::kMaxDecodeTokens * H);
   const size_t need = o_h + sizeof(float) * moe::kMaxDecodeTokens * ((size_t)routed_max * F + Fs);
   if (need > kNoAllocScratchBytes)
     return fail(MOE_ERR_CAPACITY,
@@ -131,6 +132,7 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
   p.xbuf = reinterpret_cast<uint16_t*>(sb + o_xbuf);
   p.z = reinterpret_cast<float*>(sb + o_z);
   p.gz = reinterpret_cast<float*>(sb + o_gz);
+  p.yacc = reinterpret_cast<float*>(sb + o_ya);
   p.hbuf = reinterpret_cast<float*>(sb + o_h);
   p.bar = reinterpret_cast<moe::GridBarrier*>(sb + o_bar);
   p.err = err;

@@ -97,5 +97,7 @@ def test_variant_noalloc_matches_layer(cuda_device):
         y = torch.empty_like(x)
         moe.moe_forward_noalloc(config, w, x, T, y)
         torch.cuda.synchronize()
-        assert torch.equal(y, layer.forward(x))
+        # same kernel; the fp32 reductions may add in another order
+        a, b = bf16_f64(to_host_bits(y)), bf16_f64(to_host_bits(layer.forward(x)))
+        assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-30)
     layer.close()
