@@ -58,11 +58,11 @@ struct DecodeParams {
   uint16_t* in_trace;    // [L][T][H] or null: each layer's normalised input
   int32_t* ids_out;      // [L][T][k] or null
   float* w_out;          // [L][T][k] or null
-  uint16_t* xbuf;        // [2][4][H] residual ping-pong
+  uint16_t* xbuf;        // [2][4][H] not read by the work-unit kernel (sizes the scratch)
   float* z;              // [4][E]
   float* gz;             // [4] shared-expert gate logits g . u (MOE_ROUTING_SHARED_GATE)
   float* yacc;           // [2][4][H] layer outputs, reduced in L2 (fp32)
-  float* hbuf;           // [max_units-ish][4][Fmax] fp32
+  float* hbuf;           // [units][4][Fmax] not read by the work-unit kernel (sizes the scratch)
   GridBarrier* bar;
   int* err;
   unsigned long long timeout_ns;
