@@ -84,3 +84,14 @@ def test_create_refuses_shapes_whose_single_token_decode_cannot_fit(lib):
         with pytest.raises(moe.MoeError):
             moe.moe_layer_create(_cfg(**shape), {}, False)
         assert "NULL" in moe.moe_last_error()
+
+
+def test_create_requires_the_gate_vector_of_a_gated_shared_expert(lib):
+    names = ("router_w", "router_bias", "slot_of_expert", "gate_q", "gate_s", "up_q", "up_s",
+             "down_q", "down_s", "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q",
+             "sh_down_s")
+    fake = {n: 16 for n in names}  # non-null placeholders: refused before any device access
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_create(_cfg(routing_flags=moe.ROUTING_SHARED_GATE), fake, False)
+    assert ei.value.status == moe.MOE_ERR_INVALID
+    assert "sh_gate_w" in moe.moe_last_error()
