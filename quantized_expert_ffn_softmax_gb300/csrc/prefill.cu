@@ -4,12 +4,16 @@
 //   prep       x (bf16) -> x16: fp16, scaled per token by a power of two so
 //              the row maximum lies in [1, 2), K reordered inside every group
 //              of 8 to the order in which packed 4-bit codes unpack
-//   router     z = W_r x + b as one tcgen05 GEMM with K' = 2H: W_r is split
-//              on the fly into two fp16 terms (hi + mid, 22 significant bits)
-//              so the logits keep fp32-level accuracy for the exact top-k
-//   top-k      one warp per token; softmax over the selected logits
+//   router     z = W_r x + b as one tcgen05 GEMM with K' = 2H: W_r * 2^shift
+//              is split once, at layer creation, into two fp16 terms (hi +
+//              mid, about 22 significant bits) so the logits keep
+//              fp32-level accuracy for the exact top-k
+//   top-k      one warp per token; softmax over the selected logits (or the
+//              routing variants), and the gate weight of a gated shared
+//              expert
 //   bucket     stable counting sort of the (token, slot) assignments by
-//              expert; builds the work-unit lists of the two GEMMs
+//              expert in three launches (chunk counts, one-CTA scans and the
+//              work-unit lists, chunk scatter)
 //   gate/up    per unit (expert, 128-token tile, 128-row F tile):
 //              D_g, D_u = W_g/u[128 x H] . X[tokens]^T in TMEM, epilogue
 //              h = silu(g) * u -> fp16 rows of Hmid (bucket order)
@@ -20,17 +24,23 @@
 //
 // GEMM engine: one persistent CTA per SM, warp-specialised.
 //   warps 0-3   epilogue (TMEM lanes 0-127 = the 128 rows of the tile)
-//   warps 4-11  A producers: dequantise 4-bit codes (or split fp32 router
-//               weights) into fp16 128x64 tiles in the 128-byte swizzled
-//               K-major layout, straight into the stage's shared memory
-//   B loaders   gate/up: warps 12-13 gather the unit's token rows (bucket
-//               order) with per-thread 16-byte async copies into the same
-//               swizzled layout; down/router: warp 12 loads the unit's
-//               contiguous rows as one TMA tile per K step
-//   last warp   TMEM allocator and single-thread tcgen05.mma issuer
-// A 4-stage shared-memory ring (full/empty mbarriers) feeds the MMA; two
-// TMEM accumulators let the epilogue of one unit overlap the next unit's
-// MMAs.  Every wait is bounded and gives up once the error word is set.
+//   warps 4-11  A producers: dequantise 4-bit codes from the raw ring into
+//               fp16 128x64 tiles written into tensor memory (tcgen05.st);
+//               the router's A tiles come ready-made by TMA instead
+//   B loaders   gate/up: two warps gather the unit's token rows (bucket
+//               order) with per-thread 16-byte async copies into the
+//               128-byte swizzled K-major layout; down/router: one thread
+//               loads the unit's contiguous rows as one TMA tile per K step
+//   raw loader  one warp: TMA tiles of packed codes (128 rows x 32 bytes per
+//               matrix and K step) and the block scales into a raw ring
+//   last warp   TMEM allocator and single-thread tcgen05.mma issuer (A from
+//               tensor memory, B from shared memory)
+// A stage ring (an A slot in TMEM and a B tile in shared memory per stage; 4
+// stages for gate/up, 8 for down) feeds the MMA, one tcgen05.commit per
+// step.  down keeps two TMEM accumulators so one unit's epilogue overlaps
+// the next unit's MMAs; gate/up has room for one gate|up accumulator, whose
+// epilogue stages the SwiGLU rows in shared memory and releases it early.
+// Every wait is bounded and gives up once the error word is set.
 #include <cudaTypedefs.h>
 #include <stdlib.h>
 #include <string.h>
