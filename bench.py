@@ -447,17 +447,53 @@ def headline_config(n_gpus):
 
 
 def run_reference(args):
+    """The oracle as it stands, on this host's cores, timed on a bounded
+    sample of the headline workload: one token through the first layer
+    (router, top-k, the k selected experts and the shared expert), its
+    weights drawn once before any timing.  Each step is one such layer
+    pass, scaled to the 40-layer stack, when K + W of them fit in about
+    150 s; otherwise one expert FFN of that layer, scaled by the layer /
+    expert time ratio measured once beforehand (untimed)."""
     cfg = W.CONFIGS[HEADLINE]
     import oracle
 
     oracle.build()
-    # one step = one token through 8 of the 40 layers (about 1-2 s of CPU)
-    per = []
+    wr, b = W.router(cfg, 0)
+    sh = W.shared_expert(cfg, 0)
+    x = W.activations(cfg, 100)
+    u = oracle.rmsnorm(x)
+    z = oracle.router_logits(wr, b, u)
+    ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
+    experts = [W.expert(cfg, 0, int(e)) for e in ids[0]]
+
+    def layer_pass():
+        zz = oracle.router_logits(wr, b, u)
+        ii, ww, _ = oracle.topk_softmax(zz, cfg.top_k)
+        oracle.combine_token(experts, ww[0], sh, u[0])
+
+    def expert_pass():
+        oracle.combine_token(experts[:1], np.ones(1), None, u[0])
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    t_layer = min(timed(layer_pass) for _ in range(2))
+    n = args.steps + args.warmup
+    if n * t_layer <= 150.0:
+        fn, scale = layer_pass, float(cfg.n_layers)
+        desc = ("oracle (fp64 C, 1 thread): one token through layer 0 (router, top-%d, %d experts + "
+                "shared) per step, scaled x%d to the stack" % (cfg.top_k, cfg.top_k, cfg.n_layers))
+    else:
+        t_exp = min(timed(expert_pass) for _ in range(3))
+        fn, scale = expert_pass, cfg.n_layers * t_layer / t_exp
+        desc = ("oracle (fp64 C, 1 thread): one expert FFN of layer 0 for one token per step, "
+                "scaled x%.1f (40 layers x the measured layer/expert time ratio %.2f)"
+                % (scale, t_layer / t_exp))
     for _ in range(args.warmup):
-        oracle_decode_sample(cfg, 1, 8)
-    for _ in range(args.steps):
-        s, desc = oracle_decode_sample(cfg, 1, 8)
-        per.append(s)
+        fn()
+    per = [timed(fn) * scale for _ in range(args.steps)]
     sec = float(np.mean(per))
     v = 1.0 / sec
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
