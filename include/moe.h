@@ -157,10 +157,12 @@ moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void*
 
 /* moe_stack_forward that also records, for every pointer that is not NULL
  * (device memory only): h_trace [L][T][H] = h_{l+1}, in_trace [L][T][H] =
- * u_l (bf16 bits), ids_trace [L][T][k] = each layer's top-k ids. */
+ * u_l, y_trace [L][T][H] = bf16(layer_l(u_l)) (all bf16 bits), ids_trace
+ * [L][T][k] = each layer's top-k ids. */
 moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
-                                    void* in_trace_bf16, int32_t* ids_trace, void* stream);
+                                    void* in_trace_bf16, void* y_trace_bf16, int32_t* ids_trace,
+                                    void* stream);
 
 /* Allocation-free decode of one layer (1..4 tokens), for callers that
  * cannot allocate device memory when they need a layer evaluated: code
@@ -169,18 +171,27 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
  * allowed to call cudaMalloc, and processes held to a fixed device-memory
  * budget after start-up.  The pages have no counterpart of this entry point.
  * Computes y = layer(x) like moe_forward, but from the caller's weights
- * (device pointers, layout as in moe_layer_weights, router_bias required),
- * x [n_tokens][H] bf16 (device, 16-byte aligned) and y (device).  All the
- * scratch memory the kernel needs comes from one static 4 MiB device array
- * inside the library, present on every GPU that loads it until the process
- * exits; shapes whose scratch would not fit return MOE_ERR_CAPACITY.  No
- * call allocates or frees device memory.  The first call on each device
- * looks up the array's device address with that device current: make it
- * before any stream capture.  Every call shares the array, so calls that
- * overlap on the GPU (other streams, other host threads) race on it.
- * status_out (optional, device int32) is zeroed, then receives any error a
- * kernel records (MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS); the slot table is only
- * bounds-checked by the kernel.  Asynchronous on `stream`. */
+ * (layout as in moe_layer_weights, n_slots == n_experts, router_bias
+ * required).  Every pointer must be device memory of the current device
+ * (or managed memory): the weights, router_w, slot_of_expert and
+ * sh_gate_w 16-byte aligned, x [n_tokens][H] bf16 16-byte aligned,
+ * router_bias and status_out 4-byte aligned; anything else returns
+ * MOE_ERR_INVALID before any work is queued, as do shapes outside the
+ * moe_layer_create limits.  All the scratch memory the kernel needs comes
+ * from one static 128 KiB device array inside the library, present on every
+ * GPU that loads it until the process exits; shapes whose scratch would not
+ * fit (8 * hidden * 4 bytes of output accumulators plus 16 * n_experts
+ * bytes of logits and about 1 KB more: hidden 2048 fits, hidden 4096 does
+ * not) return MOE_ERR_CAPACITY.  No call allocates or frees device memory.
+ * The first call on each device looks up the array's device address with
+ * that device current: make it before any stream capture.  Every call
+ * shares the array, so calls that overlap on the GPU (other streams, other
+ * host threads) race on it.  status_out (optional, device int32) is zeroed,
+ * then receives any error a kernel records (MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS);
+ * without it such an error goes to a scratch word that no call reads, so a
+ * failed kernel leaves a wrong y unreported.  The slot table is only
+ * bounds-checked by the kernel.  Asynchronous on `stream`; the bounded
+ * waits use the MOE_WAIT_TIMEOUT_US limit of the other calls. */
 moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weights* w,
                                const void* x_bf16, int n_tokens, void* y_bf16,
                                int32_t* status_out, void* stream);

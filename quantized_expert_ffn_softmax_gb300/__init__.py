@@ -84,7 +84,7 @@ def lib():
         L.moe_stack_forward.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp]
         L.moe_stack_forward.restype = i32
         L.moe_stack_forward_traced.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, vp, vp, vp,
-                                               vp]
+                                               vp, vp]
         L.moe_stack_forward_traced.restype = i32
         L.moe_forward_noalloc.argtypes = [ctypes.POINTER(moe_layer_config),
                                           ctypes.POINTER(moe_layer_weights), vp, i32, vp, vp, vp]
@@ -199,9 +199,9 @@ def moe_stack_forward(layers: Sequence[int], n_layers: int, x, n_tokens: int, y,
 
 
 def moe_stack_forward_traced(layers: Sequence[int], n_layers: int, x, n_tokens: int, y, h_trace,
-                             in_trace, ids_trace, stream=None) -> None:
+                             in_trace, y_trace, ids_trace, stream=None) -> None:
     _check(lib().moe_stack_forward_traced(_layer_array(layers), n_layers, _ptr(x), n_tokens,
-                                          _ptr(y), _ptr(h_trace), _ptr(in_trace),
+                                          _ptr(y), _ptr(h_trace), _ptr(in_trace), _ptr(y_trace),
                                           _ptr(ids_trace), _stream(stream)))
 
 
@@ -272,6 +272,8 @@ class MoELayer:
 
 
 def stack_forward(layers: Sequence[MoELayer], x, stream=None, trace: bool = False):
+    """Runs the pre-norm residual stack; with trace=True also returns each
+    layer's h_{l+1}, normalised input u_l, output bf16(y_l) and top-k ids."""
     import torch
 
     y = torch.empty_like(x)
@@ -283,6 +285,7 @@ def stack_forward(layers: Sequence[MoELayer], x, stream=None, trace: bool = Fals
     k = layers[0].config["top_k"]
     h_trace = torch.empty((L, T, H), dtype=x.dtype, device=x.device)
     in_trace = torch.empty((L, T, H), dtype=x.dtype, device=x.device)
+    y_trace = torch.empty((L, T, H), dtype=x.dtype, device=x.device)
     ids = torch.empty((L, T, k), dtype=torch.int32, device=x.device)
-    moe_stack_forward_traced(hs, L, x, T, y, h_trace, in_trace, ids, stream)
-    return y, h_trace, in_trace, ids
+    moe_stack_forward_traced(hs, L, x, T, y, h_trace, in_trace, y_trace, ids, stream)
+    return y, h_trace, in_trace, y_trace, ids

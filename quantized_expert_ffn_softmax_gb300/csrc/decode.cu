@@ -389,18 +389,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const float4 y1 = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8 + 1);
             const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
             const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-            uint32_t o[4];
+            uint32_t o[4], yo[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float lo = __uint_as_float(hw[q] << 16) + __bfloat162float(__float2bfloat16_rn(yy[2 * q]));
-              const float hi = __uint_as_float(hw[q] & 0xffff0000u) +
-                               __bfloat162float(__float2bfloat16_rn(yy[2 * q + 1]));
+              const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
+              const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
+              const float lo = __uint_as_float(hw[q] << 16) + __bfloat162float(ylo);
+              const float hi = __uint_as_float(hw[q] & 0xffff0000u) + __bfloat162float(yhi);
               o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+              yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
             }
             v = make_uint4(o[0], o[1], o[2], o[3]);
             if (blockIdx.x == 0 && p.h_trace)
               reinterpret_cast<uint4*>(p.h_trace + ((size_t)(l - 1) * T + t) * H)[g8] = v;
+            if (blockIdx.x == 0 && p.y_trace)
+              reinterpret_cast<uint4*>(p.y_trace + ((size_t)(l - 1) * T + t) * H)[g8] =
+                  make_uint4(yo[0], yo[1], yo[2], yo[3]);
           }
         }
         reinterpret_cast<uint4*>(stage_dst)[i] = v;
@@ -914,6 +919,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const float* yl = p.yacc + (size_t)((p.n_layers - 1) & 1) * kMaxDecodeTokens * H;
     for (int i = blockIdx.x * kDecodeThreads + tid; i < T * H; i += grid * kDecodeThreads) {
       const __nv_bfloat16 yb = __float2bfloat16_rn(__ldcg(yl + i));
+      if (p.y_trace) p.y_trace[(size_t)(p.n_layers - 1) * T * H + i] = __bfloat16_as_ushort(yb);
       if (stack) {
         const float xv = __bfloat162float(__ushort_as_bfloat16(hres[i]));
         const uint16_t xn = __bfloat16_as_ushort(__float2bfloat16_rn(xv + __bfloat162float(yb)));
@@ -926,9 +932,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 }
 
-size_t decode_smem_bytes(const DecodeParams& p) {
+size_t decode_smem_bytes(const DecodeParams& p, int num_sms) {
   const int TT = p.T == 1 ? 1 : (p.T == 2 ? 2 : 4);
-  return DecodeSmem::make(p.H, p.E, TT, 152, 1).total;
+  return DecodeSmem::make(p.H, p.E, TT, num_sms, 1).total;
 }
 
 template <int TT>

@@ -51,7 +51,18 @@ bool is_device_ptr(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
-uint64_t wait_timeout_ns() {
+struct Stage {
+  const uint16_t* x = nullptr;
+  uint16_t* y = nullptr;
+  bool y_host = false;
+};
+
+}  // namespace
+
+namespace moe {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+unsigned long long wait_timeout_ns() {
   const char* s = getenv("MOE_WAIT_TIMEOUT_US");
   if (s && *s) {
     long long us = atoll(s);
@@ -60,7 +71,7 @@ uint64_t wait_timeout_ns() {
   return 1000000000ull;  // 1 s
 }
 
-moe_status validate_config(const moe_layer_config* c) {
+moe_status validate_config(const moe_layer_config* c, int num_sms) {
   if (!c) return fail(MOE_ERR_INVALID, "config is NULL");
   if (c->hidden < 128 || c->hidden > 8192 || c->hidden % 128)
     return fail(MOE_ERR_INVALID, "hidden=%d: need a multiple of 128 in [128, 8192]", c->hidden);
@@ -96,7 +107,9 @@ moe_status validate_config(const moe_layer_config* c) {
     p.T = 1;
     p.max_units = std::min(c->top_k, c->n_experts) + 1;
     const size_t bias = c->routing_flags ? (((size_t)c->n_experts * 4 + 127) & ~(size_t)127) : 0;
-    const size_t need = moe::decode_smem_bytes(p) + bias;
+    // num_sms <= 0: no device yet; the grid that gives the smallest
+    // footprint (one router row per CTA) refuses only what fits no GPU
+    const size_t need = moe::decode_smem_bytes(p, num_sms > 0 ? num_sms : c->n_experts + 1) + bias;
     if (need > (size_t)227 * 1024)
       return fail(MOE_ERR_INVALID,
                   "hidden=%d, n_experts=%d: the decode kernel needs %zu KB of shared memory (> 227 KB)",
@@ -104,22 +117,11 @@ moe_status validate_config(const moe_layer_config* c) {
   }
   return MOE_OK;
 }
-
-struct Stage {
-  const uint16_t* x = nullptr;
-  uint16_t* y = nullptr;
-  bool y_host = false;
-};
-
-}  // namespace
-
-namespace moe {
-void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 }  // namespace moe
 
 extern "C" {
 
-int moe_version(void) { return 200; }
+int moe_version(void) { return 300; }
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
@@ -127,7 +129,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
                             int weights_on_device, moe_layer** out) {
   if (!out) return fail(MOE_ERR_INVALID, "out is NULL");
   *out = nullptr;
-  moe_status st = validate_config(cfg);
+  // shape limits first (no device needed), the exact decode footprint for
+  // this device's SM count once the weights are known to be there
+  moe_status st = moe::validate_config(cfg, 0);
   if (st != MOE_OK) return st;
   if (!w || !w->router_w || !w->slot_of_expert || !w->gate_q || !w->gate_s || !w->up_q ||
       !w->up_s || !w->down_q || !w->down_s)
@@ -137,6 +141,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     return fail(MOE_ERR_INVALID, "shared_ffn > 0 but a shared-expert pointer is NULL");
   if ((cfg->routing_flags & MOE_ROUTING_SHARED_GATE) && !w->sh_gate_w)
     return fail(MOE_ERR_INVALID, "MOE_ROUTING_SHARED_GATE but sh_gate_w is NULL");
+  int device = 0, num_sms = 0;
+  CUDA_TRY(cudaGetDevice(&device), "cudaGetDevice");
+  CUDA_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device),
+           "query the SM count");
+  if ((st = moe::validate_config(cfg, num_sms)) != MOE_OK) return st;
   const char* fault = getenv("MOE_FAULT_ALLOC");
   if (fault && atoi(fault) == 1) return fail(MOE_ERR_OOM, "allocation failure injected by MOE_FAULT_ALLOC");
 
@@ -161,8 +170,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
 
   moe_layer* L = new moe_layer();
   L->cfg = *cfg;
-  cudaGetDevice(&L->device);
-  cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  L->device = device;
+  L->num_sms = num_sms;
 
   // ---- weights: one allocation, 256-B aligned sub-buffers
   struct Piece {
@@ -236,8 +245,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
 
   // ---- workspace
-  const int Fmax = F > Fs ? F : Fs;
-  const int routed_max = (moe::kMaxDecodeTokens * k < E) ? moe::kMaxDecodeTokens * k : E;
   size_t wo = 0;
   auto wadd = [&](size_t bytes) {
     wo = align_up(wo, 256);
@@ -245,9 +252,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     wo += bytes;
     return r;
   };
-  size_t o_xbuf = wadd(sizeof(uint16_t) * 2 * moe::kMaxDecodeTokens * H);
   size_t o_z = wadd(sizeof(float) * moe::kMaxDecodeTokens * E);
-  size_t o_h = wadd(sizeof(float) * moe::kMaxDecodeTokens * ((size_t)routed_max * F + Fmax));
   size_t o_bar = wadd(sizeof(moe::GridBarrier));
   size_t o_err = wadd(sizeof(int) * 4);
   size_t o_xs = wadd(sizeof(uint16_t) * (size_t)Tm * H);
@@ -267,9 +272,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     return cuda_fail(e, "cudaMalloc(workspace)");
   }
   char* wb = static_cast<char*>(L->ws_block);
-  L->ws.xbuf = (uint16_t*)(wb + o_xbuf);
   L->ws.z = (float*)(wb + o_z);
-  L->ws.hbuf = (float*)(wb + o_h);
   L->ws.bar = (moe::GridBarrier*)(wb + o_bar);
   L->ws.err = (int*)(wb + o_err);
   L->ws.x_stage = (uint16_t*)(wb + o_xs);
@@ -360,14 +363,12 @@ moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
   p.T = T;
   p.mode = mode;
   p.max_units = ((T * c.top_k < c.n_experts) ? T * c.top_k : c.n_experts) + 1;
-  p.xbuf = L0->ws.xbuf;
   p.z = L0->ws.z;
   p.gz = L0->ws.gz;
   p.yacc = L0->ws.dyacc;
-  p.hbuf = L0->ws.hbuf;
   p.bar = L0->ws.bar;
   p.err = L0->ws.err;
-  p.timeout_ns = wait_timeout_ns();
+  p.timeout_ns = moe::wait_timeout_ns();
   const char* dbg = getenv("MOE_DEBUG_UNREACHABLE_BARRIER");
   p.debug_extra_arrivals = (dbg && atoi(dbg) == 1) ? 1 : 0;
   return p;
@@ -376,8 +377,8 @@ moe::DecodeParams decode_params(moe_layer* L0, int T, int mode) {
 // Runs `n_layers` layers on <= 4 tokens with the decode kernel (chunks of
 // kMaxLayersPerLaunch layers per launch).
 moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x, int T,
-                      uint16_t* y, uint16_t* h_trace, uint16_t* in_trace, int32_t* ids_trace,
-                      float* w_out, int mode, cudaStream_t stream) {
+                      uint16_t* y, uint16_t* h_trace, uint16_t* in_trace, uint16_t* y_trace,
+                      int32_t* ids_trace, float* w_out, int mode, cudaStream_t stream) {
   moe_layer* L0 = layers[0];
   const int H = L0->cfg.hidden;
   const uint16_t* cur = x;
@@ -389,6 +390,7 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
     p.y_out = y;
     p.h_trace = h_trace ? h_trace + (size_t)l0 * T * H : nullptr;
     p.in_trace = in_trace ? in_trace + (size_t)l0 * T * H : nullptr;
+    p.y_trace = y_trace ? y_trace + (size_t)l0 * T * H : nullptr;
     p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
     p.w_out = w_out;
     for (int l = 0; l < nl; ++l) {
@@ -436,7 +438,8 @@ __global__ void rmsnorm_kernel(const uint16_t* __restrict__ h, int T, int H,
 moe_status forward_device(moe_layer* L, const uint16_t* x, int T, uint16_t* y, cudaStream_t s) {
   if (T <= moe::kMaxDecodeTokens) {
     moe_layer* one[1] = {L};
-    return run_decode(one, 1, x, T, y, nullptr, nullptr, nullptr, nullptr, moe::kModeForward, s);
+    return run_decode(one, 1, x, T, y, nullptr, nullptr, nullptr, nullptr, nullptr,
+                      moe::kModeForward, s);
   }
   const char* why = "";
   moe_status st = moe::launch_prefill(L, x, T, y, nullptr, nullptr, false, s, &why);
@@ -499,7 +502,8 @@ moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t
   float* w = w_host ? layer->ws.w_stage : topk_w;
   if (n_tokens <= moe::kMaxDecodeTokens) {
     moe_layer* one[1] = {layer};
-    st = run_decode(one, 1, sg.x, n_tokens, nullptr, nullptr, nullptr, ids, w, moe::kModeRoute, s);
+    st = run_decode(one, 1, sg.x, n_tokens, nullptr, nullptr, nullptr, nullptr, ids, w,
+                    moe::kModeRoute, s);
   } else {
     const char* why = "";
     st = moe::launch_prefill(layer, sg.x, n_tokens, nullptr, ids, w, true, s, &why);
@@ -531,7 +535,8 @@ moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void*
 
 moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, const void* x_bf16,
                                     int n_tokens, void* y_bf16, void* h_trace_bf16,
-                                    void* in_trace_bf16, int32_t* ids_trace, void* stream) {
+                                    void* in_trace_bf16, void* y_trace_bf16, int32_t* ids_trace,
+                                    void* stream) {
   if (!layers || n_layers < 1) return fail(MOE_ERR_INVALID, "need at least one layer");
   moe_status st = check_common(layers[0], x_bf16, n_tokens);
   if (st != MOE_OK) return st;
@@ -545,7 +550,8 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
       return fail(MOE_ERR_INVALID, "layer %d has a different shape from layer 0", l);
   }
   if ((h_trace_bf16 && !is_device_ptr(h_trace_bf16)) || (ids_trace && !is_device_ptr(ids_trace)) ||
-      (in_trace_bf16 && !is_device_ptr(in_trace_bf16)))
+      (in_trace_bf16 && !is_device_ptr(in_trace_bf16)) ||
+      (y_trace_bf16 && !is_device_ptr(y_trace_bf16)))
     return fail(MOE_ERR_INVALID, "trace buffers must be device memory");
   cudaStream_t s = (cudaStream_t)stream;
   Stage sg;
@@ -553,7 +559,8 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
   const int H = c0.hidden, k = c0.top_k;
   if (n_tokens <= moe::kMaxDecodeTokens) {
     st = run_decode(layers, n_layers, sg.x, n_tokens, sg.y, (uint16_t*)h_trace_bf16,
-                    (uint16_t*)in_trace_bf16, ids_trace, nullptr, moe::kModeStack, s);
+                    (uint16_t*)in_trace_bf16, (uint16_t*)y_trace_bf16, ids_trace, nullptr,
+                    moe::kModeStack, s);
     if (st != MOE_OK) return st;
   } else {
     // prefill-sized stack: layer by layer.  h ping-pongs between the two
@@ -580,6 +587,10 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
                                ids_trace ? ids_trace + (size_t)l * n_tokens * k : nullptr, nullptr,
                                false, s, &why);
       if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
+      if (y_trace_bf16)
+        CUDA_TRY(cudaMemcpyAsync((uint16_t*)y_trace_bf16 + (size_t)l * n, Y, n * 2,
+                                 cudaMemcpyDeviceToDevice, s),
+                 "trace copy");
       uint16_t* dst = (l == n_layers - 1) ? sg.y : (cur == P ? Q : P);
       {
         moe::prof::Scope sc("moe_residual", s);
@@ -615,7 +626,7 @@ moe_status moe_last_buckets(moe_layer* layer, int n_tokens, int32_t* offsets, in
 moe_status moe_stack_forward(moe_layer* const* layers, int n_layers, const void* x_bf16,
                              int n_tokens, void* y_bf16, void* stream) {
   return moe_stack_forward_traced(layers, n_layers, x_bf16, n_tokens, y_bf16, nullptr, nullptr,
-                                  nullptr, stream);
+                                  nullptr, nullptr, stream);
 }
 
 }  // extern "C"

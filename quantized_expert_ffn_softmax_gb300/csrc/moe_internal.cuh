@@ -56,20 +56,18 @@ struct DecodeParams {
   uint16_t* y_out;       // forward: y [T][H]; stack: h_L [T][H]
   uint16_t* h_trace;     // [L][T][H] or null
   uint16_t* in_trace;    // [L][T][H] or null: each layer's normalised input
+  uint16_t* y_trace;     // [L][T][H] or null: each layer's output bf16(y_l)
   int32_t* ids_out;      // [L][T][k] or null
   float* w_out;          // [L][T][k] or null
-  uint16_t* xbuf;        // [2][4][H] not read by the work-unit kernel (sizes the scratch)
   float* z;              // [4][E]
   float* gz;             // [4] shared-expert gate logits g . u (MOE_ROUTING_SHARED_GATE)
   float* yacc;           // [2][4][H] layer outputs, reduced in L2 (fp32)
-  float* hbuf;           // [units][4][Fmax] not read by the work-unit kernel (sizes the scratch)
   GridBarrier* bar;
   int* err;
   unsigned long long timeout_ns;
   // Test hook: every grid barrier waits for this many arrivals more than the
   // grid has, so the bounded wait runs out and records MOE_ERR_TIMEOUT.
   int debug_extra_arrivals;
-  int want_dprefetch;  // set by the launcher: stage the down weights in shared memory
   int g_stages;        // set by the launcher: gate/up shared-memory stages (1 or 2)
   LayerDev layers[kMaxLayersPerLaunch];
   // per layer: MOE_ROUTING_* bits and the shared-expert gate vector [H]
@@ -80,9 +78,7 @@ struct DecodeParams {
 
 // Workspace of one layer object.
 struct Workspace {
-  uint16_t* xbuf = nullptr;
   float* z = nullptr;
-  float* hbuf = nullptr;
   GridBarrier* bar = nullptr;
   int* err = nullptr;
   uint16_t* x_stage = nullptr;  // [max_tokens][H] staging for host inputs
@@ -144,10 +140,19 @@ struct moe_layer {
 namespace moe {
 // moe_api.cu: message returned by moe_last_error() on this thread
 void set_last_error(const char* msg);
+// moe_api.cu: checks a layer shape against the library's limits and the
+// decode kernel's shared memory on a grid of num_sms CTAs (num_sms <= 0:
+// on the grid that needs the least); sets the thread's error message and
+// returns MOE_ERR_INVALID when it fails
+moe_status validate_config(const moe_layer_config* c, int num_sms);
+// moe_api.cu: limit of every bounded device-side wait (MOE_WAIT_TIMEOUT_US
+// in the environment, else 1 s)
+unsigned long long wait_timeout_ns();
 // decode.cu
 moe_status launch_decode(const DecodeParams& p, cudaStream_t stream, int num_sms,
                          const char** why);
-size_t decode_smem_bytes(const DecodeParams& p);
+// shared memory of the decode kernel for p's shape on a grid of num_sms CTAs
+size_t decode_smem_bytes(const DecodeParams& p, int num_sms);
 // prefill.cu
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
                           float* w_out, bool route_only, cudaStream_t stream, const char** why);

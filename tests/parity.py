@@ -23,12 +23,43 @@ def y_tol(y_ref) -> float:
     return 1e-2 * float(np.abs(y_ref).max()) + 1e-3
 
 
-def h_tol(y_ref, h_ref) -> float:
-    """Tolerance on a stack output h = bf16(h_in + bf16(y)): the y tolerance,
-    plus one bf16 unit in the last place (2^-7 relative, upper bound) for each
-    of the two roundings, which may land on different sides of a rounding
-    boundary when y differs within its tolerance."""
-    return y_tol(y_ref) + 2.0 ** -7 * (float(np.abs(y_ref).max()) + float(np.abs(h_ref).max()))
+def h_tol_elem(y_ref, h_ref, tol_y: float) -> np.ndarray:
+    """Per-element bound on a stack output h = bf16(h_in + bf16(y)) when the
+    GPU's y is within tol_y of y_ref (same bf16 h_in on both sides): the
+    difference in y, plus half a bf16 unit in the last place (2^-8 relative)
+    for each of the four roundings -- bf16(y) and the bf16 sum on either side
+    --, which is at most 2^-7 * (|y| + |h|) up to terms in tol_y."""
+    return tol_y * (1.0 + 2.0 ** -7) + 2.0 ** -7 * (np.abs(y_ref) + np.abs(h_ref))
+
+
+def check_stack_outputs(h_in, y_gpu, h_gpu, y_ref, where=""):
+    """One stack layer, teacher-forced: every token's y (bf16 bits from the
+    GPU's trace) against the oracle's y_ref (fp64, computed from the GPU's
+    normalised input) at the stated tolerance, and every element of the
+    residual h_{l+1} = bf16(h_l + bf16(y)) against the oracle's residual of
+    the GPU's own h_l.  Returns the worst y error over its tolerance."""
+    worst = 0.0
+    for t in range(y_ref.shape[0]):
+        tol = y_tol(y_ref[t])
+        err = float(np.max(np.abs(bf16_f64(y_gpu[t]) - y_ref[t])))
+        assert err <= tol, ("y", where, t, err, tol)
+        worst = max(worst, err / tol)
+        h_ref = bf16_f64(oracle.residual(h_in[t][None, :], y_ref[t][None, :]))[0]
+        dh = np.abs(bf16_f64(h_gpu[t]) - h_ref)
+        bound = h_tol_elem(y_ref[t], h_ref, tol)
+        assert np.all(dh <= bound), ("h", where, t, float(np.max(dh - bound)))
+    return worst
+
+
+def parallel_map(fn, items, workers: int = 0):
+    """fn over items on a thread pool (the oracle and the generator are C
+    calls that release the GIL); results in item order."""
+    import concurrent.futures as cf
+    import os
+
+    n = workers or max(1, min(16, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        return list(ex.map(fn, items))
 
 
 def config_dict(cfg: W.MoEConfig, max_tokens: int) -> dict:

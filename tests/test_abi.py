@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_empty_error(lib):
-    assert moe.moe_version() == 200
+    assert moe.moe_version() == 300
     assert isinstance(moe.moe_last_error(), str)
 
 

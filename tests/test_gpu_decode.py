@@ -12,8 +12,8 @@ import torch
 import oracle
 import quantized_expert_ffn_softmax_gb300 as moe
 import workload as W
-from parity import (bf16_f64, check_topk, h_tol, make_layer_device, make_layer_host,
-                    oracle_token, to_dev, to_host_bits, y_tol)
+from parity import (bf16_f64, check_stack_outputs, check_topk, make_layer_device,
+                    make_layer_host, oracle_token, parallel_map, to_dev, to_host_bits, y_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -120,10 +120,9 @@ def test_tiny_stack_teacher_forced(cuda_device):
     made = [make_layer_host(cfg, l) for l in range(L)]
     layers = [m[0] for m in made]
     x = W.activations(cfg, 2)
-    y, h_trace, in_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+    y, h_trace, in_trace, y_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
     assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
-    h_trace = to_host_bits(h_trace)
-    in_trace = to_host_bits(in_trace)
+    h_trace, in_trace, y_trace = to_host_bits(h_trace), to_host_bits(in_trace), to_host_bits(y_trace)
     ids_trace = ids_trace.cpu().numpy()
     assert np.array_equal(to_host_bits(y), h_trace[-1])
     h_prev = x
@@ -135,10 +134,7 @@ def test_tiny_stack_teacher_forced(cuda_device):
         adopt = [check_topk(ids_trace[l, t], z[t], cfg.top_k) for t in range(cfg.n_tokens)]
         y_ref = oracle.moe_forward(Ld, cfg.top_k, u,
                                    forced_ids=ids_trace[l] if any(adopt) else None)[0]
-        h_ref = bf16_f64(oracle.residual(h_prev, y_ref))
-        hg = bf16_f64(h_trace[l])
-        tol = h_tol(y_ref, h_ref)
-        assert np.max(np.abs(hg - h_ref)) <= tol, l
+        check_stack_outputs(h_prev, y_trace[l], h_trace[l], y_ref, where=l)
         h_prev = h_trace[l]
     # in place: x == y is allowed for stacks
     xd = to_dev(x)
@@ -189,18 +185,22 @@ def test_errors_and_timeout_status(cuda_device):
 
 # ----------------------------------------------------------------- full-size stacks
 
-def _stack_check(cfg, n_check_layers=None, tokens_to_check=None, input_index=0):
+def _stack_check(cfg, input_index=0):
     """Runs the full stack (device-generated weights) once with traces and
-    checks every layer's top-k and a sample of layers' outputs with teacher
-    forcing (the oracle takes the GPU's bf16 input of that layer)."""
+    checks EVERY layer with teacher forcing (the oracle takes the GPU's bf16
+    input of that layer): the RMS norm, every token's top-k, every token's
+    layer output y_l at the stated tolerance
+    max|y_gpu - y_ref| <= 1e-2 max|y_ref| + 1e-3, and every element of the
+    residual h_{l+1}.  Layers are checked concurrently on host threads."""
     layers = [make_layer_device(cfg, l, max_tokens=8) for l in range(cfg.n_layers)]
     try:
         x = W.activations(cfg, input_index)
-        y, h_trace, in_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+        y, h_trace, in_trace, y_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
         assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
-        h_trace = to_host_bits(h_trace)
-        in_trace = to_host_bits(in_trace)
+        h_trace, in_trace = to_host_bits(h_trace), to_host_bits(in_trace)
+        y_trace = to_host_bits(y_trace)
         ids_trace = ids_trace.cpu().numpy()
+        assert np.array_equal(to_host_bits(y), h_trace[-1])
     finally:
         for l in layers:
             l.close()
@@ -209,40 +209,39 @@ def _stack_check(cfg, n_check_layers=None, tokens_to_check=None, input_index=0):
         torch.cuda.empty_cache()
     assert np.all(np.isfinite(bf16_f64(h_trace[-1])))
     T = cfg.n_tokens
-    toks = range(T) if tokens_to_check is None else tokens_to_check
-    check_layers = set(range(cfg.n_layers)) if n_check_layers is None else set(n_check_layers)
     h_in = [x] + [h_trace[l] for l in range(cfg.n_layers - 1)]
-    n_adopted = 0
-    for l in range(cfg.n_layers):
+
+    def check_layer(l):
         u = in_trace[l]
         check_norm(u, h_in[l])
         Wr, b = W.router(cfg, l)
-        z = oracle.router_logits(Wr, b, u)
-        for t in range(T):
-            n_adopted += check_topk(ids_trace[l, t], z[t], cfg.top_k)
-        if l not in check_layers:
-            continue
         sh = W.shared_expert(cfg, l)
         cache = {}
-        for t in toks:
-            y_ref, _, _ = oracle_token(cfg, l, u[t], gpu_ids=ids_trace[l, t], router=(Wr, b),
-                                       shared=sh, expert_cache=cache)
-            h_ref = bf16_f64(oracle.residual(h_in[l][t], y_ref))
-            hg = bf16_f64(h_trace[l][t])
-            tol = h_tol(y_ref, h_ref)
-            err = np.max(np.abs(hg - h_ref))
-            assert err <= tol, (l, t, err, tol)
-    return ids_trace, n_adopted
+        y_ref = np.empty((T, cfg.hidden), np.float64)
+        adopted = 0
+        for t in range(T):
+            y_ref[t], _, a = oracle_token(cfg, l, u[t], gpu_ids=ids_trace[l, t], router=(Wr, b),
+                                          shared=sh, expert_cache=cache)
+            adopted += a
+        worst = check_stack_outputs(h_in[l], y_trace[l], h_trace[l], y_ref, where=l)
+        return adopted, worst
+
+    res = parallel_map(check_layer, range(cfg.n_layers))
+    n_adopted = sum(r[0] for r in res)
+    worst = max(r[1] for r in res)
+    return ids_trace, n_adopted, worst
 
 
 def test_decode35b_stack_parity(cuda_device):
     cfg = W.CONFIGS["decode35b"]
-    _stack_check(cfg, n_check_layers=list(range(0, 40, 3)) + [39])
+    _, _, worst = _stack_check(cfg)
+    print("decode35b: worst y error / tolerance over 40 layers = %.3f" % worst)
 
 
 def test_mtp35b_verify_batch_parity(cuda_device):
     cfg = W.CONFIGS["mtp35b"]
-    ids, _ = _stack_check(cfg, n_check_layers=[0, 1, 20, 39])
+    ids, _, worst = _stack_check(cfg)
+    print("mtp35b: worst y error / tolerance over 40 layers x 4 tokens = %.3f" % worst)
     # the calibrated drafts overlap token 0's selection by about one half
     ov = [len(set(ids[0, 0]) & set(ids[0, t])) / cfg.top_k for t in range(1, 4)]
     assert 0.2 <= np.mean(ov) <= 0.85
@@ -250,4 +249,5 @@ def test_mtp35b_verify_batch_parity(cuda_device):
 
 def test_decode125b_stack_parity(cuda_device):
     cfg = W.CONFIGS["decode125b"]
-    _stack_check(cfg, n_check_layers=[0, 1, 23, 46, 47])
+    _, _, worst = _stack_check(cfg)
+    print("decode125b: worst y error / tolerance over 48 layers = %.3f" % worst)

@@ -10,8 +10,8 @@ import torch
 import oracle
 import quantized_expert_ffn_softmax_gb300 as moe
 import workload as W
-from parity import (bf16_f64, check_topk, config_dict, h_tol, host_weights, make_layer_host,
-                    to_dev, to_host_bits, y_tol)
+from parity import (bf16_f64, check_stack_outputs, check_topk, config_dict, host_weights,
+                    make_layer_host, to_dev, to_host_bits, y_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,9 +68,10 @@ def test_variant_stack_teacher_forced(cuda_device, T):
     made = [make_layer_host(cfg, l, max_tokens=64) for l in range(L)]
     layers = [m[0] for m in made]
     x = W.activations(cfg, 4, n_tokens=T)
-    y, h_trace, in_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+    y, h_trace, in_trace, y_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
     assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
     h_trace, in_trace = to_host_bits(h_trace), to_host_bits(in_trace)
+    y_trace = to_host_bits(y_trace)
     ids_trace = ids_trace.cpu().numpy()
     h_prev = x
     for l in range(L):
@@ -79,8 +80,7 @@ def test_variant_stack_teacher_forced(cuda_device, T):
         z = oracle.router_logits(Ld["router_w"], Ld["router_b"], u)
         adopt = [check_topk(ids_trace[l, t], z[t], cfg.top_k) for t in range(T)]
         y_ref = oracle.moe_forward(Ld, cfg.top_k, u, forced_ids=ids_trace[l] if any(adopt) else None)[0]
-        h_ref = bf16_f64(oracle.residual(h_prev, y_ref))
-        assert np.max(np.abs(bf16_f64(h_trace[l]) - h_ref)) <= h_tol(y_ref, h_ref), l
+        check_stack_outputs(h_prev, y_trace[l], h_trace[l], y_ref, where=l)
         h_prev = h_trace[l]
     for lay in layers:
         lay.close()
