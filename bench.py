@@ -72,22 +72,27 @@ def prefill_flops(cfg, T) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi sampling (every 50 ms) of SM clocks and throttle reasons.
+    """nvidia-smi sampling (every 20 ms) of SM clocks and throttle reasons.
 
     Started before the warm-up so that it is running when the timed region
-    begins; each sample is stamped with the host time it arrived, and the
-    summary keeps only the samples taken between mark_start() and
-    mark_stop() (the timed region)."""
+    begins; each sample is stamped with the host time it arrived.
+    summary() keeps the samples taken between mark_start() and mark_stop()
+    (the timed region).  A short timed region (a few ms) may hold no sample,
+    so the caller can run the same step for a while after it, untimed, and
+    mark that stretch with mark_window(); report() then adds the samples of
+    that load window and says so."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.rows = []
         self.t0 = self.t1 = None
+        self.w0 = self.w1 = None
         self.thread = None
 
     def _reader(self):
@@ -98,7 +103,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             self.thread = threading.Thread(target=self._reader, daemon=True)
             self.thread.start()
@@ -115,6 +120,9 @@ class ClockSampler:
     def mark_stop(self):
         self.t1 = time.time()
 
+    def mark_window(self, t0: float, t1: float):
+        self.w0, self.w1 = t0, t1
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -125,10 +133,14 @@ class ClockSampler:
             if self.thread is not None:
                 self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, windows=None):
+        """Samples whose arrival falls in one of the (t0, t1) windows
+        (default: the timed region)."""
+        if windows is None:
+            windows = [(self.t0, self.t1)] if self.t0 is not None and self.t1 is not None else None
         rows = []
         for t, line in self.rows:
-            if self.t0 is not None and self.t1 is not None and not (self.t0 <= t <= self.t1 + 0.06):
+            if windows is not None and not any(a <= t <= b + 0.06 for a, b in windows):
                 continue
             r = next(csv.reader(io.StringIO(line)), [])
             if len(r) >= 9:
@@ -146,6 +158,19 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+    def report(self):
+        """The timed region's summary; when it holds fewer than 3 samples,
+        the median and reasons are taken over the timed region and the load
+        window after it (same step, untimed), and `source` says so."""
+        s = self.summary()
+        out = dict(s, samples_timed=s["samples"], source="timed region")
+        if s["samples"] < 3 and self.w0 is not None and self.t0 is not None:
+            out = dict(self.summary([(self.t0, self.t1), (self.w0, self.w1)]),
+                       samples_timed=s["samples"],
+                       source="timed region + %.1f s load window of the same step after it"
+                              % (self.w1 - self.w0))
+        return out
 
 
 def source_hash(*rel):
@@ -263,6 +288,17 @@ def time_steps(fn, steps, warmup, dist, ring_len, clk=None):
     torch.cuda.synchronize()
     if clk is not None:
         clk.mark_stop()
+        if clk.t1 - clk.t0 < 1.0:
+            # too short for the sampler: run the same step, untimed, for about
+            # a second so that clocks under this load are sampled too
+            w0 = time.time()
+            i = 0
+            while time.time() - w0 < 1.0:
+                for _ in range(8):
+                    fn((warmup + steps + i) % ring_len)
+                    i += 1
+                torch.cuda.synchronize()
+            clk.mark_window(w0, time.time())
     dist.barrier()
     torch.cuda.synchronize()
     return dist.max(s.elapsed_time(e) / steps)
@@ -299,7 +335,7 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
     ubuf = torch.empty_like(hbuf)
     uniq = []
     for i in range(8):
-        moe.moe_stack_forward_traced(hs, L, ring[i], T, y, hbuf, ubuf, ids)
+        moe.moe_stack_forward_traced(hs, L, ring[i], T, y, hbuf, ubuf, None, ids)
         a = ids.cpu().numpy()
         uniq.append(sum(len(set(a[l].ravel().tolist())) for l in range(L)))
     assert moe.moe_status_sync(hs[0]) == moe.MOE_OK
@@ -327,7 +363,7 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
         "bytes_incl_router": bytes_per_step + L * router_bytes(cfg),
         "unique_routed_per_layer": mean_unique_routed / L,
         "launches_per_step": launches_per_step,
-        "clocks": clk.summary(),
+        "clocks": clk.report(),
     }
     if with_e2e:
         xs = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).pin_memory() for i in range(8)]
@@ -391,7 +427,7 @@ def bench_prefill(name, steps, warmup, dist):
            "grouped_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
            "kernels": kern,
            "launches_per_step": sum(v["launches"] for v in kern.values()) / max(1, min(steps, 20)),
-           "clocks": clk.summary()}
+           "clocks": clk.report()}
     layer.close()
     torch.cuda.empty_cache()
     return out
@@ -399,42 +435,66 @@ def bench_prefill(name, steps, warmup, dist):
 
 # --------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_decode_sample(cfg, n_tokens: int, n_layers: int):
-    """Times the oracle on `n_tokens` tokens through the first `n_layers`
-    layers of the stack (expert weights drawn before the timed region).
-    Returns (seconds per token for the full stack, description)."""
+def host_cpu():
+    """(nproc, CPU model) of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    import platform
+
+    return os.cpu_count() or 1, model or platform.machine()
+
+
+def _thread_map(fn, items, workers):
+    """fn over items on `workers` host threads (the oracle's C calls release
+    the GIL); results in item order."""
+    import concurrent.futures as cf
+
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, items))
+
+
+def oracle_decode_sample(cfg, n_layers: int, threads: int):
+    """Times the oracle as it stands (fp64 C) on `threads` independent tokens
+    at once, one per host thread, each through the first `n_layers` layers
+    of the stack (its experts drawn before the timed region).  Returns
+    (tokens/s for the full stack, description)."""
     import oracle
 
     routers = [W.router(cfg, l) for l in range(n_layers)]
     shared = [W.shared_expert(cfg, l) for l in range(n_layers)]
-    xs = [W.activations(cfg, 100 + i) for i in range(n_tokens)]
-    # route once to know which experts to draw, then time the full pass
-    plans = []
-    for x in xs:
+
+    def token_pass(x, plan=None):
         h = x.copy()
-        plan = []
+        drawn = []
         for l in range(n_layers):
             u = oracle.rmsnorm(h)
             z = oracle.router_logits(*routers[l], u)
             ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
-            plan.append([W.expert(cfg, l, int(e)) for e in ids[0]])
-            y = oracle.combine_token(plan[-1], w[0], shared[l], u[0])
+            exs = plan[l] if plan is not None else [W.expert(cfg, l, int(e)) for e in ids[0]]
+            drawn.append(exs)
+            y = oracle.combine_token(exs, w[0], shared[l], u[0])
             h = oracle.residual(h, y[None, :])
-        plans.append(plan)
+        return drawn
+
+    xs = [W.activations(cfg, 100 + i) for i in range(threads)]
+    # route once to know which experts to draw (untimed), then time the pass
+    plans = _thread_map(token_pass, xs, threads)
     t0 = time.perf_counter()
-    for x, plan in zip(xs, plans):
-        h = x.copy()
-        for l in range(n_layers):
-            u = oracle.rmsnorm(h)
-            z = oracle.router_logits(*routers[l], u)
-            ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
-            y = oracle.combine_token(plan[l], w[0], shared[l], u[0])
-            h = oracle.residual(h, y[None, :])
+    _thread_map(lambda i: token_pass(xs[i], plans[i]), range(threads), threads)
     dt = time.perf_counter() - t0
-    per_token_full = dt / n_tokens * (cfg.n_layers / n_layers)
-    desc = ("oracle (fp64 C, 1 thread) on %d token(s) x %d of %d layers; expert weights drawn "
-            "before timing; scaled to the full stack" % (n_tokens, n_layers, cfg.n_layers))
-    return per_token_full, desc
+    tok_s = threads / (dt * cfg.n_layers / n_layers)
+    desc = ("oracle (fp64 C, as it stands) on %d independent tokens at once, one per host "
+            "thread, each through %d of the %d layers (router, top-%d, %d experts + shared, "
+            "residual); expert weights drawn before timing; wall time scaled x%d to the stack"
+            % (threads, n_layers, cfg.n_layers, cfg.top_k, cfg.top_k, cfg.n_layers // n_layers))
+    return tok_s, desc
 
 
 def headline_config(n_gpus):
@@ -447,60 +507,69 @@ def headline_config(n_gpus):
 
 
 def run_reference(args):
-    """The oracle as it stands, on this host's cores, timed on a bounded
-    sample of the headline workload: one token through the first layer
-    (router, top-k, the k selected experts and the shared expert), its
-    weights drawn once before any timing.  Each step is one such layer
-    pass, scaled to the 40-layer stack, when K + W of them fit in about
-    150 s; otherwise one expert FFN of that layer, scaled by the layer /
-    expert time ratio measured once beforehand (untimed)."""
+    """The oracle as it stands (fp64 C), on this host's cores, timed on a
+    bounded sample of the headline workload.  One step: `threads` different
+    tokens at once, one per host thread, each through layer 0 (router,
+    top-k, its k experts and the shared expert; the weights drawn once
+    before any timing).  The tokens/s value scales that wall time to the
+    40-layer stack; ms_per_step is the time of the work actually timed.
+    When K + W such steps would take more than about 150 s, a step is one
+    expert FFN per thread instead, scaled by the layer / expert time ratio
+    measured once beforehand (untimed)."""
     cfg = W.CONFIGS[HEADLINE]
     import oracle
 
     oracle.build()
+    nproc, model = host_cpu()
+    threads = max(1, min(16, nproc))
     wr, b = W.router(cfg, 0)
     sh = W.shared_expert(cfg, 0)
-    x = W.activations(cfg, 100)
-    u = oracle.rmsnorm(x)
-    z = oracle.router_logits(wr, b, u)
-    ids, w, _ = oracle.topk_softmax(z, cfg.top_k)
-    experts = [W.expert(cfg, 0, int(e)) for e in ids[0]]
+    us = [oracle.rmsnorm(W.activations(cfg, 100 + i)) for i in range(threads)]
 
-    def layer_pass():
-        zz = oracle.router_logits(wr, b, u)
+    def draw(u):
+        ids, _, _ = oracle.topk_softmax(oracle.router_logits(wr, b, u), cfg.top_k)
+        return [W.expert(cfg, 0, int(e)) for e in ids[0]]
+
+    experts = _thread_map(draw, us, threads)
+
+    def layer_pass(i):
+        zz = oracle.router_logits(wr, b, us[i])
         ii, ww, _ = oracle.topk_softmax(zz, cfg.top_k)
-        oracle.combine_token(experts, ww[0], sh, u[0])
+        oracle.combine_token(experts[i], ww[0], sh, us[i][0])
 
-    def expert_pass():
-        oracle.combine_token(experts[:1], np.ones(1), None, u[0])
+    def expert_pass(i):
+        oracle.combine_token(experts[i][:1], np.ones(1), None, us[i][0])
 
     def timed(fn):
         t0 = time.perf_counter()
-        fn()
+        _thread_map(fn, range(threads), threads)
         return time.perf_counter() - t0
 
     t_layer = min(timed(layer_pass) for _ in range(2))
     n = args.steps + args.warmup
     if n * t_layer <= 150.0:
         fn, scale = layer_pass, float(cfg.n_layers)
-        desc = ("oracle (fp64 C, 1 thread): one token through layer 0 (router, top-%d, %d experts + "
-                "shared) per step, scaled x%d to the stack" % (cfg.top_k, cfg.top_k, cfg.n_layers))
+        desc = ("oracle (fp64 C, as it stands) on %d host threads: per step %d different tokens "
+                "at once, one per thread, through layer 0 (router, top-%d, %d experts + shared); "
+                "scaled x%d to the stack" % (threads, threads, cfg.top_k, cfg.top_k, cfg.n_layers))
     else:
         t_exp = min(timed(expert_pass) for _ in range(3))
         fn, scale = expert_pass, cfg.n_layers * t_layer / t_exp
-        desc = ("oracle (fp64 C, 1 thread): one expert FFN of layer 0 for one token per step, "
-                "scaled x%.1f (40 layers x the measured layer/expert time ratio %.2f)"
-                % (scale, t_layer / t_exp))
+        desc = ("oracle (fp64 C, as it stands) on %d host threads: per step one expert FFN of "
+                "layer 0 for each of %d tokens at once, scaled x%.1f (40 layers x the measured "
+                "layer/expert time ratio %.2f)" % (threads, threads, scale, t_layer / t_exp))
     for _ in range(args.warmup):
-        fn()
-    per = [timed(fn) * scale for _ in range(args.steps)]
-    sec = float(np.mean(per))
-    v = 1.0 / sec
+        timed(fn)
+    per = [timed(fn) for _ in range(args.steps)]
+    step_s = float(np.mean(per))
+    v = threads / (step_s * scale)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "step_scale_to_stack": scale, "tokens_per_step": threads,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": headline_config(args.gpus),
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "nproc": nproc,
+                             "cpu": model, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -567,8 +636,11 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cfg = W.CONFIGS[HEADLINE]
-        sec, desc = oracle_decode_sample(cfg, 2, 10)
-        cpu = {"value": 1.0 / sec, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        nproc, model = host_cpu()
+        threads = max(1, min(16, nproc))
+        v, desc = oracle_decode_sample(cfg, 4, threads)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "nproc": nproc, "cpu": model,
+               "kind": "oracle", "sample": desc}
 
     src = source_hash("quantized_expert_ffn_softmax_gb300/csrc/decode.cu",
                       "quantized_expert_ffn_softmax_gb300/csrc/device_common.cuh")

@@ -67,3 +67,22 @@ def test_committed_traffic_record_is_well_formed():
         assert len(e["source_hash"]) == 16 and int(e["source_hash"], 16) >= 0
         assert isinstance(e["dram_bytes_per_launch"], int) and e["dram_bytes_per_launch"] > 0
         assert os.path.exists(os.path.join(ROOT, e["summary"]))
+
+
+def test_clock_report_adds_the_load_window_when_the_timed_region_is_short():
+    b = _bench()
+    c = b.ClockSampler(0)
+    c.rows = [(0.5, _row(1000)), (1.01, _row(2070)),
+              (2.0, _row(2060)), (2.2, _row(2040, power_cap="Active")), (2.4, _row(2070)),
+              (9.0, _row(900, thermal="Active"))]
+    c.t0, c.t1 = 1.0, 1.02            # 20 ms timed region: one sample
+    r = c.report()
+    assert r["samples_timed"] == 1 and r["samples"] == 1 and r["source"] == "timed region"
+    c.mark_window(1.9, 2.5)
+    r = c.report()
+    assert r["samples_timed"] == 1 and r["samples"] == 4
+    assert r["sm_mhz"] == 2065.0 and r["reasons"] == ["sw_power_cap"]
+    assert "load window" in r["source"]
+    c.t0, c.t1 = 1.9, 2.5             # enough samples in the timed region itself
+    r = c.report()
+    assert r["source"] == "timed region" and r["samples"] == 3
