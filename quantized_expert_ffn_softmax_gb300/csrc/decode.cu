@@ -32,6 +32,7 @@
 // fp32.  Activations are rescaled by a per-token power of two before the
 // fp16 conversion, so their range never overflows fp16.
 #include <math.h>
+#include <stdlib.h>
 
 #include "device_common.cuh"
 #include "moe_internal.cuh"
@@ -42,7 +43,18 @@ namespace {
 
 using namespace dev;
 
-constexpr int kWarps = kDecodeThreads / 32;
+constexpr int kWarps = kDecodeThreads / 32;  // compute warps; warp kWarps issues the copies
+
+// Barrier of the compute warps only (named barrier 1): the copy warp runs
+// its own schedule and never joins it.
+__device__ __forceinline__ void cta_sync() { named_bar_sync(1, kDecodeThreads); }
+
+// out[0..3] += v (fp32) with one vector reduction in L2; out 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float* out, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
 
 // Grid barrier on a counter zeroed before the launch: barrier number `n`
 // completes when the counter reaches (n + 1) * gridDim.x.  Waits are bounded
@@ -50,7 +62,7 @@ constexpr int kWarps = kDecodeThreads / 32;
 // at once, so a failing launch still ends in bounded time.
 __device__ __forceinline__ void grid_sync(GridBarrier* b, unsigned& n, int* err,
                                           uint64_t timeout_ns, int extra) {
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     const unsigned target = (n + 1) * gridDim.x + (unsigned)extra;
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&b->count) : "memory");
@@ -69,7 +81,7 @@ __device__ __forceinline__ void grid_sync(GridBarrier* b, unsigned& n, int* err,
     }
   }
   ++n;
-  __syncthreads();
+  cta_sync();
 }
 
 // Shift that brings amax into [32, 64).
@@ -280,8 +292,22 @@ struct DecodeMisc {
 };
 static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 
-// mbarrier slots
-enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarR = 4 };
+// mbarrier slots: gate/up stages full (G) and empty (E), router rows (R),
+// slot table (S), down stage full (D) and empty (DE)
+enum { kBarG0 = 0, kBarG1 = 1, kBarE0 = 2, kBarE1 = 3, kBarR = 4, kBarS = 5, kBarD = 6, kBarDE = 7,
+       kNumBars = 8 };
+// named barriers between the compute warps and the copy warp: the router
+// rows buffer is free (compute warps arrive), the unit list is ready (all sync)
+enum { kNbRowsFree = 3, kNbUnits = 2 };
+
+// Rows per box of the down-code tensor map: the largest multiple of 32 that
+// is at most 256 and divides H/4 (H/4 is a multiple of 32).
+__host__ __device__ __forceinline__ int down_qbox(int H) {
+  const int hq = H / 4;
+  for (int q = 256; q >= 32; q -= 32)
+    if (hq % q == 0) return q;
+  return 32;
+}
 
 // 4-byte async copy global -> shared (the .ca form; .cg takes 16 bytes only)
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
@@ -291,7 +317,7 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
 // kVar: some layer of the launch uses a routing variant (routing_flags != 0);
 // the default instantiation carries none of their code.
 template <int TT, bool kVar>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(kDecodeBlock, 1)
     moe_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = p.H, E = p.E, k = p.k, F = p.F, Fs = p.Fs, T = p.T;
@@ -299,8 +325,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int CF = F / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x;
-  const DecodeSmem L =
-      DecodeSmem::make(H, E, TT, grid, p.g_stages);
+  const DecodeSmem L = DecodeSmem::make(H, E, TT, grid, p.g_stages);
   const int NG = p.g_stages;  // 1 or 2
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
   DecodeMisc& M = *reinterpret_cast<DecodeMisc*>(smem + L.misc);
@@ -313,13 +338,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   unsigned char* dst_s = smem + L.dst;
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1) ? kWarps : 1);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(&mbar[i], (i == kBarE0 || i == kBarE1 || i == kBarDE) ? kWarps : 1);
     fence_mbar_init();
   }
-  __syncthreads();
-  uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
-  uint32_t ph_r = 0u;
-  unsigned nbar = 0;
+  __syncthreads();  // the only barrier of all kDecodeBlock threads
   const uint64_t tmo = p.timeout_ns;
   const bool stack = (p.mode == kModeStack);
   // Router rows of this CTA in layer l: e = blockIdx.x + j * grid, j < rows;
@@ -334,32 +357,161 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       return ((int)blockIdx.x < Er) ? (Er - (int)blockIdx.x + grid - 1) / grid : 0;
     }
   };
-
-  // Router rows of this CTA's experts for layer l (and the slot table when
-  // its size and alignment allow a bulk copy), into shared memory on the R
-  // barrier.
+  // The slot table of layer l goes to shared memory by one bulk copy when its
+  // size and alignment allow; otherwise the unit list reads it from global.
   auto slots_bulk_of = [&](int l) {
     return (E % 4) == 0 && (reinterpret_cast<uintptr_t>(p.layers[l].slot_of) & 15u) == 0;
   };
-  auto prefetch_router = [&](int l) {
-    const LayerDev& W = p.layers[l];
-    const bool slots_bulk = slots_bulk_of(l);
-    const int rows = router_rows(l);
-    if (warp == kWarps - 1) {
-      const uint32_t bytes = (uint32_t)rows * H * 4u + (slots_bulk ? (uint32_t)E * 4u : 0u);
-      if (lane == 0 && bytes) mbar_expect_tx(&mbar[kBarR], bytes);
+  // Work units: a unit is (expert unit, 32-row block of its F); CTA c takes
+  // units c, c + grid, ...; each has two 16-row gate/up items.
+  const int ipu = F / 16;  // gate/up items per routed unit
+  const int bpu = F / 32;  // blocks per routed unit
+  const int Hq = H / 4;
+  auto my_units = [&](int n_routed) {
+    const int n_wu = n_routed * bpu + Fs / 32;
+    return ((int)blockIdx.x < n_wu) ? (n_wu - (int)blockIdx.x + grid - 1) / grid : 0;
+  };
+  auto item_of = [&](int q) { return 2 * ((int)blockIdx.x + (q >> 1) * grid) + (q & 1); };
+  // unit and block of this CTA's j-th work unit
+  auto wu_of = [&](int j, int n_routed, int& u, int& b) {
+    const int w = blockIdx.x + j * grid;
+    if (w < n_routed * bpu) {
+      u = w / bpu;
+      b = w - u * bpu;
+    } else {
+      u = n_routed;
+      b = w - n_routed * bpu;
+    }
+  };
+
+  // ------------------------------------------------ the copy warp
+  // Issuing a bulk or tensor copy costs its thread on the order of 150 ns,
+  // so one warp issues them all and the compute warps only wait on the
+  // mbarriers: per layer, the next layer's router rows once this CTA's
+  // router product has read the buffer, then (after the unit list) the
+  // first gate/up items, the first down block and the next layer's slot
+  // table, and refills as the compute warps release stages.
+  if (warp == kWarps) {
+    auto issue_rows = [&](int l) {  // all lanes
+      const LayerDev& W = p.layers[l];
+      const int rows = router_rows(l);
+      if (lane == 0 && rows) mbar_expect_tx(&mbar[kBarR], (uint32_t)rows * H * 4u);
       __syncwarp();
       for (int j = lane; j < rows; j += 32) {
         const int e = blockIdx.x + j * grid;
         bulk_g2s(wr + (size_t)j * H, (!kVar || e < E) ? W.router_w + (size_t)e * H : p.sh_gate_w[l],
                  H * 4u, &mbar[kBarR]);
       }
-      if (slots_bulk && lane == 31) bulk_g2s(slots, W.slot_of, (uint32_t)E * 4u, &mbar[kBarR]);
+    };
+    auto issue_slots = [&](int l) {  // lane 0
+      if (lane == 0 && slots_bulk_of(l)) {
+        mbar_expect_tx(&mbar[kBarS], (uint32_t)E * 4u);
+        bulk_g2s(slots, p.layers[l].slot_of, (uint32_t)E * 4u, &mbar[kBarS]);
+      }
+    };
+    // gate/up item q into stage q % NG: lane 0 arms the stage, lanes 0..3
+    // issue one copy each
+    auto issue_g = [&](int l, int q, int n_routed) {
+      const LayerDev& W = p.layers[l];
+      const int it = item_of(q);
+      const uint8_t* gq;
+      const uint16_t* gs;
+      const uint8_t* uq;
+      const uint16_t* us;
+      if (it < n_routed * ipu) {
+        const int u = it / ipu;
+        const int f0 = (it - u * ipu) * 16;
+        const size_t slot = (size_t)M.unit_slot[u];
+        gq = W.gate_q + (slot * F + f0) * (H / 2);
+        uq = W.up_q + (slot * F + f0) * (H / 2);
+        gs = W.gate_s + (slot * F + f0) * C;
+        us = W.up_s + (slot * F + f0) * C;
+      } else {
+        const int f0 = (it - n_routed * ipu) * 16;
+        gq = W.sh_gate_q + (size_t)f0 * (H / 2);
+        uq = W.sh_up_q + (size_t)f0 * (H / 2);
+        gs = W.sh_gate_s + (size_t)f0 * C;
+        us = W.sh_up_s + (size_t)f0 * C;
+      }
+      unsigned char* st = gbuf + (size_t)(q % NG) * L.g_stage;
+      uint64_t* bar = &mbar[kBarG0 + (q % NG)];
+      if (lane == 0) mbar_expect_tx(bar, (uint32_t)L.g_stage);
+      __syncwarp();
+      if (lane == 0) bulk_g2s(st, gq, 16u * (H / 2), bar);
+      else if (lane == 1) bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
+      else if (lane == 2) bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
+      else if (lane == 3) bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
+    };
+    // Down block of work unit j: codes of every output row, row r at
+    // position (r % 4) * H/4 + r / 4 (4-D TMA boxes), and the block's H scales
+    // from the block-major copy (one bulk copy); lanes in parallel.
+    auto issue_d = [&](int l, int j, int n_routed) {
+      const LayerDev& W = p.layers[l];
+      int u, b;
+      wu_of(j, n_routed, u, b);
+      const bool routed = u < n_routed;
+      const size_t slot = routed ? (size_t)M.unit_slot[u] : 0;
+      const int QB = down_qbox(H), nqb = Hq / QB;
+      if (lane == 0) mbar_expect_tx(&mbar[kBarD], (uint32_t)H * 18u);
+      __syncwarp();
+      const CUtensorMap* tm = routed ? &p.tm_down[l] : &p.tm_sh_down[l];
+      for (int i = lane; i <= 4 * nqb; i += 32) {
+        if (i < 4 * nqb) {
+          const int jr = i / nqb, qb = i - jr * nqb;
+          tma_load_4d(dst_s + ((size_t)jr * Hq + (size_t)qb * QB) * 16, tm, 16 * b, jr, qb * QB,
+                      (int)slot, &mbar[kBarD]);
+        } else {
+          const uint16_t* sb = routed ? W.down_sb + (slot * CF + b) * H : W.sh_down_sb + (size_t)b * H;
+          bulk_g2s(dst_s + (size_t)H * 16, sb, (uint32_t)H * 2u, &mbar[kBarD]);
+        }
+      }
+    };
+    // waits by lane 0, result shared with the warp (lanes stay converged)
+    auto wait0 = [&](uint64_t* bar, uint32_t parity) {
+      int r = 1;
+      if (lane == 0) r = mbar_wait(bar, parity, p.err, tmo) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, r, 0) != 0;
+    };
+    issue_slots(0);
+    issue_rows(0);
+    uint32_t e_done[2] = {0u, 0u}, d_done = 0u;  // stage releases seen (phase parity)
+    bool ok = true;  // false after a failed wait: keep the barrier schedule, issue nothing
+    for (int l = 0; l < p.n_layers; ++l) {
+      named_bar_sync(kNbRowsFree, kDecodeBlock);
+      if (ok && l + 1 < p.n_layers && p.mode != kModeRoute) issue_rows(l + 1);
+      named_bar_sync(kNbUnits, kDecodeBlock);
+      if (p.mode == kModeRoute) continue;
+      const int n_routed = M.n_routed;
+      const int my_wu = my_units(n_routed), n_items = 2 * my_wu;
+      if (ok) {
+        for (int q = 0; q < NG && q < n_items; ++q) issue_g(l, q, n_routed);
+        if (p.down_tma && my_wu > 0) issue_d(l, 0, n_routed);
+        if (l + 1 < p.n_layers) issue_slots(l + 1);
+      }
+      for (int q = 0; q < n_items; ++q) {
+        const int sg = q % NG;
+        if (q + NG < n_items) {
+          if (ok) ok = wait0(&mbar[kBarE0 + sg], e_done[sg] & 1u);
+          if (ok) issue_g(l, q + NG, n_routed);
+        }
+        ++e_done[sg];
+        if (p.down_tma && (q & 1)) {
+          const int j = q >> 1;
+          if (j + 1 < my_wu) {
+            if (ok) ok = wait0(&mbar[kBarDE], d_done & 1u);
+            if (ok) issue_d(l, j + 1, n_routed);
+          }
+          ++d_done;
+        }
+      }
     }
-    if (!slots_bulk)
-      for (int e = tid; e < E; e += kDecodeThreads) slots[e] = __ldg(W.slot_of + e);
-  };
-  prefetch_router(0);
+    return;
+  }
+
+  // ------------------------------------------------ the compute warps
+  uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
+  uint32_t ph_r = 0u, ph_s = 0u, ph_d = 0u;  // router rows, slot table, down stage fills waited for
+  unsigned nbar = 0;
 
   for (int l = 0; l < p.n_layers; ++l) {
     const LayerDev& W = p.layers[l];
@@ -432,7 +584,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           M.red_mx[warp][t] = b;
         }
       }
-      __syncthreads();
+      cta_sync();
       float inv[TT], sc[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
@@ -491,17 +643,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         xp[(t * 4 + (g & 3)) * C + (g >> 2)] = make_uint4(out[0], out[1], out[2], out[3]);
       }
-      __syncthreads();
+      cta_sync();
     }
-    // router: this CTA's expert rows e = blockIdx + j*grid (prefetched W_r
-    // rows); row j is split over the warps w with w % my_rows == j, each
-    // summing one slice of H; the slices meet in shared memory
+    // router: this CTA's expert rows e = blockIdx + j*grid (W_r rows staged
+    // in shared memory by the copy warp); row j is split over the warps w
+    // with w % nr == j, each summing one slice of H; the slices meet in
+    // shared memory
     const int my_rows = router_rows(l);
     // this thread's router bias (read before the row wait, off the critical path)
     const float bias_mine =
         (tid < min(my_rows, kWarps) * T && (!kVar || (int)blockIdx.x + (tid / T) * grid < E))
             ? __ldg(W.router_b + blockIdx.x + (tid / T) * grid) : 0.0f;
-    if (my_rows > 0 || slots_bulk_of(l)) {  // the R barrier was armed for this layer
+    if (my_rows > 0) {
       mbar_wait(&mbar[kBarR], ph_r, p.err, tmo);
       ph_r ^= 1u;
     }
@@ -531,7 +684,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const float s = warp_sum(acc[t]);
         if (lane == 0) M.red_z[warp][t] = s;
       }
-      __syncthreads();
+      cta_sync();
       if (tid < nr * T) {
         const int jr = tid / T, t = tid - (tid / T) * T;
         float z = 0.0f;
@@ -542,8 +695,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         else
           p.gz[t] = z;  // the shared-expert gate logit
       }
-      __syncthreads();  // red_z is reused by the next batch
+      // the rows were read through the generic proxy; the copy warp refills
+      // the buffer by bulk copies after this batch
+      fence_proxy_async_smem();
+      cta_sync();  // red_z is reused by the next batch
     }
+    named_bar_arrive(kNbRowsFree, kDecodeBlock);  // the copy warp may refill the rows buffer
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
 
     // ------------------------------------------------ top-k + softmax + units
@@ -552,7 +709,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (E <= 256) topk_level1<1>(p.z, T, E, k, M.cand);
     else if (E <= 512) topk_level1<2>(p.z, T, E, k, M.cand);
     else topk_level1<4>(p.z, T, E, k, M.cand);
-    __syncthreads();
+    cta_sync();
     {
       const int nc = kWarps * k;                // candidates per token
       const int ncp = nc <= 64 ? 64 : 128;      // padded with empty entries
@@ -574,7 +731,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (part == 0 && c < nc && r < k && mine != 0ull) M.sel_key[t][r] = mine;
       }
     }
-    __syncthreads();
+    cta_sync();
     if (warp < T) {
       const uint64_t sk = (lane < k) ? M.sel_key[warp][lane] : 0ull;
       uint32_t ok2 = (uint32_t)(sk >> 32);
@@ -624,17 +781,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         M.sel_w[warp][lane] = ex / den;
       }
     }
+    // the slot table of this layer (bulk-copied during the previous layer)
+    const bool slots_bulk = slots_bulk_of(l);
+    if (slots_bulk) {
+      mbar_wait(&mbar[kBarS], ph_s, p.err, tmo);
+      ph_s ^= 1u;
+    }
+    auto slot_lookup = [&](int e) { return slots_bulk ? slots[e] : __ldg(W.slot_of + e); };
     if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
     for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)
       (&M.unit_w[0][0])[i] = 0.0f;
-    __syncthreads();
+    cta_sync();
     if (TT == 1) {
       // one token: the units are the selection itself, in selection order
       if (tid < k) {
         const int e = M.sel_id[0][tid];
         M.unit_w[tid][0] = M.sel_w[0][tid];
         M.unit_expert[tid] = e;
-        int s = slots[e];
+        int s = slot_lookup(e);
         if (s < 0 || s >= E) {
           atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
           s = 0;
@@ -647,7 +811,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     } else {
       if (tid < T * k) atomicOr(&M.bitmap[M.sel_id[tid / k][tid % k] >> 5], 1u << (M.sel_id[tid / k][tid % k] & 31));
-      __syncthreads();
+      cta_sync();
       if (warp == 0) {  // exclusive prefix of the bitmap's popcounts
         const int c = __popc(M.bitmap[lane]);
         int x = c;
@@ -663,14 +827,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           M.n_units = x + (Fs > 0 ? 1 : 0);
         }
       }
-      __syncthreads();
+      cta_sync();
       if (tid < T * k) {
         const int t = tid / k, r = tid % k;
         const int e = M.sel_id[t][r];
         const int u = M.prefix[e >> 5] + __popc(M.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
         M.unit_w[u][t] = M.sel_w[t][r];
         M.unit_expert[u] = e;
-        int s = slots[e];
+        int s = slot_lookup(e);
         if (s < 0 || s >= E) {
           atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
           s = 0;
@@ -693,10 +857,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         M.unit_w[nr][tid] = (tid < T) ? ws : 0.0f;
       }
     }
-    // the router rows and slot table were read through the generic proxy;
-    // the next layer's bulk copies (async proxy) overwrite them
+    // the slot table was read through the generic proxy; the next layer's
+    // bulk copy (async proxy) overwrites it.  The unit list is ready: the
+    // copy warp starts this layer's weight copies.
     fence_proxy_async_smem();
-    __syncthreads();
+    named_bar_sync(kNbUnits, kDecodeBlock);
     if (p.mode == kModeRoute) continue;
     const int n_routed = M.n_routed;
     // the other accumulator held the previous layer's output, which every
@@ -707,64 +872,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int i = blockIdx.x * kDecodeThreads + tid; i < TT * H; i += grid * kDecodeThreads) ynext[i] = 0.0f;
     }
 
-    // ------------------------------------------------ work units and their copies
+    // ------------------------------------------------ work units
     // A work unit is (unit, 32-row block of its F): gate/up rows of the block
     // (two 16-row items through the stage ring), then the block's columns of
-    // the down matrix against all H outputs.  CTA c takes units c, c + grid, ..
-    const int ipu = F / 16;  // gate/up items per routed unit
-    const int bpu = F / 32;  // blocks per routed unit
-    const int n_wu = n_routed * bpu + Fs / 32;
-    const int my_wu = ((int)blockIdx.x < n_wu) ? (n_wu - (int)blockIdx.x + grid - 1) / grid : 0;
+    // the down matrix against all H outputs.  The copy warp brings the data.
+    const int my_wu = my_units(n_routed);
     const int n_my_items = 2 * my_wu;
-    auto item_of = [&](int q) { return 2 * ((int)blockIdx.x + (q >> 1) * grid) + (q & 1); };
-    auto issue_g = [&](int q) {  // gate/up item q of this CTA into stage q % NG
-      if (q >= n_my_items) return;
-      const int it = item_of(q);
-      const uint8_t* gq;
-      const uint16_t* gs;
-      const uint8_t* uq;
-      const uint16_t* us;
-      if (it < n_routed * ipu) {
-        const int u = it / ipu;
-        const int f0 = (it - u * ipu) * 16;
-        const size_t slot = (size_t)M.unit_slot[u];
-        gq = W.gate_q + (slot * F + f0) * (H / 2);
-        uq = W.up_q + (slot * F + f0) * (H / 2);
-        gs = W.gate_s + (slot * F + f0) * C;
-        us = W.up_s + (slot * F + f0) * C;
-      } else {
-        const int f0 = (it - n_routed * ipu) * 16;
-        gq = W.sh_gate_q + (size_t)f0 * (H / 2);
-        uq = W.sh_up_q + (size_t)f0 * (H / 2);
-        gs = W.sh_gate_s + (size_t)f0 * C;
-        us = W.sh_up_s + (size_t)f0 * C;
-      }
-      unsigned char* st = gbuf + (size_t)(q % NG) * L.g_stage;
-      uint64_t* bar = &mbar[kBarG0 + (q % NG)];
-      mbar_expect_tx(bar, (uint32_t)L.g_stage);
-      bulk_g2s(st, gq, 16u * (H / 2), bar);
-      bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
-      bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
-      bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
-    };
-    // unit and block of this CTA's j-th work unit
-    auto wu_of = [&](int j, int& u, int& b) {
-      const int w = blockIdx.x + j * grid;
-      if (w < n_routed * bpu) {
-        u = w / bpu;
-        b = w - u * bpu;
-      } else {
-        u = n_routed;
-        b = w - n_routed * bpu;
-      }
-    };
-    // Down block of work unit j into the down stage, straight from the packed
-    // rows: every thread copies the block's 16 code bytes of its output rows
-    // and the 4-byte scale pair holding the block's scale (async copies, one
-    // commit group per thread).
-    auto issue_d = [&](int j) {
+    // caller-layout layers (no tensor maps): the down block is copied per
+    // thread, 16 code bytes and the 4-byte scale pair holding the block's
+    // scale per row, at the same row positions as the TMA path
+    auto issue_d_threads = [&](int j) {
       int u, b;
-      wu_of(j, u, b);
+      wu_of(j, n_routed, u, b);
       const uint8_t* cq;
       const uint16_t* cs;
       int Fu;
@@ -780,14 +899,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       const uint32_t s_codes = smem_u32(dst_s), s_scales = smem_u32(dst_s + (size_t)H * 16);
       for (int r = tid; r < H; r += kDecodeThreads) {
-        cp_async_16(s_codes + (uint32_t)r * 16u, cq + (size_t)r * (Fu / 2) + 16 * b);
-        cp_async_4(s_scales + (uint32_t)r * 4u, cs + (size_t)r * (Fu / 32) + (b & ~1));
+        const uint32_t pos = (uint32_t)((r & 3) * Hq + (r >> 2));
+        cp_async_16(s_codes + pos * 16u, cq + (size_t)r * (Fu / 2) + 16 * b);
+        cp_async_4(s_scales + pos * 4u, cs + (size_t)r * (Fu / 32) + (b & ~1));
       }
       cp_async_commit();
     };
-    if (warp == 0 && lane == 0)
-      for (int q = 0; q < NG; ++q) issue_g(q);
-    if (my_wu > 0) issue_d(0);
+    if (!p.down_tma && my_wu > 0) issue_d_threads(0);
 
     // ------------------------------------------------ gate/up + SwiGLU, then down per block
     {
@@ -848,17 +966,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const float h = g / (1.0f + __expf(-g)) * uu;
           M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
         }
-        __syncthreads();  // the item's 16 rows of w*h are staged
-        // refill this stage with item q + NG once every warp has read it
-        if (warp == 0 && lane == 0 && q + NG < n_my_items) {
-          mbar_wait(&mbar[kBarE0 + sg], par, p.err, tmo);
-          issue_g(q + NG);
-        }
+        cta_sync();  // the item's 16 rows of w*h are staged
         if ((q & 1) == 0) continue;
         // ---- down block of work unit j: both halves of its 32 rows are staged
         const int j = q >> 1;
         int ub, b;
-        wu_of(j, ub, b);
+        wu_of(j, n_routed, ub, b);
         if (tid < TT * 4) {
           // fp16 pair planes of the block's 32 w*h values per token, in the
           // code unpack order, scaled by a power of two that puts the
@@ -879,8 +992,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           M.actD[t][qw] = make_uint4(o[0], o[1], o[2], o[3]);
           if (qw == 0) M.dsh[t] = sh;
         }
-        cp_async_wait<0>();
-        __syncthreads();  // the act planes, and every thread's copies of the down block
+        if (p.down_tma) {
+          mbar_wait(&mbar[kBarD], ph_d, p.err, tmo);
+          ph_d ^= 1u;
+        } else {
+          cp_async_wait<0>();
+        }
+        cta_sync();  // the act planes, and every thread's copies of the down block
         uint4 act[TT][4];
         float ysc[TT];
         bool live[TT];
@@ -891,23 +1009,46 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           ysc[t] = pow2f(M.dsh[t]);
           live[t] = (t < T) && M.unit_w[ub][t] != 0.0f;
         }
+        // four consecutive output rows 4 q4 .. 4 q4 + 3 per thread and step,
+        // added into the layer output with one vector reduction per token
         const unsigned char* dc = dst_s;
         const unsigned char* dsc = dst_s + (size_t)H * 16;
-        for (int r = tid; r < H; r += kDecodeThreads) {
-          const uint4 wv = *reinterpret_cast<const uint4*>(dc + (size_t)r * 16);
-          const uint32_t sp = *reinterpret_cast<const uint32_t*>(dsc + (size_t)r * 4);
-          const float s = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sp >> 16) : (sp & 0xffffu))));
-          float d[TT];
-          dot_block<TT>(wv, act, d);
+        for (int q4 = tid; q4 < Hq; q4 += kDecodeThreads) {
+          float d[4][TT], sc4[4];
+          if (p.down_tma) {  // rows 4 q4 .. 4 q4 + 3 of the block-major scales
+            const uint2 sv = *reinterpret_cast<const uint2*>(dsc + (size_t)q4 * 8);
+            sc4[0] = __half2float(__ushort_as_half((uint16_t)(sv.x & 0xffffu)));
+            sc4[1] = __half2float(__ushort_as_half((uint16_t)(sv.x >> 16)));
+            sc4[2] = __half2float(__ushort_as_half((uint16_t)(sv.y & 0xffffu)));
+            sc4[3] = __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)));
+          } else {
+#pragma unroll
+            for (int jr = 0; jr < 4; ++jr) {
+              const uint32_t sp = *reinterpret_cast<const uint32_t*>(dsc + ((size_t)jr * Hq + q4) * 4);
+              sc4[jr] = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sp >> 16) : (sp & 0xffffu))));
+            }
+          }
+#pragma unroll
+          for (int jr = 0; jr < 4; ++jr) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(dc + ((size_t)jr * Hq + q4) * 16);
+            dot_block<TT>(wv, act, d[jr]);
+          }
 #pragma unroll
           for (int t = 0; t < TT; ++t)
-            if (live[t]) atomicAdd(ycur + (size_t)t * H + r, s * d[t] * ysc[t]);
+            if (live[t])
+              red_add_v4(ycur + (size_t)t * H + 4 * q4, sc4[0] * d[0][t] * ysc[t],
+                         sc4[1] * d[1][t] * ysc[t], sc4[2] * d[2][t] * ysc[t],
+                         sc4[3] * d[3][t] * ysc[t]);
         }
-        __syncthreads();  // every thread is done with the down stage and the act planes
-        if (j + 1 < my_wu) issue_d(j + 1);
+        // the copy warp refills the stage by TMA (async proxy) once every
+        // warp has released it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mbar[kBarDE]);
+        cta_sync();  // every thread is done with the down stage and the act planes
+        if (!p.down_tma && j + 1 < my_wu) issue_d_threads(j + 1);
       }
     }
-    if (l + 1 < p.n_layers) prefetch_router(l + 1);
     // the next layer's bulk copies land in shared memory this layer read
     // through the generic proxy: order those reads before them
     fence_proxy_async_smem();
@@ -930,6 +1071,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     }
   }
+}
+
+// 4-D map over one matrix of down codes [slots][H][Fd/2] (bytes): dims
+// {Fd/2, 4, H/4, slots} with strides {Fd/2, 2 Fd, H Fd/2} -- row r of a slot
+// is (j, q) = (r % 4, r / 4) -- and box {16, 1, down_qbox(H), 1}: one
+// 32-column block of down_qbox(H) rows of one row plane.
+static bool encode_down_map(CUtensorMap* m, const void* base, int H, int Fd, int slots) {
+  auto enc = tmap_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)Fd / 2, 4, (cuuint64_t)H / 4, (cuuint64_t)slots};
+  cuuint64_t strides[3] = {(cuuint64_t)Fd / 2, 2 * (cuuint64_t)Fd, (cuuint64_t)H * Fd / 2};
+  cuuint32_t box[4] = {16, 1, (cuuint32_t)down_qbox(H), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status decode_prepare(moe_layer* L, const char** why) {
+  const moe_layer_config& c = L->cfg;
+  const bool sh = c.shared_ffn > 0;
+  if (!encode_down_map(&L->tm_dec_down, L->dev.down_q, c.hidden, c.ffn, c.n_slots) ||
+      !encode_down_map(&L->tm_dec_sh_down, sh ? L->dev.sh_down_q : L->dev.down_q, c.hidden,
+                       sh ? c.shared_ffn : c.ffn, 1)) {
+    *why = "cuTensorMapEncodeTiled failed (decode down codes)";
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 size_t decode_smem_bytes(const DecodeParams& p, int num_sms) {
@@ -964,7 +1133,7 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
     return MOE_ERR_CUDA;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeBlock, smem) !=
           cudaSuccess ||
       per_sm < 1) {
     *why = "decode kernel cannot be resident (occupancy query)";
@@ -978,7 +1147,7 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
   }
   void* args[] = {&p};
   prof::Scope scope("moe_decode_kernel", stream);
-  cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kDecodeThreads),
+  cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kDecodeBlock),
                                               args, smem, stream);
   if (e != cudaSuccess) {
     *why = cudaGetErrorString(e);

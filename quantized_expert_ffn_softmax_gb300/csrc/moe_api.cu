@@ -51,6 +51,19 @@ bool is_device_ptr(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// dst [S][CB][H] = src [S][H][CB] (binary16 bits): the down scales of each
+// slot with the 32-column block index outermost
+__global__ void scales_block_major(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                   int S, int H, int CB) {
+  const size_t n = (size_t)S * H * CB;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t s = i / ((size_t)H * CB), rem = i - s * H * CB;
+    const size_t r = rem / CB, b = rem - r * CB;
+    dst[(s * CB + b) * H + r] = src[i];
+  }
+}
+
 struct Stage {
   const uint16_t* x = nullptr;
   uint16_t* y = nullptr;
@@ -207,6 +220,10 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   const bool gated = (cfg->routing_flags & MOE_ROUTING_SHARED_GATE) != 0;
   size_t i_sgw = 0;
   if (gated) i_sgw = add(w->sh_gate_w, sizeof(float) * H);
+  // block-major copies of the down scales for the decode kernel (filled
+  // from the row-major ones below)
+  const size_t i_dsb = add(nullptr, ds);
+  const size_t i_sdsb = Fs > 0 ? add(nullptr, (size_t)H * (Fs / 32) * 2) : 0;
   L->weights_bytes = align_up(off, 256);
   cudaError_t e = cudaMalloc(&L->weights_block, L->weights_bytes);
   if (e != cudaSuccess) {
@@ -218,7 +235,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     if (p.src)
       e = cudaMemcpy(base + p.off, p.src, p.bytes, kind);
     else
-      e = cudaMemset(base + p.off, 0, p.bytes);  // router bias omitted: zero
+      e = cudaMemset(base + p.off, 0, p.bytes);  // router bias omitted: zero (or filled below)
     if (e != cudaSuccess) {
       moe_layer_destroy(L);
       return cuda_fail(e, "copy weights");
@@ -243,6 +260,29 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     L->dev.sh_down_s = (const uint16_t*)at(i_sds);
   }
   L->sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
+  L->dev.down_sb = (const uint16_t*)at(i_dsb);
+  L->dev.sh_down_sb = Fs > 0 ? (const uint16_t*)at(i_sdsb) : nullptr;
+  {
+    const size_t n = (size_t)S * H * (F / 32);
+    scales_block_major<<<(unsigned)((n + 255) / 256), 256>>>(L->dev.down_s, (uint16_t*)L->dev.down_sb,
+                                                            S, H, F / 32);
+    if (Fs > 0) {
+      const size_t ns = (size_t)H * (Fs / 32);
+      scales_block_major<<<(unsigned)((ns + 255) / 256), 256>>>(
+          L->dev.sh_down_s, (uint16_t*)L->dev.sh_down_sb, 1, H, Fs / 32);
+    }
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      moe_layer_destroy(L);
+      return cuda_fail(e, "block-major down scales");
+    }
+    const char* why = "";
+    if ((st = moe::decode_prepare(L, &why)) != MOE_OK) {
+      moe_layer_destroy(L);
+      return fail(st, "decode tensor maps: %s", why);
+    }
+  }
 
   // ---- workspace
   size_t wo = 0;
@@ -393,8 +433,11 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
     p.y_trace = y_trace ? y_trace + (size_t)l0 * T * H : nullptr;
     p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
     p.w_out = w_out;
+    p.down_tma = 1;
     for (int l = 0; l < nl; ++l) {
       p.layers[l] = layers[l0 + l]->dev;
+      p.tm_down[l] = layers[l0 + l]->tm_dec_down;
+      p.tm_sh_down[l] = layers[l0 + l]->tm_dec_sh_down;
       p.routing_flags[l] = layers[l0 + l]->cfg.routing_flags;
       p.sh_gate_w[l] = layers[l0 + l]->sh_gate_w;
     }

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "../../include/moe.h"
@@ -15,7 +16,8 @@ constexpr int kMaxLayersPerLaunch = 64;
 constexpr int kMaxDecodeTokens = 4;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
-constexpr int kDecodeThreads = 256;
+constexpr int kDecodeThreads = 256;                 // compute threads of a decode CTA
+constexpr int kDecodeBlock = kDecodeThreads + 32;   // + the copy warp
 constexpr int kMaxUnits = kMaxDecodeTokens * kMaxTopK + 1;  // routed + shared
 
 // Device pointers of one layer's weights (library-owned copies).
@@ -35,6 +37,10 @@ struct LayerDev {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
+  // library layers only: the down scales again, block-major, for the decode
+  // kernel's one-copy-per-block loads: [S][F/32][H] and [Fs/32][H]
+  const uint16_t* down_sb;
+  const uint16_t* sh_down_sb;
 };
 
 // Generation-counting grid barrier state (one per workspace, 128-B aligned).
@@ -47,6 +53,12 @@ struct GridBarrier {
 enum DecodeMode : int { kModeForward = 0, kModeStack = 1, kModeRoute = 2 };
 
 struct DecodeParams {
+  // library layers: 4-D tensor maps over each layer's down codes (routed
+  // [S][H][F/2], shared [H][Fs/2]) that fetch one 32-column block of every
+  // output row in four row planes (row r to position (r % 4) * H/4 + r / 4)
+  CUtensorMap tm_down[kMaxLayersPerLaunch];
+  CUtensorMap tm_sh_down[kMaxLayersPerLaunch];
+  int down_tma;  // 1: down blocks by TMA + block-major scales; 0: per-thread copies
   int H, E, k, F, Fs;
   int T;          // real tokens (1..4)
   int n_layers;
@@ -127,6 +139,8 @@ struct moe_layer {
   CUtensorMap tmap_sh_gate;  // shared expert [Fs][H/2]
   CUtensorMap tmap_sh_up;    // shared expert [Fs][H/2]
   CUtensorMap tmap_sh_down;  // shared expert [H][Fs/2]
+  CUtensorMap tm_dec_down;     // decode: 4-D view of down codes (see DecodeParams::tm_down)
+  CUtensorMap tm_dec_sh_down;  // decode: the same over the shared expert's down codes
   int router_shift = 0;               // router weights are scaled by 2^router_shift
   const float* sh_gate_w = nullptr;   // [H] device copy of the shared-expert gate vector, or null
   void* weights_block = nullptr;  // one allocation holding all weight copies
@@ -153,6 +167,10 @@ moe_status launch_decode(const DecodeParams& p, cudaStream_t stream, int num_sms
                          const char** why);
 // shared memory of the decode kernel for p's shape on a grid of num_sms CTAs
 size_t decode_smem_bytes(const DecodeParams& p, int num_sms);
+// prefill.cu: cuTensorMapEncodeTiled from the driver (null when unavailable)
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
+// decode.cu: the decode tensor maps of a layer (after its weights are in place)
+moe_status decode_prepare(moe_layer* L, const char** why);
 // prefill.cu
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
                           float* w_out, bool route_only, cudaStream_t stream, const char** why);

@@ -52,6 +52,23 @@
 #include "profile.cuh"
 
 namespace moe {
+
+// cuTensorMapEncodeTiled from the driver (null when unavailable)
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
 namespace {
 
 using namespace dev;
@@ -1090,25 +1107,10 @@ struct PrefillSizes {
   }
 };
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    else
-      cudaGetLastError();
-  }
-  return fn;
-}
-
 // 2-D fp16 map [rows][cols], box {64, 128} (128 rows of 128 bytes: one
 // K step of a B tile), 128B swizzle; rows past the end read as zero.
 bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode();
+  auto enc = tmap_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
@@ -1122,7 +1124,7 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows)
 // 2-D map over packed 4-bit codes [rows][bytes_per_row], box {32, 128}:
 // one K step (64 codes) of 128 weight rows, stored densely (32-byte rows).
 bool encode_codes(CUtensorMap* m, const void* base, uint64_t bytes_per_row, uint64_t rows) {
-  auto enc = get_encode();
+  auto enc = tmap_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {bytes_per_row, rows};
   cuuint64_t strides[1] = {bytes_per_row};
