@@ -246,13 +246,17 @@ def job_tokens_per_s(n_ranks: int, tokens_per_rank_step: int, ms_per_step_max: f
     return n_ranks * tokens_per_rank_step / (ms_per_step_max / 1e3)
 
 
-def build_stack(cfg, max_tokens):
+def build_stack(cfg, max_tokens, n_slots=None, profile=False):
+    """Library layers of a workload (device-generated weights).  n_slots <
+    n_experts keeps only that many experts per layer in HBM (the rest in
+    the library's host tier); profile places the Zipf-favoured experts first
+    (usage profile = exp of the router's log-Zipf bias)."""
     import quantized_expert_ffn_softmax_gb300 as moe
     import torch
 
     config = dict(hidden=cfg.hidden, n_experts=cfg.n_experts, top_k=cfg.top_k, ffn=cfg.ffn,
                   shared_ffn=cfg.shared_ffn, max_tokens=max_tokens,
-                  routing_flags=cfg.routing_flags)
+                  routing_flags=cfg.routing_flags, n_slots=n_slots or cfg.n_experts)
     layers = []
     for l in range(cfg.n_layers):
         D = W.device_layer(cfg, l)
@@ -264,6 +268,9 @@ def build_stack(cfg, max_tokens):
                 w["sh_" + n] = D["sh_" + n]
         if "sh_gate_w" in D:
             w["sh_gate_w"] = D["sh_gate_w"]
+        if profile:
+            _, b = W.router(cfg, l)
+            w["expert_profile"] = torch.from_numpy(np.exp(b.astype(np.float64)).astype(np.float32)).cuda()
         torch.cuda.synchronize()
         layers.append(moe.MoELayer(config, w, True))
         del D, w
@@ -318,13 +325,13 @@ def kernel_profile(fn, steps, ring_len):
     return moe.moe_profile_read()
 
 
-def bench_decode(name, steps, warmup, dist, with_e2e=False):
+def bench_decode(name, steps, warmup, dist, with_e2e=False, n_slots=None, profile=False):
     import quantized_expert_ffn_softmax_gb300 as moe
     import torch
 
     cfg = W.CONFIGS[name]
     T = cfg.n_tokens
-    layers = build_stack(cfg, max_tokens=8)
+    layers = build_stack(cfg, max_tokens=8, n_slots=n_slots, profile=profile)
     hs = [l.handle for l in layers]
     ring = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).cuda() for i in range(64)]
     y = torch.empty_like(ring[0])
@@ -346,8 +353,11 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
     def step(i):
         moe.moe_stack_forward(hs, L, ring[i], T, y)
 
+    for h in hs:
+        moe.moe_cache_stats(h, reset=True)
     with ClockSampler(dist.local) as clk:
         ms = time_steps(step, steps, warmup, dist, len(ring), clk)
+    cache = [moe.moe_cache_stats(h) for h in hs]
     prof = kernel_profile(step, min(steps, 50), len(ring))
     assert moe.moe_status_sync(hs[0]) == moe.MOE_OK
     kcount, kms = prof.get("moe_decode_kernel", (0, 0.0))
@@ -365,6 +375,12 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False):
         "launches_per_step": launches_per_step,
         "clocks": clk.report(),
     }
+    if n_slots and n_slots < cfg.n_experts:
+        hits, misses = sum(c[0] for c in cache), sum(c[1] for c in cache)
+        out["cache"] = {"n_slots": n_slots, "n_experts": cfg.n_experts, "profile": bool(profile),
+                        "hits": hits, "misses": misses,
+                        "hit_rate": hits / max(1, hits + misses),
+                        "note": "hits/misses over warm-up, timed steps and clock window"}
     if with_e2e:
         xs = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).pin_memory() for i in range(8)]
         yh = torch.empty_like(xs[0]).pin_memory()
@@ -589,6 +605,10 @@ def main():
                          "decode125b, decode35b_variants or prefill125b")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only on a decode workload: use the first N layers")
+    ap.add_argument("--slots", type=int, default=None,
+                    help="with --only on a decode workload: experts per layer kept in HBM")
+    ap.add_argument("--profile", action="store_true",
+                    help="with --slots: place experts by the usage profile")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -608,7 +628,8 @@ def main():
         if args.only.startswith("prefill"):
             r = bench_prefill(args.only, args.steps, args.warmup, dist)
         else:
-            r = bench_decode(args.only, args.steps, args.warmup, dist)
+            r = bench_decode(args.only, args.steps, args.warmup, dist, n_slots=args.slots,
+                             profile=args.profile)
         if dist.rank == 0:
             print(json.dumps({"only": args.only, "layers": args.layers, "result": r}), flush=True)
         dist.close()
@@ -621,6 +642,15 @@ def main():
             r = bench_decode(nm, max(20, args.steps // 2), args.warmup, dist)
             r["frac_of_peak_kernel"] = r["gbs_kernel"] / hbm if r["gbs_kernel"] else None
             extra[nm] = r
+        # partial residency: half and a quarter of the experts in HBM (placed
+        # by the usage profile), and a quarter placed without one
+        for tag, ns, pr in (("decode35b_half_resident", 128, True),
+                            ("decode35b_quarter_resident", 64, True),
+                            ("decode35b_quarter_resident_noprofile", 64, False)):
+            r = bench_decode(HEADLINE, max(20, args.steps // 2), args.warmup, dist, n_slots=ns,
+                             profile=pr)
+            r["frac_of_peak_kernel"] = r["gbs_kernel"] / hbm if r["gbs_kernel"] else None
+            extra[tag] = r
         # routing variants: per-layer time beside the default headline stack
         v = extra["decode35b_variants"]
         v["us_per_layer"] = v["ms_per_step"] * 1e3 / W.CONFIGS["decode35b_variants"].n_layers

@@ -19,8 +19,11 @@
  *                               logits W_r x without b
  *   MOE_ROUTING_SHARED_GATE     the shared expert is scaled per token by
  *                               sigmoid(g . x), g = sh_gate_w [H] fp32
- * Every expert is reached through a resident slot table (the pages' VRAM
- * expert cache, here sized to hold all experts in HBM).  Expert weights are
+ * Every expert is reached through a slot table (the pages' VRAM expert
+ * cache).  By default every expert has a slot in HBM (n_slots == n_experts);
+ * with n_slots < n_experts only n_slots experts per layer stay in HBM, the
+ * rest in a library-owned pinned host tier (the pages' RAM tier) read by
+ * the GPU over the host link: see moe_layer_config.n_slots.  Expert weights are
  * symmetric 4-bit codes in blocks of 32 along the reduction dimension with
  * one binary16 scale per block (the block-scale idea of the pages' int8 KV
  * cache, one scale per 32 values): weight = (nibble - 8) * scale.
@@ -71,7 +74,7 @@ enum {
 /* Layer shape.  Limits: hidden % 128 == 0 and 128 <= hidden <= 8192;
  * 1 <= n_experts <= 1024; 1 <= top_k <= min(16, n_experts);
  * ffn % 128 == 0 and 128 <= ffn <= 4096; shared_ffn == 0 or a multiple of
- * 128 up to 4096; n_slots == n_experts (the slot table holds every expert);
+ * 128 up to 4096; min(n_experts, 4 * top_k) <= n_slots <= n_experts;
  * 1 <= max_tokens <= 65536 (sizes the workspaces); routing_flags a
  * combination of the MOE_ROUTING_* bits (0: the default routing above).
  * moe_layer_create also refuses shapes whose single-token decode does not
@@ -84,23 +87,40 @@ typedef struct {
   int32_t top_k;      /* k */
   int32_t ffn;        /* F: routed expert intermediate size */
   int32_t shared_ffn; /* Fs: shared expert intermediate size, 0 = none */
-  int32_t n_slots;    /* S: expert-cache slots */
+  int32_t n_slots;    /* S: expert-cache slots in HBM (see below) */
   int32_t max_tokens; /* largest n_tokens any call will pass */
   int32_t routing_flags; /* MOE_ROUTING_* bits */
 } moe_layer_config;
+/* Partial residency (n_slots < n_experts).  A copy of every expert stays in
+ * pinned host memory owned by the library; n_slots experts also hold an HBM
+ * slot, first the n_slots with the largest moe_layer_weights.expert_profile
+ * values (ties: lower id; no profile: experts 0..n_slots-1).  Single-layer
+ * and stack calls on 1..4 tokens look each selected expert up; a miss is
+ * served in the same call: the layer's CTAs read the expert from the host
+ * tier over the host link into the least recently used slot that this call
+ * does not use (so the cache evolves with the traffic), then the layer
+ * proceeds from HBM; results are the same as with every expert resident.
+ * Larger batches (the prefill path) stream the experts their tokens select
+ * from HBM slots or the host tier into a staging buffer shared by the
+ * partially resident layers of the process (one layer's worth of experts),
+ * then run as usual; calls on partially resident layers must not overlap on
+ * the GPU.  moe_cache_stats reports hits and misses. */
 
 /* Packed weights, all row-major with the reduction dimension contiguous.
  * A packed row of K weights is K/2 bytes of codes (byte i holds element 2i
  * in its low nibble and element 2i+1 in its high nibble) and K/32 binary16
- * scales (raw bits).  Routed tensors are indexed by slot:
- *   gate_q, up_q  [S][F][H/2]   gate_s, up_s  [S][F][H/32]
- *   down_q        [S][H][F/2]   down_s        [S][H][F/32]
+ * scales (raw bits).  Routed tensors hold all E experts, expert e in row
+ * slot_of_expert[e]:
+ *   gate_q, up_q  [E][F][H/2]   gate_s, up_s  [E][F][H/32]
+ *   down_q        [E][H][F/2]   down_s        [E][H][F/32]
  *   sh_gate_q, sh_up_q [Fs][H/2], sh_*_s [Fs][H/32]
  *   sh_down_q [H][Fs/2], sh_down_s [H][Fs/32]        (NULL when Fs == 0)
  *   router_w [E][H] fp32, router_bias [E] fp32 or NULL (zero bias)
- *   slot_of_expert [E]: a permutation of 0..S-1 (validated at create)
+ *   slot_of_expert [E]: a permutation of 0..E-1 (validated at create)
  *   sh_gate_w [H] fp32: shared-expert gate vector, read only with
- *   MOE_ROUTING_SHARED_GATE (NULL otherwise). */
+ *   MOE_ROUTING_SHARED_GATE (NULL otherwise)
+ *   expert_profile [E] fp32 or NULL: expected use of each expert, read only
+ *   with n_slots < n_experts to choose the experts first placed in HBM. */
 typedef struct {
   const float* router_w;
   const float* router_bias;
@@ -118,6 +138,7 @@ typedef struct {
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
   const float* sh_gate_w;
+  const float* expert_profile;
 } moe_layer_weights;
 
 /* Creates a layer: validates cfg and the slot table, allocates the layer's
@@ -204,6 +225,16 @@ moe_status moe_forward_noalloc(const moe_layer_config* cfg, const moe_layer_weig
  * be the batch of that call. */
 moe_status moe_last_buckets(moe_layer* layer, int n_tokens, int32_t* offsets, int32_t* perm_token,
                             void* stream);
+
+/* Expert-cache statistics of a layer (synchronises `stream`): *hits and
+ * *misses count the routed-expert lookups of the decode path (1..4-token
+ * calls) since creation or the last reset (reset != 0 zeroes them after
+ * reading); with every expert resident every lookup is a hit.
+ * slot_of_expert (host pointer, [E], or NULL) receives the current slot of
+ * every expert, -1 for those only in the host tier.  Any pointer may be
+ * NULL. */
+moe_status moe_cache_stats(moe_layer* layer, uint64_t* hits, uint64_t* misses,
+                           int32_t* slot_of_expert, int reset, void* stream);
 
 /* Synchronises `stream`, then returns and clears the layer's device error
  * word (MOE_ERR_BOUNDS or MOE_ERR_TIMEOUT if a kernel recorded one). */

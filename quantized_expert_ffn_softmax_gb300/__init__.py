@@ -50,7 +50,7 @@ ROUTING_SHARED_GATE = 4
 
 WEIGHT_FIELDS = ("router_w", "router_bias", "slot_of_expert", "gate_q", "gate_s", "up_q", "up_s",
                  "down_q", "down_s", "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q",
-                 "sh_down_s", "sh_gate_w")
+                 "sh_down_s", "sh_gate_w", "expert_profile")
 
 
 class moe_layer_weights(ctypes.Structure):
@@ -97,6 +97,8 @@ def lib():
         L.moe_profile_read.restype = i32
         L.moe_status_sync.argtypes = [vp, vp]
         L.moe_status_sync.restype = i32
+        L.moe_cache_stats.argtypes = [vp, vp, vp, vp, i32, vp]
+        L.moe_cache_stats.restype = i32
         _lib = L
     return _lib
 
@@ -208,6 +210,24 @@ def moe_stack_forward_traced(layers: Sequence[int], n_layers: int, x, n_tokens: 
 def moe_last_buckets(layer: int, n_tokens: int, offsets, perm_token, stream=None) -> None:
     _check(lib().moe_last_buckets(layer, n_tokens, _ptr(offsets), _ptr(perm_token),
                                   _stream(stream)))
+
+
+def moe_cache_stats(layer: int, reset: bool = False, stream=None):
+    """(hits, misses) of a layer's expert cache; reset zeroes them after reading."""
+    h = ctypes.c_uint64()
+    m = ctypes.c_uint64()
+    _check(lib().moe_cache_stats(layer, ctypes.byref(h), ctypes.byref(m), None, int(bool(reset)),
+                                 _stream(stream)))
+    return h.value, m.value
+
+
+def moe_cache_slots(layer: int, n_experts: int, stream=None):
+    """Current slot of every expert of a layer (-1: host tier only)."""
+    import numpy as np
+
+    tab = np.empty(n_experts, np.int32)
+    _check(lib().moe_cache_stats(layer, None, None, tab.ctypes.data, 0, _stream(stream)))
+    return tab
 
 
 def moe_status_sync(layer: int, stream=None) -> int:

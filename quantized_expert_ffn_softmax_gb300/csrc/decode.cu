@@ -49,6 +49,12 @@ constexpr int kWarps = kDecodeThreads / 32;  // compute warps; warp kWarps issue
 // its own schedule and never joins it.
 __device__ __forceinline__ void cta_sync() { named_bar_sync(1, kDecodeThreads); }
 
+// Orders this thread's generic-proxy global writes before later async-proxy
+// (TMA) accesses, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // out[0..3] += v (fp32) with one vector reduction in L2; out 16-byte aligned.
 __device__ __forceinline__ void red_add_v4(float* out, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(a), "f"(b),
@@ -289,6 +295,11 @@ struct DecodeMisc {
   float hst[2][16][4];  // w*h of a gate/up item's 16 rows (double-buffered by item)
   uint4 actD[kMaxDecodeTokens][4];  // w*h of a work unit's 32 rows as fp16 pair planes
   int dsh[kMaxDecodeTokens];        // their power-of-two shifts
+  // expert cache of a partially resident layer
+  int n_miss;
+  int miss_unit[kMaxUnits];         // routed units whose expert has no slot
+  unsigned inuse[kMaxExperts / 32];  // slots of this call's resident units
+  unsigned long long red_key[kWarps];
 };
 static_assert(sizeof(DecodeMisc) <= 12288, "misc region too small");
 
@@ -481,6 +492,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       if (ok && l + 1 < p.n_layers && p.mode != kModeRoute) issue_rows(l + 1);
       named_bar_sync(kNbUnits, kDecodeBlock);
       if (p.mode == kModeRoute) continue;
+      fence_proxy_async_global();  // slots just filled by generic stores (expert-cache misses)
       const int n_routed = M.n_routed;
       const int my_wu = my_units(n_routed), n_items = 2 * my_wu;
       if (ok) {
@@ -515,6 +527,8 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
 
   for (int l = 0; l < p.n_layers; ++l) {
     const LayerDev& W = p.layers[l];
+    // slots of this layer's expert table (fewer than E when partially resident)
+    const int S_l = W.cache ? __ldg(&W.cache->n_slots) : E;
     // the previous layer's output, reduced in L2 (layers after the first)
     const float* yprev = p.yacc + (size_t)((l + 1) & 1) * kMaxDecodeTokens * H;
 
@@ -788,6 +802,16 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       ph_s ^= 1u;
     }
     auto slot_lookup = [&](int e) { return slots_bulk ? slots[e] : __ldg(W.slot_of + e); };
+    // a partially resident layer's table holds -1 for experts without a slot
+    const bool partial = W.cache != nullptr && p.mode != kModeRoute;
+    auto slot_checked = [&](int e) {
+      int s = slot_lookup(e);
+      if (s >= S_l || (s < 0 && !partial)) {
+        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+        s = 0;
+      }
+      return s;
+    };
     if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
     for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)
       (&M.unit_w[0][0])[i] = 0.0f;
@@ -798,11 +822,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         const int e = M.sel_id[0][tid];
         M.unit_w[tid][0] = M.sel_w[0][tid];
         M.unit_expert[tid] = e;
-        int s = slot_lookup(e);
-        if (s < 0 || s >= E) {
-          atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-          s = 0;
-        }
+        const int s = slot_checked(e);
         M.unit_slot[tid] = s;
       }
       if (tid == 0) {
@@ -834,11 +854,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         const int u = M.prefix[e >> 5] + __popc(M.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
         M.unit_w[u][t] = M.sel_w[t][r];
         M.unit_expert[u] = e;
-        int s = slot_lookup(e);
-        if (s < 0 || s >= E) {
-          atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-          s = 0;
-        }
+        const int s = slot_checked(e);
         M.unit_slot[u] = s;
       }
     }
@@ -855,6 +871,117 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         if (kVar && (p.routing_flags[l] & MOE_ROUTING_SHARED_GATE) && tid < T)
           ws = 1.0f / (1.0f + __expf(-__ldcg(p.gz + tid)));
         M.unit_w[nr][tid] = (tid < T) ? ws : 0.0f;
+      }
+    }
+    if (partial) {
+      // ---- expert cache: misses are served before the units run
+      const CacheDev* cd = W.cache;
+      const int nr_l = (TT == 1) ? k : M.n_routed;
+      if (tid < kMaxExperts / 32) M.inuse[tid] = 0u;
+      cta_sync();  // the unit list is complete
+      if (tid == 0) {
+        int n = 0;
+        for (int u = 0; u < nr_l; ++u)
+          if (M.unit_slot[u] < 0) M.miss_unit[n++] = u;
+        M.n_miss = n;
+      }
+      if (tid < nr_l && M.unit_slot[tid] >= 0)
+        atomicOr(&M.inuse[M.unit_slot[tid] >> 5], 1u << (M.unit_slot[tid] & 31));
+      cta_sync();
+      const int n_miss = M.n_miss;  // the same in every CTA (same tables, same selection)
+      if (n_miss > 0) {
+        // victims: the least recently used slots this call does not use
+        // (ties to the lower slot), one block-wide argmin per miss; every
+        // CTA reaches the same choice
+        unsigned long long key[kMaxExperts / kDecodeThreads];
+#pragma unroll
+        for (int j = 0; j < kMaxExperts / kDecodeThreads; ++j) {
+          const int sl = tid + j * kDecodeThreads;
+          key[j] = (sl < S_l) ? (((unsigned long long)__ldcg(cd->last_use + sl) << 32) | (unsigned)sl)
+                              : ~0ull;
+        }
+        for (int i = 0; i < n_miss; ++i) {
+          unsigned long long best = ~0ull;
+#pragma unroll
+          for (int j = 0; j < kMaxExperts / kDecodeThreads; ++j) {
+            const int sl = tid + j * kDecodeThreads;
+            if (sl < S_l && !((M.inuse[sl >> 5] >> (sl & 31)) & 1u) && key[j] < best) best = key[j];
+          }
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other < best ? other : best;
+          }
+          if (lane == 0) M.red_key[warp] = best;
+          cta_sync();
+          if (tid == 0) {
+            unsigned long long b = ~0ull;
+            for (int w = 0; w < kWarps; ++w) b = M.red_key[w] < b ? M.red_key[w] : b;
+            int v = (int)(b & 0xffffffffu);
+            if (b == ~0ull) {  // no free slot (n_slots too small): not reachable after validation
+              atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+              v = 0;
+            }
+            M.inuse[v >> 5] |= 1u << (v & 31);
+            M.unit_slot[M.miss_unit[i]] = v;
+          }
+          cta_sync();
+        }
+        // the missed experts, from the host tier into their new slots: this
+        // CTA copies its 1/grid share of each of their seven tensors
+        {
+          const size_t gqe = (size_t)F * (H / 2), gse = (size_t)F * C * 2;
+          const size_t dqe = (size_t)H * (F / 2), dse = (size_t)H * CF * 2;
+          for (int i = 0; i < n_miss; ++i) {
+            const int u = M.miss_unit[i];
+            const size_t hr = (size_t)__ldg(cd->host_row + M.unit_expert[u]);
+            const size_t v = (size_t)M.unit_slot[u];
+#pragma unroll 1
+            for (int t = 0; t < 7; ++t) {
+              const size_t n = (t == 0 || t == 2) ? gqe : (t == 1 || t == 3) ? gse : (t == 4) ? dqe : dse;
+              const char* sb = t == 0 ? (const char*)cd->gate_q : t == 1 ? (const char*)cd->gate_s
+                             : t == 2 ? (const char*)cd->up_q : t == 3 ? (const char*)cd->up_s
+                             : t == 4 ? (const char*)cd->down_q : t == 5 ? (const char*)cd->down_s
+                             : (const char*)cd->down_sb;
+              char* db = t == 0 ? (char*)W.gate_q : t == 1 ? (char*)W.gate_s : t == 2 ? (char*)W.up_q
+                       : t == 3 ? (char*)W.up_s : t == 4 ? (char*)W.down_q : t == 5 ? (char*)W.down_s
+                       : (char*)W.down_sb;
+              const uint4* s4 = reinterpret_cast<const uint4*>(sb + hr * n);
+              uint4* d4 = reinterpret_cast<uint4*>(db + v * n);
+              const size_t nv = n / 16;
+              const size_t lo = nv * blockIdx.x / grid, hi = nv * (blockIdx.x + 1) / grid;
+              size_t q = lo + tid;
+              for (; q + 3 * kDecodeThreads < hi; q += 4 * kDecodeThreads) {
+                const uint4 a = s4[q], b2 = s4[q + kDecodeThreads], c2 = s4[q + 2 * kDecodeThreads],
+                            d2 = s4[q + 3 * kDecodeThreads];
+                d4[q] = a;
+                d4[q + kDecodeThreads] = b2;
+                d4[q + 2 * kDecodeThreads] = c2;
+                d4[q + 3 * kDecodeThreads] = d2;
+              }
+              for (; q < hi; q += kDecodeThreads) d4[q] = s4[q];
+            }
+          }
+          fence_proxy_async_global();  // the slots are read next by TMA
+        }
+        grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
+        // every CTA has its copy of the tables and stamps: CTA 0 records the
+        // new residency
+        if (blockIdx.x == 0 && tid == 0) {
+          int32_t* so = const_cast<int32_t*>(W.slot_of);
+          for (int i = 0; i < n_miss; ++i) {
+            const int u = M.miss_unit[i], e = M.unit_expert[u], v = M.unit_slot[u];
+            const int old = cd->slot_expert[v];
+            if (old >= 0 && old < E) so[old] = -1;
+            so[e] = v;
+            cd->slot_expert[v] = e;
+          }
+        }
+      }
+      if (blockIdx.x == 0 && tid < nr_l) cd->last_use[M.unit_slot[tid]] = p.step;
+      if (blockIdx.x == 0 && tid == 0) {
+        atomicAdd(&cd->stats[0], (unsigned long long)(nr_l - n_miss));
+        atomicAdd(&cd->stats[1], (unsigned long long)n_miss);
       }
     }
     // the slot table was read through the generic proxy; the next layer's

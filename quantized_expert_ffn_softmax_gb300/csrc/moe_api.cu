@@ -7,6 +7,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -64,6 +66,179 @@ __global__ void scales_block_major(const uint16_t* __restrict__ src, uint16_t* _
   }
 }
 
+// ------------------------------------------------------------ partial residency
+
+// Staging buffer of the prefill path for partially resident layers: one
+// layer's routed experts (every expert e in row e), shared by the layers of
+// one shape on one device; the last layer to release it frees it.
+}  // namespace
+struct StreamBuf {
+  int device = 0, H = 0, F = 0, E = 0;
+  int refs = 0;
+  void* base = nullptr;
+  uint8_t* gate_q = nullptr;
+  uint16_t* gate_s = nullptr;
+  uint8_t* up_q = nullptr;
+  uint16_t* up_s = nullptr;
+  uint8_t* down_q = nullptr;
+  uint16_t* down_s = nullptr;
+  int32_t* ident = nullptr;  // [E] identity slot table
+};
+namespace {
+std::mutex g_stream_mu;
+std::vector<StreamBuf*> g_streams;
+
+moe_status stream_acquire(moe_layer* L) {
+  const moe_layer_config& c = L->cfg;
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  for (StreamBuf* b : g_streams)
+    if (b->device == L->device && b->H == c.hidden && b->F == c.ffn && b->E == c.n_experts) {
+      ++b->refs;
+      L->stream = b;
+      return MOE_OK;
+    }
+  StreamBuf* b = new StreamBuf();
+  b->device = L->device;
+  b->H = c.hidden;
+  b->F = c.ffn;
+  b->E = c.n_experts;
+  const size_t E = c.n_experts, H = c.hidden, F = c.ffn;
+  const size_t gq = E * F * (H / 2), gs = E * F * (H / 32) * 2, dq = E * H * (F / 2),
+               ds = E * H * (F / 32) * 2, id = E * 4;
+  size_t o[8], off = 0;
+  const size_t sz[7] = {gq, gs, gq, gs, dq, ds, id};
+  for (int i = 0; i < 7; ++i) {
+    o[i] = off;
+    off = align_up(off + sz[i], 256);
+  }
+  cudaError_t e = cudaMalloc(&b->base, off);
+  if (e != cudaSuccess) {
+    delete b;
+    return cuda_fail(e, "cudaMalloc(prefill staging buffer)");
+  }
+  char* p = static_cast<char*>(b->base);
+  b->gate_q = (uint8_t*)(p + o[0]);
+  b->gate_s = (uint16_t*)(p + o[1]);
+  b->up_q = (uint8_t*)(p + o[2]);
+  b->up_s = (uint16_t*)(p + o[3]);
+  b->down_q = (uint8_t*)(p + o[4]);
+  b->down_s = (uint16_t*)(p + o[5]);
+  b->ident = (int32_t*)(p + o[6]);
+  std::vector<int32_t> ident(E);
+  for (size_t i = 0; i < E; ++i) ident[i] = (int32_t)i;
+  e = cudaMemset(b->base, 0, off);
+  if (e == cudaSuccess) e = cudaMemcpy(b->ident, ident.data(), id, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(b->base);
+    delete b;
+    return cuda_fail(e, "initialise prefill staging buffer");
+  }
+  b->refs = 1;
+  g_streams.push_back(b);
+  L->stream = b;
+  return MOE_OK;
+}
+
+void stream_release(moe_layer* L) {
+  if (!L->stream) return;
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  StreamBuf* b = L->stream;
+  L->stream = nullptr;
+  if (--b->refs > 0) return;
+  for (size_t i = 0; i < g_streams.size(); ++i)
+    if (g_streams[i] == b) {
+      g_streams.erase(g_streams.begin() + i);
+      break;
+    }
+  cudaFree(b->base);
+  delete b;
+}
+
+// The slots and host tier of a partially resident layer (its weights block
+// is allocated; slot i must receive expert resident[i]).  rows[e] is the
+// caller's row of expert e.
+moe_status fill_partial(moe_layer* L, const moe_layer_weights* w, cudaMemcpyKind kind,
+                        const std::vector<int32_t>& rows, const std::vector<int32_t>& resident,
+                        const std::vector<int32_t>& res_slot) {
+  const moe_layer_config& c = L->cfg;
+  const size_t E = c.n_experts, S = c.n_slots, H = c.hidden, F = c.ffn;
+  const size_t gqe = F * (H / 2), gse = F * (H / 32) * 2, dqe = H * (F / 2), dse = H * (F / 32) * 2;
+  // the resident experts into their slots
+  const void* src[6] = {w->gate_q, w->gate_s, w->up_q, w->up_s, w->down_q, w->down_s};
+  void* dst[6] = {(void*)L->dev.gate_q, (void*)L->dev.gate_s, (void*)L->dev.up_q,
+                  (void*)L->dev.up_s,   (void*)L->dev.down_q, (void*)L->dev.down_s};
+  const size_t per[6] = {gqe, gse, gqe, gse, dqe, dse};
+  for (size_t i = 0; i < S; ++i) {
+    const size_t row = (size_t)rows[resident[i]];
+    for (int t = 0; t < 6; ++t)
+      CUDA_TRY(cudaMemcpy(static_cast<char*>(dst[t]) + i * per[t],
+                          static_cast<const char*>(src[t]) + row * per[t], per[t], kind),
+               "copy a resident expert");
+  }
+  CUDA_TRY(cudaMemcpy((void*)L->dev.slot_of, res_slot.data(), sizeof(int32_t) * E,
+                      cudaMemcpyHostToDevice),
+           "write the slot table");
+  // host tier: every expert in the caller's row order, plus block-major down scales
+  size_t o[8], off = 0;
+  const size_t sz[7] = {E * gqe, E * gse, E * gqe, E * gse, E * dqe, E * dse, E * dse};
+  for (int i = 0; i < 7; ++i) {
+    o[i] = off;
+    off = align_up(off + sz[i], 256);
+  }
+  CUDA_TRY(cudaHostAlloc(&L->host_tier, off, cudaHostAllocMapped | cudaHostAllocPortable),
+           "cudaHostAlloc(host tier)");
+  L->host_tier_bytes = off;
+  char* hb = static_cast<char*>(L->host_tier);
+  const cudaMemcpyKind to_host =
+      (kind == cudaMemcpyDeviceToDevice) ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost;
+  for (int t = 0; t < 6; ++t)
+    CUDA_TRY(cudaMemcpy(hb + o[t], src[t], sz[t], to_host), "fill the host tier");
+  {
+    const size_t CB = F / 32;
+    const uint16_t* rs = reinterpret_cast<const uint16_t*>(hb + o[5]);
+    uint16_t* bs = reinterpret_cast<uint16_t*>(hb + o[6]);
+    for (size_t r = 0; r < E; ++r)
+      for (size_t h = 0; h < H; ++h)
+        for (size_t b = 0; b < CB; ++b) bs[(r * CB + b) * H + h] = rs[(r * H + h) * CB + b];
+  }
+  void* hd = nullptr;
+  CUDA_TRY(cudaHostGetDevicePointer(&hd, L->host_tier, 0), "map the host tier");
+  char* hdb = static_cast<char*>(hd);
+  // cache state on the device: CacheDev | host_row [E] | slot_expert [S] |
+  // last_use [S] | stats [2]
+  size_t co[5], coff = 0;
+  const size_t csz[5] = {sizeof(moe::CacheDev), 4 * E, 4 * S, 4 * S, 16};
+  for (int i = 0; i < 5; ++i) {
+    co[i] = coff;
+    coff = align_up(coff + csz[i], 256);
+  }
+  void* cb = nullptr;
+  CUDA_TRY(cudaMalloc(&cb, coff), "cudaMalloc(expert cache state)");
+  L->cache_dev = static_cast<moe::CacheDev*>(cb);
+  char* cbb = static_cast<char*>(cb);
+  moe::CacheDev& C = L->cache_host;
+  C.n_slots = (int)S;
+  C.host_row = (const int32_t*)(cbb + co[1]);
+  C.slot_expert = (int32_t*)(cbb + co[2]);
+  C.last_use = (uint32_t*)(cbb + co[3]);
+  C.stats = (unsigned long long*)(cbb + co[4]);
+  C.gate_q = (const uint8_t*)(hdb + o[0]);
+  C.gate_s = (const uint16_t*)(hdb + o[1]);
+  C.up_q = (const uint8_t*)(hdb + o[2]);
+  C.up_s = (const uint16_t*)(hdb + o[3]);
+  C.down_q = (const uint8_t*)(hdb + o[4]);
+  C.down_s = (const uint16_t*)(hdb + o[5]);
+  C.down_sb = (const uint16_t*)(hdb + o[6]);
+  CUDA_TRY(cudaMemset(cb, 0, coff), "clear expert cache state");
+  CUDA_TRY(cudaMemcpy(cb, &C, sizeof C, cudaMemcpyHostToDevice), "write expert cache state");
+  CUDA_TRY(cudaMemcpy((void*)C.host_row, rows.data(), 4 * E, cudaMemcpyHostToDevice),
+           "write host rows");
+  CUDA_TRY(cudaMemcpy(C.slot_expert, resident.data(), 4 * S, cudaMemcpyHostToDevice),
+           "write slot experts");
+  L->dev.cache = L->cache_dev;
+  return MOE_OK;
+}
+
 struct Stage {
   const uint16_t* x = nullptr;
   uint16_t* y = nullptr;
@@ -74,6 +249,11 @@ struct Stage {
 
 namespace moe {
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+unsigned next_step() {
+  static std::atomic<unsigned> step{0u};
+  return ++step;
+}
 
 unsigned long long wait_timeout_ns() {
   const char* s = getenv("MOE_WAIT_TIMEOUT_US");
@@ -97,8 +277,12 @@ moe_status validate_config(const moe_layer_config* c, int num_sms) {
   if (c->shared_ffn < 0 || c->shared_ffn > 4096 || c->shared_ffn % 128)
     return fail(MOE_ERR_INVALID, "shared_ffn=%d: need 0 or a multiple of 128 up to 4096",
                 c->shared_ffn);
-  if (c->n_slots != c->n_experts)
-    return fail(MOE_ERR_INVALID, "n_slots=%d must equal n_experts=%d", c->n_slots, c->n_experts);
+  {
+    const int smin = std::min(c->n_experts, kMaxDecodeTokens * c->top_k);
+    if (c->n_slots < smin || c->n_slots > c->n_experts)
+      return fail(MOE_ERR_INVALID, "n_slots=%d: need %d..n_experts=%d (a 4-token batch's experts fit)",
+                  c->n_slots, smin, c->n_experts);
+  }
   if (c->max_tokens < 1 || c->max_tokens > 65536)
     return fail(MOE_ERR_INVALID, "max_tokens=%d: need 1..65536", c->max_tokens);
   const int known = MOE_ROUTING_NO_RENORM | MOE_ROUTING_BIAS_SELECT_ONLY | MOE_ROUTING_SHARED_GATE;
@@ -166,19 +350,37 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   const int S = cfg->n_slots, k = cfg->top_k, Tm = cfg->max_tokens;
   const cudaMemcpyKind kind = weights_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
 
-  // slot table: must be a permutation of 0..S-1
+  // slot table: the caller's row of every expert, a permutation of 0..E-1
   std::vector<int32_t> slots(E);
   CUDA_TRY(cudaMemcpy(slots.data(), w->slot_of_expert, sizeof(int32_t) * E,
                       weights_on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost),
            "read slot table");
   {
-    std::vector<char> seen(S, 0);
+    std::vector<char> seen(E, 0);
     for (int e = 0; e < E; ++e) {
       const int s = slots[e];
-      if (s < 0 || s >= S || seen[s])
+      if (s < 0 || s >= E || seen[s])
         return fail(MOE_ERR_INVALID, "slot_of_expert is not a permutation (expert %d -> %d)", e, s);
       seen[s] = 1;
     }
+  }
+  const bool partial = S < E;
+  // partial residency: the experts first placed in HBM (largest profile
+  // value first, ties to the lower id), slot i holding resident[i]
+  std::vector<int32_t> resident, res_slot(E, -1);
+  if (partial) {
+    std::vector<float> prof(E, 0.0f);
+    if (w->expert_profile)
+      CUDA_TRY(cudaMemcpy(prof.data(), w->expert_profile, sizeof(float) * E,
+                          weights_on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost),
+               "read expert profile");
+    std::vector<int32_t> order(E);
+    for (int e = 0; e < E; ++e) order[e] = e;
+    if (w->expert_profile)
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int a, int b) { return prof[a] > prof[b]; });
+    resident.assign(order.begin(), order.begin() + S);
+    for (int i = 0; i < S; ++i) res_slot[resident[i]] = i;
   }
 
   moe_layer* L = new moe_layer();
@@ -202,12 +404,14 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   };
   const size_t gq = (size_t)S * F * (H / 2), gs = (size_t)S * F * (H / 32) * 2;
   const size_t dq = (size_t)S * H * (F / 2), ds = (size_t)S * H * (F / 32) * 2;
+  // fully resident: the caller's arrays are copied whole (slot = caller row);
+  // partial: the slots are filled expert by expert below
   size_t i_rw = add(w->router_w, sizeof(float) * E * H);
   size_t i_rb = add(w->router_bias, sizeof(float) * E);
-  size_t i_sl = add(w->slot_of_expert, sizeof(int32_t) * E);
-  size_t i_gq = add(w->gate_q, gq), i_gs = add(w->gate_s, gs);
-  size_t i_uq = add(w->up_q, gq), i_us = add(w->up_s, gs);
-  size_t i_dq = add(w->down_q, dq), i_ds = add(w->down_s, ds);
+  size_t i_sl = add(partial ? nullptr : w->slot_of_expert, sizeof(int32_t) * E);
+  size_t i_gq = add(partial ? nullptr : w->gate_q, gq), i_gs = add(partial ? nullptr : w->gate_s, gs);
+  size_t i_uq = add(partial ? nullptr : w->up_q, gq), i_us = add(partial ? nullptr : w->up_s, gs);
+  size_t i_dq = add(partial ? nullptr : w->down_q, dq), i_ds = add(partial ? nullptr : w->down_s, ds);
   size_t i_sgq = 0, i_sgs = 0, i_suq = 0, i_sus = 0, i_sdq = 0, i_sds = 0;
   if (Fs > 0) {
     i_sgq = add(w->sh_gate_q, (size_t)Fs * (H / 2));
@@ -260,6 +464,10 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     L->dev.sh_down_s = (const uint16_t*)at(i_sds);
   }
   L->sh_gate_w = gated ? (const float*)at(i_sgw) : nullptr;
+  if (partial && (st = fill_partial(L, w, kind, slots, resident, res_slot)) != MOE_OK) {
+    moe_layer_destroy(L);
+    return st;
+  }
   L->dev.down_sb = (const uint16_t*)at(i_dsb);
   L->dev.sh_down_sb = Fs > 0 ? (const uint16_t*)at(i_sdsb) : nullptr;
   {
@@ -361,6 +569,28 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       return fail(st, "prefill router weights: %s", why);
     }
   }
+  if (partial) {
+    // prefill view: the routed experts of a call are staged, expert e in row
+    // e of the shared buffer, under an identity slot table
+    if ((st = stream_acquire(L)) != MOE_OK) {
+      moe_layer_destroy(L);
+      return st;
+    }
+    L->pf_dev = L->dev;
+    L->pf_dev.slot_of = L->stream->ident;
+    L->pf_dev.gate_q = L->stream->gate_q;
+    L->pf_dev.gate_s = L->stream->gate_s;
+    L->pf_dev.up_q = L->stream->up_q;
+    L->pf_dev.up_s = L->stream->up_s;
+    L->pf_dev.down_q = L->stream->down_q;
+    L->pf_dev.down_s = L->stream->down_s;
+    L->pf_dev.cache = nullptr;
+    const char* why = "";
+    if ((st = moe::prefill_bind_stream(L, &why)) != MOE_OK) {
+      moe_layer_destroy(L);
+      return fail(st, "prefill staging maps: %s", why);
+    }
+  }
   *out = L;
   return MOE_OK;
 }
@@ -370,8 +600,31 @@ void moe_layer_destroy(moe_layer* layer) {
   cudaDeviceSynchronize();
   if (layer->weights_block) cudaFree(layer->weights_block);
   if (layer->ws_block) cudaFree(layer->ws_block);
+  if (layer->cache_dev) cudaFree(layer->cache_dev);
+  if (layer->host_tier) cudaFreeHost(layer->host_tier);
+  stream_release(layer);
   cudaGetLastError();
   delete layer;
+}
+
+moe_status moe_cache_stats(moe_layer* layer, uint64_t* hits, uint64_t* misses,
+                           int32_t* slot_of_expert, int reset, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID, "layer is NULL");
+  CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
+  unsigned long long st[2] = {0ull, 0ull};
+  if (layer->cache_dev) {
+    CUDA_TRY(cudaMemcpy(st, layer->cache_host.stats, sizeof st, cudaMemcpyDeviceToHost),
+             "read cache statistics");
+    if (reset)
+      CUDA_TRY(cudaMemset(layer->cache_host.stats, 0, sizeof st), "reset cache statistics");
+  }
+  if (hits) *hits = st[0];
+  if (misses) *misses = st[1];
+  if (slot_of_expert)
+    CUDA_TRY(cudaMemcpy(slot_of_expert, layer->dev.slot_of, sizeof(int32_t) * layer->cfg.n_experts,
+                        cudaMemcpyDeviceToHost),
+             "read the slot table");
+  return MOE_OK;
 }
 
 moe_status moe_status_sync(moe_layer* layer, void* stream) {
@@ -434,6 +687,7 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
     p.ids_out = ids_trace ? ids_trace + (size_t)l0 * T * L0->cfg.top_k : nullptr;
     p.w_out = w_out;
     p.down_tma = 1;
+    p.step = moe::next_step();
     for (int l = 0; l < nl; ++l) {
       p.layers[l] = layers[l0 + l]->dev;
       p.tm_down[l] = layers[l0 + l]->tm_dec_down;

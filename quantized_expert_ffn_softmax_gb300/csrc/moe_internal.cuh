@@ -20,6 +20,24 @@ constexpr int kDecodeThreads = 256;                 // compute threads of a deco
 constexpr int kDecodeBlock = kDecodeThreads + 32;   // + the copy warp
 constexpr int kMaxUnits = kMaxDecodeTokens * kMaxTopK + 1;  // routed + shared
 
+// Expert cache of a partially resident layer (n_slots < n_experts), in
+// device memory: the host tier holds every expert (caller row order) in
+// pinned memory the GPU reads over the host link.
+struct CacheDev {
+  int n_slots;
+  const int32_t* host_row;        // [E] row of expert e in the host tier
+  int32_t* slot_expert;           // [S] expert held by each slot, -1 = none
+  uint32_t* last_use;             // [S] launch number of the slot's last use
+  unsigned long long* stats;      // [2] hits, misses (decode lookups)
+  const uint8_t* gate_q;          // host tier [E][F][H/2] (device-accessible)
+  const uint16_t* gate_s;         // [E][F][H/32]
+  const uint8_t* up_q;
+  const uint16_t* up_s;
+  const uint8_t* down_q;          // [E][H][F/2]
+  const uint16_t* down_s;         // [E][H][F/32]
+  const uint16_t* down_sb;        // [E][F/32][H] block-major down scales
+};
+
 // Device pointers of one layer's weights (library-owned copies).
 struct LayerDev {
   const float* router_w;  // [E][H]
@@ -41,6 +59,9 @@ struct LayerDev {
   // kernel's one-copy-per-block loads: [S][F/32][H] and [Fs/32][H]
   const uint16_t* down_sb;
   const uint16_t* sh_down_sb;
+  // partially resident layers: the cache (device memory); slot_of then holds
+  // each expert's slot or -1 and is rewritten by the decode kernel
+  const CacheDev* cache;
 };
 
 // Generation-counting grid barrier state (one per workspace, 128-B aligned).
@@ -59,6 +80,7 @@ struct DecodeParams {
   CUtensorMap tm_down[kMaxLayersPerLaunch];
   CUtensorMap tm_sh_down[kMaxLayersPerLaunch];
   int down_tma;  // 1: down blocks by TMA + block-major scales; 0: per-thread copies
+  unsigned step;  // launch number (least-recently-used stamps of the expert caches)
   int H, E, k, F, Fs;
   int T;          // real tokens (1..4)
   int n_layers;
@@ -149,6 +171,13 @@ struct moe_layer {
   moe::Workspace ws;
   int device = 0;
   int num_sms = 0;
+  // partial residency (cfg.n_slots < cfg.n_experts)
+  void* host_tier = nullptr;        // pinned, mapped: every expert (caller row order)
+  size_t host_tier_bytes = 0;
+  moe::CacheDev cache_host{};       // host copy of the device CacheDev
+  moe::CacheDev* cache_dev = nullptr;  // in ws_block
+  moe::LayerDev pf_dev{};           // prefill view: routed experts in the staging buffer
+  struct StreamBuf* stream = nullptr;  // staging buffer shared by partial layers
 };
 
 namespace moe {
@@ -167,6 +196,11 @@ moe_status launch_decode(const DecodeParams& p, cudaStream_t stream, int num_sms
                          const char** why);
 // shared memory of the decode kernel for p's shape on a grid of num_sms CTAs
 size_t decode_smem_bytes(const DecodeParams& p, int num_sms);
+// moe_api.cu: next launch number (expert-cache stamps)
+unsigned next_step();
+// prefill.cu: re-encodes the routed-code tensor maps over the staging buffer
+// of a partially resident layer (L->pf_dev)
+moe_status prefill_bind_stream(moe_layer* L, const char** why);
 // prefill.cu: cuTensorMapEncodeTiled from the driver (null when unavailable)
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 // decode.cu: the decode tensor maps of a layer (after its weights are in place)

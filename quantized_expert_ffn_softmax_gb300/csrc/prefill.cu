@@ -1226,6 +1226,19 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   return MOE_OK;
 }
 
+moe_status prefill_bind_stream(moe_layer* L, const char** why) {
+  const moe_layer_config& c = L->cfg;
+  const uint64_t E = c.n_experts, H = c.hidden, F = c.ffn;
+  const LayerDev& d = L->pf_dev;
+  if (!encode_codes(&L->tmap_gate, d.gate_q, H / 2, E * F) ||
+      !encode_codes(&L->tmap_up, d.up_q, H / 2, E * F) ||
+      !encode_codes(&L->tmap_down, d.down_q, F / 2, E * H)) {
+    *why = "cuTensorMapEncodeTiled failed (staging buffer)";
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 moe_status prefill_prepare_router(moe_layer* L, const char** why) {
   const moe_layer_config& c = L->cfg;
   router_split_kernel<<<4 * L->num_sms, 256>>>(L->dev.router_w, c.n_experts, c.hidden, L->router_shift,
@@ -1241,6 +1254,49 @@ moe_status prefill_prepare_router(moe_layer* L, const char** why) {
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// Partially resident layers, before the grouped GEMMs: every expert with a
+// nonempty bucket is copied into row e of the staging buffer, from its HBM
+// slot or (not resident) from the host tier over the host link.  Block
+// (e, tensor t, part) copies one slice of one of the six routed tensors.
+__global__ void stream_in_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ slot_of,
+                                 const CacheDev* __restrict__ cache, LayerDev slots, LayerDev stage,
+                                 int H, int F) {
+  const int e = blockIdx.x, t = blockIdx.y;
+  if (__ldg(offsets + e + 1) == __ldg(offsets + e)) return;
+  const size_t gqe = (size_t)F * (H / 2), gse = (size_t)F * (H / 32) * 2;
+  const size_t dqe = (size_t)H * (F / 2), dse = (size_t)H * (F / 32) * 2;
+  const size_t per[6] = {gqe, gse, gqe, gse, dqe, dse};
+  const int sl = __ldg(slot_of + e);
+  const char* src;
+  char* dst;
+  const size_t n = per[t];
+  {
+    const char* sp[6] = {(const char*)slots.gate_q, (const char*)slots.gate_s, (const char*)slots.up_q,
+                         (const char*)slots.up_s, (const char*)slots.down_q, (const char*)slots.down_s};
+    const char* hp[6] = {(const char*)cache->gate_q, (const char*)cache->gate_s,
+                         (const char*)cache->up_q, (const char*)cache->up_s,
+                         (const char*)cache->down_q, (const char*)cache->down_s};
+    char* dp[6] = {(char*)stage.gate_q, (char*)stage.gate_s, (char*)stage.up_q,
+                   (char*)stage.up_s, (char*)stage.down_q, (char*)stage.down_s};
+    src = (sl >= 0) ? sp[t] + (size_t)sl * n : hp[t] + (size_t)__ldg(cache->host_row + e) * n;
+    dst = dp[t] + (size_t)e * n;
+  }
+  const size_t nv = n / 16;  // every tensor is a multiple of 16 bytes
+  const size_t lo = nv * blockIdx.z / gridDim.z, hi = nv * (blockIdx.z + 1) / gridDim.z;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  size_t i = lo + threadIdx.x;
+  for (; i + 3 * blockDim.x < hi; i += 4 * blockDim.x) {  // four loads in flight per thread
+    const uint4 a = s4[i], b = s4[i + blockDim.x], c = s4[i + 2 * blockDim.x],
+                d = s4[i + 3 * blockDim.x];
+    d4[i] = a;
+    d4[i + blockDim.x] = b;
+    d4[i + 2 * blockDim.x] = c;
+    d4[i + 3 * blockDim.x] = d;
+  }
+  for (; i < hi; i += blockDim.x) d4[i] = s4[i];
 }
 
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
@@ -1340,6 +1396,16 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
     bucket_scatter_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
   }
 
+  if (L->dev.cache) {
+    // partial residency: stage the experts this batch selects, then run the
+    // GEMMs on the staging buffer (identity slot table)
+    {
+      prof::Scope sc("moe_stream_in", s);
+      stream_in_kernel<<<dim3(E, 6, 4), 256, 0, s>>>(ws.offsets, L->dev.slot_of, L->dev.cache, L->dev,
+                                                       L->pf_dev, H, c.ffn);
+    }
+    gp.W = L->pf_dev;
+  }
   gp.units = ws.gu_units;
   gp.n_units = ws.n_units;
   if ((st = launch_gemm<kSwiglu>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;

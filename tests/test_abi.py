@@ -46,7 +46,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(hidden=100), dict(hidden=0), dict(n_experts=0),
                                  dict(n_experts=2000), dict(top_k=0), dict(top_k=17),
                                  dict(top_k=20, n_experts=16), dict(ffn=96), dict(shared_ffn=64),
-                                 dict(max_tokens=0), dict(n_slots=8), dict(routing_flags=8),
+                                 dict(max_tokens=0), dict(n_slots=7), dict(n_slots=17), dict(routing_flags=8),
                                  dict(routing_flags=-1), dict(routing_flags=4, shared_ffn=0)])
 def test_create_rejects_bad_configs_before_touching_the_device(lib, bad):
     with pytest.raises(moe.MoeError) as ei:
