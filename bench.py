@@ -402,18 +402,25 @@ def bench_decode(name, steps, warmup, dist, with_e2e=False, n_slots=None, profil
     return out
 
 
-def bench_prefill(name, steps, warmup, dist):
+def bench_prefill(name, steps, warmup, dist, n_layers=1):
+    """The prefill chunk through one layer (moe_forward), or through an
+    n_layers stack of that shape (moe_stack_forward)."""
     import quantized_expert_ffn_softmax_gb300 as moe
     import torch
 
-    cfg = W.CONFIGS[name]
+    cfg = W.CONFIGS[name].replace(n_layers=n_layers)
     T = cfg.n_tokens
-    layer = build_stack(cfg, max_tokens=T)[0]
+    stack = build_stack(cfg, max_tokens=T)
+    layer = stack[0]
+    hs = [l.handle for l in stack]
     xs = [torch.from_numpy(W.activations(cfg, i).view(np.int16)).cuda() for i in range(2)]
     y = torch.empty_like(xs[0])
 
     def step(i):
-        moe.moe_forward(layer.handle, xs[i], T, y)
+        if n_layers == 1:
+            moe.moe_forward(layer.handle, xs[i], T, y)
+        else:
+            moe.moe_stack_forward(hs, n_layers, xs[i], T, y)
 
     with ClockSampler(dist.local) as clk:
         ms = time_steps(step, steps, warmup, dist, 2, clk)
@@ -423,7 +430,7 @@ def bench_prefill(name, steps, warmup, dist):
     H, F, Fs, k, E = cfg.hidden, cfg.ffn, cfg.shared_ffn, cfg.top_k, cfg.n_experts
     fl = {"moe_gemm_gateup_swiglu": 2.0 * T * (k * 2 * H * F + 2 * H * Fs),
           "moe_gemm_down_scatter": 2.0 * T * (k * H * F + H * Fs),
-          "moe_gemm_router": 2.0 * T * E * H}
+          "moe_gemm_router": 2.0 * T * E * H}  # per launch (one layer)
     kern = {}
     total_k_ms = 0.0
     for nm, (c, tms) in prof.items():
@@ -438,13 +445,15 @@ def bench_prefill(name, steps, warmup, dist):
     gemm_ms = sum(kern[n]["avg_ms"] for n in ("moe_gemm_gateup_swiglu", "moe_gemm_down_scatter")
                   if n in kern)
     gemm_fl = fl["moe_gemm_gateup_swiglu"] + fl["moe_gemm_down_scatter"]
-    out = {"ms_per_step": ms, "tok_s": dist.n * T / (ms / 1e3),
-           "tflops_step": prefill_flops(cfg, T) / (ms / 1e3) / 1e12,
+    out = {"ms_per_step": ms, "tok_s": dist.n * T / (ms / 1e3), "layers": n_layers,
+           "tflops_step": n_layers * prefill_flops(cfg, T) / (ms / 1e3) / 1e12,
            "grouped_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
            "kernels": kern,
            "launches_per_step": sum(v["launches"] for v in kern.values()) / max(1, min(steps, 20)),
            "clocks": clk.report()}
-    layer.close()
+    for l in stack:
+        l.close()
+    del stack, layer
     torch.cuda.empty_cache()
     return out
 
@@ -626,7 +635,7 @@ def main():
         if args.layers:
             W.CONFIGS[args.only] = W.CONFIGS[args.only].replace(n_layers=args.layers)
         if args.only.startswith("prefill"):
-            r = bench_prefill(args.only, args.steps, args.warmup, dist)
+            r = bench_prefill(args.only, args.steps, args.warmup, dist, n_layers=args.layers or 1)
         else:
             r = bench_decode(args.only, args.steps, args.warmup, dist, n_slots=args.slots,
                              profile=args.profile)
@@ -662,6 +671,10 @@ def main():
                                  "note": "fp16 operands; fp16 dense peak = bf16 peak"}
         pf["grouped_gemm_frac"] = (pf["grouped_gemm_tflops"] or 0) / bf16
         extra["prefill125b"] = pf
+        # the same chunk through the 48-layer stack of that shape
+        ps = bench_prefill("prefill125b", max(3, args.steps // 100), args.warmup, dist, n_layers=48)
+        ps["grouped_gemm_frac"] = (ps["grouped_gemm_tflops"] or 0) / bf16
+        extra["prefill125b_stack48"] = ps
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

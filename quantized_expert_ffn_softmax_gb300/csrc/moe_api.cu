@@ -505,7 +505,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   size_t o_err = wadd(sizeof(int) * 4);
   size_t o_xs = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_ys = wadd(sizeof(uint16_t) * (size_t)Tm * H);
-  size_t o_yl = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_ul = wadd(sizeof(uint16_t) * (size_t)Tm * H);
   size_t o_is = wadd(sizeof(int32_t) * (size_t)Tm * k);
   size_t o_ws = wadd(sizeof(float) * (size_t)Tm * k);
@@ -525,7 +524,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->ws.err = (int*)(wb + o_err);
   L->ws.x_stage = (uint16_t*)(wb + o_xs);
   L->ws.y_stage = (uint16_t*)(wb + o_ys);
-  L->ws.y_layer = (uint16_t*)(wb + o_yl);
   L->ws.u_layer = (uint16_t*)(wb + o_ul);
   L->ws.ids_stage = (int32_t*)(wb + o_is);
   L->ws.w_stage = (float*)(wb + o_ws);
@@ -703,33 +701,6 @@ moe_status run_decode(moe_layer* const* layers, int n_layers, const uint16_t* x,
   return MOE_OK;
 }
 
-__global__ void residual_kernel(const uint16_t* __restrict__ h, const uint16_t* __restrict__ y,
-                                uint16_t* __restrict__ out, size_t n) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const float a = __bfloat162float(__ushort_as_bfloat16(h[i]));
-    const float b = __bfloat162float(__ushort_as_bfloat16(y[i]));
-    out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a + b));
-  }
-}
-
-// u = bf16(h / sqrt(mean(h^2) + 1e-6)) per row (one warp per row).
-__global__ void rmsnorm_kernel(const uint16_t* __restrict__ h, int T, int H,
-                               uint16_t* __restrict__ u) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const uint16_t* row = h + (size_t)t * H;
-  float ss = 0.0f;
-  for (int i = lane; i < H; i += 32) {
-    const float v = __bfloat162float(__ushort_as_bfloat16(row[i]));
-    ss = fmaf(v, v, ss);
-  }
-  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / (float)H + 1e-6f);
-  for (int i = lane; i < H; i += 32)
-    u[(size_t)t * H + i] = __bfloat16_as_ushort(
-        __float2bfloat16_rn(__bfloat162float(__ushort_as_bfloat16(row[i])) * inv));
-}
-
 // One layer on any token count: decode kernel for <= 4 tokens, the prefill
 // path above that.
 moe_status forward_device(moe_layer* L, const uint16_t* x, int T, uint16_t* y, cudaStream_t s) {
@@ -860,46 +831,41 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
                     moe::kModeStack, s);
     if (st != MOE_OK) return st;
   } else {
-    // prefill-sized stack: layer by layer.  h ping-pongs between the two
-    // staging buffers, u_l = rmsnorm(h_l) and y_l have buffers of their own.
+    // prefill-sized stack, layer by layer.  Each layer boundary is one
+    // kernel: the previous layer's fp32 output becomes the residual
+    // h_{l+1} = bf16(h_l + bf16(y_l)), then u_{l+1} = rmsnorm(h_{l+1}) and its
+    // fp16 operand rows go straight into the next layer's workspace.  h
+    // ping-pongs between two staging buffers (or lands in the h trace).
     moe_layer* L0 = layers[0];
     const size_t n = (size_t)n_tokens * H;
     uint16_t* P = L0->ws.x_stage;
     uint16_t* Q = L0->ws.y_stage;
     uint16_t* U = L0->ws.u_layer;
-    uint16_t* Y = L0->ws.y_layer;
+    uint16_t* ht = (uint16_t*)h_trace_bf16;
+    uint16_t* it = (uint16_t*)in_trace_bf16;
+    uint16_t* yt = (uint16_t*)y_trace_bf16;
     const uint16_t* cur = sg.x;
+    const char* why = "";
+    st = moe::launch_stack_boundary(layers[0], cur, nullptr, n_tokens, H, const_cast<uint16_t*>(cur),
+                                    nullptr, it ? it : U, s, &why);
+    if (st != MOE_OK) return fail(st, "stack input: %s", why);
     for (int l = 0; l < n_layers; ++l) {
-      {
-        moe::prof::Scope sc("moe_rmsnorm", s);
-        rmsnorm_kernel<<<(n_tokens + 7) / 8, 256, 0, s>>>(cur, n_tokens, H, U);
-      }
-      CUDA_TRY(cudaGetLastError(), "rmsnorm kernel");
-      if (in_trace_bf16)
-        CUDA_TRY(cudaMemcpyAsync((uint16_t*)in_trace_bf16 + (size_t)l * n, U, n * 2,
-                                 cudaMemcpyDeviceToDevice, s),
-                 "trace copy");
-      const char* why = "";
-      st = moe::launch_prefill(layers[l], U, n_tokens, Y,
+      const uint16_t* u_l = it ? it + (size_t)l * n : U;
+      st = moe::launch_prefill(layers[l], u_l, n_tokens, nullptr,
                                ids_trace ? ids_trace + (size_t)l * n_tokens * k : nullptr, nullptr,
-                               false, s, &why);
+                               false, s, &why, /*prepped=*/true, /*keep_yacc=*/true);
       if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
-      if (y_trace_bf16)
-        CUDA_TRY(cudaMemcpyAsync((uint16_t*)y_trace_bf16 + (size_t)l * n, Y, n * 2,
-                                 cudaMemcpyDeviceToDevice, s),
-                 "trace copy");
-      uint16_t* dst = (l == n_layers - 1) ? sg.y : (cur == P ? Q : P);
-      {
-        moe::prof::Scope sc("moe_residual", s);
-        residual_kernel<<<2 * L0->num_sms, 256, 0, s>>>(cur, Y, dst, n);  // elementwise: in place is safe
-      }
-      CUDA_TRY(cudaGetLastError(), "residual kernel");
-      if (h_trace_bf16)
-        CUDA_TRY(cudaMemcpyAsync((uint16_t*)h_trace_bf16 + (size_t)l * n, dst, n * 2,
-                                 cudaMemcpyDeviceToDevice, s),
-                 "trace copy");
+      const bool last = l == n_layers - 1;
+      moe_layer* next = last ? nullptr : layers[l + 1];
+      uint16_t* dst = ht ? ht + (size_t)l * n : (last ? sg.y : (cur == P ? Q : P));
+      st = moe::launch_stack_boundary(next, cur, layers[l]->ws.yacc, n_tokens, H, dst,
+                                      yt ? yt + (size_t)l * n : nullptr,
+                                      next ? (it ? it + (size_t)(l + 1) * n : U) : nullptr, s, &why);
+      if (st != MOE_OK) return fail(st, "layer %d boundary: %s", l, why);
       cur = dst;
     }
+    if (ht)
+      CUDA_TRY(cudaMemcpyAsync(sg.y, cur, n * 2, cudaMemcpyDeviceToDevice, s), "stack output");
   }
   return stage_out(layers[0], n_tokens, y_bf16, sg, s);
 }

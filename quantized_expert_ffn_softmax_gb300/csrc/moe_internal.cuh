@@ -117,8 +117,7 @@ struct Workspace {
   int* err = nullptr;
   uint16_t* x_stage = nullptr;  // [max_tokens][H] staging for host inputs
   uint16_t* y_stage = nullptr;  // [max_tokens][H] staging for host outputs
-  uint16_t* y_layer = nullptr;  // [max_tokens][H] per-layer output in prefill-sized stacks
-  uint16_t* u_layer = nullptr;  // [max_tokens][H] per-layer normalised input (same)
+  uint16_t* u_layer = nullptr;  // [max_tokens][H] per-layer normalised input in prefill-sized stacks
   int32_t* ids_stage = nullptr; // [max_tokens][k]
   float* w_stage = nullptr;     // [max_tokens][k]
   float* gz = nullptr;          // [4] decode: shared-expert gate logits
@@ -206,8 +205,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 // decode.cu: the decode tensor maps of a layer (after its weights are in place)
 moe_status decode_prepare(moe_layer* L, const char** why);
 // prefill.cu
+// prepped: the layer's fp16 operand rows (ws.x16/xshift) already hold x;
+// keep_yacc: leave the output in the fp32 accumulator ws.yacc (y unused)
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
-                          float* w_out, bool route_only, cudaStream_t stream, const char** why);
+                          float* w_out, bool route_only, cudaStream_t stream, const char** why,
+                          bool prepped = false, bool keep_yacc = false);
+// Layer boundary of a prefill-sized stack: h_out = bf16(h + bf16(yacc))
+// (h_out = h when yacc is null), and for the next layer (null after the
+// last) u = rmsnorm(h_out) and its fp16 operand rows in next's workspace.
+moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const float* yacc, int T,
+                                 int H, uint16_t* h_out, uint16_t* y_trace, uint16_t* u,
+                                 cudaStream_t s, const char** why);
 size_t prefill_workspace_bytes(const moe_layer_config& c);
 // Carves the prefill workspace out of `scratch` and encodes the tensor maps.
 moe_status prefill_init(moe_layer* L, void* scratch, const char** why);

@@ -1299,14 +1299,129 @@ __global__ void stream_in_kernel(const int32_t* __restrict__ offsets, const int3
   for (; i < hi; i += blockDim.x) d4[i] = s4[i];
 }
 
+// Layer boundary of a prefill-sized stack, one warp per token:
+//   y  = bf16(yacc)              (the previous layer's fp32 output; skipped
+//   h' = bf16(h + y)              for the first layer, where h' = h)
+//   u  = bf16(h' / sqrt(mean(h'^2) + 1e-6))
+// and the next layer's fp16 operand rows of u (per-token power-of-two
+// shift, K pairs in the nibble unpack order, as prep_x16_kernel).  With
+// norm == 0 (after the last layer) only h' is formed.  Trace pointers may
+// be null.
+__global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const float* __restrict__ yacc,
+                                      int T, int H, int norm, uint16_t* __restrict__ h_out,
+                                      uint16_t* __restrict__ y_trace, uint16_t* __restrict__ u,
+                                      __half* __restrict__ x16, int32_t* __restrict__ xshift) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int G = H / 8;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)t * H);
+  uint4* ho = reinterpret_cast<uint4*>(h_out + (size_t)t * H);
+  // pass 1: h' (and y), sum of squares
+  float ss = 0.0f;
+  for (int g = lane; g < G; g += 32) {
+    uint4 v = hr[g];
+    if (yacc) {
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(yacc + (size_t)t * H) + 2 * g);
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(yacc + (size_t)t * H) + 2 * g + 1);
+      const float yy[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4], yo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
+        const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
+        const float lo = __uint_as_float(w[q] << 16) + __bfloat162float(ylo);
+        const float hi = __uint_as_float(w[q] & 0xffff0000u) + __bfloat162float(yhi);
+        o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+        yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
+      }
+      v = make_uint4(o[0], o[1], o[2], o[3]);
+      if (y_trace) reinterpret_cast<uint4*>(y_trace + (size_t)t * H)[g] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+    }
+    if (yacc || h_out != h) ho[g] = v;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
+  }
+  if (!norm) return;
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)H + 1e-6f);
+  __syncwarp();
+  // pass 2: u and its max |u| (the row is read back from this warp's writes)
+  const uint4* hh = reinterpret_cast<const uint4*>(h_out + (size_t)t * H);
+  uint4* ur = reinterpret_cast<uint4*>(u + (size_t)t * H);
+  float m = 0.0f;
+  for (int g = lane; g < G; g += 32) {
+    const uint4 v = hh[g];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat16 lo = __float2bfloat16_rn(__uint_as_float(w[q] << 16) * inv);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(__uint_as_float(w[q] & 0xffff0000u) * inv);
+      m = fmaxf(m, fmaxf(fabsf(__bfloat162float(lo)), fabsf(__bfloat162float(hi))));
+      o[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+    }
+    ur[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  m = warp_max(m);
+  int sft = 0;
+  if (m > 0.0f && isfinite(m)) sft = ((__float_as_int(m) >> 23) & 0xff) - 127;
+  sft = sft < -60 ? -60 : (sft > 60 ? 60 : sft);
+  if (lane == 0) xshift[t] = sft;
+  const float sc = pow2f(-sft);
+  __syncwarp();
+  // pass 3: the fp16 operand row
+  uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * H);
+  for (int g = lane; g < G; g += 32) {
+    const uint4 v = ur[g];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float e[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e[2 * i] = __uint_as_float(w[i] << 16) * sc;
+      e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * sc;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      __half2 hv = __floats2half2_rn(e[jj], e[jj + 4]);
+      o[jj] = *reinterpret_cast<uint32_t*>(&hv);
+    }
+    out[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const float* yacc, int T,
+                                 int H, uint16_t* h_out, uint16_t* y_trace, uint16_t* u,
+                                 cudaStream_t s, const char** why) {
+  {
+    prof::Scope sc("moe_stack_boundary", s);
+    stack_boundary_kernel<<<(T + 7) / 8, 256, 0, s>>>(h, yacc, T, H, next ? 1 : 0, h_out, y_trace, u,
+                                                      next ? next->ws.x16 : nullptr,
+                                                      next ? next->ws.xshift : nullptr);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
-                          float* w_out, bool route_only, cudaStream_t s, const char** why) {
+                          float* w_out, bool route_only, cudaStream_t s, const char** why,
+                          bool prepped, bool keep_yacc) {
   const moe_layer_config& c = L->cfg;
   const Workspace& ws = L->ws;
   const int H = c.hidden, E = c.n_experts, k = c.top_k;
   cudaError_t e;
 
-  {
+  if (!prepped) {
     prof::Scope sc("moe_prep_x16", s);
     prep_x16_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, ws.x16, ws.xshift);
   }
@@ -1416,7 +1531,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.units = ws.dn_units;
   gp.n_units = ws.n_units + 1;
   if ((st = launch_gemm<kScatter>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;
-  {
+  if (!keep_yacc) {
     prof::Scope sc("moe_finalize", s);
     if ((reinterpret_cast<uintptr_t>(y) & 15u) == 0)
       finalize_kernel<<<4 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);

@@ -203,3 +203,59 @@ def test_prefill125b_chunk_parity(cuda_device):
     worst = max(parallel_map(check_token, toks))
     print("prefill125b: %d tokens' y checked (largest bucket %d: %d rows), worst error / "
           "tolerance %.3f" % (toks.size, e_big, counts[e_big], worst))
+
+
+def test_prefill125b_48_layer_stack_teacher_forced(cuda_device):
+    """The 8192-token chunk through the 48-layer 125B-shaped stack (pre-norm
+    residual, fused layer boundaries).  On five layers spread over the stack
+    (teacher forced: the oracle takes the GPU's input of the layer): the RMS
+    norm of every token, every token's top-k against the oracle's logits,
+    and 32 tokens' y at the stated tolerance with their residual; every
+    layer's output finite."""
+    cfg = W.CONFIGS["prefill125b"].replace(n_layers=48)
+    T, L = cfg.n_tokens, cfg.n_layers
+    layers = [make_layer_device(cfg, l, max_tokens=T) for l in range(L)]
+    try:
+        x = W.activations(cfg, 2)
+        y, h_trace, in_trace, y_trace, ids_trace = moe.stack_forward(layers, to_dev(x), trace=True)
+        assert moe.moe_status_sync(layers[0].handle) == moe.MOE_OK
+        check = [0, 1, 23, 46, 47]
+        y_last = to_host_bits(y)
+        h_in = {l: (x if l == 0 else to_host_bits(h_trace[l - 1])) for l in check}
+        h_out = {l: to_host_bits(h_trace[l]) for l in check}
+        u_tr = {l: to_host_bits(in_trace[l]) for l in check}
+        y_tr = {l: to_host_bits(y_trace[l]) for l in check}
+        ids_tr = {l: ids_trace[l].cpu().numpy() for l in check}
+        finite = bool(torch.isfinite(y_trace.view(torch.bfloat16).float()).all())
+        assert np.array_equal(y_last, to_host_bits(h_trace[L - 1]))
+    finally:
+        for l in layers:
+            l.close()
+        del layers
+        gc.collect()
+        torch.cuda.empty_cache()
+    assert finite
+    rng = np.random.default_rng(1)
+    for l in check:
+        u = u_tr[l]
+        u_ref = bf16_f64(oracle.rmsnorm(h_in[l]))
+        assert np.all(np.abs(bf16_f64(u) - u_ref) <= 2.0 ** -7 * np.abs(u_ref) + 1e-30), l
+        Wr, b = W.router(cfg, l)
+        slices = np.array_split(np.arange(T), 64)
+
+        def topk_slice(ts):
+            zs = oracle.router_logits(Wr, b, u[ts])
+            return sum(check_topk(ids_tr[l][t], zs[i], cfg.top_k) for i, t in enumerate(ts))
+
+        parallel_map(topk_slice, slices)
+        toks = np.sort(rng.choice(T, 32, replace=False))
+        sh = W.shared_expert(cfg, l)
+        need = sorted(set(ids_tr[l][toks].ravel().tolist()))
+        cache = dict(zip(((l, e) for e in need), parallel_map(lambda e: W.expert(cfg, l, e), need)))
+
+        def y_ref_of(t):
+            return oracle_token(cfg, l, u[t], gpu_ids=ids_tr[l][t], router=(Wr, b), shared=sh,
+                                expert_cache=cache)[0]
+
+        y_ref = np.stack(parallel_map(y_ref_of, toks))
+        check_stack_outputs(h_in[l][toks], y_tr[l][toks], h_out[l][toks], y_ref, where=l)
