@@ -325,6 +325,62 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Expert-cache misses of one layer, from the host tier into their slots.
+// The bytes of all misses form one index space of 16-byte vectors (miss,
+// tensor, offset; tensors in the order gate codes, gate scales, up codes, up
+// scales, down codes, down scales, block-major down scales, each a multiple
+// of 16 bytes); this CTA copies its 1/grid slice with four loads in flight
+// per thread, so the layer's misses cost about one host round trip per four
+// vectors of a thread, not one per tensor and miss.
+__device__ __forceinline__ void copy_misses(const CacheDev* cd, const LayerDev& W, int F, int H,
+                                         int n_miss, const int* miss_unit, const int* unit_expert,
+                                         const int* unit_slot, int tid) {
+  const size_t gqe = (size_t)F * (H / 2), gse = (size_t)F * (H / 32) * 2;
+  const size_t dqe = (size_t)H * (F / 2), dse = (size_t)H * (F / 32) * 2;
+  const size_t per16 = (2 * (gqe + gse) + dqe + 2 * dse) / 16;  // vectors per expert
+  const size_t nvec = per16 * (size_t)n_miss;
+  const size_t lo = nvec * blockIdx.x / gridDim.x, hi = nvec * (blockIdx.x + 1) / gridDim.x;
+  auto locate = [&](size_t g, bool dst) -> char* {
+    const size_t i = g / per16;
+    size_t o = (g - i * per16) * 16;
+    const int u = miss_unit[i];
+    const size_t row = dst ? (size_t)unit_slot[u] : (size_t)__ldg(cd->host_row + unit_expert[u]);
+    const char* base;
+    size_t n;
+    if (o < gqe) {
+      base = dst ? (const char*)W.gate_q : (const char*)cd->gate_q, n = gqe;
+    } else if ((o -= gqe) < gse) {
+      base = dst ? (const char*)W.gate_s : (const char*)cd->gate_s, n = gse;
+    } else if ((o -= gse) < gqe) {
+      base = dst ? (const char*)W.up_q : (const char*)cd->up_q, n = gqe;
+    } else if ((o -= gqe) < gse) {
+      base = dst ? (const char*)W.up_s : (const char*)cd->up_s, n = gse;
+    } else if ((o -= gse) < dqe) {
+      base = dst ? (const char*)W.down_q : (const char*)cd->down_q, n = dqe;
+    } else if ((o -= dqe) < dse) {
+      base = dst ? (const char*)W.down_s : (const char*)cd->down_s, n = dse;
+    } else {
+      o -= dse;
+      base = dst ? (const char*)W.down_sb : (const char*)cd->down_sb, n = dse;
+    }
+    return const_cast<char*>(base) + row * n + o;
+  };
+  constexpr int kInFlight = 4;
+  for (size_t g0 = lo + tid; g0 < hi; g0 += (size_t)kInFlight * kDecodeThreads) {
+    uint4 val[kInFlight];
+#pragma unroll
+    for (int q = 0; q < kInFlight; ++q) {
+      const size_t g = g0 + (size_t)q * kDecodeThreads;
+      if (g < hi) val[q] = *reinterpret_cast<const uint4*>(locate(g, false));
+    }
+#pragma unroll
+    for (int q = 0; q < kInFlight; ++q) {
+      const size_t g = g0 + (size_t)q * kDecodeThreads;
+      if (g < hi) *reinterpret_cast<uint4*>(locate(g, true)) = val[q];
+    }
+  }
+}
+
 // kVar: some layer of the launch uses a routing variant (routing_flags != 0);
 // the default instantiation carries none of their code.
 template <int TT, bool kVar>
@@ -927,41 +983,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           }
           cta_sync();
         }
-        // the missed experts, from the host tier into their new slots: this
-        // CTA copies its 1/grid share of each of their seven tensors
+        // the missed experts, from the host tier into their new slots
         {
-          const size_t gqe = (size_t)F * (H / 2), gse = (size_t)F * C * 2;
-          const size_t dqe = (size_t)H * (F / 2), dse = (size_t)H * CF * 2;
-          for (int i = 0; i < n_miss; ++i) {
-            const int u = M.miss_unit[i];
-            const size_t hr = (size_t)__ldg(cd->host_row + M.unit_expert[u]);
-            const size_t v = (size_t)M.unit_slot[u];
-#pragma unroll 1
-            for (int t = 0; t < 7; ++t) {
-              const size_t n = (t == 0 || t == 2) ? gqe : (t == 1 || t == 3) ? gse : (t == 4) ? dqe : dse;
-              const char* sb = t == 0 ? (const char*)cd->gate_q : t == 1 ? (const char*)cd->gate_s
-                             : t == 2 ? (const char*)cd->up_q : t == 3 ? (const char*)cd->up_s
-                             : t == 4 ? (const char*)cd->down_q : t == 5 ? (const char*)cd->down_s
-                             : (const char*)cd->down_sb;
-              char* db = t == 0 ? (char*)W.gate_q : t == 1 ? (char*)W.gate_s : t == 2 ? (char*)W.up_q
-                       : t == 3 ? (char*)W.up_s : t == 4 ? (char*)W.down_q : t == 5 ? (char*)W.down_s
-                       : (char*)W.down_sb;
-              const uint4* s4 = reinterpret_cast<const uint4*>(sb + hr * n);
-              uint4* d4 = reinterpret_cast<uint4*>(db + v * n);
-              const size_t nv = n / 16;
-              const size_t lo = nv * blockIdx.x / grid, hi = nv * (blockIdx.x + 1) / grid;
-              size_t q = lo + tid;
-              for (; q + 3 * kDecodeThreads < hi; q += 4 * kDecodeThreads) {
-                const uint4 a = s4[q], b2 = s4[q + kDecodeThreads], c2 = s4[q + 2 * kDecodeThreads],
-                            d2 = s4[q + 3 * kDecodeThreads];
-                d4[q] = a;
-                d4[q + kDecodeThreads] = b2;
-                d4[q + 2 * kDecodeThreads] = c2;
-                d4[q + 3 * kDecodeThreads] = d2;
-              }
-              for (; q < hi; q += kDecodeThreads) d4[q] = s4[q];
-            }
-          }
+          copy_misses(cd, W, F, H, n_miss, M.miss_unit, M.unit_expert, M.unit_slot, tid);
           fence_proxy_async_global();  // the slots are read next by TMA
         }
         grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
