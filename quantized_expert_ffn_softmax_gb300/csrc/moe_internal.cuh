@@ -125,6 +125,7 @@ struct Workspace {
   float* gw = nullptr;          // [max_tokens] prefill: shared-expert gate weights
   // prefill
   __half* x16 = nullptr;        // [max_tokens][H] fp16, per-token scaled, K-permuted
+  __half* xg = nullptr;         // [max_tokens*k][H] x16 rows in bucket order (routed gate/up B)
   int32_t* xshift = nullptr;    // [max_tokens] per-token power-of-two shift
   float* zf = nullptr;          // [max_tokens][E] router logits
   int32_t* topk_ids = nullptr;  // [max_tokens][k]
@@ -151,6 +152,7 @@ struct moe_layer {
   moe_layer_config cfg;
   moe::LayerDev dev;
   CUtensorMap tmap_x16;      // x16 rows, box {64, 128}, 128B swizzle
+  CUtensorMap tmap_xg;       // xg rows, same box
   CUtensorMap tmap_hr;       // hmid_r rows, same box
   CUtensorMap tmap_hs;       // hmid_s rows, same box
   CUtensorMap tmap_wr16;     // wr16 rows [E][2H], box {64, 128}, 128B swizzle

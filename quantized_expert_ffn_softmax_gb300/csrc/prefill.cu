@@ -14,6 +14,8 @@
 //   bucket     stable counting sort of the (token, slot) assignments by
 //              expert in three launches (chunk counts, one-CTA scans and the
 //              work-unit lists, chunk scatter)
+//   gather     the x16 row of every assignment, copied into bucket order
+//              (operand B of the routed gate/up GEMM)
 //   gate/up    per unit (expert, 128-token tile, 128-row F tile):
 //              D_g, D_u = W_g/u[128 x H] . X[tokens]^T in TMEM, epilogue
 //              h = silu(g) * u -> fp16 rows of Hmid (bucket order)
@@ -25,19 +27,21 @@
 // GEMM engine: one persistent CTA per SM, warp-specialised.
 //   warps 0-3   epilogue (TMEM lanes 0-127 = the 128 rows of the tile)
 //   warps 4-11  A producers: dequantise 4-bit codes from the raw ring into
-//               fp16 128x64 tiles written into tensor memory (tcgen05.st);
-//               the router's A tiles come ready-made by TMA instead
-//   B loaders   gate/up: two warps gather the unit's token rows (bucket
-//               order) with per-thread 16-byte async copies into the
-//               128-byte swizzled K-major layout; down/router: one thread
-//               loads the unit's contiguous rows as one TMA tile per K step
-//   raw loader  one warp: TMA tiles of packed codes (128 rows x 32 bytes per
-//               matrix and K step) and the block scales into a raw ring
-//   last warp   TMEM allocator and single-thread tcgen05.mma issuer (A from
-//               tensor memory, B from shared memory)
+//               fp16 128x64 tiles written into tensor memory (tcgen05.st),
+//               each thread reading its own row's block scales from global
+//               memory four K steps per load; the router's A tiles come
+//               ready-made by TMA instead
+//   B loader    one thread loads the unit's contiguous token rows (bucket
+//               order; the shared expert's in token order) as one TMA tile
+//               per K step, 128-byte swizzled K-major
+//   raw loader  one thread: TMA tiles of packed codes (128 rows x 32 bytes
+//               per matrix and K step) into a raw ring
+//   MMA warps   one tcgen05.mma issuer thread per A matrix (gate and up: two
+//               warps; down, router: one), A from tensor memory, B from
+//               shared memory; the first also allocates TMEM
 // A stage ring (an A slot in TMEM and a B tile in shared memory per stage; 4
-// stages for gate/up, 8 for down) feeds the MMA, one tcgen05.commit per
-// step.  down keeps two TMEM accumulators so one unit's epilogue overlaps
+// stages for gate/up, 8 for down) feeds the MMAs, one tcgen05.commit per
+// step and issuer.  down keeps two TMEM accumulators so one unit's epilogue overlaps
 // the next unit's MMAs; gate/up has room for one gate|up accumulator, whose
 // epilogue stages the SwiGLU rows in shared memory and releases it early.
 // Every wait is bounded and gives up once the error word is set.
@@ -80,12 +84,9 @@ constexpr int kRawTile = 128 * 32; // bytes: 128 rows x 64 packed 4-bit codes
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp0 = 4;
 constexpr int kProdWarps = 8;
-constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBWarp0 = 12;
 constexpr int kBucketThreads = 1024;
 constexpr int kMaxBucketChunks = 256;  // chunks of assignments in the bucketing
-constexpr int kScaleLead = 3;      // K steps of block scales the raw loader loads ahead
-constexpr int kBLag = 2;           // K steps of gathered token rows each B loader keeps in flight
 
 enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 
@@ -97,11 +98,10 @@ enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 //   raw ring    SR stages of NA packed-code tiles, filled by TMA; the gate/up
 //               and down GEMMs dequantise from it (the router GEMM reads its
 //               fp32 weights directly and has no raw ring)
-// Warps after the epilogue (0-3) and A producers (4-11): B loaders (gate/up
-// gathers its token rows with two warps of per-thread async copies; down
-// and router load contiguous rows as one TMA tile per K step), the raw
-// loader, and the MMA issuer.  At most 16 warps, so that no SM
-// sub-partition holds more than four and a thread may use 128 registers.
+// Warps after the epilogue (0-3) and A producers (4-11): the B loader (one
+// TMA tile of contiguous token rows per K step), the raw loader, and the
+// MMA issuers.  At most 16 warps, so that no SM sub-partition holds more
+// than four and a thread may use 128 registers.
 template <int MODE>
 struct Gemm {
   // gate/up and down stage their dequantised A tiles in tensor memory (the
@@ -118,16 +118,22 @@ struct Gemm {
   static constexpr int kACols = NA * 32;     // 64 fp16 of K per matrix = 32 columns
   static_assert(kAccBufs * kAccCols <= kACol0, "accumulators below the A stages");
   static_assert(!kTmemA || kACol0 + S * kACols <= 512, "A stages fit in TMEM");
-  static constexpr int kBWarps = (MODE == kSwiglu) ? 2 : 1;
+  static constexpr int kBWarps = 1;
   static constexpr int kRawWarp = kBWarp0 + kBWarps;
+  // MMA issuers: one thread per A matrix, each in its own warp.  A thread
+  // needs about 50 cycles to issue one tcgen05.mma, and an M128 x N128 x K16
+  // MMA keeps the tensor core busy for 64: one thread issuing both the gate
+  // and the up MMAs of a K step, plus its waits and commit, leaves the
+  // tensor core idle a third of the time.  The first issuer warp also owns
+  // the TMEM allocation.
   static constexpr int kMmaWarp = kRawWarp + (SR > 0 ? 1 : 0);
-  static constexpr int kThreads = (kMmaWarp + 1) * 32;
-  static constexpr int kRawBytes = NA * (kRawTile + 128 * 4);  // codes, then scales
+  static constexpr int kThreads = (kMmaWarp + NA) * 32;
+  static constexpr int kRawBytes = NA * kRawTile;  // packed codes of the NA matrices
   static constexpr int kBOff = kTmemA ? 0 : NA * kTileA;       // B tile offset in a stage
   static constexpr int kStageBytes = kBOff + kTileB;
   static constexpr int OFF_RAW = S * kStageBytes;
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
-  static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 4) + 4) + 127) & ~127;
+  static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 6) + 4) + 127) & ~127;
   static constexpr int OFF_META = OFF_BAR + kBarBytes;
   // gate/up: the unit's SwiGLU rows staged as fp16 [128 tokens][128 f] so the
   // accumulator is released before the rows are written out
@@ -137,11 +143,9 @@ struct Gemm {
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(OFF_META % 16 == 0, "token factors are read as 16-byte vectors");
-  static_assert(MODE == kRouter || kBLag < S, "B loaders retire a step before reusing its slot");
-  // down producers take K steps in pairs (every K/64 is even: K is a
-  // multiple of 128), halving the per-step waits and fences; gate/up does
-  // more work per step and is faster one step at a time
-  static constexpr int kGroup = (MODE == kScatter) ? 2 : 1;
+  // producers take K steps in pairs (every K/64 is even: K is a multiple
+  // of 128), halving the per-step waits and fences
+  static constexpr int kGroup = (MODE == kRouter) ? 1 : 2;
   static_assert(MODE == kRouter || (S >= 2 * kGroup && SR >= 2 * kGroup), "ring depth per group");
 };
 
@@ -149,7 +153,7 @@ struct Gemm {
 struct GemmMaps {
   CUtensorMap a_routed[2];  // packed codes of the routed experts (gate, up | down)
   CUtensorMap a_shared[2];  // packed codes of the shared expert
-  CUtensorMap b[2];         // B rows: router x16 | down hmid_r, hmid_s
+  CUtensorMap b[2];         // B rows, routed | shared: gate/up xg, x16; down hmid_r, hmid_s; router x16
 };
 
 struct GemmParams {
@@ -221,6 +225,35 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// First block scale of weight row r of a unit's 128-row tile, for the
+// matrix a producer thread dequantises (gate/up: part = matrix).
+template <int MODE>
+__device__ __forceinline__ const uint16_t* scale_row(const GemmParams& p, const UnitInfo& U, int part, int r) {
+  const LayerDev& W = p.W;
+  const int slot = U.shared ? 0 : __ldg(W.slot_of + U.e);
+  const size_t C = (size_t)(U.K / 32);
+  if (MODE == kSwiglu) {
+    const size_t row = (U.shared ? 0 : (size_t)slot * p.F) + (size_t)U.mt * 128 + r;
+    const uint16_t* base = part ? (U.shared ? W.sh_up_s : W.up_s) : (U.shared ? W.sh_gate_s : W.gate_s);
+    return base + row * C;
+  }
+  const size_t row = (U.shared ? 0 : (size_t)slot * p.H) + (size_t)U.mt * 128 + r;
+  return (U.shared ? W.sh_down_s : W.down_s) + row * C;
+}
+
+// The scale words (two fp16 each) of K steps s0..s0+3 of one row: one
+// 16-byte load when aligned and whole, else one word per step that exists.
+__device__ __forceinline__ uint4 load_scale_quad(const uint16_t* srow, int s0, int nks) {
+  const uint16_t* q = srow + 2 * s0;
+  if (s0 + 4 <= nks && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(q));
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(q);
+  uint4 v = make_uint4(__ldg(w), 0u, 0u, 0u);
+  if (s0 + 1 < nks) v.y = __ldg(w + 1);
+  if (s0 + 2 < nks) v.z = __ldg(w + 2);
+  if (s0 + 3 < nks) v.w = __ldg(w + 3);
+  return v;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ GemmMaps maps) {
@@ -238,7 +271,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
   uint64_t* raw_empty = raw_full + G::SRb;
   uint64_t* tfull = raw_empty + G::SRb;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tdrain = tempty + 2;  // per MMA issuer: its own MMAs are complete (error path)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tdrain + 2);
   // per-unit token metadata of the epilogue: two words per token column
   int* meta_i = reinterpret_cast<int*>(smem + G::OFF_META);
   float* meta_f = reinterpret_cast<float*>(meta_i + kNT);
@@ -247,17 +281,18 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_a[s], kProdThreads);
-      mbar_init(&full_b[s], MODE == kSwiglu ? G::kBWarps * 32 : 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full_a[s], kProdWarps);
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty[s], NA);  // one commit per MMA issuer
     }
     for (int s = 0; s < SR; ++s) {
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kProdWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
+      mbar_init(&tfull[b], NA);
       mbar_init(&tempty[b], kEpiWarps * 32);
+      mbar_init(&tdrain[b], 1);
     }
     fence_mbar_init();
   }
@@ -426,278 +461,210 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     uint32_t it = 0;
     bool alive = true;
     // (the router GEMM has no A producers: its A tiles arrive by TMA)
-    for (int u = blockIdx.x; u < n_units && alive && MODE != kRouter; u += gridDim.x) {
-      const UnitInfo U = unit_info<MODE>(p, u);
-      const int nks = U.K / 64;
-      if constexpr (MODE != kRouter) {
-        // Codes and block scales come from the raw ring, filled by the raw
-        // loader warp (codes: one TMA tile per matrix; scales: one 32-bit
-        // word per row holding the step's two fp16 block scales).
-        //   gate/up: part = matrix, all 64 K of the step
-        //   down:    part = which 32-element half of the step
-        // thread = (part, row r), r = 32*(warp%4) + lane: the TMEM lane it
-        // writes (a warp reaches only its own quarter of the 128 lanes)
-        const int r = 32 * (warp & 3) + lane;
-        const int part = pi >> 7;
-        const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
-        // K steps go in groups of P (nks is even): one set of waits, one
-        // proxy fence and one round of hand-backs per group
-        constexpr int P = G::kGroup;
-        for (int ks = 0; ks < nks && alive; ks += P) {
-          bool ok = true;
-          uint4 ca[P], cb[P];
-          uint32_t sw[P];  // each step's two block scales of this row
+    if constexpr (MODE != kRouter) {
+      // thread = (part, row r), r = 32*(warp%4) + lane: the TMEM lane it
+      // writes (a warp reaches only its own quarter of the 128 lanes)
+      //   gate/up: part = matrix, all 64 K of the step
+      //   down:    part = which 32-element half of the step
+      // Codes come from the raw ring (one TMA tile per matrix and step).
+      // K steps go in groups of P (nks is even): one set of waits and one
+      // round of hand-backs per group.  Per group: the raw stages' words
+      // into registers (every lane waits for the stage itself, so that its
+      // own reads follow the TMA's completion), the raw stages handed back
+      // at once (the arrive orders the reads before the refill), the
+      // dequantisation, and only then the wait for free A stages: the
+      // dequantisation overlaps the MMAs still reading them.
+      const int r = 32 * (warp & 3) + lane;
+      const int part = pi >> 7;
+      const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
+      constexpr int P = G::kGroup;
+      constexpr int OW = (MODE == kSwiglu) ? 32 : 16;  // TMEM columns per thread and step
+      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        const int nks = U.K / 64;
+        // this row's block scales, one 32-bit word (two fp16) per K step,
+        // read four steps at a time, a quad ahead of their use
+        const uint16_t* srow = scale_row<MODE>(p, U, part, r);
+        uint4 sq = load_scale_quad(srow, 0, nks);
+        for (int ks0 = 0; ks0 < nks && alive; ks0 += 4) {
+          const uint4 sn = (ks0 + 4 < nks) ? load_scale_quad(srow, ks0 + 4, nks) : sq;
+          const uint32_t sqw[4] = {sq.x, sq.y, sq.z, sq.w};
 #pragma unroll
-          for (int q = 0; q < P; ++q) {
-            const uint32_t iq = it + q;
-            const int sr = iq % SR;
-            if (lane == 0 && ok) ok = mbar_wait(&raw_full[sr], (iq / SR) & 1, p.err, tmo);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok) {
-              (void)mbar_test(&raw_full[sr], (iq / SR) & 1);  // every lane acquires
-              const unsigned char* rs = sR + sr * G::kRawBytes;
-              sw[q] = reinterpret_cast<const uint32_t*>(rs + NA * kRawTile)[(MODE == kSwiglu ? part * 128 : 0) + r];
+          for (int dd = 0; dd < 4; dd += P) {
+            if (ks0 + dd >= nks || !alive) break;
+            bool ok = true;
+            uint4 ca[P], cb[P];
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+              const uint32_t iq = it + q;
+              const int sr = iq % SR;
+              if (ok) ok = mbar_wait(&raw_full[sr], (iq / SR) & 1, p.err, tmo);
+              ok = __all_sync(0xffffffffu, ok);
+              if (ok) {
+                const unsigned char* rs = sR + sr * G::kRawBytes;
+                if (MODE == kSwiglu) {
+                  const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
+                  const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
+                  ca[q] = h ? q1 : q0;
+                  cb[q] = h ? q0 : q1;
+                } else {
+                  ca[q] = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
+                  cb[q] = ca[q];
+                }
+              }
+            }
+            if (!ok) {
+              alive = false;
+              break;
+            }
+            __syncwarp();
+            if (lane == 0)
+#pragma unroll
+              for (int q = 0; q < P; ++q) mbar_arrive(&raw_empty[(it + q) % SR]);
+            uint32_t o[P][OW];
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
               if (MODE == kSwiglu) {
-                const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
-                ca[q] = h ? q1 : q0;
-                cb[q] = h ? q0 : q1;
+                const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] & 0xffffu)));
+                const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] >> 16)));
+                const uint32_t wds[8] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w,
+                                         cb[q].x, cb[q].y, cb[q].z, cb[q].w};
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                  const uint4 d = dequant_word(wds[w], w < 4 ? slo : shi);
+                  o[q][4 * w] = d.x;
+                  o[q][4 * w + 1] = d.y;
+                  o[q][4 * w + 2] = d.z;
+                  o[q][4 * w + 3] = d.w;
+                }
               } else {
-                ca[q] = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
-                cb[q] = ca[q];
+                const __half2 s2 =
+                    __half2half2(__ushort_as_half((uint16_t)(part ? sqw[dd + q] >> 16 : sqw[dd + q] & 0xffffu)));
+                const uint32_t wds[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const uint4 d = dequant_word(wds[w], s2);
+                  o[q][4 * w] = d.x;
+                  o[q][4 * w + 1] = d.y;
+                  o[q][4 * w + 2] = d.z;
+                  o[q][4 * w + 3] = d.w;
+                }
               }
             }
-          }
 #pragma unroll
-          for (int q = 0; q < P; ++q) {
-            const uint32_t iq = it + q;
-            if (lane == 0 && ok) ok = mbar_wait(&empty[iq % S], ((iq / S) & 1) ^ 1, p.err, tmo);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-          }
-          if (!ok) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();  // the MMAs that read these A stages are complete
-          const uint32_t arow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)G::kACol0;
-#pragma unroll
-          for (int q = 0; q < P; ++q) {
-            const uint32_t acol = arow + (uint32_t)(((it + q) % S) * G::kACols);
-            if (MODE == kSwiglu) {
-              const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sw[q] & 0xffffu)));
-              const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sw[q] >> 16)));
-              const uint32_t wds[8] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w,
-                                       cb[q].x, cb[q].y, cb[q].z, cb[q].w};
-              uint32_t o[32];
-#pragma unroll
-              for (int w = 0; w < 8; ++w) {
-                const uint4 d = dequant_word(wds[w], w < 4 ? slo : shi);
-                o[4 * w] = d.x;
-                o[4 * w + 1] = d.y;
-                o[4 * w + 2] = d.z;
-                o[4 * w + 3] = d.w;
-              }
-              tmem_st32(acol + (uint32_t)(part * 32), o);
-            } else {
-              const __half2 s2 =
-                  __half2half2(__ushort_as_half((uint16_t)(part ? sw[q] >> 16 : sw[q] & 0xffffu)));
-              const uint32_t wds[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
-              uint32_t o[16];
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const uint4 d = dequant_word(wds[w], s2);
-                o[4 * w] = d.x;
-                o[4 * w + 1] = d.y;
-                o[4 * w + 2] = d.z;
-                o[4 * w + 3] = d.w;
-              }
-              tmem_st16(acol + (uint32_t)(part * 16), o);
+            for (int q = 0; q < P; ++q) {
+              const uint32_t iq = it + q;
+              if (lane == 0 && ok) ok = mbar_wait(&empty[iq % S], ((iq / S) & 1) ^ 1, p.err, tmo);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
             }
+            if (!ok) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();  // the MMAs that read these A stages are complete
+            const uint32_t arow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)G::kACol0;
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+              const uint32_t acol = arow + (uint32_t)(((it + q) % S) * G::kACols) + (uint32_t)(part * OW);
+              if constexpr (OW == 32)
+                tmem_st32(acol, o[q]);
+              else
+                tmem_st16(acol, o[q]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();  // the warp's stores are complete: one arrive for the warp
+            if (lane == 0)
+#pragma unroll
+              for (int q = 0; q < P; ++q) mbar_arrive(&full_a[(it + q) % S]);
+            it += P;
           }
-          tmem_wait_st();
-          tc_fence_before();
-#pragma unroll
-          for (int q = 0; q < P; ++q) mbar_arrive(&full_a[(it + q) % S]);
-          // the raw stages were read through the generic proxy and are
-          // refilled by TMA (async proxy): fence before handing them back
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < P; ++q) mbar_arrive(&raw_empty[(it + q) % SR]);
-          it += P;
+          sq = sn;
         }
       }
     }
   } else if (warp < G::kRawWarp) {
-    // ------------------------------------------------------------ B loaders
+    // ------------------------------------------------------------ B loader
+    // One TMA tile (kNT rows x 64 fp16) per K step at the unit's first row:
+    // gate/up reads the bucket-ordered copy of x16 (routed units) or x16
+    // (shared expert), down the SwiGLU rows, the router x16 and, on the
+    // same barrier, its A tile.  Rows past a unit's end belong to the next
+    // unit (or read as zero past the buffer); their columns are discarded.
     uint32_t it = 0;
     bool alive = true;
-    if (MODE == kSwiglu) {
-      // lane l of B warp bw copies 16-byte chunk (l & 7) of rows
-      // bw*RW + 4i + (l >> 3), i < RW/4: every warp instruction moves four
-      // whole 128-byte rows.  A thread's copies of K step j form one async
-      // group; it retires step j (wait, proxy fence, arrive) kBLag steps later.
-      constexpr int RW = kNT / G::kBWarps;  // rows per warp
-      const int bw = warp - kBWarp0;
-      const int c = lane & 7;
+    if (lane == 0) {
+      const int kpp = p.H / 64;
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
         const UnitInfo U = unit_info<MODE>(p, u);
-        const int neff = (U.n + 15) & ~15;
-        uint32_t src[RW / 4];  // element offset of the chunk in x16
-        uint32_t dst[RW / 4];  // byte offset in the B tile, or ~0 if not loaded
-#pragma unroll
-        for (int i = 0; i < RW / 4; ++i) {
-          const int row = bw * RW + 4 * i + (lane >> 3);
-          int t = row < U.n ? row : U.n - 1;  // padding rows repeat a valid row
-          const int tok = U.shared ? (U.p0 + t) : __ldg(p.perm_tok + U.p0 + t);
-          src[i] = (uint32_t)tok * (uint32_t)p.H + (uint32_t)(c * 8);
-          dst[i] = (row < neff) ? (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4)) : 0xffffffffu;
-        }
+        const CUtensorMap* tm = (MODE == kRouter) ? &maps.b[0] : &maps.b[U.shared ? 1 : 0];
         const int nks = U.K / 64;
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int st = it % S;
-          bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
+          if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo)) {
             alive = false;
             break;
           }
-          const uint32_t tile = smem_u32(smem + st * G::kStageBytes + G::kBOff);
-#pragma unroll
-          for (int i = 0; i < RW / 4; ++i)
-            if (dst[i] != 0xffffffffu) cp_async_16(tile + dst[i], p.x16 + src[i] + ks * 64);
-          cp_async_commit();
-          if (it >= (uint32_t)kBLag) {
-            cp_async_wait<kBLag>();
-            fence_proxy_async_smem();
-            mbar_arrive(&full_b[(it - kBLag) % S]);
+          if (MODE == kRouter) {
+            // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
+            mbar_expect_tx(&full_b[st], (uint32_t)(kTileA + kTileB));
+            tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, &full_b[st]);
+          } else {
+            mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
           }
+          const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
+          tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, &full_b[st]);
         }
       }
-      // every copy lands before the CTA can exit; retire the last steps
-      cp_async_wait<0>();
-      if (alive) {
-        fence_proxy_async_smem();
-        for (uint32_t q = it > (uint32_t)kBLag ? it - kBLag : 0u; q < it; ++q)
-          mbar_arrive(&full_b[q % S]);
-      }
-    } else {
+      // let every copy this thread issued land before the CTA can exit
+      const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+      for (uint32_t q = first; q < it; ++q) drain_wait(&full_b[q % S], (q / S) & 1, tmo);
+    }
+    __syncwarp();
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ raw loader
+    // Per K step: one TMA tile of packed codes (128 rows x 32 bytes) per
+    // matrix into the raw ring.  (The block scales are read by the
+    // producers themselves, four K steps per load.)
+    if constexpr (SR > 0) {
       if (lane == 0) {
-        const int kpp = p.H / 64;
+        uint32_t it = 0;
+        bool alive = true;
+        const LayerDev& Wd = p.W;
         for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
           const UnitInfo U = unit_info<MODE>(p, u);
-          const CUtensorMap* tm = (MODE == kScatter) ? &maps.b[U.shared ? 1 : 0] : &maps.b[0];
+          const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
+          const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
+          const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * 128;
+          const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
+          const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
           const int nks = U.K / 64;
           for (int ks = 0; ks < nks; ++ks, ++it) {
-            const int st = it % S;
-            if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo)) {
+            const int sr = it % SR;
+            if (!mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo)) {
               alive = false;
               break;
             }
-            if (MODE == kRouter) {
-              // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
-              mbar_expect_tx(&full_b[st], (uint32_t)(kTileA + kTileB));
-              tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, &full_b[st]);
-            } else {
-              mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
-            }
-            const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-            tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, &full_b[st]);
+            unsigned char* dst = sR + sr * G::kRawBytes;
+            mbar_expect_tx(&raw_full[sr], (uint32_t)(NA * kRawTile));
+            tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
+            if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
           }
         }
-        // let every copy this thread issued land before the CTA can exit
-        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-        for (uint32_t q = first; q < it; ++q) drain_wait(&full_b[q % S], (q / S) & 1, tmo);
-      }
-      __syncwarp();
-    }
-  } else if (warp < kMmaWarp) {
-    // ------------------------------------------------------------ raw loader
-    // Per K step and matrix: lane 0 issues one TMA tile of packed codes (128
-    // rows x 32 bytes); every lane stages the block scales of four rows (one
-    // 32-bit word per row: the step's two fp16 scales) from a register ring
-    // loaded kScaleLead steps ahead.  The scale stores precede lane 0's
-    // arrive on raw_full, which publishes them together with the codes.
-    if constexpr (SR > 0) {
-      uint32_t it = 0;
-      bool alive = true;
-      const LayerDev& Wd = p.W;
-      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
-        const UnitInfo U = unit_info<MODE>(p, u);
-        const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
-        const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
-        const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * 128;
-        const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
-        const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
-        const int C = U.K / 32;  // scales per weight row
-        const uint16_t* sb[NA];  // this lane's first row of scales, per matrix
-        if (MODE == kSwiglu) {
-          sb[0] = (U.shared ? Wd.sh_gate_s : Wd.gate_s) + ((size_t)row + lane) * C;
-          if (NA == 2) sb[NA - 1] = (U.shared ? Wd.sh_up_s : Wd.up_s) + ((size_t)row + lane) * C;
-        } else {
-          sb[0] = (U.shared ? Wd.sh_down_s : Wd.down_s) + ((size_t)row + lane) * C;
-        }
-        const size_t rstep = (size_t)32 * C;  // 32 rows further
-        const int nks = U.K / 64;
-        uint32_t sv[kScaleLead][NA * 4];
-#pragma unroll
-        for (int d = 0; d < kScaleLead; ++d)
-          if (d < nks)
-#pragma unroll
-            for (int m = 0; m < NA; ++m)
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                sv[d][m * 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(sb[m] + j * rstep + 2 * d));
-        for (int ks0 = 0; ks0 < nks && alive; ks0 += kScaleLead) {
-#pragma unroll
-          for (int d = 0; d < kScaleLead; ++d) {
-            const int ks = ks0 + d;
-            if (ks < nks && alive) {
-              const int sr = it % SR;
-              bool ok = true;
-              if (lane == 0) ok = mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
-              if (!ok) {
-                alive = false;
-              } else {
-                unsigned char* dst = sR + sr * G::kRawBytes;
-                uint32_t* sdst = reinterpret_cast<uint32_t*>(dst + NA * kRawTile);
-#pragma unroll
-                for (int m = 0; m < NA; ++m)
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) sdst[m * 128 + j * 32 + lane] = sv[d][m * 4 + j];
-                __syncwarp();
-                if (lane == 0) {
-                  mbar_expect_tx(&raw_full[sr], (uint32_t)(NA * kRawTile));
-                  tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
-                  if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
-                }
-                ++it;
-                const int kn = ks + kScaleLead;
-                if (kn < nks)
-#pragma unroll
-                  for (int m = 0; m < NA; ++m)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                      sv[d][m * 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(sb[m] + j * rstep + 2 * kn));
-              }
-            }
-          }
-        }
-      }
-      if (lane == 0) {
         const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
         for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
       }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer m (warp kMmaWarp + m, lane 0) issues the MMAs of A matrix m
+    // (gate or up; the only matrix of down and router) into accumulator
+    // column block m.  Both wait for the same stages; a stage is released,
+    // and an accumulator published, when every issuer has committed.
+    const int m = warp - kMmaWarp;
     if (lane == 0) {
       uint32_t it = 0;
-      int j = 0, committed = -1;
+      int j = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
         const UnitInfo U = unit_info<MODE>(p, u);
         const int neff = (U.n + 15) & ~15;
@@ -705,7 +672,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
         if (!mbar_wait(&tempty[b], tpar ^ 1, p.err, tmo)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(b * G::kAccCols), d1 = d0 + 128;
+        const uint32_t d = tmem + (uint32_t)(b * G::kAccCols + 128 * m);
         const uint32_t idesc = idesc_f16_m128(neff);
         const int nks = U.K / 64;
         bool ok = true;
@@ -721,34 +688,26 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           const uint32_t s_addr = smem_u32(smem + st * G::kStageBytes);
           const uint64_t db = smem_desc_sw128(s_addr + G::kBOff);
           if constexpr (G::kTmemA) {
-            const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols);
+            const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols + 32 * m);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // 16 K = 8 TMEM columns per MMA
-              const uint32_t acc = (ks | kk) ? 1u : 0u;
-              umma_f16_ts(d0, a0 + 8 * kk, db + 2 * kk, idesc, acc);
-              if (NA == 2) umma_f16_ts(d1, a0 + 32 + 8 * kk, db + 2 * kk, idesc, acc);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // 16 K = 8 TMEM columns per MMA
+              umma_f16_ts(d, a0 + 8 * kk, db + 2 * kk, idesc, (ks | kk) ? 1u : 0u);
           } else {
             const uint64_t da0 = smem_desc_sw128(s_addr);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t acc = (ks | kk) ? 1u : 0u;
-              umma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            }
+            for (int kk = 0; kk < 4; ++kk) umma_f16(d, da0 + 2 * kk, db + 2 * kk, idesc, (ks | kk) ? 1u : 0u);
           }
           umma_commit(&empty[st]);
         }
         if (!ok) break;
         umma_commit(&tfull[b]);
-        committed = j;
       }
       // Normally the epilogue has consumed every committed accumulator.  On
-      // an error path, wait (bounded) for the last commit so that no MMA is
-      // still writing TMEM when it is released.
-      if (committed >= 0 && ld_relaxed_i32(p.err) != 0) {
-        const int cb = (G::kAccBufs == 2) ? (committed & 1) : 0;
-        const uint32_t cp = (G::kAccBufs == 2) ? ((committed >> 1) & 1) : (committed & 1);
-        drain_wait(&tfull[cb], cp, tmo);
+      // an error path, wait (bounded) until this thread's MMAs are complete,
+      // so that none still writes TMEM when it is released.
+      if (ld_relaxed_i32(p.err) != 0) {
+        umma_commit(&tdrain[m]);
+        drain_wait(&tdrain[m], 0, tmo);
       }
     }
     __syncwarp();
@@ -1017,6 +976,24 @@ __global__ void __launch_bounds__(kBucketThreads, 1) bucket_scan_kernel(const Bu
 }
 
 // y (bf16) = yacc (fp32): scalar version for a y that is not 16-byte aligned.
+// Operand B of the routed gate/up GEMM: the x16 row of every bucketed
+// (token, expert) assignment, copied into bucket order so that a unit's K
+// step is one TMA tile.  One warp per row, 16-byte copies.
+__global__ void gather_rows_kernel(const __half* __restrict__ x16, const int32_t* __restrict__ perm_tok,
+                                   int n_rows, int T, int H, __half* __restrict__ xg) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int chunks = H / 8;  // 16-byte chunks per row
+  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < n_rows; p += nwarps) {
+    int tok = __ldg(perm_tok + p);
+    if ((unsigned)tok >= (unsigned)T) tok = 0;  // cannot happen after a clean bucketing
+    const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)tok * H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
+#pragma unroll 8
+    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
 __global__ void finalize_scalar_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(yacc[i]));
@@ -1069,7 +1046,7 @@ __global__ void router_split_kernel(const float* __restrict__ wr, int E, int H, 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillSizes {
-  size_t x16, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16,
+  size_t x16, xg, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16,
       ccount;
   int max_gu, max_dn;
   static PrefillSizes make(const moe_layer_config& c) {
@@ -1082,6 +1059,7 @@ struct PrefillSizes {
     s.max_gu = (int)(routed_tiles * (F / 128) + shared_tiles * (Fs / 128));
     s.max_dn = (int)((routed_tiles + shared_tiles) * (H / 128));
     s.x16 = Tm * H * 2;
+    s.xg = Tk * H * 2;
     s.xshift = Tm * 4;
     s.zf = Tm * E * 4;
     s.ids = Tk * 4;
@@ -1100,7 +1078,7 @@ struct PrefillSizes {
     return s;
   }
   size_t total() const {
-    return align256(x16) + align256(xshift) + align256(zf) + align256(ids) + align256(w) +
+    return align256(x16) + align256(xg) + align256(xshift) + align256(zf) + align256(ids) + align256(w) +
            align256(offsets) + align256(perm_tok) + align256(perm_w) + align256(gu) + align256(dn) +
            align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc) + align256(wr16) +
            align256(ccount);
@@ -1154,7 +1132,8 @@ moe_status launch_gemm(const GemmParams& gp, moe_layer* L, int grid, cudaStream_
     maps.a_routed[1] = L->tmap_up;
     maps.a_shared[0] = L->tmap_sh_gate;
     maps.a_shared[1] = L->tmap_sh_up;
-    maps.b[0] = maps.b[1] = L->tmap_x16;  // unused: gate/up gathers with cp.async
+    maps.b[0] = L->tmap_xg;
+    maps.b[1] = L->tmap_x16;
   } else if (MODE == kScatter) {
     maps.a_routed[0] = maps.a_routed[1] = L->tmap_down;
     maps.a_shared[0] = maps.a_shared[1] = L->tmap_sh_down;
@@ -1188,6 +1167,7 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   };
   Workspace& w = L->ws;
   w.x16 = (__half*)take(z.x16);
+  w.xg = (__half*)take(z.xg);
   w.xshift = (int32_t*)take(z.xshift);
   w.zf = (float*)take(z.zf);
   w.topk_ids = (int32_t*)take(z.ids);
@@ -1212,6 +1192,7 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   const uint64_t S = c.n_slots, H = c.hidden, F = c.ffn;
   const bool sh = c.shared_ffn > 0;
   if (!encode_rows(&L->tmap_x16, w.x16, c.hidden, Tm) ||
+      !encode_rows(&L->tmap_xg, w.xg, c.hidden, Tm * c.top_k) ||
       !encode_rows(&L->tmap_hr, w.hmid_r, c.ffn, Tm * c.top_k) ||
       !encode_rows(&L->tmap_hs, w.hmid_s, Fs, Tm) ||
       !encode_codes(&L->tmap_gate, d.gate_q, H / 2, S * F) ||
@@ -1509,6 +1490,13 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   {
     prof::Scope sc("moe_bucket_scatter", s);
     bucket_scatter_kernel<<<bp.nc, 32, sizeof(int) * E, s>>>(bp);
+  }
+
+  {
+    prof::Scope sc("moe_gather_rows", s);
+    const int rows = T * k;
+    const int blocks = std::max(1, std::min((rows + 7) / 8, 8 * L->num_sms));
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(ws.x16, ws.perm_tok, rows, T, H, ws.xg);
   }
 
   if (L->dev.cache) {
