@@ -832,7 +832,8 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
     if (st != MOE_OK) return st;
   } else {
     // prefill-sized stack, layer by layer.  Each layer boundary is one
-    // kernel: the previous layer's fp32 output becomes the residual
+    // kernel: the sum of the previous layer's partial output rows, y_l,
+    // becomes the residual
     // h_{l+1} = bf16(h_l + bf16(y_l)), then u_{l+1} = rmsnorm(h_{l+1}) and its
     // fp16 operand rows go straight into the next layer's workspace.  h
     // ping-pongs between two staging buffers (or lands in the h trace).
@@ -853,12 +854,12 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
       const uint16_t* u_l = it ? it + (size_t)l * n : U;
       st = moe::launch_prefill(layers[l], u_l, n_tokens, nullptr,
                                ids_trace ? ids_trace + (size_t)l * n_tokens * k : nullptr, nullptr,
-                               false, s, &why, /*prepped=*/true, /*keep_yacc=*/true);
+                               false, s, &why, /*prepped=*/true, /*keep_parts=*/true);
       if (st != MOE_OK) return fail(st, "prefill layer %d: %s", l, why);
       const bool last = l == n_layers - 1;
       moe_layer* next = last ? nullptr : layers[l + 1];
       uint16_t* dst = ht ? ht + (size_t)l * n : (last ? sg.y : (cur == P ? Q : P));
-      st = moe::launch_stack_boundary(next, cur, layers[l]->ws.yacc, n_tokens, H, dst,
+      st = moe::launch_stack_boundary(next, cur, layers[l], n_tokens, H, dst,
                                       yt ? yt + (size_t)l * n : nullptr,
                                       next ? (it ? it + (size_t)(l + 1) * n : U) : nullptr, s, &why);
       if (st != MOE_OK) return fail(st, "layer %d boundary: %s", l, why);

@@ -125,7 +125,10 @@ struct Workspace {
   float* gw = nullptr;          // [max_tokens] prefill: shared-expert gate weights
   // prefill
   __half* x16 = nullptr;        // [max_tokens][H] fp16, per-token scaled, K-permuted
-  __half* xg = nullptr;         // [max_tokens*k][H] x16 rows in bucket order (routed gate/up B)
+  // [max_tokens*(k+1)][H]: x16 rows in bucket order (operand B of the routed
+  // gate/up GEMM); after it, the down GEMM's weighted output rows (routed in
+  // bucket order, then the shared expert's in token order)
+  __half* xg = nullptr;
   int32_t* xshift = nullptr;    // [max_tokens] per-token power-of-two shift
   float* zf = nullptr;          // [max_tokens][E] router logits
   int32_t* topk_ids = nullptr;  // [max_tokens][k]
@@ -133,12 +136,12 @@ struct Workspace {
   int32_t* offsets = nullptr;   // [E+1] bucket offsets
   int32_t* perm_tok = nullptr;  // [max_tokens*k] token of each bucketed row
   float* perm_w = nullptr;      // [max_tokens*k] routing weight of each bucketed row
+  int32_t* pos = nullptr;       // [max_tokens*k] bucket position of each (token, slot), -1 if none
   int4* gu_units = nullptr;     // gate/up work units
   int4* dn_units = nullptr;     // down work units
   int32_t* n_units = nullptr;   // [2] counts of the two lists
   __half* hmid_r = nullptr;     // [max_tokens*k][F] routed SwiGLU output (bucket order)
   __half* hmid_s = nullptr;     // [max_tokens][Fs] shared-expert SwiGLU output
-  float* yacc = nullptr;        // [max_tokens][H] fp32 combine accumulator
   __half* wr16 = nullptr;       // [E][2H] router weights * 2^shift as fp16 hi | mid terms
   int32_t* ccount = nullptr;    // [chunks][E] bucketing counts / chunk bases
   int max_gu_units = 0, max_dn_units = 0;
@@ -208,14 +211,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 moe_status decode_prepare(moe_layer* L, const char** why);
 // prefill.cu
 // prepped: the layer's fp16 operand rows (ws.x16/xshift) already hold x;
-// keep_yacc: leave the output in the fp32 accumulator ws.yacc (y unused)
+// keep_parts: leave the output as the down GEMM's weighted partial rows (y
+// unused), for launch_stack_boundary to sum
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
                           float* w_out, bool route_only, cudaStream_t stream, const char** why,
-                          bool prepped = false, bool keep_yacc = false);
-// Layer boundary of a prefill-sized stack: h_out = bf16(h + bf16(yacc))
-// (h_out = h when yacc is null), and for the next layer (null after the
+                          bool prepped = false, bool keep_parts = false);
+// Layer boundary of a prefill-sized stack: y = the sum of prev's partial
+// output rows (launch_prefill with keep_parts), h_out = bf16(h + bf16(y))
+// (h_out = h when prev is null), and for the next layer (null after the
 // last) u = rmsnorm(h_out) and its fp16 operand rows in next's workspace.
-moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const float* yacc, int T,
+moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const moe_layer* prev, int T,
                                  int H, uint16_t* h_out, uint16_t* y_trace, uint16_t* u,
                                  cudaStream_t s, const char** why);
 size_t prefill_workspace_bytes(const moe_layer_config& c);

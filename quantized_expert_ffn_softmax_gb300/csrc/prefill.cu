@@ -19,10 +19,13 @@
 //   gate/up    per unit (expert, 128-token tile, 128-row F tile):
 //              D_g, D_u = W_g/u[128 x H] . X[tokens]^T in TMEM, epilogue
 //              h = silu(g) * u -> fp16 rows of Hmid (bucket order)
-//   down       per unit (expert, token tile, 128-row H tile):
-//              D = W_d[128 x F] . Hmid[tokens]^T, epilogue y += w * D
-//              scattered to the tokens' rows (fp32 reductions in L2)
-//   finalize   y (fp32) -> bf16
+//   down       per unit (expert, token tile, 256-row H tile as two 128-row
+//              A matrices): D = W_d[256 x F] . Hmid[tokens]^T, epilogue
+//              w * D as fp16 rows of a partial-output buffer (bucket order;
+//              the shared expert's rows after the routed ones, in token
+//              order)
+//   combine    per token, the sum of its k + 1 partial rows -> bf16 y (in a
+//              prefill-sized stack, inside the layer-boundary kernel)
 //
 // GEMM engine: one persistent CTA per SM, warp-specialised.
 //   warps 0-3   epilogue (TMEM lanes 0-127 = the 128 rows of the tile)
@@ -36,14 +39,13 @@
 //               per K step, 128-byte swizzled K-major
 //   raw loader  one thread: TMA tiles of packed codes (128 rows x 32 bytes
 //               per matrix and K step) into a raw ring
-//   MMA warps   one tcgen05.mma issuer thread per A matrix (gate and up: two
-//               warps; down, router: one), A from tensor memory, B from
+//   MMA warps   one tcgen05.mma issuer thread per A matrix (gate/up and
+//               down: two warps; router: one), A from tensor memory, B from
 //               shared memory; the first also allocates TMEM
-// A stage ring (an A slot in TMEM and a B tile in shared memory per stage; 4
-// stages for gate/up, 8 for down) feeds the MMAs, one tcgen05.commit per
-// step and issuer.  down keeps two TMEM accumulators so one unit's epilogue overlaps
-// the next unit's MMAs; gate/up has room for one gate|up accumulator, whose
-// epilogue stages the SwiGLU rows in shared memory and releases it early.
+// A stage ring (the A slots in TMEM and a B tile in shared memory per stage,
+// 4 stages) feeds the MMAs, one tcgen05.commit per step and issuer.  The two
+// 128-column accumulators fill TMEM's lower half; the epilogue stages the
+// unit's output rows in shared memory and releases them early.
 // Every wait is bounded and gives up once the error word is set.
 #include <cudaTypedefs.h>
 #include <stdlib.h>
@@ -108,11 +110,12 @@ struct Gemm {
   // MMA reads A from TMEM, B from shared memory); the router keeps A in
   // shared memory.  TMEM columns: accumulators from 0, A stages from kACol0.
   static constexpr bool kTmemA = (MODE != kRouter);
-  static constexpr int NA = (MODE == kSwiglu) ? 2 : 1;
-  static constexpr int S = (MODE == kSwiglu) ? 4 : (MODE == kScatter ? 8 : 6);
-  static constexpr int SR = (MODE == kSwiglu) ? 12 : (MODE == kScatter ? 12 : 0);
+  // A matrices per unit: gate and up, or two 128-row tiles of W_d
+  static constexpr int NA = (MODE == kRouter) ? 1 : 2;
+  static constexpr int S = (MODE == kRouter) ? 6 : 4;
+  static constexpr int SR = (MODE == kRouter) ? 0 : 12;
   static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
-  static constexpr int kAccBufs = (MODE == kSwiglu) ? 1 : 2;
+  static constexpr int kAccBufs = (MODE == kRouter) ? 2 : 1;
   static constexpr int kAccCols = NA * 128;  // gate | up, or one accumulator
   static constexpr int kACol0 = 256;
   static constexpr int kACols = NA * 32;     // 64 fp16 of K per matrix = 32 columns
@@ -135,9 +138,10 @@ struct Gemm {
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
   static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 6) + 4) + 127) & ~127;
   static constexpr int OFF_META = OFF_BAR + kBarBytes;
-  // gate/up: the unit's SwiGLU rows staged as fp16 [128 tokens][128 f] so the
-  // accumulator is released before the rows are written out
-  static constexpr int kHStage = (MODE == kSwiglu) ? kNT * 128 * 2 : 0;
+  // gate/up and down: the unit's output rows staged as fp16 [128 tokens][128
+  // or 256] so the accumulator is released before the rows are written out
+  static constexpr int kHCols = (MODE == kScatter) ? 256 : 128;
+  static constexpr int kHStage = (MODE != kRouter) ? kNT * kHCols * 2 : 0;
   static constexpr int OFF_HST = OFF_META + 8 * kNT;
   static constexpr int kSmem = OFF_HST + kHStage + 1024;  // + slack for 1 KB alignment
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
@@ -168,7 +172,7 @@ struct GemmParams {
   const int32_t* xshift;
   __half* hmid_r;
   __half* hmid_s;
-  float* yacc;
+  __half* ypart;             // down: weighted partial output rows (routed, then shared)
   float* z;
   const float* gw;           // [T] shared-expert gate weights, or null (weight 1)
   int router_shift;
@@ -225,8 +229,9 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// First block scale of weight row r of a unit's 128-row tile, for the
-// matrix a producer thread dequantises (gate/up: part = matrix).
+// First block scale of weight row r of the A matrix `part` of a unit (gate
+// or up of the F tile; the first or second 128 rows of the H tile), or null
+// for rows past the matrix.
 template <int MODE>
 __device__ __forceinline__ const uint16_t* scale_row(const GemmParams& p, const UnitInfo& U, int part, int r) {
   const LayerDev& W = p.W;
@@ -237,13 +242,16 @@ __device__ __forceinline__ const uint16_t* scale_row(const GemmParams& p, const 
     const uint16_t* base = part ? (U.shared ? W.sh_up_s : W.up_s) : (U.shared ? W.sh_gate_s : W.gate_s);
     return base + row * C;
   }
-  const size_t row = (U.shared ? 0 : (size_t)slot * p.H) + (size_t)U.mt * 128 + r;
+  const int h = U.mt * 256 + part * 128 + r;  // output row of W_d
+  if (h >= p.H) return nullptr;                // second half of the last tile when H % 256 == 128
+  const size_t row = (U.shared ? 0 : (size_t)slot * p.H) + h;
   return (U.shared ? W.sh_down_s : W.down_s) + row * C;
 }
 
 // The scale words (two fp16 each) of K steps s0..s0+3 of one row: one
 // 16-byte load when aligned and whole, else one word per step that exists.
 __device__ __forceinline__ uint4 load_scale_quad(const uint16_t* srow, int s0, int nks) {
+  if (!srow) return make_uint4(0u, 0u, 0u, 0u);  // rows past the matrix: zero weights
   const uint16_t* q = srow + 2 * s0;
   if (s0 + 4 <= nks && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(q));
   const uint32_t* w = reinterpret_cast<const uint32_t*>(q);
@@ -330,10 +338,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           meta_f[r] = pow2f(sx);
           reinterpret_cast<float*>(meta_i)[r] = pow2f(-sx);
         } else if (MODE == kScatter) {
-          const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
-          const float wgt = U.shared ? (p.gw ? __ldg(p.gw + tok) : 1.0f) : __ldg(p.perm_w + U.p0 + r);
-          meta_i[r] = tok;
-          meta_f[r] = wgt * pow2f(2 * __ldg(p.xshift + tok));
+          // the routing weight (or the shared expert's gate); the rows keep
+          // the inputs' 2^-2sx, which the combine restores per token
+          meta_f[r] = U.shared ? (p.gw ? __ldg(p.gw + U.p0 + r) : 1.0f) : __ldg(p.perm_w + U.p0 + r);
         } else {
           meta_f[r] = pow2f(__ldg(p.xshift + U.p0 + r) - p.router_shift);
         }
@@ -404,54 +411,74 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             }
           }
         }
+      } else if (MODE == kScatter) {
+        // drain: w * D of both 128-row halves as fp16 into the staging rows
+        // [token][256]
+        for (int c0 = 0; c0 < neff; c0 += CW) {
+          uint32_t v0[CW], v1[CW];
+          tmem_ld(tbase + c0, v0);
+          tmem_ld(tbase + 128 + c0, v1);
+          tmem_wait_ld();
+          float tf[CW];
+#pragma unroll
+          for (int q = 0; q < CW; q += 4) {
+            const float4 vf = *reinterpret_cast<const float4*>(meta_f + c0 + q);
+            tf[q] = vf.x, tf[q + 1] = vf.y, tf[q + 2] = vf.z, tf[q + 3] = vf.w;
+          }
+#pragma unroll
+          for (int jj = 0; jj < CW; ++jj) {
+            hst[(c0 + jj) * 256 + r] = __float2half_rn(__uint_as_float(v0[jj]) * tf[jj]);
+            hst[(c0 + jj) * 256 + 128 + r] = __float2half_rn(__uint_as_float(v1[jj]) * tf[jj]);
+          }
+        }
       } else {
         for (int c0 = 0; c0 < neff; c0 += CW) {
           uint32_t v0[CW];
           tmem_ld(tbase + c0, v0);
           tmem_wait_ld();
-          // per 16 tokens: factors into registers first, then the stores or
-          // reductions (a shared load after a global store through a generic
-          // pointer would have to wait for it)
+          // per 16 tokens: factors into registers first, then the stores (a
+          // shared load after a global store through a generic pointer
+          // would have to wait for it)
 #pragma unroll
           for (int hq = 0; hq < CW; hq += 16) {
             float tf[16];
-            int ti[16];
 #pragma unroll
             for (int q = 0; q < 16; q += 4) {
               const float4 vf = *reinterpret_cast<const float4*>(meta_f + c0 + hq + q);
               tf[q] = vf.x, tf[q + 1] = vf.y, tf[q + 2] = vf.z, tf[q + 3] = vf.w;
-              if (MODE == kScatter) {
-                const int4 vi = *reinterpret_cast<const int4*>(meta_i + c0 + hq + q);
-                ti[q] = vi.x, ti[q + 1] = vi.y, ti[q + 2] = vi.z, ti[q + 3] = vi.w;
-              }
             }
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int t = c0 + hq + jj;
-              if (t >= U.n) continue;
-              const float v = __uint_as_float(v0[hq + jj]) * tf[jj];
-              if (MODE == kScatter) {
-                atomicAdd(p.yacc + (size_t)ti[jj] * p.H + U.mt * 128 + r, v);
-              } else {
-                const int e = U.mt * 128 + r;
-                if (e < p.E) p.z[(size_t)(U.p0 + t) * p.E + e] = v + bias_r;
-              }
+              const int e = U.mt * 128 + r;
+              if (t < U.n && e < p.E)
+                p.z[(size_t)(U.p0 + t) * p.E + e] = __uint_as_float(v0[hq + jj]) * tf[jj] + bias_r;
             }
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty[b]);
-      if (MODE == kSwiglu) {
+      if (MODE != kRouter) {
         // write the staged rows out (16-byte stores) while the MMAs of the
         // next unit already run in the released accumulator
         named_bar_sync(2, kEpiWarps * 32);
-        const size_t hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
-        __half* hbase = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + U.mt * 128;
-        for (int idx = r; idx < U.n * 16; idx += kEpiWarps * 32) {
-          const int t = idx >> 4, c = idx & 15;
+        size_t hstride;
+        __half* hbase;
+        int lg;  // log2 of the 16-byte chunks a row holds
+        if (MODE == kSwiglu) {
+          hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
+          hbase = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + U.mt * 128;
+          lg = 4;
+        } else {
+          hstride = (size_t)p.H;
+          hbase = p.ypart + ((size_t)(U.shared ? p.Tk : 0) + U.p0) * hstride + U.mt * 256;
+          lg = (U.mt * 256 + 256 <= p.H) ? 5 : 4;  // only the first half exists past H
+        }
+        for (int idx = r; idx < (U.n << lg); idx += kEpiWarps * 32) {
+          const int t = idx >> lg, c = idx & ((1 << lg) - 1);
           *reinterpret_cast<uint4*>(hbase + (size_t)t * hstride + c * 8) =
-              *reinterpret_cast<const uint4*>(hst + t * 128 + c * 8);
+              *reinterpret_cast<const uint4*>(hst + t * G::kHCols + c * 8);
         }
       }
     }
@@ -464,8 +491,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     if constexpr (MODE != kRouter) {
       // thread = (part, row r), r = 32*(warp%4) + lane: the TMEM lane it
       // writes (a warp reaches only its own quarter of the 128 lanes)
-      //   gate/up: part = matrix, all 64 K of the step
-      //   down:    part = which 32-element half of the step
+      // and part = the A matrix (gate or up; the first or second 128 rows of
+      // the down GEMM's H tile), all 64 K of the step
       // Codes come from the raw ring (one TMA tile per matrix and step).
       // K steps go in groups of P (nks is even): one set of waits and one
       // round of hand-backs per group.  Per group: the raw stages' words
@@ -478,7 +505,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       const int part = pi >> 7;
       const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
       constexpr int P = G::kGroup;
-      constexpr int OW = (MODE == kSwiglu) ? 32 : 16;  // TMEM columns per thread and step
+      constexpr int OW = 32;  // TMEM columns per thread and step: 64 fp16
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
         const UnitInfo U = unit_info<MODE>(p, u);
         const int nks = U.K / 64;
@@ -502,15 +529,10 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
               ok = __all_sync(0xffffffffu, ok);
               if (ok) {
                 const unsigned char* rs = sR + sr * G::kRawBytes;
-                if (MODE == kSwiglu) {
-                  const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
-                  const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
-                  ca[q] = h ? q1 : q0;
-                  cb[q] = h ? q0 : q1;
-                } else {
-                  ca[q] = *reinterpret_cast<const uint4*>(rs + r * 32 + part * 16);
-                  cb[q] = ca[q];
-                }
+                const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
+                ca[q] = h ? q1 : q0;
+                cb[q] = h ? q0 : q1;
               }
             }
             if (!ok) {
@@ -524,31 +546,17 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             uint32_t o[P][OW];
 #pragma unroll
             for (int q = 0; q < P; ++q) {
-              if (MODE == kSwiglu) {
-                const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] & 0xffffu)));
-                const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] >> 16)));
-                const uint32_t wds[8] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w,
-                                         cb[q].x, cb[q].y, cb[q].z, cb[q].w};
+              const __half2 slo = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] & 0xffffu)));
+              const __half2 shi = __half2half2(__ushort_as_half((uint16_t)(sqw[dd + q] >> 16)));
+              const uint32_t wds[8] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w,
+                                       cb[q].x, cb[q].y, cb[q].z, cb[q].w};
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                  const uint4 d = dequant_word(wds[w], w < 4 ? slo : shi);
-                  o[q][4 * w] = d.x;
-                  o[q][4 * w + 1] = d.y;
-                  o[q][4 * w + 2] = d.z;
-                  o[q][4 * w + 3] = d.w;
-                }
-              } else {
-                const __half2 s2 =
-                    __half2half2(__ushort_as_half((uint16_t)(part ? sqw[dd + q] >> 16 : sqw[dd + q] & 0xffffu)));
-                const uint32_t wds[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                  const uint4 d = dequant_word(wds[w], s2);
-                  o[q][4 * w] = d.x;
-                  o[q][4 * w + 1] = d.y;
-                  o[q][4 * w + 2] = d.z;
-                  o[q][4 * w + 3] = d.w;
-                }
+              for (int w = 0; w < 8; ++w) {
+                const uint4 d = dequant_word(wds[w], w < 4 ? slo : shi);
+                o[q][4 * w] = d.x;
+                o[q][4 * w + 1] = d.y;
+                o[q][4 * w + 2] = d.z;
+                o[q][4 * w + 3] = d.w;
               }
             }
 #pragma unroll
@@ -566,10 +574,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
 #pragma unroll
             for (int q = 0; q < P; ++q) {
               const uint32_t acol = arow + (uint32_t)(((it + q) % S) * G::kACols) + (uint32_t)(part * OW);
-              if constexpr (OW == 32)
-                tmem_st32(acol, o[q]);
-              else
-                tmem_st16(acol, o[q]);
+              tmem_st32(acol, o[q]);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -634,7 +639,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           const UnitInfo U = unit_info<MODE>(p, u);
           const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
           const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
-          const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * 128;
+          // gate/up: both matrices at the F tile's rows; down: the two
+          // 128-row halves of the 256-row H tile (past H: the next expert's
+          // rows or zero fill, never used)
+          const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * (MODE == kScatter ? 256 : 128);
+          const int row1 = (MODE == kScatter) ? row + 128 : row;
           const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
           const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
           const int nks = U.K / 64;
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             unsigned char* dst = sR + sr * G::kRawBytes;
             mbar_expect_tx(&raw_full[sr], (uint32_t)(NA * kRawTile));
             tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
-            if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row, &raw_full[sr]);
+            if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row1, &raw_full[sr]);
           }
         }
         const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
@@ -812,6 +821,7 @@ struct BucketParams {
   int32_t* offsets;
   int32_t* perm_tok;
   float* perm_w;
+  int32_t* pos;      // [T*k] bucket position of each assignment, -1 if its id is invalid
   int4* gu_units;
   int4* dn_units;
   int32_t* n_units;
@@ -887,6 +897,7 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const BucketParams p
     int e = (a < a_end) ? __ldg(p.ids + a) : -1;
     const float wv = (a < a_end) ? __ldg(p.w + a) : 0.0f;
     if (e >= E) e = -1;
+    if (e < 0 && a < a_end) p.pos[a] = -1;
     const unsigned same = __match_any_sync(0xffffffffu, e);
     int base = 0;
     if (e >= 0) base = cur[e];
@@ -895,6 +906,7 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const BucketParams p
       const int pos = base + __popc(same & lt_mask);
       p.perm_tok[pos] = a / k;
       p.perm_w[pos] = wv;
+      p.pos[a] = pos;
       if ((same & lt_mask) == 0) cur[e] = base + __popc(same);
     }
     __syncwarp();
@@ -946,7 +958,7 @@ __global__ void __launch_bounds__(kBucketThreads, 1) bucket_scan_kernel(const Bu
   __syncthreads();
   // work units: routed tiles g -> (expert, tile) by binary search on tbase
   const int ntiles = tbase[E];
-  const int mF = p.F / 128, mH = p.H / 128, mS = p.Fs / 128;
+  const int mF = p.F / 128, mH = (p.H + 255) / 256, mS = p.Fs / 128;  // down: 256-row H tiles
   for (int g = tid; g < ntiles; g += kBucketThreads) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {  // last e with tbase[e] <= g
@@ -975,7 +987,6 @@ __global__ void __launch_bounds__(kBucketThreads, 1) bucket_scan_kernel(const Bu
   }
 }
 
-// y (bf16) = yacc (fp32): scalar version for a y that is not 16-byte aligned.
 // Operand B of the routed gate/up GEMM: the x16 row of every bucketed
 // (token, expert) assignment, copied into bucket order so that a unit's K
 // step is one TMA tile.  One warp per row, 16-byte copies.
@@ -994,25 +1005,76 @@ __global__ void gather_rows_kernel(const __half* __restrict__ x16, const int32_t
   }
 }
 
-__global__ void finalize_scalar_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(yacc[i]));
+// The partial output rows of one layer's down GEMM and what the combine
+// needs to sum them per token: y[t] = 2^(2 sx_t) * (sum over the token's
+// assignments of its row + its shared-expert row).
+struct PartsView {
+  const __half* rows;     // [T*k routed, bucket order | T shared, token order][H]
+  const int32_t* pos;     // [T*k] bucket position of (token, slot), -1 if none
+  const int32_t* xshift;  // [T] the inputs' power-of-two shifts
+  int T, k, shared;
+};
+
+// Eight consecutive outputs (chunk g of 8) of token t; pj[j] (j < k) is the
+// bucket position of the token's slot j, or -1.
+__device__ __forceinline__ void combine8(const PartsView& v, int t, int g, int H, const int (&pj)[kMaxTopK],
+                                         float sc, float (&y)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = 0.0f;
+  auto add = [&](size_t row) {
+    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(v.rows + row * H) + g);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      y[2 * i] += f.x;
+      y[2 * i + 1] += f.y;
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < v.k && pj[j] >= 0) add((size_t)pj[j]);
+  if (v.shared) add((size_t)v.T * v.k + t);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] *= sc;
 }
 
-// y (bf16) = yacc (fp32), 8 elements per step (n is a multiple of 8, y
-// 16-byte aligned).
-__global__ void finalize_kernel(const float* __restrict__ yacc, size_t n, uint16_t* __restrict__ y) {
-  const size_t n8 = n / 8;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i);
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i + 1);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// The bucket positions of token t's slots, read by lanes 0..k-1 and
+// shared across the warp (every lane must call this).
+__device__ __forceinline__ void combine_pos(const PartsView& v, int t, int lane, int (&pj)[kMaxTopK]) {
+  const int n = v.T * v.k;
+  int p = lane < v.k ? __ldg(v.pos + (size_t)t * v.k + lane) : -1;
+  p = (p >= 0 && p < n) ? p : -1;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) pj[j] = __shfl_sync(0xffffffffu, p, j);
+}
+
+// y (bf16 [T][H]) = the combined partial rows; one warp per token.
+__global__ void combine_kernel(const PartsView v, int H, uint16_t* __restrict__ y) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= v.T) return;
+  int pj[kMaxTopK];
+  combine_pos(v, t, lane, pj);
+  const float sc = pow2f(2 * __ldg(v.xshift + t));
+  const bool vec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
+  for (int g = lane; g < H / 8; g += 32) {
+    float yy[8];
+    combine8(v, t, g, H, pj, sc, yy);
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j])) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j + 1])) << 16);
-    reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int q = 0; q < 4; ++q)
+      o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yy[2 * q])) |
+             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yy[2 * q + 1])) << 16);
+    uint16_t* dst = y + (size_t)t * H + 8 * g;
+    if (vec) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dst[2 * q] = (uint16_t)(o[q] & 0xffffu);
+        dst[2 * q + 1] = (uint16_t)(o[q] >> 16);
+      }
+    }
   }
 }
 
@@ -1046,7 +1108,7 @@ __global__ void router_split_kernel(const float* __restrict__ wr, int E, int H, 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillSizes {
-  size_t x16, xg, xshift, zf, ids, w, offsets, perm_tok, perm_w, gu, dn, nunits, hmid_r, hmid_s, yacc, wr16,
+  size_t x16, xg, xshift, zf, ids, w, offsets, perm_tok, perm_w, pos, gu, dn, nunits, hmid_r, hmid_s, wr16,
       ccount;
   int max_gu, max_dn;
   static PrefillSizes make(const moe_layer_config& c) {
@@ -1057,9 +1119,9 @@ struct PrefillSizes {
     const size_t routed_tiles = (Tk + kNT - 1) / kNT + E;
     const size_t shared_tiles = Fs ? (Tm + kNT - 1) / kNT : 0;
     s.max_gu = (int)(routed_tiles * (F / 128) + shared_tiles * (Fs / 128));
-    s.max_dn = (int)((routed_tiles + shared_tiles) * (H / 128));
+    s.max_dn = (int)((routed_tiles + shared_tiles) * ((H + 255) / 256));
     s.x16 = Tm * H * 2;
-    s.xg = Tk * H * 2;
+    s.xg = (Tk + Tm) * H * 2;  // gate/up operand rows, then the down GEMM's output rows
     s.xshift = Tm * 4;
     s.zf = Tm * E * 4;
     s.ids = Tk * 4;
@@ -1067,20 +1129,20 @@ struct PrefillSizes {
     s.offsets = (E + 1) * 4;
     s.perm_tok = Tk * 4;
     s.perm_w = Tk * 4;
+    s.pos = Tk * 4;
     s.gu = (size_t)s.max_gu * 16;
     s.dn = (size_t)s.max_dn * 16;
     s.nunits = 16;
     s.hmid_r = Tk * F * 2;
     s.hmid_s = Tm * (Fs ? Fs : 128) * 2;
-    s.yacc = Tm * H * 4;
     s.wr16 = E * 2 * H * 2;
     s.ccount = (size_t)kMaxBucketChunks * E * 4;
     return s;
   }
   size_t total() const {
     return align256(x16) + align256(xg) + align256(xshift) + align256(zf) + align256(ids) + align256(w) +
-           align256(offsets) + align256(perm_tok) + align256(perm_w) + align256(gu) + align256(dn) +
-           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(yacc) + align256(wr16) +
+           align256(offsets) + align256(perm_tok) + align256(perm_w) + align256(pos) + align256(gu) + align256(dn) +
+           align256(nunits) + align256(hmid_r) + align256(hmid_s) + align256(wr16) +
            align256(ccount);
   }
 };
@@ -1175,12 +1237,12 @@ moe_status prefill_init(moe_layer* L, void* scratch, const char** why) {
   w.offsets = (int32_t*)take(z.offsets);
   w.perm_tok = (int32_t*)take(z.perm_tok);
   w.perm_w = (float*)take(z.perm_w);
+  w.pos = (int32_t*)take(z.pos);
   w.gu_units = (int4*)take(z.gu);
   w.dn_units = (int4*)take(z.dn);
   w.n_units = (int32_t*)take(z.nunits);
   w.hmid_r = (__half*)take(z.hmid_r);
   w.hmid_s = (__half*)take(z.hmid_s);
-  w.yacc = (float*)take(z.yacc);
   w.wr16 = (__half*)take(z.wr16);
   w.ccount = (int32_t*)take(z.ccount);
   w.max_gu_units = z.max_gu;
@@ -1288,7 +1350,7 @@ __global__ void stream_in_kernel(const int32_t* __restrict__ offsets, const int3
 // shift, K pairs in the nibble unpack order, as prep_x16_kernel).  With
 // norm == 0 (after the last layer) only h' is formed.  Trace pointers may
 // be null.
-__global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const float* __restrict__ yacc,
+__global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const PartsView parts,
                                       int T, int H, int norm, uint16_t* __restrict__ h_out,
                                       uint16_t* __restrict__ y_trace, uint16_t* __restrict__ u,
                                       __half* __restrict__ x16, int32_t* __restrict__ xshift) {
@@ -1297,14 +1359,20 @@ __global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const floa
   const int G = H / 8;
   const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)t * H);
   uint4* ho = reinterpret_cast<uint4*>(h_out + (size_t)t * H);
-  // pass 1: h' (and y), sum of squares
+  const bool has_y = parts.rows != nullptr;
+  int pj[kMaxTopK];
+  float ysc = 1.0f;
+  if (has_y) {
+    combine_pos(parts, t, lane, pj);
+    ysc = pow2f(2 * __ldg(parts.xshift + t));
+  }
+  // pass 1: y (the sum of the layer's partial rows), h', sum of squares
   float ss = 0.0f;
   for (int g = lane; g < G; g += 32) {
     uint4 v = hr[g];
-    if (yacc) {
-      const float4 a = __ldcs(reinterpret_cast<const float4*>(yacc + (size_t)t * H) + 2 * g);
-      const float4 b = __ldcs(reinterpret_cast<const float4*>(yacc + (size_t)t * H) + 2 * g + 1);
-      const float yy[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (has_y) {
+      float yy[8];
+      combine8(parts, t, g, H, pj, ysc, yy);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t o[4], yo[4];
 #pragma unroll
@@ -1320,7 +1388,7 @@ __global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const floa
       v = make_uint4(o[0], o[1], o[2], o[3]);
       if (y_trace) reinterpret_cast<uint4*>(y_trace + (size_t)t * H)[g] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
     }
-    if (yacc || h_out != h) ho[g] = v;
+    if (has_y || h_out != h) ho[g] = v;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -1377,12 +1445,26 @@ __global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const floa
   }
 }
 
-moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const float* yacc, int T,
+static PartsView parts_of(const moe_layer* L, int T) {
+  PartsView v;
+  v.rows = L->ws.xg;
+  v.pos = L->ws.pos;
+  v.xshift = L->ws.xshift;
+  v.T = T;
+  v.k = L->cfg.top_k;
+  v.shared = L->cfg.shared_ffn > 0 ? 1 : 0;
+  return v;
+}
+
+moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const moe_layer* prev, int T,
                                  int H, uint16_t* h_out, uint16_t* y_trace, uint16_t* u,
                                  cudaStream_t s, const char** why) {
+  PartsView parts;
+  memset(&parts, 0, sizeof parts);
+  if (prev) parts = parts_of(prev, T);
   {
     prof::Scope sc("moe_stack_boundary", s);
-    stack_boundary_kernel<<<(T + 7) / 8, 256, 0, s>>>(h, yacc, T, H, next ? 1 : 0, h_out, y_trace, u,
+    stack_boundary_kernel<<<(T + 7) / 8, 256, 0, s>>>(h, parts, T, H, next ? 1 : 0, h_out, y_trace, u,
                                                       next ? next->ws.x16 : nullptr,
                                                       next ? next->ws.xshift : nullptr);
   }
@@ -1396,7 +1478,7 @@ moe_status launch_stack_boundary(moe_layer* next, const uint16_t* h, const float
 
 moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, int32_t* ids_out,
                           float* w_out, bool route_only, cudaStream_t s, const char** why,
-                          bool prepped, bool keep_yacc) {
+                          bool prepped, bool keep_parts) {
   const moe_layer_config& c = L->cfg;
   const Workspace& ws = L->ws;
   const int H = c.hidden, E = c.n_experts, k = c.top_k;
@@ -1423,7 +1505,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.xshift = ws.xshift;
   gp.hmid_r = ws.hmid_r;
   gp.hmid_s = ws.hmid_s;
-  gp.yacc = ws.yacc;
+  gp.ypart = ws.xg;  // the gather rows are dead once gate/up is done
   gp.z = ws.zf;
   gp.gw = (c.routing_flags & MOE_ROUTING_SHARED_GATE) ? L->ws.gw : nullptr;
   gp.router_shift = L->router_shift;
@@ -1472,6 +1554,7 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   bp.offsets = ws.offsets;
   bp.perm_tok = ws.perm_tok;
   bp.perm_w = ws.perm_w;
+  bp.pos = ws.pos;
   bp.gu_units = ws.gu_units;
   bp.dn_units = ws.dn_units;
   bp.n_units = ws.n_units;
@@ -1512,19 +1595,12 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   gp.units = ws.gu_units;
   gp.n_units = ws.n_units;
   if ((st = launch_gemm<kSwiglu>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;
-  if ((e = cudaMemsetAsync(ws.yacc, 0, sizeof(float) * (size_t)T * H, s)) != cudaSuccess) {
-    *why = cudaGetErrorString(e);
-    return MOE_ERR_CUDA;
-  }
   gp.units = ws.dn_units;
   gp.n_units = ws.n_units + 1;
   if ((st = launch_gemm<kScatter>(gp, L, L->num_sms, s, why)) != MOE_OK) return st;
-  if (!keep_yacc) {
-    prof::Scope sc("moe_finalize", s);
-    if ((reinterpret_cast<uintptr_t>(y) & 15u) == 0)
-      finalize_kernel<<<4 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
-    else
-      finalize_scalar_kernel<<<2 * L->num_sms, 256, 0, s>>>(ws.yacc, (size_t)T * H, y);
+  if (!keep_parts) {
+    prof::Scope sc("moe_combine", s);
+    combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts_of(L, T), H, y);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) {
     *why = cudaGetErrorString(e);
