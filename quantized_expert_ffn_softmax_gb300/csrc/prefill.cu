@@ -94,8 +94,10 @@ enum GemmMode : int { kSwiglu = 0, kScatter = 1, kRouter = 2 };
 
 // Shared-memory rings and warp roles of one GEMM kernel.
 //   stage ring  S stages, each NA dequantised fp16 128x64 tiles (MMA operand
-//               A) and one fp16 kNTx64 token tile (operand B); full_a and
-//               full_b mark the two halves ready, one tcgen05.commit per K
+//               A) and one fp16 kNTx64 token tile (operand B); full_a marks
+//               the stage ready (the producer warps' arrivals and the B
+//               tile's bytes; the router's A and B tiles both arrive by
+//               TMA on full_b instead), one tcgen05.commit per K
 //               step releases the whole stage
 //   raw ring    SR stages of NA packed-code tiles, filled by TMA; the gate/up
 //               and down GEMMs dequantise from it (the router GEMM reads its
@@ -113,7 +115,7 @@ struct Gemm {
   // A matrices per unit: gate and up, or two 128-row tiles of W_d
   static constexpr int NA = (MODE == kRouter) ? 1 : 2;
   static constexpr int S = (MODE == kRouter) ? 6 : 4;
-  static constexpr int SR = (MODE == kRouter) ? 0 : 12;
+  static constexpr int SR = (MODE == kRouter) ? 0 : (MODE == kScatter ? 11 : 12);
   static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
   static constexpr int kAccBufs = (MODE == kRouter) ? 2 : 1;
   static constexpr int kAccCols = NA * 128;  // gate | up, or one accumulator
@@ -138,10 +140,14 @@ struct Gemm {
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
   static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 6) + 4) + 127) & ~127;
   static constexpr int OFF_META = OFF_BAR + kBarBytes;
-  // gate/up and down: the unit's output rows staged as fp16 [128 tokens][128
-  // or 256] so the accumulator is released before the rows are written out
-  static constexpr int kHCols = (MODE == kScatter) ? 256 : 128;
-  static constexpr int kHStage = (MODE != kRouter) ? kNT * kHCols * 2 : 0;
+  // gate/up and down: the unit's outputs staged as fp16 [128 or 256 rows of
+  // the accumulators][kNT tokens, padded to kTS] so the accumulators are
+  // released as soon as they are read (each thread stores its row's tokens
+  // 16 bytes at a time; the 272-byte row stride keeps those stores free of
+  // bank conflicts); the write-out transposes to token-major rows
+  static constexpr int kTS = kNT + 8;
+  static constexpr int kHRows = (MODE == kScatter) ? 256 : 128;
+  static constexpr int kHStage = (MODE != kRouter) ? kHRows * kTS * 2 : 0;
   static constexpr int OFF_HST = OFF_META + 8 * kNT;
   static constexpr int kSmem = OFF_HST + kHStage + 1024;  // + slack for 1 KB alignment
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_a[s], kProdWarps);
+      mbar_init(&full_a[s], kProdWarps + 1);  // + the B loader's arrive with the tile's bytes
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], NA);  // one commit per MMA issuer
     }
@@ -356,11 +362,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       tc_fence_after();
       const int neff = (U.n + 15) & ~15;
       const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * G::kAccCols);
-      // gate/up: column of row r inside the tile's 128 (8-groups in the
-      // unpack order 0,4,1,5,2,6,3,7, as the down GEMM's K expects)
-      const int qloc = (r & ~7) | ((r & 4) ? (((r & 3) << 1) | 1) : ((r & 3) << 1));
       constexpr int CW = (NA == 2) ? 16 : 32;  // columns per TMEM load
-      if (MODE == kSwiglu) {
+      if constexpr (MODE == kSwiglu) {
         // drain: the next chunk's TMEM loads are issued before this chunk is
         // processed; per element one scale, SiLU, one product, one store
         const float* sA = meta_f;
@@ -396,12 +399,10 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
                                                 __uint_as_float(u0[jj + 1]) * fb[jj + 1]);
             hv[jj / 2] = __hmul2(silu_fast2(g), u);
           }
-#pragma unroll
-          for (int jj = 0; jj < CW; jj += 2) {
-            const int t = c0 + jj;
-            hst[t * 128 + qloc] = __low2half(hv[jj / 2]);
-            hst[(t + 1) * 128 + qloc] = __high2half(hv[jj / 2]);
-          }
+          static_assert(CW == 16, "two 16-byte stores per chunk");
+          uint4* dst = reinterpret_cast<uint4*>(hst + r * G::kTS + c0);
+          dst[0] = *reinterpret_cast<const uint4*>(&hv[0]);
+          dst[1] = *reinterpret_cast<const uint4*>(&hv[4]);
           if (more) {
             tmem_wait_ld();
 #pragma unroll
@@ -411,24 +412,47 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             }
           }
         }
-      } else if (MODE == kScatter) {
+      } else if constexpr (MODE == kScatter) {
         // drain: w * D of both 128-row halves as fp16 into the staging rows
-        // [token][256]
+        // [token][256]; the next chunk's TMEM loads are issued before this
+        // chunk is processed
+        uint32_t v0[CW], v1[CW];
+        tmem_ld(tbase, v0);
+        tmem_ld(tbase + 128, v1);
+        tmem_wait_ld();
         for (int c0 = 0; c0 < neff; c0 += CW) {
-          uint32_t v0[CW], v1[CW];
-          tmem_ld(tbase + c0, v0);
-          tmem_ld(tbase + 128 + c0, v1);
-          tmem_wait_ld();
+          uint32_t n0[CW], n1[CW];
+          const bool more = c0 + CW < neff;
+          if (more) {
+            tmem_ld(tbase + c0 + CW, n0);
+            tmem_ld(tbase + 128 + c0 + CW, n1);
+          }
           float tf[CW];
 #pragma unroll
           for (int q = 0; q < CW; q += 4) {
             const float4 vf = *reinterpret_cast<const float4*>(meta_f + c0 + q);
             tf[q] = vf.x, tf[q + 1] = vf.y, tf[q + 2] = vf.z, tf[q + 3] = vf.w;
           }
+          __half2 a[CW / 2], c[CW / 2];
 #pragma unroll
-          for (int jj = 0; jj < CW; ++jj) {
-            hst[(c0 + jj) * 256 + r] = __float2half_rn(__uint_as_float(v0[jj]) * tf[jj]);
-            hst[(c0 + jj) * 256 + 128 + r] = __float2half_rn(__uint_as_float(v1[jj]) * tf[jj]);
+          for (int jj = 0; jj < CW; jj += 2) {
+            a[jj / 2] = __floats2half2_rn(__uint_as_float(v0[jj]) * tf[jj], __uint_as_float(v0[jj + 1]) * tf[jj + 1]);
+            c[jj / 2] = __floats2half2_rn(__uint_as_float(v1[jj]) * tf[jj], __uint_as_float(v1[jj + 1]) * tf[jj + 1]);
+          }
+          static_assert(CW == 16, "two 16-byte stores per chunk and half");
+          uint4* d0 = reinterpret_cast<uint4*>(hst + r * G::kTS + c0);
+          uint4* d1 = reinterpret_cast<uint4*>(hst + (128 + r) * G::kTS + c0);
+          d0[0] = *reinterpret_cast<const uint4*>(&a[0]);
+          d0[1] = *reinterpret_cast<const uint4*>(&a[4]);
+          d1[0] = *reinterpret_cast<const uint4*>(&c[0]);
+          d1[1] = *reinterpret_cast<const uint4*>(&c[4]);
+          if (more) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+              v0[jj] = n0[jj];
+              v1[jj] = n1[jj];
+            }
           }
         }
       } else {
@@ -465,20 +489,43 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         named_bar_sync(2, kEpiWarps * 32);
         size_t hstride;
         __half* hbase;
-        int lg;  // log2 of the 16-byte chunks a row holds
+        int nch;  // 16-byte chunks of a token's output row
         if (MODE == kSwiglu) {
           hstride = U.shared ? (size_t)p.Fs : (size_t)p.F;
           hbase = (U.shared ? p.hmid_s : p.hmid_r) + (size_t)U.p0 * hstride + U.mt * 128;
-          lg = 4;
+          nch = 16;
         } else {
           hstride = (size_t)p.H;
           hbase = p.ypart + ((size_t)(U.shared ? p.Tk : 0) + U.p0) * hstride + U.mt * 256;
-          lg = (U.mt * 256 + 256 <= p.H) ? 5 : 4;  // only the first half exists past H
+          nch = (U.mt * 256 + 256 <= p.H) ? 32 : 16;  // only the first half exists past H
         }
-        for (int idx = r; idx < (U.n << lg); idx += kEpiWarps * 32) {
-          const int t = idx >> lg, c = idx & ((1 << lg) - 1);
-          *reinterpret_cast<uint4*>(hbase + (size_t)t * hstride + c * 8) =
-              *reinterpret_cast<const uint4*>(hst + t * G::kHCols + c * 8);
+        // 8 x 8 blocks (staging rows 8c..8c+7, tokens 8tb..8tb+7): eight
+        // 16-byte shared loads, a transpose in registers, and one 16-byte
+        // output chunk per token.  Gate/up: row 8c+i goes to position
+        // 8c + (0,2,4,6,1,3,5,7)[i], the unpack order of the down GEMM's K,
+        // so output word j pairs rows j and j+4; down: rows 2j and 2j+1.
+        const int ntb = (U.n + 7) >> 3;
+        for (int blk = r; blk < nch * ntb; blk += kEpiWarps * 32) {
+          const int c = blk / ntb, tb = blk % ntb;
+          uint4 rows[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            rows[i] = *reinterpret_cast<const uint4*>(hst + (8 * c + i) * G::kTS + 8 * tb);
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            const int t = 8 * tb + tt;
+            if (t >= U.n) break;
+            const uint32_t sel = (tt & 1) ? 0x7632u : 0x5410u;
+            uint32_t w[4];
+#pragma unroll
+            for (int jw = 0; jw < 4; ++jw) {
+              const int ra = (MODE == kSwiglu) ? jw : 2 * jw, rb = (MODE == kSwiglu) ? jw + 4 : 2 * jw + 1;
+              const uint32_t* pa = reinterpret_cast<const uint32_t*>(&rows[ra]);
+              const uint32_t* pb = reinterpret_cast<const uint32_t*>(&rows[rb]);
+              w[jw] = __byte_perm(pa[tt >> 1], pb[tt >> 1], sel);
+            }
+            *reinterpret_cast<uint4*>(hbase + (size_t)t * hstride + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
     }
@@ -597,6 +644,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     // unit (or read as zero past the buffer); their columns are discarded.
     uint32_t it = 0;
     bool alive = true;
+    uint64_t* fulls = (MODE == kRouter) ? full_b : full_a;  // the stage's ready barriers
     if (lane == 0) {
       const int kpp = p.H / 64;
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
@@ -605,24 +653,25 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         const int nks = U.K / 64;
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int st = it % S;
+          uint64_t* fullb = &fulls[st];
           if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo)) {
             alive = false;
             break;
           }
           if (MODE == kRouter) {
             // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
-            mbar_expect_tx(&full_b[st], (uint32_t)(kTileA + kTileB));
-            tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, &full_b[st]);
+            mbar_expect_tx(fullb, (uint32_t)(kTileA + kTileB));
+            tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, fullb);
           } else {
-            mbar_expect_tx(&full_b[st], (uint32_t)kTileB);
+            mbar_expect_tx(fullb, (uint32_t)kTileB);
           }
           const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-          tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, &full_b[st]);
+          tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, fullb);
         }
       }
       // let every copy this thread issued land before the CTA can exit
       const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-      for (uint32_t q = first; q < it; ++q) drain_wait(&full_b[q % S], (q / S) & 1, tmo);
+      for (uint32_t q = first; q < it; ++q) drain_wait(&fulls[q % S], (q / S) & 1, tmo);
     }
     __syncwarp();
   } else if (warp < kMmaWarp) {
@@ -688,8 +737,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         for (int ks = 0; ks < nks; ++ks, ++it) {
           const int st = it % S;
           const uint32_t ph = (it / S) & 1;
-          if ((MODE != kRouter && !mbar_wait(&full_a[st], ph, p.err, tmo)) ||
-              !mbar_wait(&full_b[st], ph, p.err, tmo)) {
+          if (!mbar_wait(MODE == kRouter ? &full_b[st] : &full_a[st], ph, p.err, tmo)) {
             ok = false;
             break;
           }
