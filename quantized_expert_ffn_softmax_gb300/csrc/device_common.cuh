@@ -339,94 +339,5 @@ __device__ __forceinline__ float silu_fast(float g) {
   return g * fmaf(0.5f, th, 0.5f);
 }
 
-// Top-k of one token's E logits (logit e read by lane e % 32), descending by
-// value, ties to the lower id; then softmax over the selected logits.  Lane
-// r < k receives id and weight r.  Returns false if a non-finite logit left
-// no valid candidate.  LDCG: read the logits through L2 only (they were
-// written by other CTAs of the same launch).  Routing variants: with bsel
-// (the bias, which then only selects) the weights use z_e - bsel[e]; with
-// renorm false they are the softmax over all E such values, taken at the
-// selection, instead of the softmax over the selection.
-template <bool LDCG>
-__device__ __forceinline__ bool warp_topk_softmax_impl(const float* z, int E, int k,
-                                                       const float* bsel, bool renorm,
-                                                       int* id_out, float* w_out) {
-  const int lane = threadIdx.x & 31;
-  float v[kMaxExperts / 32];
-  const int nj = (E + 31) / 32;
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = (j < nj && e < E) ? (LDCG ? __ldcg(z + e) : z[e]) : -INFINITY;
-  }
-  uint32_t taken = 0;
-  int my_id = 0;
-  float my_z = 0.0f, z0 = 0.0f;
-  bool ok = true;
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      if (j < nj && !((taken >> j) & 1u)) {
-        const int e = lane + 32 * j;
-        if (e < E && (v[j] > bv || (v[j] == bv && e < bi))) {
-          bv = v[j];
-          bi = e;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi < 0 || bi >= E) {  // only reachable with non-finite logits
-      ok = false;
-      bi = r;
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (r == 0) z0 = bv;
-    if (lane == r) {
-      my_id = bi;
-      my_z = bv;
-    }
-  }
-  const float base = (bsel && lane < k) ? my_z - __ldg(bsel + my_id) : my_z;
-  float m = z0, den;
-  if (renorm) {
-    if (bsel) m = warp_max(lane < k ? base : -INFINITY);
-    den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
-  } else {
-    float mm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      const int e = lane + 32 * j;
-      if (j < nj && e < E) mm = fmaxf(mm, v[j] - (bsel ? __ldg(bsel + e) : 0.0f));
-    }
-    m = warp_max(mm);
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      const int e = lane + 32 * j;
-      if (j < nj && e < E) acc += __expf(v[j] - (bsel ? __ldg(bsel + e) : 0.0f) - m);
-    }
-    den = warp_sum(acc);
-  }
-  const float ex = (lane < k) ? __expf(base - m) : 0.0f;
-  *id_out = my_id;
-  *w_out = ex / den;
-  return ok;
-}
-
-__device__ __forceinline__ bool warp_topk_softmax(const float* z, int E, int k, const float* bsel,
-                                                  bool renorm, int* id_out, float* w_out) {
-  return warp_topk_softmax_impl<false>(z, E, k, bsel, renorm, id_out, w_out);
-}
-
 }  // namespace dev
 }  // namespace moe

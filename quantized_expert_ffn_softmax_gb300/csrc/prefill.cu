@@ -821,9 +821,103 @@ __global__ void prep_x16_kernel(const uint16_t* __restrict__ x, int T, int H,
   }
 }
 
+// Top-k of one token's E logits held by one warp (logit e in lane e % 32,
+// slot e / 32; NJ = slots per lane, E <= 32 NJ), descending by value, ties
+// to the lower expert id; then the softmax weights.  Each lane keeps the
+// best logit it has not given away; per round the warp takes the maximum of
+// the 32 lane bests and only the winning lane rescans its slots.  Lane r < k
+// receives id and weight r.  Returns false if a non-finite logit left no
+// valid candidate.  Routing variants: with bsel (the bias, which then only
+// selects) the weights use z_e - bsel[e]; with renorm false they are the
+// softmax over all E such values, taken at the selection, instead of the
+// softmax over the selection.
+template <int NJ>
+__device__ __forceinline__ bool warp_topk_softmax(const float* z, int E, int k, const float* bsel,
+                                                  bool renorm, int* id_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  float v[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? z[e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  // this lane's best slot not yet taken (ties: lower slot = lower id)
+  auto lane_best = [&](float& bv, int& bi) {
+    bv = -INFINITY;
+    bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+  };
+  float lv;
+  int li;
+  lane_best(lv, li);
+  int my_id = 0;
+  float my_z = 0.0f, z0 = 0.0f;
+  bool ok = true;
+  for (int r = 0; r < k; ++r) {
+    float bv = lv;
+    int bi = li;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < 0 || bi >= E) {  // only reachable with non-finite logits
+      ok = false;
+      bi = r;
+    }
+    if ((bi & 31) == lane) {
+      taken |= 1u << (bi >> 5);
+      lane_best(lv, li);
+    }
+    if (r == 0) z0 = bv;
+    if (lane == r) {
+      my_id = bi;
+      my_z = bv;
+    }
+  }
+  const float base = (bsel && lane < k) ? my_z - __ldg(bsel + my_id) : my_z;
+  float m = z0, den;
+  if (renorm) {
+    if (bsel) m = warp_max(lane < k ? base : -INFINITY);
+    den = warp_sum(lane < k ? __expf(base - m) : 0.0f);
+  } else {
+    float mm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) mm = fmaxf(mm, v[j] - (bsel ? __ldg(bsel + e) : 0.0f));
+    }
+    m = warp_max(mm);
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) acc += __expf(v[j] - (bsel ? __ldg(bsel + e) : 0.0f) - m);
+    }
+    den = warp_sum(acc);
+  }
+  const float ex = (lane < k) ? __expf(base - m) : 0.0f;
+  *id_out = my_id;
+  *w_out = ex / den;
+  return ok;
+}
+
 // One warp per token: top-k and routing weights (with the layer's routing
 // variants: bsel = the bias when it only selects, renorm), and, for a gated
 // shared expert, gw[t] = sigmoid(gate . x_t) over the bf16 input row.
+template <int NJ>
 __global__ void topk_kernel(const float* __restrict__ z, int T, int E, int k,
                             const float* __restrict__ bsel, int renorm,
                             const float* __restrict__ gate, const uint16_t* __restrict__ x, int H,
@@ -833,7 +927,7 @@ __global__ void topk_kernel(const float* __restrict__ z, int T, int E, int k,
   if (t >= T) return;
   int id;
   float wt;
-  const bool ok = warp_topk_softmax(z + (size_t)t * E, E, k, bsel, renorm != 0, &id, &wt);
+  const bool ok = warp_topk_softmax<NJ>(z + (size_t)t * E, E, k, bsel, renorm != 0, &id, &wt);
   if (!ok && lane == 0) atomicCAS(err, 0, (int)MOE_ERR_BOUNDS);
   if (lane < k) {
     ids[(size_t)t * k + lane] = id;
@@ -1049,7 +1143,7 @@ __global__ void gather_rows_kernel(const __half* __restrict__ x16, const int32_t
     const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)tok * H);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll 8
-    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    for (int c = lane; c < chunks; c += 32) __stcs(dst + c, __ldg(src + c));  // streaming: keep x16 in L2
   }
 }
 
@@ -1063,20 +1157,37 @@ struct PartsView {
   int T, k, shared;
 };
 
-// Eight consecutive outputs (chunk g of 8) of token t; pj[j] (j < k) is the
-// bucket position of the token's slot j, or -1.
-__device__ __forceinline__ void combine8(const PartsView& v, int t, int g, int H, const int (&pj)[kMaxTopK],
-                                         float sc, float (&y)[8]) {
+constexpr int kCombChunks = 8;  // 16-byte chunks per lane and pass: 2048 outputs per warp pass
+
+// Outputs of token t in the chunks g = g0 + lane + 32 i (i < kCombChunks,
+// g < G) of 8 values: the sum of the token's partial rows times sc, each row
+// read in one sweep.  pj[j] (j < k) is the bucket position of the token's
+// slot j, or -1.
+__device__ __forceinline__ void combine_block(const PartsView& v, int t, int g0, int G, int H,
+                                              const int (&pj)[kMaxTopK], float sc,
+                                              float (&y)[kCombChunks][8]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = 0.0f;
+  for (int i = 0; i < kCombChunks; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[i][e] = 0.0f;
   auto add = [&](size_t row) {
-    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(v.rows + row * H) + g);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint4* src = reinterpret_cast<const uint4*>(v.rows + row * H);
+    uint4 q[kCombChunks];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      y[2 * i] += f.x;
-      y[2 * i + 1] += f.y;
+    for (int i = 0; i < kCombChunks; ++i) {
+      const int g = g0 + lane + 32 * i;
+      q[i] = g < G ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kCombChunks; ++i) {
+      const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        y[i][2 * e] += f.x;
+        y[i][2 * e + 1] += f.y;
+      }
     }
   };
 #pragma unroll
@@ -1084,7 +1195,9 @@ __device__ __forceinline__ void combine8(const PartsView& v, int t, int g, int H
     if (j < v.k && pj[j] >= 0) add((size_t)pj[j]);
   if (v.shared) add((size_t)v.T * v.k + t);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] *= sc;
+  for (int i = 0; i < kCombChunks; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[i][e] *= sc;
 }
 
 // The bucket positions of token t's slots, read by lanes 0..k-1 and
@@ -1105,22 +1218,28 @@ __global__ void combine_kernel(const PartsView v, int H, uint16_t* __restrict__ 
   combine_pos(v, t, lane, pj);
   const float sc = pow2f(2 * __ldg(v.xshift + t));
   const bool vec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
-  for (int g = lane; g < H / 8; g += 32) {
-    float yy[8];
-    combine8(v, t, g, H, pj, sc, yy);
-    uint32_t o[4];
+  const int G = H / 8;
+  for (int g0 = 0; g0 < G; g0 += 32 * kCombChunks) {
+    float yb[kCombChunks][8];
+    combine_block(v, t, g0, G, H, pj, sc, yb);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yy[2 * q])) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yy[2 * q + 1])) << 16);
-    uint16_t* dst = y + (size_t)t * H + 8 * g;
-    if (vec) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-    } else {
+    for (int i = 0; i < kCombChunks; ++i) {
+      const int g = g0 + lane + 32 * i;
+      if (g >= G) break;
+      uint32_t o[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dst[2 * q] = (uint16_t)(o[q] & 0xffffu);
-        dst[2 * q + 1] = (uint16_t)(o[q] >> 16);
+      for (int q = 0; q < 4; ++q)
+        o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yb[i][2 * q])) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yb[i][2 * q + 1])) << 16);
+      uint16_t* dst = y + (size_t)t * H + 8 * g;
+      if (vec) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dst[2 * q] = (uint16_t)(o[q] & 0xffffu);
+          dst[2 * q + 1] = (uint16_t)(o[q] >> 16);
+        }
       }
     }
   }
@@ -1416,32 +1535,38 @@ __global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const Part
   }
   // pass 1: y (the sum of the layer's partial rows), h', sum of squares
   float ss = 0.0f;
-  for (int g = lane; g < G; g += 32) {
-    uint4 v = hr[g];
-    if (has_y) {
-      float yy[8];
-      combine8(parts, t, g, H, pj, ysc, yy);
+  for (int g0 = 0; g0 < G; g0 += 32 * kCombChunks) {
+    float yb[kCombChunks][8];
+    if (has_y) combine_block(parts, t, g0, G, H, pj, ysc, yb);
+#pragma unroll
+    for (int i = 0; i < kCombChunks; ++i) {
+      const int g = g0 + lane + 32 * i;
+      if (g >= G) break;
+      uint4 v = hr[g];
+      if (has_y) {
+        const float (&yy)[8] = yb[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4], yo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
+          const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
+          const float lo = __uint_as_float(w[q] << 16) + __bfloat162float(ylo);
+          const float hi = __uint_as_float(w[q] & 0xffff0000u) + __bfloat162float(yhi);
+          o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+          yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
+        }
+        v = make_uint4(o[0], o[1], o[2], o[3]);
+        if (y_trace) reinterpret_cast<uint4*>(y_trace + (size_t)t * H)[g] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+      }
+      if (has_y || h_out != h) ho[g] = v;
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4], yo[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
-        const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
-        const float lo = __uint_as_float(w[q] << 16) + __bfloat162float(ylo);
-        const float hi = __uint_as_float(w[q] & 0xffff0000u) + __bfloat162float(yhi);
-        o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-        yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
+        const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
       }
-      v = make_uint4(o[0], o[1], o[2], o[3]);
-      if (y_trace) reinterpret_cast<uint4*>(y_trace + (size_t)t * H)[g] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
-    }
-    if (has_y || h_out != h) ho[g] = v;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
-      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
     }
   }
   if (!norm) return;
@@ -1572,7 +1697,8 @@ moe_status launch_prefill(moe_layer* L, const uint16_t* x, int T, uint16_t* y, i
   {
     prof::Scope sc("moe_topk", s);
     const int rf = c.routing_flags;
-    topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(
+    auto kern = (E <= 256) ? topk_kernel<8> : (E <= 512) ? topk_kernel<16> : topk_kernel<kMaxExperts / 32>;
+    kern<<<(T + 7) / 8, 256, 0, s>>>(
         ws.zf, T, E, k, (rf & MOE_ROUTING_BIAS_SELECT_ONLY) ? L->dev.router_b : nullptr,
         (rf & MOE_ROUTING_NO_RENORM) ? 0 : 1, (rf & MOE_ROUTING_SHARED_GATE) ? L->sh_gate_w : nullptr,
         x, H, L->ws.gw, ids, wts, ws.err);
