@@ -545,9 +545,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       // round of hand-backs per group.  Per group: the raw stages' words
       // into registers (every lane waits for the stage itself, so that its
       // own reads follow the TMA's completion), the raw stages handed back
-      // at once (the arrive orders the reads before the refill), the
-      // dequantisation, and only then the wait for free A stages: the
-      // dequantisation overlaps the MMAs still reading them.
+      // at once (after a proxy fence), the dequantisation, and only then the
+      // wait for free A stages: the dequantisation overlaps the MMAs still
+      // reading them.
       const int r = 32 * (warp & 3) + lane;
       const int part = pi >> 7;
       const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
@@ -586,6 +586,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
               alive = false;
               break;
             }
+            // the stages were read through the generic proxy and are refilled
+            // by TMA (async proxy): fence before handing them back
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
 #pragma unroll
