@@ -75,7 +75,10 @@ enum {
  * 1 <= n_experts <= 1024; 1 <= top_k <= min(16, n_experts);
  * ffn % 128 == 0 and 128 <= ffn <= 4096; shared_ffn == 0 or a multiple of
  * 128 up to 4096; min(n_experts, 4 * top_k) <= n_slots <= n_experts;
- * 1 <= max_tokens <= 65536 (sizes the workspaces); routing_flags a
+ * 1 <= max_tokens <= 65536 (sizes the workspaces: above 4 tokens the
+ * prefill workspace takes about 2 * max_tokens * ((top_k + 2) * hidden +
+ * top_k * ffn + shared_ffn) bytes, 0.6 GB at 8192 tokens of a hidden 2048,
+ * top-10, ffn 768 layer); routing_flags a
  * combination of the MOE_ROUTING_* bits (0: the default routing above).
  * moe_layer_create also refuses shapes whose single-token decode does not
  * fit the decode kernel's 227 KB of shared memory (one 16-row gate/up stage
@@ -162,7 +165,9 @@ moe_status moe_route(moe_layer* layer, const void* x_bf16, int n_tokens, int32_t
 
 /* One layer: y_bf16 [T][H] = layer(x_bf16 [T][H]).  x and y must not
  * overlap.  n_tokens <= 4 runs the decode path (fused dequant GEMVs);
- * larger batches run the prefill path (bucketed grouped GEMM on tcgen05). */
+ * larger batches run the prefill path (bucketed grouped GEMM on tcgen05),
+ * whose results are bit-identical from call to call (each expert's
+ * weighted rows are summed per token in one fixed order). */
 moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void* y_bf16,
                        void* stream);
 
