@@ -114,13 +114,17 @@ struct Gemm {
   static constexpr bool kTmemA = (MODE != kRouter);
   // A matrices per unit: gate and up, or two 128-row tiles of W_d
   static constexpr int NA = (MODE == kRouter) ? 1 : 2;
-  static constexpr int S = (MODE == kRouter) ? 6 : 4;
+  // K steps (of 64) per stage: gate/up and down take two, so that each MMA
+  // issuer waits and commits once per 8 MMAs (its fixed cost per stage is
+  // about as long as four MMAs of 128 tokens)
+  static constexpr int KS = (MODE == kRouter) ? 1 : 2;
+  static constexpr int S = (MODE == kRouter) ? 6 : 2;
   static constexpr int SR = (MODE == kRouter) ? 0 : (MODE == kScatter ? 11 : 12);
   static constexpr int SRb = SR > 0 ? SR : 1;  // barrier slots
   static constexpr int kAccBufs = (MODE == kRouter) ? 2 : 1;
   static constexpr int kAccCols = NA * 128;  // gate | up, or one accumulator
   static constexpr int kACol0 = 256;
-  static constexpr int kACols = NA * 32;     // 64 fp16 of K per matrix = 32 columns
+  static constexpr int kACols = KS * NA * 32;  // per stage: 64 fp16 of K per matrix and step = 32 columns
   static_assert(kAccBufs * kAccCols <= kACol0, "accumulators below the A stages");
   static_assert(!kTmemA || kACol0 + S * kACols <= 512, "A stages fit in TMEM");
   static constexpr int kBWarps = 1;
@@ -135,7 +139,7 @@ struct Gemm {
   static constexpr int kThreads = (kMmaWarp + NA) * 32;
   static constexpr int kRawBytes = NA * kRawTile;  // packed codes of the NA matrices
   static constexpr int kBOff = kTmemA ? 0 : NA * kTileA;       // B tile offset in a stage
-  static constexpr int kStageBytes = kBOff + kTileB;
+  static constexpr int kStageBytes = kBOff + KS * kTileB;
   static constexpr int OFF_RAW = S * kStageBytes;
   static constexpr int OFF_BAR = OFF_RAW + SR * kRawBytes;
   static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 6) + 4) + 127) & ~127;
@@ -156,7 +160,7 @@ struct Gemm {
   // producers take K steps in pairs (every K/64 is even: K is a multiple
   // of 128), halving the per-step waits and fences
   static constexpr int kGroup = (MODE == kRouter) ? 1 : 2;
-  static_assert(MODE == kRouter || (S >= 2 * kGroup && SR >= 2 * kGroup), "ring depth per group");
+  static_assert(MODE == kRouter || (kGroup == KS && SR >= 2 * kGroup), "a producer group fills one stage");
 };
 
 // Tensor maps of one GEMM launch.
@@ -609,12 +613,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
                 o[q][4 * w + 3] = d.w;
               }
             }
-#pragma unroll
-            for (int q = 0; q < P; ++q) {
-              const uint32_t iq = it + q;
-              if (lane == 0 && ok) ok = mbar_wait(&empty[iq % S], ((iq / S) & 1) ^ 1, p.err, tmo);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
-            }
+            const uint32_t bs = it / G::KS;  // the group's stage
+            if (lane == 0) ok = mbar_wait(&empty[bs % S], ((bs / S) & 1) ^ 1, p.err, tmo);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
               alive = false;
               break;
@@ -623,15 +624,13 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             const uint32_t arow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)G::kACol0;
 #pragma unroll
             for (int q = 0; q < P; ++q) {
-              const uint32_t acol = arow + (uint32_t)(((it + q) % S) * G::kACols) + (uint32_t)(part * OW);
+              const uint32_t acol = arow + (uint32_t)((bs % S) * G::kACols + q * NA * 32) + (uint32_t)(part * OW);
               tmem_st32(acol, o[q]);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();  // the warp's stores are complete: one arrive for the warp
-            if (lane == 0)
-#pragma unroll
-              for (int q = 0; q < P; ++q) mbar_arrive(&full_a[(it + q) % S]);
+            if (lane == 0) mbar_arrive(&full_a[bs % S]);
             it += P;
           }
           sq = sn;
@@ -655,26 +654,30 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         const CUtensorMap* tm = (MODE == kRouter) ? &maps.b[0] : &maps.b[U.shared ? 1 : 0];
         const int nks = U.K / 64;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int st = it % S;
+          const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
+          const int st = bs % S;
           uint64_t* fullb = &fulls[st];
-          if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, p.err, tmo)) {
-            alive = false;
-            break;
-          }
-          if (MODE == kRouter) {
-            // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
-            mbar_expect_tx(fullb, (uint32_t)(kTileA + kTileB));
-            tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, fullb);
-          } else {
-            mbar_expect_tx(fullb, (uint32_t)kTileB);
+          if (sub == 0) {
+            if (!mbar_wait(&empty[st], ((bs / S) & 1) ^ 1, p.err, tmo)) {
+              alive = false;
+              break;
+            }
+            if (MODE == kRouter) {
+              // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
+              mbar_expect_tx(fullb, (uint32_t)(kTileA + kTileB));
+              tma_load_2d(smem + st * G::kStageBytes, &maps.a_routed[0], ks * 64, U.mt * 128, fullb);
+            } else {
+              mbar_expect_tx(fullb, (uint32_t)(G::KS * kTileB));  // the stage's K steps
+            }
           }
           const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
-          tma_load_2d(smem + st * G::kStageBytes + G::kBOff, tm, col, U.p0, fullb);
+          tma_load_2d(smem + st * G::kStageBytes + G::kBOff + sub * kTileB, tm, col, U.p0, fullb);
         }
       }
       // let every copy this thread issued land before the CTA can exit
-      const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-      for (uint32_t q = first; q < it; ++q) drain_wait(&fulls[q % S], (q / S) & 1, tmo);
+      const uint32_t nst = (it + G::KS - 1) / G::KS;
+      const uint32_t first = nst > (uint32_t)S ? nst - S : 0u;
+      for (uint32_t q = first; q < nst; ++q) drain_wait(&fulls[q % S], (q / S) & 1, tmo);
     }
     __syncwarp();
   } else if (warp < kMmaWarp) {
@@ -738,17 +741,19 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         const int nks = U.K / 64;
         bool ok = true;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int st = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(MODE == kRouter ? &full_b[st] : &full_a[st], ph, p.err, tmo)) {
-            ok = false;
-            break;
+          const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
+          const int st = bs % S;
+          if (sub == 0) {
+            if (!mbar_wait(MODE == kRouter ? &full_b[st] : &full_a[st], (bs / S) & 1, p.err, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
           const uint32_t s_addr = smem_u32(smem + st * G::kStageBytes);
-          const uint64_t db = smem_desc_sw128(s_addr + G::kBOff);
+          const uint64_t db = smem_desc_sw128(s_addr + G::kBOff + sub * kTileB);
           if constexpr (G::kTmemA) {
-            const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols + 32 * m);
+            const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols + sub * NA * 32 + 32 * m);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // 16 K = 8 TMEM columns per MMA
               umma_f16_ts(d, a0 + 8 * kk, db + 2 * kk, idesc, (ks | kk) ? 1u : 0u);
@@ -757,7 +762,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) umma_f16(d, da0 + 2 * kk, db + 2 * kk, idesc, (ks | kk) ? 1u : 0u);
           }
-          umma_commit(&empty[st]);
+          if (sub == G::KS - 1) umma_commit(&empty[st]);
         }
         if (!ok) break;
         umma_commit(&tfull[b]);
