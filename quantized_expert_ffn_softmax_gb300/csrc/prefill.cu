@@ -145,13 +145,13 @@ struct Gemm {
   static constexpr int kBarBytes = ((8 * (3 * S + 2 * SRb + 6) + 4) + 127) & ~127;
   static constexpr int OFF_META = OFF_BAR + kBarBytes;
   // gate/up and down: the unit's outputs staged as fp16 [128 or 256 rows of
-  // the accumulators][kNT tokens, padded to kTS] so the accumulators are
-  // released as soon as they are read (each thread stores its row's tokens
-  // 16 bytes at a time; the 272-byte row stride keeps those stores free of
-  // bank conflicts); the write-out transposes to token-major rows
-  static constexpr int kTS = kNT + 8;
+  // the accumulators][kNT tokens] so the accumulators are released as soon
+  // as they are read; the write-out transposes to token-major rows.  The
+  // 16-byte chunks of a row are XOR-swizzled (stage_off) so that both the
+  // drain's row-wise stores and the write-out's column-wise loads are free
+  // of bank conflicts.
   static constexpr int kHRows = (MODE == kScatter) ? 256 : 128;
-  static constexpr int kHStage = (MODE != kRouter) ? kHRows * kTS * 2 : 0;
+  static constexpr int kHStage = (MODE != kRouter) ? kHRows * kNT * 2 : 0;
   static constexpr int OFF_HST = OFF_META + 8 * kNT;
   static constexpr int kSmem = OFF_HST + kHStage + 1024;  // + slack for 1 KB alignment
   static_assert(kThreads <= 16 * 32, "at most 16 warps");
@@ -270,6 +270,14 @@ __device__ __forceinline__ uint4 load_scale_quad(const uint16_t* srow, int s0, i
   if (s0 + 2 < nks) v.z = __ldg(w + 2);
   if (s0 + 3 < nks) v.w = __ldg(w + 3);
   return v;
+}
+
+// Offset (fp16 elements) of chunk j (tokens 8j..8j+7) of staging row `row`:
+// rows of kNT tokens, chunk slots XOR-swizzled by the row and the row's
+// 8-group, so 8 consecutive rows writing one chunk, or 8 rows 8 apart
+// reading one chunk, touch 8 different 16-byte bank groups.
+__device__ __forceinline__ int stage_off(int row, int j) {
+  return row * kNT + (((j & ~7) | ((j ^ row ^ (row >> 3)) & 7)) << 3);
 }
 
 template <int MODE>
@@ -404,9 +412,8 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             hv[jj / 2] = __hmul2(silu_fast2(g), u);
           }
           static_assert(CW == 16, "two 16-byte stores per chunk");
-          uint4* dst = reinterpret_cast<uint4*>(hst + r * G::kTS + c0);
-          dst[0] = *reinterpret_cast<const uint4*>(&hv[0]);
-          dst[1] = *reinterpret_cast<const uint4*>(&hv[4]);
+          *reinterpret_cast<uint4*>(hst + stage_off(r, c0 >> 3)) = *reinterpret_cast<const uint4*>(&hv[0]);
+          *reinterpret_cast<uint4*>(hst + stage_off(r, (c0 >> 3) + 1)) = *reinterpret_cast<const uint4*>(&hv[4]);
           if (more) {
             tmem_wait_ld();
 #pragma unroll
@@ -444,12 +451,10 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             c[jj / 2] = __floats2half2_rn(__uint_as_float(v1[jj]) * tf[jj], __uint_as_float(v1[jj + 1]) * tf[jj + 1]);
           }
           static_assert(CW == 16, "two 16-byte stores per chunk and half");
-          uint4* d0 = reinterpret_cast<uint4*>(hst + r * G::kTS + c0);
-          uint4* d1 = reinterpret_cast<uint4*>(hst + (128 + r) * G::kTS + c0);
-          d0[0] = *reinterpret_cast<const uint4*>(&a[0]);
-          d0[1] = *reinterpret_cast<const uint4*>(&a[4]);
-          d1[0] = *reinterpret_cast<const uint4*>(&c[0]);
-          d1[1] = *reinterpret_cast<const uint4*>(&c[4]);
+          *reinterpret_cast<uint4*>(hst + stage_off(r, c0 >> 3)) = *reinterpret_cast<const uint4*>(&a[0]);
+          *reinterpret_cast<uint4*>(hst + stage_off(r, (c0 >> 3) + 1)) = *reinterpret_cast<const uint4*>(&a[4]);
+          *reinterpret_cast<uint4*>(hst + stage_off(128 + r, c0 >> 3)) = *reinterpret_cast<const uint4*>(&c[0]);
+          *reinterpret_cast<uint4*>(hst + stage_off(128 + r, (c0 >> 3) + 1)) = *reinterpret_cast<const uint4*>(&c[4]);
           if (more) {
             tmem_wait_ld();
 #pragma unroll
@@ -508,13 +513,15 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
         // output chunk per token.  Gate/up: row 8c+i goes to position
         // 8c + (0,2,4,6,1,3,5,7)[i], the unpack order of the down GEMM's K,
         // so output word j pairs rows j and j+4; down: rows 2j and 2j+1.
+        // Consecutive lanes take consecutive chunks c of the same tokens, so
+        // each warp store writes whole contiguous row segments.
         const int ntb = (U.n + 7) >> 3;
         for (int blk = r; blk < nch * ntb; blk += kEpiWarps * 32) {
-          const int c = blk / ntb, tb = blk % ntb;
+          const int c = blk % nch, tb = blk / nch;
           uint4 rows[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            rows[i] = *reinterpret_cast<const uint4*>(hst + (8 * c + i) * G::kTS + 8 * tb);
+            rows[i] = *reinterpret_cast<const uint4*>(hst + stage_off(8 * c + i, tb));
 #pragma unroll
           for (int tt = 0; tt < 8; ++tt) {
             const int t = 8 * tb + tt;
