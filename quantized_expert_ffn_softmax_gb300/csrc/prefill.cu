@@ -18,12 +18,12 @@
 //              (operand B of the routed gate/up GEMM)
 //   gate/up    per unit (expert, 128-token tile, 128-row F tile):
 //              D_g, D_u = W_g/u[128 x H] . X[tokens]^T in TMEM, epilogue
-//              h = silu(g) * u -> fp16 rows of Hmid (bucket order)
+//              h = w * silu(g) * u -> fp16 rows of Hmid (bucket order; w the
+//              assignment's routing weight or the shared expert's gate)
 //   down       per unit (expert, token tile, 256-row H tile as two 128-row
 //              A matrices): D = W_d[256 x F] . Hmid[tokens]^T, epilogue
-//              w * D as fp16 rows of a partial-output buffer (bucket order;
-//              the shared expert's rows after the routed ones, in token
-//              order)
+//              D as fp16 rows of a partial-output buffer (bucket order; the
+//              shared expert's rows after the routed ones, in token order)
 //   combine    per token, the sum of its k + 1 partial rows -> bf16 y (in a
 //              prefill-sized stack, inside the layer-boundary kernel)
 //
@@ -350,16 +350,17 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       named_bar_sync(1, kEpiWarps * 32);  // the previous unit is done with meta
       if (r < U.n) {
         if (MODE == kSwiglu) {
-          // D * 2^sx restores x; h is stored * 2^-2sx, i.e. silu(g) * D_u * 2^-sx
+          // D * 2^sx restores x; h is stored * w * 2^-2sx, i.e.
+          // silu(g) * (D_u * w * 2^-sx): the routing weight w (or the shared
+          // expert's gate) rides on u's factor, exactly (a power of two
+          // times w), so that the down GEMM's output needs no factor; the
+          // combine restores 2^2sx per token
           const int tok = U.shared ? (U.p0 + r) : __ldg(p.perm_tok + U.p0 + r);
           const int sx = __ldg(p.xshift + tok);
+          const float w = U.shared ? (p.gw ? __ldg(p.gw + tok) : 1.0f) : __ldg(p.perm_w + U.p0 + r);
           meta_f[r] = pow2f(sx);
-          reinterpret_cast<float*>(meta_i)[r] = pow2f(-sx);
-        } else if (MODE == kScatter) {
-          // the routing weight (or the shared expert's gate); the rows keep
-          // the inputs' 2^-2sx, which the combine restores per token
-          meta_f[r] = U.shared ? (p.gw ? __ldg(p.gw + U.p0 + r) : 1.0f) : __ldg(p.perm_w + U.p0 + r);
-        } else {
+          reinterpret_cast<float*>(meta_i)[r] = pow2f(-sx) * w;
+        } else if (MODE == kRouter) {
           meta_f[r] = pow2f(__ldg(p.xshift + U.p0 + r) - p.router_shift);
         }
       }
@@ -424,9 +425,9 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           }
         }
       } else if constexpr (MODE == kScatter) {
-        // drain: w * D of both 128-row halves as fp16 into the staging rows
-        // [token][256]; the next chunk's TMEM loads are issued before this
-        // chunk is processed
+        // drain: D of both 128-row halves (the SwiGLU rows already carry the
+        // routing weight) as fp16 into the staging rows [token][256]; the
+        // next chunk's TMEM loads are issued before this chunk is processed
         uint32_t v0[CW], v1[CW];
         tmem_ld(tbase, v0);
         tmem_ld(tbase + 128, v1);
@@ -438,17 +439,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             tmem_ld(tbase + c0 + CW, n0);
             tmem_ld(tbase + 128 + c0 + CW, n1);
           }
-          float tf[CW];
-#pragma unroll
-          for (int q = 0; q < CW; q += 4) {
-            const float4 vf = *reinterpret_cast<const float4*>(meta_f + c0 + q);
-            tf[q] = vf.x, tf[q + 1] = vf.y, tf[q + 2] = vf.z, tf[q + 3] = vf.w;
-          }
           __half2 a[CW / 2], c[CW / 2];
 #pragma unroll
           for (int jj = 0; jj < CW; jj += 2) {
-            a[jj / 2] = __floats2half2_rn(__uint_as_float(v0[jj]) * tf[jj], __uint_as_float(v0[jj + 1]) * tf[jj + 1]);
-            c[jj / 2] = __floats2half2_rn(__uint_as_float(v1[jj]) * tf[jj], __uint_as_float(v1[jj + 1]) * tf[jj + 1]);
+            a[jj / 2] = __floats2half2_rn(__uint_as_float(v0[jj]), __uint_as_float(v0[jj + 1]));
+            c[jj / 2] = __floats2half2_rn(__uint_as_float(v1[jj]), __uint_as_float(v1[jj + 1]));
           }
           static_assert(CW == 16, "two 16-byte stores per chunk and half");
           *reinterpret_cast<uint4*>(hst + stage_off(r, c0 >> 3)) = *reinterpret_cast<const uint4*>(&a[0]);
