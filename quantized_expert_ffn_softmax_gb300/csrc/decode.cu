@@ -452,32 +452,37 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   };
 
   // ------------------------------------------------ the copy warp
-  // Issuing a bulk or tensor copy costs its thread on the order of 150 ns,
-  // so one warp issues them all and the compute warps only wait on the
-  // mbarriers: per layer, the next layer's router rows once this CTA's
-  // router product has read the buffer, then (after the unit list) the
-  // first gate/up items, the first down block and the next layer's slot
-  // table, and refills as the compute warps release stages.
+  // One warp issues every bulk and tensor copy and the compute warps only
+  // wait on the mbarriers: per layer, the next layer's router rows once this
+  // CTA's router product has read the buffer, then (after the unit list)
+  // the first gate/up items, the first down block and the next layer's slot
+  // table, and refills as the compute warps release stages.  The warp stays
+  // converged; each group of copies is issued by one elected lane
+  // (elect.sync): copies issued from lane-divergent code are taken one lane
+  // at a time, each at a multiple of the cost.
   if (warp == kWarps) {
     auto issue_rows = [&](int l) {  // all lanes
       const LayerDev& W = p.layers[l];
       const int rows = router_rows(l);
-      if (lane == 0 && rows) mbar_expect_tx(&mbar[kBarR], (uint32_t)rows * H * 4u);
-      __syncwarp();
-      for (int j = lane; j < rows; j += 32) {
-        const int e = blockIdx.x + j * grid;
-        bulk_g2s(wr + (size_t)j * H, (!kVar || e < E) ? W.router_w + (size_t)e * H : p.sh_gate_w[l],
-                 H * 4u, &mbar[kBarR]);
+      if (rows && elect_one()) {
+        mbar_expect_tx(&mbar[kBarR], (uint32_t)rows * H * 4u);
+        for (int j = 0; j < rows; ++j) {
+          const int e = blockIdx.x + j * grid;
+          bulk_g2s(wr + (size_t)j * H, (!kVar || e < E) ? W.router_w + (size_t)e * H : p.sh_gate_w[l],
+                   H * 4u, &mbar[kBarR]);
+        }
       }
+      __syncwarp();
     };
-    auto issue_slots = [&](int l) {  // lane 0
-      if (lane == 0 && slots_bulk_of(l)) {
+    auto issue_slots = [&](int l) {  // all lanes
+      if (slots_bulk_of(l) && elect_one()) {
         mbar_expect_tx(&mbar[kBarS], (uint32_t)E * 4u);
         bulk_g2s(slots, p.layers[l].slot_of, (uint32_t)E * 4u, &mbar[kBarS]);
       }
+      __syncwarp();
     };
-    // gate/up item q into stage q % NG: lane 0 arms the stage, lanes 0..3
-    // issue one copy each
+    // gate/up item q into stage q % NG: one elected lane arms the stage and
+    // issues its four copies
     auto issue_g = [&](int l, int q, int n_routed) {
       const LayerDev& W = p.layers[l];
       const int it = item_of(q);
@@ -502,16 +507,18 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       }
       unsigned char* st = gbuf + (size_t)(q % NG) * L.g_stage;
       uint64_t* bar = &mbar[kBarG0 + (q % NG)];
-      if (lane == 0) mbar_expect_tx(bar, (uint32_t)L.g_stage);
+      if (elect_one()) {
+        mbar_expect_tx(bar, (uint32_t)L.g_stage);
+        bulk_g2s(st, gq, 16u * (H / 2), bar);
+        bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
+        bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
+        bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
+      }
       __syncwarp();
-      if (lane == 0) bulk_g2s(st, gq, 16u * (H / 2), bar);
-      else if (lane == 1) bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
-      else if (lane == 2) bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
-      else if (lane == 3) bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
     };
     // Down block of work unit j: codes of every output row, row r at
     // position (r % 4) * H/4 + r / 4 (4-D TMA boxes), and the block's H scales
-    // from the block-major copy (one bulk copy); lanes in parallel.
+    // from the block-major copy (one bulk copy); one elected lane.
     auto issue_d = [&](int l, int j, int n_routed) {
       const LayerDev& W = p.layers[l];
       int u, b;
@@ -519,19 +526,17 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       const bool routed = u < n_routed;
       const size_t slot = routed ? (size_t)M.unit_slot[u] : 0;
       const int QB = down_qbox(H), nqb = Hq / QB;
-      if (lane == 0) mbar_expect_tx(&mbar[kBarD], (uint32_t)H * 18u);
-      __syncwarp();
       const CUtensorMap* tm = routed ? &p.tm_down[l] : &p.tm_sh_down[l];
-      for (int i = lane; i <= 4 * nqb; i += 32) {
-        if (i < 4 * nqb) {
-          const int jr = i / nqb, qb = i - jr * nqb;
-          tma_load_4d(dst_s + ((size_t)jr * Hq + (size_t)qb * QB) * 16, tm, 16 * b, jr, qb * QB,
-                      (int)slot, &mbar[kBarD]);
-        } else {
-          const uint16_t* sb = routed ? W.down_sb + (slot * CF + b) * H : W.sh_down_sb + (size_t)b * H;
-          bulk_g2s(dst_s + (size_t)H * 16, sb, (uint32_t)H * 2u, &mbar[kBarD]);
-        }
+      if (elect_one()) {
+        mbar_expect_tx(&mbar[kBarD], (uint32_t)H * 18u);
+        for (int jr = 0; jr < 4; ++jr)
+          for (int qb = 0; qb < nqb; ++qb)
+            tma_load_4d(dst_s + ((size_t)jr * Hq + (size_t)qb * QB) * 16, tm, 16 * b, jr, qb * QB,
+                        (int)slot, &mbar[kBarD]);
+        const uint16_t* sb = routed ? W.down_sb + (slot * CF + b) * H : W.sh_down_sb + (size_t)b * H;
+        bulk_g2s(dst_s + (size_t)H * 16, sb, (uint32_t)H * 2u, &mbar[kBarD]);
       }
+      __syncwarp();
     };
     // waits by lane 0, result shared with the warp (lanes stay converged)
     auto wait0 = [&](uint64_t* bar, uint32_t parity) {

@@ -194,6 +194,22 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
+// One lane of a converged warp (elect.sync over the full mask).  The PTX ISA
+// defines the election as deterministic: the same mask elects the same lane
+// every time, so MMAs and the commits that track them, issued under
+// separate elections, come from one thread.  Issuing tcgen05 and TMA
+// instructions under this predicate, inside warp-uniform control flow, lets
+// them take warp-uniform operands directly: on this part an MMA then costs
+// its issuing warp about 16 cycles instead of about 50 when the same loop
+// runs inside `if (lane == 0)`.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }

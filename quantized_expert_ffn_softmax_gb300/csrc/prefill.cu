@@ -34,16 +34,20 @@
 //               each thread reading its own row's block scales from global
 //               memory four K steps per load; the router's A tiles come
 //               ready-made by TMA instead
-//   B loader    one thread loads the unit's contiguous token rows (bucket
-//               order; the shared expert's in token order) as one TMA tile
-//               per K step, 128-byte swizzled K-major
-//   raw loader  one thread: TMA tiles of packed codes (128 rows x 32 bytes
-//               per matrix and K step) into a raw ring
-//   MMA warps   one tcgen05.mma issuer thread per A matrix (gate/up and
-//               down: two warps; router: one), A from tensor memory, B from
-//               shared memory; the first also allocates TMEM
-// A stage ring (the A slots in TMEM and a B tile in shared memory per stage,
-// 4 stages) feeds the MMAs, one tcgen05.commit per step and issuer.  The two
+//   B loader    one warp, one elected lane issuing: the unit's contiguous
+//               token rows (bucket order; the shared expert's in token
+//               order) as one TMA tile per K step, 128-byte swizzled K-major
+//   raw loader  one warp, one elected lane issuing: TMA tiles of packed
+//               codes (128 rows x 32 bytes per matrix and K step) into a
+//               raw ring
+//   MMA warps   one warp per A matrix (gate/up and down: two; router: one),
+//               one elected lane issuing tcgen05.mma, A from tensor memory,
+//               B from shared memory; the first also allocates TMEM
+// Every role runs its loop warp-wide and issues its tcgen05 and TMA
+// instructions under elect.sync: issued from inside `if (lane == 0)` an
+// MMA costs its thread about three times as long.  A stage ring (two
+// stages of two K steps: the A slots in TMEM, two B tiles in shared memory)
+// feeds the MMAs, one tcgen05.commit per stage and issuer.  The two
 // 128-column accumulators fill TMEM's lower half; the epilogue stages the
 // unit's output rows in shared memory and releases them early.
 // Every wait is bounded and gives up once the error word is set.
@@ -646,24 +650,26 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
     // (shared expert), down the SwiGLU rows, the router x16 and, on the
     // same barrier, its A tile.  Rows past a unit's end belong to the next
     // unit (or read as zero past the buffer); their columns are discarded.
+    // The warp runs the loop (warp-uniform waits and exits); one elected
+    // lane issues the copies.
     uint32_t it = 0;
     bool alive = true;
     uint64_t* fulls = (MODE == kRouter) ? full_b : full_a;  // the stage's ready barriers
-    if (lane == 0) {
-      const int kpp = p.H / 64;
-      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
-        const UnitInfo U = unit_info<MODE>(p, u);
-        const CUtensorMap* tm = (MODE == kRouter) ? &maps.b[0] : &maps.b[U.shared ? 1 : 0];
-        const int nks = U.K / 64;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
-          const int st = bs % S;
-          uint64_t* fullb = &fulls[st];
+    const int kpp = p.H / 64;
+    for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+      const UnitInfo U = unit_info<MODE>(p, u);
+      const CUtensorMap* tm = (MODE == kRouter) ? &maps.b[0] : &maps.b[U.shared ? 1 : 0];
+      const int nks = U.K / 64;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
+        const int st = bs % S;
+        uint64_t* fullb = &fulls[st];
+        if (sub == 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((bs / S) & 1) ^ 1, p.err, tmo))) {
+          alive = false;
+          break;
+        }
+        if (elect_one()) {
           if (sub == 0) {
-            if (!mbar_wait(&empty[st], ((bs / S) & 1) ^ 1, p.err, tmo)) {
-              alive = false;
-              break;
-            }
             if (MODE == kRouter) {
               // router: the A tile (fp16 hi | mid router weights) rides on the same barrier
               mbar_expect_tx(fullb, (uint32_t)(kTileA + kTileB));
@@ -675,85 +681,92 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           const int col = ((MODE == kRouter) ? (ks % kpp) : ks) * 64;
           tma_load_2d(smem + st * G::kStageBytes + G::kBOff + sub * kTileB, tm, col, U.p0, fullb);
         }
+        __syncwarp();
       }
-      // let every copy this thread issued land before the CTA can exit
-      const uint32_t nst = (it + G::KS - 1) / G::KS;
-      const uint32_t first = nst > (uint32_t)S ? nst - S : 0u;
-      for (uint32_t q = first; q < nst; ++q) drain_wait(&fulls[q % S], (q / S) & 1, tmo);
     }
+    // let every copy this warp issued land before the CTA can exit
+    const uint32_t nst = (it + G::KS - 1) / G::KS;
+    const uint32_t first = nst > (uint32_t)S ? nst - S : 0u;
+    for (uint32_t q = first; q < nst; ++q) drain_wait(&fulls[q % S], (q / S) & 1, tmo);
     __syncwarp();
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ raw loader
     // Per K step: one TMA tile of packed codes (128 rows x 32 bytes) per
     // matrix into the raw ring.  (The block scales are read by the
-    // producers themselves, four K steps per load.)
+    // producers themselves, four K steps per load.)  The warp runs the
+    // loop; one elected lane issues the copies.
     if constexpr (SR > 0) {
-      if (lane == 0) {
-        uint32_t it = 0;
-        bool alive = true;
-        const LayerDev& Wd = p.W;
-        for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
-          const UnitInfo U = unit_info<MODE>(p, u);
-          const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
-          const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
-          // gate/up: both matrices at the F tile's rows; down: the two
-          // 128-row halves of the 256-row H tile (past H: the next expert's
-          // rows or zero fill, never used)
-          const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * (MODE == kScatter ? 256 : 128);
-          const int row1 = (MODE == kScatter) ? row + 128 : row;
-          const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
-          const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
-          const int nks = U.K / 64;
-          for (int ks = 0; ks < nks; ++ks, ++it) {
-            const int sr = it % SR;
-            if (!mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo)) {
-              alive = false;
-              break;
-            }
+      uint32_t it = 0;
+      bool alive = true;
+      const LayerDev& Wd = p.W;
+      for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        const int slot = U.shared ? 0 : __ldg(Wd.slot_of + U.e);
+        const int rows_per_slot = (MODE == kSwiglu) ? p.F : p.H;
+        // gate/up: both matrices at the F tile's rows; down: the two
+        // 128-row halves of the 256-row H tile (past H: the next expert's
+        // rows or zero fill, never used)
+        const int row = (U.shared ? 0 : slot * rows_per_slot) + U.mt * (MODE == kScatter ? 256 : 128);
+        const int row1 = (MODE == kScatter) ? row + 128 : row;
+        const CUtensorMap* m0 = U.shared ? &maps.a_shared[0] : &maps.a_routed[0];
+        const CUtensorMap* m1 = U.shared ? &maps.a_shared[1] : &maps.a_routed[1];
+        const int nks = U.K / 64;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int sr = it % SR;
+          if (!__all_sync(0xffffffffu, mbar_wait(&raw_empty[sr], ((it / SR) & 1) ^ 1, p.err, tmo))) {
+            alive = false;
+            break;
+          }
+          if (elect_one()) {
             unsigned char* dst = sR + sr * G::kRawBytes;
             mbar_expect_tx(&raw_full[sr], (uint32_t)(NA * kRawTile));
             tma_load_2d(dst, m0, ks * 32, row, &raw_full[sr]);
             if (NA == 2) tma_load_2d(dst + kRawTile, m1, ks * 32, row1, &raw_full[sr]);
           }
+          __syncwarp();
         }
-        const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
-        for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
       }
+      const uint32_t first = it > (uint32_t)SR ? it - SR : 0u;
+      for (uint32_t q = first; q < it; ++q) drain_wait(&raw_full[q % SR], (q / SR) & 1, tmo);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer m (warp kMmaWarp + m, lane 0) issues the MMAs of A matrix m
-    // (gate or up; the only matrix of down and router) into accumulator
-    // column block m.  Both wait for the same stages; a stage is released,
-    // and an accumulator published, when every issuer has committed.
+    // Issuer m (warp kMmaWarp + m) issues the MMAs of A matrix m (gate or
+    // up; the only matrix of down and router) into accumulator column block
+    // m.  Both wait for the same stages; a stage is released, and an
+    // accumulator published, when every issuer has committed.  The whole
+    // warp runs the loop and waits on the barriers (the exits stay
+    // warp-uniform); one elected lane issues the MMAs and the commits (the
+    // same lane every time: a commit tracks its own thread's MMAs).
     const int m = warp - kMmaWarp;
-    if (lane == 0) {
-      uint32_t it = 0;
-      int j = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
-        const UnitInfo U = unit_info<MODE>(p, u);
-        const int neff = (U.n + 15) & ~15;
-        const int b = (G::kAccBufs == 2) ? (j & 1) : 0;
-        const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
-        if (!mbar_wait(&tempty[b], tpar ^ 1, p.err, tmo)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * G::kAccCols + 128 * m);
-        const uint32_t idesc = idesc_f16_m128(neff);
-        const int nks = U.K / 64;
-        bool ok = true;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
-          const int st = bs % S;
-          if (sub == 0) {
-            if (!mbar_wait(MODE == kRouter ? &full_b[st] : &full_a[st], (bs / S) & 1, p.err, tmo)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+    uint32_t it = 0;
+    int j = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
+      const UnitInfo U = unit_info<MODE>(p, u);
+      const int neff = (U.n + 15) & ~15;
+      const int b = (G::kAccBufs == 2) ? (j & 1) : 0;
+      const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[b], tpar ^ 1, p.err, tmo))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(b * G::kAccCols + 128 * m);
+      const uint32_t idesc = idesc_f16_m128(neff);
+      const int nks = U.K / 64;
+      bool ok = true;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const uint32_t bs = it / G::KS, sub = it % G::KS;  // stage, K step within it
+        const int st = bs % S;
+        if (sub == 0) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(MODE == kRouter ? &full_b[st] : &full_a[st], (bs / S) & 1, p.err, tmo))) {
+            ok = false;
+            break;
           }
-          const uint32_t s_addr = smem_u32(smem + st * G::kStageBytes);
-          const uint64_t db = smem_desc_sw128(s_addr + G::kBOff + sub * kTileB);
+          tc_fence_after();
+        }
+        const uint32_t s_addr = smem_u32(smem + st * G::kStageBytes);
+        const uint64_t db = smem_desc_sw128(s_addr + G::kBOff + sub * kTileB);
+        if (elect_one()) {
           if constexpr (G::kTmemA) {
             const uint32_t a0 = tmem + (uint32_t)(G::kACol0 + st * G::kACols + sub * NA * 32 + 32 * m);
 #pragma unroll
@@ -766,16 +779,19 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
           }
           if (sub == G::KS - 1) umma_commit(&empty[st]);
         }
-        if (!ok) break;
-        umma_commit(&tfull[b]);
+        __syncwarp();
       }
-      // Normally the epilogue has consumed every committed accumulator.  On
-      // an error path, wait (bounded) until this thread's MMAs are complete,
-      // so that none still writes TMEM when it is released.
-      if (ld_relaxed_i32(p.err) != 0) {
-        umma_commit(&tdrain[m]);
-        drain_wait(&tdrain[m], 0, tmo);
-      }
+      if (!ok) break;
+      if (elect_one()) umma_commit(&tfull[b]);
+      __syncwarp();
+    }
+    // Normally the epilogue has consumed every committed accumulator.  On
+    // an error path, wait (bounded) until this warp's MMAs are complete, so
+    // that none still writes TMEM when it is released.
+    if (__any_sync(0xffffffffu, ld_relaxed_i32(p.err) != 0)) {
+      if (elect_one()) umma_commit(&tdrain[m]);
+      __syncwarp();
+      drain_wait(&tdrain[m], 0, tmo);
     }
     __syncwarp();
   }
