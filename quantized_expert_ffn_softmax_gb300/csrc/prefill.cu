@@ -200,6 +200,17 @@ struct UnitInfo {
 };
 
 template <int MODE>
+__device__ __forceinline__ UnitInfo unit_from(const GemmParams& p, int4 v) {
+  UnitInfo U;
+  U.e = v.x;
+  U.p0 = v.y;
+  U.n = v.z;
+  U.mt = v.w;
+  U.shared = (v.x == p.E);
+  U.K = (MODE == kSwiglu) ? p.H : (U.shared ? p.Fs : p.F);
+  return U;
+}
+template <int MODE>
 __device__ __forceinline__ UnitInfo unit_info(const GemmParams& p, int u) {
   UnitInfo U;
   if (MODE == kRouter) {
@@ -212,13 +223,7 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmParams& p, int u) {
     U.shared = false;
     U.K = 2 * p.H;
   } else {
-    const int4 v = p.units[u];
-    U.e = v.x;
-    U.p0 = v.y;
-    U.n = v.z;
-    U.mt = v.w;
-    U.shared = (v.x == p.E);
-    U.K = (MODE == kSwiglu) ? p.H : (U.shared ? p.Fs : p.F);
+    U = unit_from<MODE>(p, p.units[u]);
   }
   return U;
 }
@@ -244,12 +249,12 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
 }
 
 // First block scale of weight row r of the A matrix `part` of a unit (gate
-// or up of the F tile; the first or second 128 rows of the H tile), or null
-// for rows past the matrix.
+// or up of the F tile; the first or second 128 rows of the H tile) whose
+// expert sits in `slot`, or null for rows past the matrix.
 template <int MODE>
-__device__ __forceinline__ const uint16_t* scale_row(const GemmParams& p, const UnitInfo& U, int part, int r) {
+__device__ __forceinline__ const uint16_t* scale_row(const GemmParams& p, const UnitInfo& U, int slot, int part,
+                                                     int r) {
   const LayerDev& W = p.W;
-  const int slot = U.shared ? 0 : __ldg(W.slot_of + U.e);
   const size_t C = (size_t)(U.K / 32);
   if (MODE == kSwiglu) {
     const size_t row = (U.shared ? 0 : (size_t)slot * p.F) + (size_t)U.mt * 128 + r;
@@ -370,9 +375,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       }
       const int b = (G::kAccBufs == 2) ? (j & 1) : 0;
       const uint32_t tpar = (G::kAccBufs == 2) ? ((j >> 1) & 1) : (j & 1);
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&tfull[b], tpar, p.err, tmo);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[b], tpar, p.err, tmo));
       // meta is ready, and the four warps agree on whether to go on (the
       // break must be uniform: the named barriers wait for all of them)
       if (!named_bar_and(1, kEpiWarps * 32, ok)) break;
@@ -563,15 +566,38 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
       constexpr int P = G::kGroup;
       constexpr int OW = 32;  // TMEM columns per thread and step: 64 fp16
+      // This row's block scales: one 32-bit word (two fp16) per K step, read
+      // four steps at a time, a quad ahead of their use; the next unit's
+      // first quad during the current unit's last one.  The next unit's
+      // descriptor is read at the start of a unit and its expert's slot one
+      // quad later, so that no chain of dependent loads stalls a unit start.
+      int nks = 0;
+      const uint16_t* srow = nullptr;
+      uint4 sq = make_uint4(0u, 0u, 0u, 0u);
+      if ((int)blockIdx.x < n_units) {
+        const UnitInfo U0 = unit_info<MODE>(p, blockIdx.x);
+        nks = U0.K / 64;
+        srow = scale_row<MODE>(p, U0, U0.shared ? 0 : __ldg(p.W.slot_of + U0.e), part, r);
+        sq = load_scale_quad(srow, 0, nks);
+      }
       for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
-        const UnitInfo U = unit_info<MODE>(p, u);
-        const int nks = U.K / 64;
-        // this row's block scales, one 32-bit word (two fp16) per K step,
-        // read four steps at a time, a quad ahead of their use
-        const uint16_t* srow = scale_row<MODE>(p, U, part, r);
-        uint4 sq = load_scale_quad(srow, 0, nks);
+        const bool has_next = u + (int)gridDim.x < n_units;
+        const int4 vn = has_next ? p.units[u + gridDim.x] : make_int4(0, 0, 0, 0);
+        int slot_n = 0, nks_n = 0;
+        const uint16_t* srow_n = nullptr;
         for (int ks0 = 0; ks0 < nks && alive; ks0 += 4) {
-          const uint4 sn = (ks0 + 4 < nks) ? load_scale_quad(srow, ks0 + 4, nks) : sq;
+          const bool last = ks0 + 4 >= nks;
+          if (has_next && (ks0 == 4 || (last && ks0 < 4)))
+            slot_n = (vn.x == p.E) ? 0 : __ldg(p.W.slot_of + vn.x);
+          uint4 sn = sq;
+          if (!last) {
+            sn = load_scale_quad(srow, ks0 + 4, nks);
+          } else if (has_next) {
+            const UnitInfo Un = unit_from<MODE>(p, vn);
+            nks_n = Un.K / 64;
+            srow_n = scale_row<MODE>(p, Un, slot_n, part, r);
+            sn = load_scale_quad(srow_n, 0, nks_n);
+          }
           const uint32_t sqw[4] = {sq.x, sq.y, sq.z, sq.w};
 #pragma unroll
           for (int dd = 0; dd < 4; dd += P) {
@@ -600,9 +626,10 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             // by TMA (async proxy): fence before handing them back
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0)
+            if (elect_one())
 #pragma unroll
               for (int q = 0; q < P; ++q) mbar_arrive(&raw_empty[(it + q) % SR]);
+            __syncwarp();
             uint32_t o[P][OW];
 #pragma unroll
             for (int q = 0; q < P; ++q) {
@@ -620,8 +647,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
               }
             }
             const uint32_t bs = it / G::KS;  // the group's stage
-            if (lane == 0) ok = mbar_wait(&empty[bs % S], ((bs / S) & 1) ^ 1, p.err, tmo);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = __all_sync(0xffffffffu, mbar_wait(&empty[bs % S], ((bs / S) & 1) ^ 1, p.err, tmo));
             if (!ok) {
               alive = false;
               break;
@@ -636,11 +662,14 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();  // the warp's stores are complete: one arrive for the warp
-            if (lane == 0) mbar_arrive(&full_a[bs % S]);
+            if (elect_one()) mbar_arrive(&full_a[bs % S]);
+            __syncwarp();
             it += P;
           }
           sq = sn;
         }
+        nks = nks_n;
+        srow = srow_n;
       }
     }
   } else if (warp < G::kRawWarp) {
