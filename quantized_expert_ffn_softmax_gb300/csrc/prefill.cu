@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
       // reading them.
       const int r = 32 * (warp & 3) + lane;
       const int part = pi >> 7;
-      const int h = (r >> 2) & 1;  // gate/up: which 16-byte half is read first
+      const int h = (r >> 2) & 1;  // the swizzle bit of row r in a raw tile
       constexpr int P = G::kGroup;
       constexpr int OW = 32;  // TMEM columns per thread and step: 64 fp16
       // This row's block scales: one 32-bit word (two fp16) per K step, read
@@ -611,11 +611,11 @@ __global__ void __launch_bounds__(Gemm<MODE>::kThreads, 1)
               if (ok) ok = mbar_wait(&raw_full[sr], (iq / SR) & 1, p.err, tmo);
               ok = __all_sync(0xffffffffu, ok);
               if (ok) {
-                const unsigned char* rs = sR + sr * G::kRawBytes;
-                const uint4 q0 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * h);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(rs + part * kRawTile + r * 32 + 16 * (h ^ 1));
-                ca[q] = h ? q1 : q0;
-                cb[q] = h ? q0 : q1;
+                // row r's first 16 bytes sit at 16 h, its second at 16 (h ^ 1)
+                // (the tile's 32-byte swizzle)
+                const unsigned char* rs = sR + sr * G::kRawBytes + part * kRawTile + r * 32;
+                ca[q] = *reinterpret_cast<const uint4*>(rs + 16 * h);
+                cb[q] = *reinterpret_cast<const uint4*>(rs + 16 * (h ^ 1));
               }
             }
             if (!ok) {
@@ -1384,7 +1384,9 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows)
 }
 
 // 2-D map over packed 4-bit codes [rows][bytes_per_row], box {32, 128}:
-// one K step (64 codes) of 128 weight rows, stored densely (32-byte rows).
+// one K step (64 codes) of 128 weight rows, stored as 32-byte rows with the
+// 32-byte swizzle: row r's 16-byte halves swap places when (r >> 2) & 1, so
+// that a warp reading one half of 32 consecutive rows meets no bank twice.
 bool encode_codes(CUtensorMap* m, const void* base, uint64_t bytes_per_row, uint64_t rows) {
   auto enc = tmap_encode_fn();
   if (!enc) return false;
@@ -1393,7 +1395,7 @@ bool encode_codes(CUtensorMap* m, const void* base, uint64_t bytes_per_row, uint
   cuuint32_t box[2] = {32, 128};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
