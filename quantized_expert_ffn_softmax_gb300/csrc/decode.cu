@@ -754,12 +754,17 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           acc[t] = fmaf(wv.w, __uint_as_float(xv.y & 0xffff0000u), acc[t]);
         }
       }
+      // this thread is done reading the rows (generic proxy), which the copy
+      // warp refills by bulk copies once the batch is summed
+      fence_proxy_async_smem();
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         const float s = warp_sum(acc[t]);
         if (lane == 0) M.red_z[warp][t] = s;
       }
       cta_sync();
+      const bool last_batch = j0 + kWarps >= my_rows;
+      if (last_batch) named_bar_arrive(kNbRowsFree, kDecodeBlock);  // the copy warp may refill the rows buffer
       if (tid < nr * T) {
         const int jr = tid / T, t = tid - (tid / T) * T;
         float z = 0.0f;
@@ -770,12 +775,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         else
           p.gz[t] = z;  // the shared-expert gate logit
       }
-      // the rows were read through the generic proxy; the copy warp refills
-      // the buffer by bulk copies after this batch
-      fence_proxy_async_smem();
-      cta_sync();  // red_z is reused by the next batch
+      if (!last_batch) cta_sync();  // red_z is reused by the next batch
     }
-    named_bar_arrive(kNbRowsFree, kDecodeBlock);  // the copy warp may refill the rows buffer
+    if (my_rows <= 0) named_bar_arrive(kNbRowsFree, kDecodeBlock);
     grid_sync(p.bar, nbar, p.err, tmo, p.debug_extra_arrivals);
 
     // ------------------------------------------------ top-k + softmax + units
