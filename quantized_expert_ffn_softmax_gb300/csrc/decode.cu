@@ -238,6 +238,36 @@ __device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
   }
 }
 
+// Level 2: the kWarps * k candidates of each token rank one another (the
+// number of larger keys is the rank; keys are distinct), P lanes per
+// candidate, each scanning 128 / P entries of the candidate list padded to
+// 128 / P * P entries with zeros (empty).  P = 4 when the list holds at most
+// 64 candidates, else 2; compile-time, so the lane split and the scan are
+// plain shifts and an unrolled loop.
+template <int P>
+__device__ __forceinline__ void rank_candidates(const uint64_t (*cand)[kWarps * kMaxTopK],
+                                                uint64_t (*sel_key)[kMaxTopK], int T, int k, int tid) {
+  constexpr int ncp = kDecodeThreads / P;  // padded list length: 64 or 128
+  constexpr int per = ncp / P;             // entries each lane scans: 16 or 64
+  static_assert(ncp <= kWarps * kMaxTopK, "the padded list fits the candidate array");
+  const int nc = kWarps * k;
+  const int c = tid / P, part = tid % P;
+  for (int t = 0; t < T; ++t) {
+    const uint64_t mine = (c < nc) ? cand[t][c] : 0ull;
+    int r = 0;
+    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(&cand[t][part * per]);
+#pragma unroll
+    for (int q = 0; q < per / 2; ++q) {
+      const ulonglong2 o = src[q];
+      r += (part * per + 2 * q < nc && o.x > mine) ? 1 : 0;
+      r += (part * per + 2 * q + 1 < nc && o.y > mine) ? 1 : 0;
+    }
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    if (P == 4) r += __shfl_xor_sync(0xffffffffu, r, 2);
+    if (part == 0 && c < nc && r < k && mine != 0ull) sel_key[t][r] = mine;
+  }
+}
+
 }  // namespace
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
@@ -787,27 +817,8 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
     else if (E <= 512) topk_level1<2>(p.z, T, E, k, M.cand);
     else topk_level1<4>(p.z, T, E, k, M.cand);
     cta_sync();
-    {
-      const int nc = kWarps * k;                // candidates per token
-      const int ncp = nc <= 64 ? 64 : 128;      // padded with empty entries
-      const int P = kDecodeThreads / ncp;       // lanes per candidate: 4 or 2
-      const int c = tid / P, part = tid - (tid / P) * P;
-      const int per = ncp / P;                  // entries each lane scans: 16 or 64
-      for (int t = 0; t < T; ++t) {
-        const uint64_t mine = (c < nc) ? M.cand[t][c] : 0ull;
-        int r = 0;
-        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(&M.cand[t][part * per]);
-#pragma unroll 4
-        for (int q = 0; q < per / 2; ++q) {
-          const ulonglong2 o = src[q];
-          r += (part * per + 2 * q < nc && o.x > mine) ? 1 : 0;
-          r += (part * per + 2 * q + 1 < nc && o.y > mine) ? 1 : 0;
-        }
-        r += __shfl_xor_sync(0xffffffffu, r, 1);
-        if (P == 4) r += __shfl_xor_sync(0xffffffffu, r, 2);
-        if (part == 0 && c < nc && r < k && mine != 0ull) M.sel_key[t][r] = mine;
-      }
-    }
+    if (kWarps * k <= 64) rank_candidates<4>(M.cand, M.sel_key, T, k, tid);
+    else rank_candidates<2>(M.cand, M.sel_key, T, k, tid);
     cta_sync();
     if (warp < T) {
       const uint64_t sk = (lane < k) ? M.sel_key[warp][lane] : 0ull;
