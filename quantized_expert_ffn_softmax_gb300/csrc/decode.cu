@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       __syncwarp();
     };
     // Down block of work unit j: codes of every output row, row r at
-    // position (r % 4) * H/4 + r / 4 (4-D TMA boxes), and the block's H scales
+    // position (r % 4) * H/4 + r / 4 (one 5-D TMA box), and the block's H scales
     // from the block-major copy (one bulk copy); one elected lane.
     auto issue_d = [&](int l, int j, int n_routed) {
       const LayerDev& W = p.layers[l];
@@ -555,14 +555,10 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       wu_of(j, n_routed, u, b);
       const bool routed = u < n_routed;
       const size_t slot = routed ? (size_t)M.unit_slot[u] : 0;
-      const int QB = down_qbox(H), nqb = Hq / QB;
       const CUtensorMap* tm = routed ? &p.tm_down[l] : &p.tm_sh_down[l];
       if (elect_one()) {
         mbar_expect_tx(&mbar[kBarD], (uint32_t)H * 18u);
-        for (int jr = 0; jr < 4; ++jr)
-          for (int qb = 0; qb < nqb; ++qb)
-            tma_load_4d(dst_s + ((size_t)jr * Hq + (size_t)qb * QB) * 16, tm, 16 * b, jr, qb * QB,
-                        (int)slot, &mbar[kBarD]);
+        tma_load_5d(dst_s, tm, 16 * b, 0, 0, 0, (int)slot, &mbar[kBarD]);
         const uint16_t* sb = routed ? W.down_sb + (slot * CF + b) * H : W.sh_down_sb + (size_t)b * H;
         bulk_g2s(dst_s + (size_t)H * 16, sb, (uint32_t)H * 2u, &mbar[kBarD]);
       }
@@ -1242,18 +1238,22 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   }
 }
 
-// 4-D map over one matrix of down codes [slots][H][Fd/2] (bytes): dims
-// {Fd/2, 4, H/4, slots} with strides {Fd/2, 2 Fd, H Fd/2} -- row r of a slot
-// is (j, q) = (r % 4, r / 4) -- and box {16, 1, down_qbox(H), 1}: one
-// 32-column block of down_qbox(H) rows of one row plane.
+// 5-D map over one matrix of down codes [slots][H][Fd/2] (bytes) in which
+// row r = 4 q + j of a slot, q = QB q_hi + q_lo, is addressed as
+// (byte, q_lo, q_hi, j, slot): dims {Fd/2, QB, H/(4 QB), 4, slots}, strides
+// {2 Fd, 2 Fd QB, Fd/2, H Fd/2} bytes, QB = down_qbox(H).  The box {16, QB,
+// H/(4 QB), 4, 1} is one whole 32-column block of a slot in one copy, landing
+// with row r at position j * H/4 + q: the four row planes one after another.
 static bool encode_down_map(CUtensorMap* m, const void* base, int H, int Fd, int slots) {
   auto enc = tmap_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)Fd / 2, 4, (cuuint64_t)H / 4, (cuuint64_t)slots};
-  cuuint64_t strides[3] = {(cuuint64_t)Fd / 2, 2 * (cuuint64_t)Fd, (cuuint64_t)H * Fd / 2};
-  cuuint32_t box[4] = {16, 1, (cuuint32_t)down_qbox(H), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+  const int QB = down_qbox(H), nqb = H / 4 / QB;
+  cuuint64_t dims[5] = {(cuuint64_t)Fd / 2, (cuuint64_t)QB, (cuuint64_t)nqb, 4, (cuuint64_t)slots};
+  cuuint64_t strides[4] = {2 * (cuuint64_t)Fd, 2 * (cuuint64_t)Fd * QB, (cuuint64_t)Fd / 2,
+                           (cuuint64_t)H * Fd / 2};
+  cuuint32_t box[5] = {16, (cuuint32_t)QB, (cuuint32_t)nqb, 4, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
