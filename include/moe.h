@@ -36,7 +36,13 @@
  *  - Activation pointers (x, y, ids, weights) may be device pointers or host
  *    pointers (pinned or pageable).  Host inputs are copied into library
  *    buffers on the stream; when an output is a host pointer the call copies
- *    it back and synchronises the stream before returning.
+ *    it back and synchronises the stream before returning.  Exception: in
+ *    moe_forward and moe_stack_forward with at most 4 tokens, a pinned
+ *    (page-locked, device-mapped) x with 16-byte alignment is read by the
+ *    kernels in place and a pinned y is written in place, without staging
+ *    copies; such an x, like the source of a stream-ordered copy, must stay
+ *    unchanged until the stream reaches the call, and the call still
+ *    synchronises before returning when y is a host pointer.
  *  - The library owns all device memory it uses (weights and workspaces are
  *    allocated in moe_layer_create); no other call allocates device memory.
  *  - Calls that use the same layer object must not run concurrently (they

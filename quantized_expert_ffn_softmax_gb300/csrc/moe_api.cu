@@ -53,6 +53,25 @@ bool is_device_ptr(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// Where a caller's activation buffer lives: device (or managed) memory,
+// pinned host memory mapped into the device's address space (`dev` receives
+// the device address), or pageable host memory.
+enum class PtrKind { Device, PinnedHost, Pageable };
+PtrKind ptr_kind(const void* p, void** dev) {
+  *dev = nullptr;
+  cudaPointerAttributes a;
+  if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return PtrKind::Pageable;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return PtrKind::Device;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *dev = a.devicePointer;
+    return PtrKind::PinnedHost;
+  }
+  return PtrKind::Pageable;
+}
+
 // dst [S][CB][H] = src [S][H][CB] (binary16 bits): the down scales of each
 // slot with the 32-column block index outermost
 __global__ void scales_block_major(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
@@ -242,7 +261,8 @@ moe_status fill_partial(moe_layer* L, const moe_layer_weights* w, cudaMemcpyKind
 struct Stage {
   const uint16_t* x = nullptr;
   uint16_t* y = nullptr;
-  bool y_host = false;
+  bool y_host = false;  // y is copied back from the staging buffer, then the stream synchronised
+  bool y_sync = false;  // y is pinned host memory written in place: synchronise before returning
 };
 
 }  // namespace
@@ -724,31 +744,51 @@ moe_status check_common(moe_layer* L, const void* x, int T) {
 }
 
 // Brings x to the device (staging host input) and picks the y target.
-moe_status stage_in(moe_layer* L, const void* x, int T, void* y, Stage* st, cudaStream_t s) {
+// Decode-sized calls (`in_place`) read a pinned host x and write a pinned
+// host y through their device addresses: 4 KB per token each way, which the
+// kernel moves faster than two extra stream operations would.  Such an x,
+// like the source of a stream-ordered copy, must stay unchanged until the
+// stream reaches the call.
+moe_status stage_in(moe_layer* L, const void* x, int T, void* y, Stage* st, cudaStream_t s,
+                    bool in_place = false) {
   const size_t bytes = sizeof(uint16_t) * (size_t)T * L->cfg.hidden;
-  if (is_device_ptr(x)) {
+  void* xd = nullptr;
+  const PtrKind xk = ptr_kind(x, &xd);
+  if (xk == PtrKind::Device) {
     if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
       st->x = static_cast<const uint16_t*>(x);
     } else {  // the kernels read x with 16-byte loads: realign through the staging buffer
       CUDA_TRY(cudaMemcpyAsync(L->ws.x_stage, x, bytes, cudaMemcpyDeviceToDevice, s), "realign x");
       st->x = L->ws.x_stage;
     }
+  } else if (in_place && xk == PtrKind::PinnedHost && (reinterpret_cast<uintptr_t>(xd) & 15u) == 0) {
+    st->x = static_cast<const uint16_t*>(xd);
   } else {
     CUDA_TRY(cudaMemcpyAsync(L->ws.x_stage, x, bytes, cudaMemcpyHostToDevice, s), "copy x to device");
     st->x = L->ws.x_stage;
   }
   if (y) {
-    st->y_host = !is_device_ptr(y);
-    st->y = st->y_host ? L->ws.y_stage : static_cast<uint16_t*>(y);
+    void* yd = nullptr;
+    const PtrKind yk = ptr_kind(y, &yd);
+    if (yk == PtrKind::Device) {
+      st->y = static_cast<uint16_t*>(y);
+    } else if (in_place && yk == PtrKind::PinnedHost) {
+      st->y = static_cast<uint16_t*>(yd);
+      st->y_sync = true;
+    } else {
+      st->y = L->ws.y_stage;
+      st->y_host = true;
+    }
   }
   return MOE_OK;
 }
 
 moe_status stage_out(moe_layer* L, int T, void* y, const Stage& st, cudaStream_t s) {
-  if (!st.y_host) return MOE_OK;
-  const size_t bytes = sizeof(uint16_t) * (size_t)T * L->cfg.hidden;
-  CUDA_TRY(cudaMemcpyAsync(y, st.y, bytes, cudaMemcpyDeviceToHost, s), "copy y to host");
-  CUDA_TRY(cudaStreamSynchronize(s), "synchronise after copying y");
+  if (st.y_host) {
+    const size_t bytes = sizeof(uint16_t) * (size_t)T * L->cfg.hidden;
+    CUDA_TRY(cudaMemcpyAsync(y, st.y, bytes, cudaMemcpyDeviceToHost, s), "copy y to host");
+  }
+  if (st.y_host || st.y_sync) CUDA_TRY(cudaStreamSynchronize(s), "synchronise after writing y");
   return MOE_OK;
 }
 
@@ -796,7 +836,8 @@ moe_status moe_forward(moe_layer* layer, const void* x_bf16, int n_tokens, void*
   if (x_bf16 == y_bf16) return fail(MOE_ERR_INVALID, "x and y must not overlap");
   cudaStream_t s = (cudaStream_t)stream;
   Stage sg;
-  if ((st = stage_in(layer, x_bf16, n_tokens, y_bf16, &sg, s)) != MOE_OK) return st;
+  if ((st = stage_in(layer, x_bf16, n_tokens, y_bf16, &sg, s, n_tokens <= moe::kMaxDecodeTokens)) != MOE_OK)
+    return st;
   if ((st = forward_device(layer, sg.x, n_tokens, sg.y, s)) != MOE_OK) return st;
   return stage_out(layer, n_tokens, y_bf16, sg, s);
 }
@@ -823,7 +864,9 @@ moe_status moe_stack_forward_traced(moe_layer* const* layers, int n_layers, cons
     return fail(MOE_ERR_INVALID, "trace buffers must be device memory");
   cudaStream_t s = (cudaStream_t)stream;
   Stage sg;
-  if ((st = stage_in(layers[0], x_bf16, n_tokens, y_bf16, &sg, s)) != MOE_OK) return st;
+  if ((st = stage_in(layers[0], x_bf16, n_tokens, y_bf16, &sg, s, n_tokens <= moe::kMaxDecodeTokens)) !=
+      MOE_OK)
+    return st;
   const int H = c0.hidden, k = c0.top_k;
   if (n_tokens <= moe::kMaxDecodeTokens) {
     st = run_decode(layers, n_layers, sg.x, n_tokens, sg.y, (uint16_t*)h_trace_bf16,

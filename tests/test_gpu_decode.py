@@ -96,6 +96,40 @@ def test_tiny_host_pointers_match_device_pointers(cuda_device):
     layer.close()
 
 
+def test_tiny_pinned_host_buffers_read_and_written_in_place(cuda_device):
+    """Decode-sized calls read a pinned host x and write a pinned host y
+    through their device addresses (no staging copies); the results equal the
+    device-pointer calls up to the order of the fp32 reductions, for a layer,
+    a stack, and a stack with x == y."""
+    cfg = _tiny()
+    L = 3
+    made = [make_layer_host(cfg, l) for l in range(L)]
+    layers = [m[0] for m in made]
+    hs = [l.handle for l in layers]
+    x = W.activations(cfg, 6)
+    T = x.shape[0]
+
+    def close(a_bits, b_bits):
+        a, b = bf16_f64(a_bits), bf16_f64(b_bits)
+        return np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-30)
+
+    xp = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+    yp = torch.zeros_like(xp).pin_memory()
+    y_dev = to_host_bits(layers[0].forward(to_dev(x)))
+    moe.moe_forward(hs[0], xp, T, yp)  # returns after y is written
+    assert close(yp.numpy().view(np.uint16), y_dev)
+    yd = to_dev(np.zeros_like(x))
+    moe.moe_stack_forward(hs, L, to_dev(x), T, yd)
+    ys_dev = to_host_bits(yd)
+    yp.zero_()
+    moe.moe_stack_forward(hs, L, xp, T, yp)
+    assert close(yp.numpy().view(np.uint16), ys_dev)
+    moe.moe_stack_forward(hs, L, xp, T, xp)  # in place: x == y
+    assert close(xp.numpy().view(np.uint16), ys_dev)
+    for l in layers:
+        l.close()
+
+
 def test_tiny_no_shared_expert_and_top1(cuda_device):
     cfg = _tiny(shared_ffn=0, top_k=1)
     layer, Ld = make_layer_host(cfg, 0)
