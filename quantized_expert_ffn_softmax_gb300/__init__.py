@@ -190,7 +190,15 @@ def moe_forward(layer: int, x, n_tokens: int, y, stream=None) -> None:
     _check(lib().moe_forward(layer, _ptr(x), n_tokens, _ptr(y), _stream(stream)))
 
 
-def _layer_array(layers: Sequence[int]):
+def _layer_array(layers):
+    if isinstance(layers, ctypes.Array):
+        return layers
+    return (ctypes.c_void_p * len(layers))(*layers)
+
+
+def layer_array(layers: Sequence[int]):
+    """The layer handles of a stack as the C array moe_stack_forward takes;
+    a caller that runs the same stack repeatedly can build it once."""
     return (ctypes.c_void_p * len(layers))(*layers)
 
 

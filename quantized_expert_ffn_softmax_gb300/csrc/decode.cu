@@ -32,6 +32,8 @@
 // fp32.  Activations are rescaled by a per-token power of two before the
 // fp16 conversion, so their range never overflows fp16.
 #include <math.h>
+
+#include <mutex>
 #include <stdlib.h>
 
 #include "device_common.cuh"
@@ -611,6 +613,10 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
   uint32_t ph_r = 0u, ph_s = 0u, ph_d = 0u;  // router rows, slot table, down stage fills waited for
   unsigned nbar = 0;
+  // the first layer reduces into accumulator 0: zero it here (the layer's
+  // first grid barrier orders this before any reduction; the kernel zeroes
+  // the other accumulator for each next layer)
+  for (int i = blockIdx.x * kDecodeThreads + tid; i < TT * H; i += grid * kDecodeThreads) p.yacc[i] = 0.0f;
 
   for (int l = 0; l < p.n_layers; ++l) {
     const LayerDev& W = p.layers[l];
@@ -1296,22 +1302,32 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
     return MOE_ERR_INVALID;
   }
   const size_t smem = sm.total;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess) {
-    *why = "cudaFuncSetAttribute(max dynamic smem) failed";
-    return MOE_ERR_CUDA;
+  // the shared-memory limit and the residency check, once per instantiation
+  // and footprint (a host-side cost on every call otherwise)
+  static std::mutex mu;
+  static size_t checked_smem[16][2] = {};  // per device and routing instantiation: largest footprint verified
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || smem > checked_smem[dev][var ? 1 : 0]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess) {
+        *why = "cudaFuncSetAttribute(max dynamic smem) failed";
+        return MOE_ERR_CUDA;
+      }
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeBlock, smem) !=
+              cudaSuccess ||
+          per_sm < 1) {
+        *why = "decode kernel cannot be resident (occupancy query)";
+        return MOE_ERR_CUDA;
+      }
+      if (dev >= 0) checked_smem[dev][var ? 1 : 0] = smem;
+    }
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeBlock, smem) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    *why = "decode kernel cannot be resident (occupancy query)";
-    return MOE_ERR_CUDA;
-  }
-  if (cudaMemsetAsync(p.bar, 0, sizeof(GridBarrier), stream) != cudaSuccess ||
-      // the first layer reduces into accumulator 0; the kernel zeroes the other
-      cudaMemsetAsync(p.yacc, 0, sizeof(float) * kMaxDecodeTokens * p.H, stream) != cudaSuccess) {
-    *why = "cudaMemsetAsync(barrier / accumulator) failed";
+  if (cudaMemsetAsync(p.bar, 0, sizeof(GridBarrier), stream) != cudaSuccess) {
+    *why = "cudaMemsetAsync(barrier) failed";
     return MOE_ERR_CUDA;
   }
   void* args[] = {&p};
