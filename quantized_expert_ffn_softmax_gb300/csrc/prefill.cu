@@ -1212,71 +1212,83 @@ struct PartsView {
   int T, k, shared;
 };
 
-constexpr int kCombChunks = 8;  // 16-byte chunks per lane and pass: 2048 outputs per warp pass
+constexpr int kCombChunks = 4;  // 16-byte chunks per lane and pass: 1024 outputs per warp pass
+constexpr int kCombRows = 4;    // partial rows loaded at once (in flight) per warp
+
+// The partial row that lane j stands for: j < k, the token's slot j (its
+// bucket position, -1 if none); j == k, the token's shared-expert row when
+// the layer has one; -1 otherwise.  Every lane must call this.
+__device__ __forceinline__ long long combine_row(const PartsView& v, int t, int lane) {
+  const int n = v.T * v.k;
+  long long r = -1;
+  if (lane < v.k) {
+    const int p = __ldg(v.pos + (size_t)t * v.k + lane);
+    r = (p >= 0 && p < n) ? p : -1;
+  } else if (lane == v.k && v.shared) {
+    r = (long long)n + t;
+  }
+  return r;
+}
 
 // Outputs of token t in the chunks g = g0 + lane + 32 i (i < kCombChunks,
-// g < G) of 8 values: the sum of the token's partial rows times sc, each row
-// read in one sweep.  pj[j] (j < k) is the bucket position of the token's
-// slot j, or -1.
+// g < G) of 8 values: the sum of the token's partial rows (slot order, then
+// the shared row) times sc.  `myrow` is this lane's combine_row.  Rows are
+// loaded kCombRows at a time, so that a warp keeps that many in flight.
 __device__ __forceinline__ void combine_block(const PartsView& v, int t, int g0, int G, int H,
-                                              const int (&pj)[kMaxTopK], float sc,
+                                              long long myrow, float sc,
                                               float (&y)[kCombChunks][8]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < kCombChunks; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) y[i][e] = 0.0f;
-  auto add = [&](size_t row) {
-    const uint4* src = reinterpret_cast<const uint4*>(v.rows + row * H);
-    uint4 q[kCombChunks];
+  const int nrows = v.k + 1;  // lanes 0..k
+  for (int j0 = 0; j0 < nrows; j0 += kCombRows) {
+    uint4 q[kCombRows][kCombChunks];
+    bool has[kCombRows];
 #pragma unroll
-    for (int i = 0; i < kCombChunks; ++i) {
-      const int g = g0 + lane + 32 * i;
-      q[i] = g < G ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int b = 0; b < kCombRows; ++b) {
+      const long long row = __shfl_sync(0xffffffffu, myrow, (j0 + b) & 31);
+      has[b] = j0 + b < nrows && row >= 0;  // the same in every lane
+      const uint4* src = reinterpret_cast<const uint4*>(v.rows + (size_t)(has[b] ? row : 0) * H);
 #pragma unroll
-    for (int i = 0; i < kCombChunks; ++i) {
-      const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-        y[i][2 * e] += f.x;
-        y[i][2 * e + 1] += f.y;
+      for (int i = 0; i < kCombChunks; ++i) {
+        const int g = g0 + lane + 32 * i;
+        q[b][i] = (has[b] && g < G) ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
       }
     }
-  };
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < v.k && pj[j] >= 0) add((size_t)pj[j]);
-  if (v.shared) add((size_t)v.T * v.k + t);
+    for (int b = 0; b < kCombRows; ++b) {
+      if (!has[b]) continue;
+#pragma unroll
+      for (int i = 0; i < kCombChunks; ++i) {
+        const uint32_t w[4] = {q[b][i].x, q[b][i].y, q[b][i].z, q[b][i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          y[i][2 * e] += f.x;
+          y[i][2 * e + 1] += f.y;
+        }
+      }
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kCombChunks; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) y[i][e] *= sc;
 }
 
-// The bucket positions of token t's slots, read by lanes 0..k-1 and
-// shared across the warp (every lane must call this).
-__device__ __forceinline__ void combine_pos(const PartsView& v, int t, int lane, int (&pj)[kMaxTopK]) {
-  const int n = v.T * v.k;
-  int p = lane < v.k ? __ldg(v.pos + (size_t)t * v.k + lane) : -1;
-  p = (p >= 0 && p < n) ? p : -1;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) pj[j] = __shfl_sync(0xffffffffu, p, j);
-}
-
 // y (bf16 [T][H]) = the combined partial rows; one warp per token.
 __global__ void combine_kernel(const PartsView v, int H, uint16_t* __restrict__ y) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= v.T) return;
-  int pj[kMaxTopK];
-  combine_pos(v, t, lane, pj);
+  const long long myrow = combine_row(v, t, lane);
   const float sc = pow2f(2 * __ldg(v.xshift + t));
   const bool vec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
   const int G = H / 8;
   for (int g0 = 0; g0 < G; g0 += 32 * kCombChunks) {
     float yb[kCombChunks][8];
-    combine_block(v, t, g0, G, H, pj, sc, yb);
+    combine_block(v, t, g0, G, H, myrow, sc, yb);
 #pragma unroll
     for (int i = 0; i < kCombChunks; ++i) {
       const int g = g0 + lane + 32 * i;
@@ -1584,17 +1596,17 @@ __global__ void stack_boundary_kernel(const uint16_t* __restrict__ h, const Part
   const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)t * H);
   uint4* ho = reinterpret_cast<uint4*>(h_out + (size_t)t * H);
   const bool has_y = parts.rows != nullptr;
-  int pj[kMaxTopK];
+  long long myrow = -1;
   float ysc = 1.0f;
   if (has_y) {
-    combine_pos(parts, t, lane, pj);
+    myrow = combine_row(parts, t, lane);
     ysc = pow2f(2 * __ldg(parts.xshift + t));
   }
   // pass 1: y (the sum of the layer's partial rows), h', sum of squares
   float ss = 0.0f;
   for (int g0 = 0; g0 < G; g0 += 32 * kCombChunks) {
     float yb[kCombChunks][8];
-    if (has_y) combine_block(parts, t, g0, G, H, pj, ysc, yb);
+    if (has_y) combine_block(parts, t, g0, G, H, myrow, ysc, yb);
 #pragma unroll
     for (int i = 0; i < kCombChunks; ++i) {
       const int g = g0 + lane + 32 * i;
