@@ -244,16 +244,21 @@ __device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
 // number of larger keys is the rank; keys are distinct), P lanes per
 // candidate, each scanning 128 / P entries of the candidate list padded to
 // 128 / P * P entries with zeros (empty).  P = 4 when the list holds at most
-// 64 candidates, else 2; compile-time, so the lane split and the scan are
-// plain shifts and an unrolled loop.
+// 64 candidates, else 2.  The P lanes of a candidate sit 32 / P lanes apart
+// (lane = candidate-in-warp + (32 / P) * part): a warp's 16-byte shared loads
+// are served eight lanes at a time, and eight consecutive lanes then read
+// one address (a broadcast) instead of P addresses in the same banks, which
+// cost P times as long.
 template <int P>
 __device__ __forceinline__ void rank_candidates(const uint64_t (*cand)[kWarps * kMaxTopK],
                                                 uint64_t (*sel_key)[kMaxTopK], int T, int k, int tid) {
   constexpr int ncp = kDecodeThreads / P;  // padded list length: 64 or 128
   constexpr int per = ncp / P;             // entries each lane scans: 16 or 64
+  constexpr int CW = 32 / P;               // candidates per warp
   static_assert(ncp <= kWarps * kMaxTopK, "the padded list fits the candidate array");
   const int nc = kWarps * k;
-  const int c = tid / P, part = tid % P;
+  const int lane = tid & 31;
+  const int c = (tid >> 5) * CW + (lane % CW), part = lane / CW;
   for (int t = 0; t < T; ++t) {
     const uint64_t mine = (c < nc) ? cand[t][c] : 0ull;
     int r = 0;
@@ -264,8 +269,8 @@ __device__ __forceinline__ void rank_candidates(const uint64_t (*cand)[kWarps * 
       r += (part * per + 2 * q < nc && o.x > mine) ? 1 : 0;
       r += (part * per + 2 * q + 1 < nc && o.y > mine) ? 1 : 0;
     }
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
-    if (P == 4) r += __shfl_xor_sync(0xffffffffu, r, 2);
+#pragma unroll
+    for (int o = CW; o < 32; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
     if (part == 0 && c < nc && r < k && mine != 0ull) sel_key[t][r] = mine;
   }
 }
