@@ -715,7 +715,14 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       }
       // pass 2, one 8-group (32c + 8q .. +7) per step: u (stacks) and the
       // fp16 pair planes xp[(t*4 + q)*C + c] = pairs (x[32c+8q+j], x[32c+8q+j+4])
-      for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
+      const int NI = TT * (H / 8);
+      for (int i0 = tid; i0 < NI; i0 += kDecodeThreads) {
+        // within a full aligned block of 32 steps, lane L takes step
+        // 4 (L % 8) + ((L % 8) / 2 + L / 8) % 4 of the block: every quarter
+        // warp's 16-byte accesses of stage_dst / xb (at i) and of the pair
+        // planes (at g / 4) then fall in eight different bank groups
+        const int L = i0 & 31, base = i0 & ~31;
+        const int i = (base + 32 <= NI) ? base + 4 * (L & 7) + ((((L & 7) >> 1) + (L >> 3)) & 3) : i0;
         const int t = i / (H / 8), g = i - t * (H / 8);
         float inv_t = 1.0f, sc_t = 1.0f;
 #pragma unroll
