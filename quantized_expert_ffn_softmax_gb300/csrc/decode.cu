@@ -1149,8 +1149,11 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           const float h = g / (1.0f + __expf(-g)) * uu;
           M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
         }
-        cta_sync();  // the item's 16 rows of w*h are staged
+        // the down block after the odd item reads both items' rows: the
+        // even item needs no barrier of its own (the next item writes the
+        // other half of hst, and the stages are guarded by mbarriers)
         if ((q & 1) == 0) continue;
+        cta_sync();  // both items' 16 rows of w*h are staged
         // ---- down block of work unit j: both halves of its 32 rows are staged
         const int j = q >> 1;
         int ub, b;
@@ -1228,8 +1231,13 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&mbar[kBarDE]);
-        cta_sync();  // every thread is done with the down stage and the act planes
-        if (!p.down_tma && j + 1 < my_wu) issue_d_threads(j + 1);
+        // every thread is done with the down stage and the act planes before
+        // the next unit's; after the last unit the grid barrier's own CTA
+        // barrier comes first
+        if (j + 1 < my_wu) {
+          cta_sync();
+          if (!p.down_tma) issue_d_threads(j + 1);
+        }
       }
     }
     // the next layer's bulk copies land in shared memory this layer read
