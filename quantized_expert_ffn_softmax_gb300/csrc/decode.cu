@@ -579,7 +579,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
     };
     issue_slots(0);
     issue_rows(0);
-    uint32_t e_done[2] = {0u, 0u}, d_done = 0u;  // stage releases seen (phase parity)
+    // stage releases seen per gate/up stage (phase parity), as two scalars:
+    // an array indexed by the stage would live in local memory
+    uint32_t e_done0 = 0u, e_done1 = 0u, d_done = 0u;
     bool ok = true;  // false after a failed wait: keep the barrier schedule, issue nothing
     for (int l = 0; l < p.n_layers; ++l) {
       named_bar_sync(kNbRowsFree, kDecodeBlock);
@@ -597,10 +599,11 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       for (int q = 0; q < n_items; ++q) {
         const int sg = q % NG;
         if (q + NG < n_items) {
-          if (ok) ok = wait0(&mbar[kBarE0 + sg], e_done[sg] & 1u);
+          if (ok) ok = wait0(&mbar[kBarE0 + sg], (sg ? e_done1 : e_done0) & 1u);
           if (ok) issue_g(l, q + NG, n_routed);
         }
-        ++e_done[sg];
+        if (sg) ++e_done1;
+        else ++e_done0;
         if (p.down_tma && (q & 1)) {
           const int j = q >> 1;
           if (j + 1 < my_wu) {
@@ -615,7 +618,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   }
 
   // ------------------------------------------------ the compute warps
-  uint32_t gcount[2] = {0u, 0u};  // items consumed per gate/up stage (phase parity)
+  // items consumed per gate/up stage (phase parity), as two scalars: an
+  // array indexed by the stage would live in local memory
+  uint32_t gcount0 = 0u, gcount1 = 0u;
   uint32_t ph_r = 0u, ph_s = 0u, ph_d = 0u;  // router rows, slot table, down stage fills waited for
   unsigned nbar = 0;
   // the first layer reduces into accumulator 0: zero it here (the layer's
@@ -1098,8 +1103,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         const int it = item_of(q);
         const int u = (it < n_routed * ipu) ? it / ipu : n_routed;
         const int sg = q % NG;
-        const uint32_t par = gcount[sg] & 1u;
-        ++gcount[sg];
+        const uint32_t par = (sg ? gcount1 : gcount0) & 1u;
+        if (sg) ++gcount1;
+        else ++gcount0;
         const unsigned char* st = gbuf + (size_t)sg * L.g_stage;
         mbar_wait(&mbar[kBarG0 + sg], par, p.err, tmo);
         float acc[4][TT];  // rows: gate 2w, gate 2w+1, up 2w, up 2w+1
