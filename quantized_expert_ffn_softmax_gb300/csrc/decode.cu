@@ -839,6 +839,23 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
     if (kWarps * k <= 64) rank_candidates<4>(M.cand, M.sel_key, T, k, tid);
     else rank_candidates<2>(M.cand, M.sel_key, T, k, tid);
     cta_sync();
+    // the slot table of this layer (bulk-copied during the previous layer)
+    const bool slots_bulk = slots_bulk_of(l);
+    if (slots_bulk) {
+      mbar_wait(&mbar[kBarS], ph_s, p.err, tmo);
+      ph_s ^= 1u;
+    }
+    auto slot_lookup = [&](int e) { return slots_bulk ? slots[e] : __ldg(W.slot_of + e); };
+    // a partially resident layer's table holds -1 for experts without a slot
+    const bool partial = W.cache != nullptr && p.mode != kModeRoute;
+    auto slot_checked = [&](int e) {
+      int s = slot_lookup(e);
+      if (s >= S_l || (s < 0 && !partial)) {
+        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
+        s = 0;
+      }
+      return s;
+    };
     if (warp < T) {
       const uint64_t sk = (lane < k) ? M.sel_key[warp][lane] : 0ull;
       uint32_t ok2 = (uint32_t)(sk >> 32);
@@ -886,43 +903,25 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       if (lane < k) {
         M.sel_id[warp][lane] = oi2;
         M.sel_w[warp][lane] = ex / den;
+        if constexpr (TT == 1) {  // the units: the selection in selection order
+          M.unit_w[lane][0] = ex / den;
+          M.unit_expert[lane] = oi2;
+          M.unit_slot[lane] = slot_checked(oi2);
+        }
       }
-    }
-    // the slot table of this layer (bulk-copied during the previous layer)
-    const bool slots_bulk = slots_bulk_of(l);
-    if (slots_bulk) {
-      mbar_wait(&mbar[kBarS], ph_s, p.err, tmo);
-      ph_s ^= 1u;
-    }
-    auto slot_lookup = [&](int e) { return slots_bulk ? slots[e] : __ldg(W.slot_of + e); };
-    // a partially resident layer's table holds -1 for experts without a slot
-    const bool partial = W.cache != nullptr && p.mode != kModeRoute;
-    auto slot_checked = [&](int e) {
-      int s = slot_lookup(e);
-      if (s >= S_l || (s < 0 && !partial)) {
-        atomicCAS(p.err, 0, (int)MOE_ERR_BOUNDS);
-        s = 0;
-      }
-      return s;
-    };
-    if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
-    for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)
-      (&M.unit_w[0][0])[i] = 0.0f;
-    cta_sync();
-    if (TT == 1) {
-      // one token: the units are the selection itself, in selection order
-      if (tid < k) {
-        const int e = M.sel_id[0][tid];
-        M.unit_w[tid][0] = M.sel_w[0][tid];
-        M.unit_expert[tid] = e;
-        const int s = slot_checked(e);
-        M.unit_slot[tid] = s;
-      }
-      if (tid == 0) {
+      if (TT == 1 && lane == 0) {
         M.n_routed = k;
         M.n_units = k + (Fs > 0 ? 1 : 0);
       }
+    }
+    if constexpr (TT == 1) {
+      // one token: the units are the selection itself, in selection order,
+      // written by the softmax warp above (only unit_w[u][0] is read)
     } else {
+      if (tid < kMaxExperts / 32) M.bitmap[tid] = 0u;
+      for (int i = tid; i < kMaxUnits * kMaxDecodeTokens; i += kDecodeThreads)
+        (&M.unit_w[0][0])[i] = 0.0f;
+      cta_sync();
       if (tid < T * k) atomicOr(&M.bitmap[M.sel_id[tid / k][tid % k] >> 5], 1u << (M.sel_id[tid / k][tid % k] & 31));
       cta_sync();
       if (warp == 0) {  // exclusive prefix of the bitmap's popcounts
