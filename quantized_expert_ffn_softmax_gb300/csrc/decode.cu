@@ -157,6 +157,37 @@ __device__ __forceinline__ void dot_block(const uint4 w, const uint4 (&act)[TT][
   }
 }
 
+// Tensor-core form of the same dot products, for more than one token
+// (mma.sync m16n8k16, fp16 operands, fp32 accumulation).  In an MMA the 16
+// k of lane c (= lane % 4) are those of word c of a code block: the k slots
+// 2c, 2c+1 hold pair j of the word and 2c+8, 2c+9 pair j+1 (j = 0 in the
+// first MMA of a block, 2 in the second), and operand B holds the same pairs
+// of the activations.  The codes go in still biased, 1024 + n (pairs 0, 2)
+// or 64 + n (pairs 1, 3): fp16 products are exact in fp32, and the bias,
+// the sum of 1032 or 72 times each activation of the block, is taken off
+// through the accumulator's initial value.  That costs about ten of the
+// accumulator's 24 bits and saves the fp16 subtractions of the unpack.
+__device__ __forceinline__ void unpack_biased(uint32_t w, uint32_t (&v)[4]) {
+  const uint32_t w8 = w >> 8;
+  v[0] = (w & 0x000F000Fu) | 0x64006400u;   // (1024 + n0, 1024 + n4)
+  v[1] = (w & 0x00F000F0u) | 0x54005400u;   // (64 + n1, 64 + n5)
+  v[2] = (w8 & 0x000F000Fu) | 0x64006400u;  // (1024 + n2, 1024 + n6)
+  v[3] = (w8 & 0x00F000F0u) | 0x54005400u;  // (64 + n3, 64 + n7)
+}
+
+// d += A B for one m16n8k16 tile.  Lane (g = lane / 4, c = lane % 4) holds
+// A rows g and g + 8 at k 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3), B
+// column g at k 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1), and D rows g and g + 8
+// at columns 2c and 2c+1 (d0, d1 and d2, d3).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Reduce-scatter of N values (power of two, <= 32) across a warp: returns the
 // warp sum of value index (lane >> (5 - log2 N)).
 template <int N>
@@ -334,6 +365,7 @@ struct DecodeMisc {
   float hst[2][16][4];  // w*h of a gate/up item's 16 rows (double-buffered by item)
   uint4 actD[kMaxDecodeTokens][4];  // w*h of a work unit's 32 rows as fp16 pair planes
   int dsh[kMaxDecodeTokens];        // their power-of-two shifts
+  float corrd[kMaxDecodeTokens];    // their code-bias sums (tensor path, more than one token)
   // expert cache of a partially resident layer
   int n_miss;
   int miss_unit[kMaxUnits];         // routed units whose expert has no slot
@@ -1176,14 +1208,25 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           const int sh = range_shift(m);
           const float sc = pow2f(-sh);
           uint32_t o[4];
+          float cb = 0.0f;  // bias of this word's codes in the tensor path
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int e0 = 8 * qw + jj, e1 = e0 + 4;
             __half2 hh = __floats2half2_rn(M.hst[e0 >> 4][e0 & 15][t] * sc, M.hst[e1 >> 4][e1 & 15][t] * sc);
             o[jj] = *reinterpret_cast<uint32_t*>(&hh);
+            if constexpr (TT > 1) {
+              const float2 f = __half22float2(hh);
+              cb += ((jj & 1) ? 72.0f : 1032.0f) * (f.x + f.y);
+            }
           }
           M.actD[t][qw] = make_uint4(o[0], o[1], o[2], o[3]);
           if (qw == 0) M.dsh[t] = sh;
+          if constexpr (TT > 1) {  // the four words of token t sit in lanes 4t .. 4t + 3
+            constexpr unsigned mask = (TT * 4 >= 32) ? 0xffffffffu : ((1u << (TT * 4)) - 1u);
+            cb += __shfl_xor_sync(mask, cb, 1);
+            cb += __shfl_xor_sync(mask, cb, 2);
+            if (qw == 0) M.corrd[t] = cb;
+          }
         }
         if (p.down_tma) {
           mbar_wait(&mbar[kBarD], ph_d, p.err, tmo);
@@ -1192,46 +1235,113 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           cp_async_wait<0>();
         }
         cta_sync();  // the act planes, and every thread's copies of the down block
-        uint4 act[TT][4];
-        float ysc[TT];
-        bool live[TT];
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) act[t][qq] = M.actD[t][qq];
-          ysc[t] = pow2f(M.dsh[t]);
-          live[t] = (t < T) && M.unit_w[ub][t] != 0.0f;
-        }
-        // four consecutive output rows 4 q4 .. 4 q4 + 3 per thread and step,
-        // added into the layer output with one vector reduction per token
         const unsigned char* dc = dst_s;
         const unsigned char* dsc = dst_s + (size_t)H * 16;
-        for (int q4 = tid; q4 < Hq; q4 += kDecodeThreads) {
-          float d[4][TT], sc4[4];
-          if (p.down_tma) {  // rows 4 q4 .. 4 q4 + 3 of the block-major scales
-            const uint2 sv = *reinterpret_cast<const uint2*>(dsc + (size_t)q4 * 8);
-            sc4[0] = __half2float(__ushort_as_half((uint16_t)(sv.x & 0xffffu)));
-            sc4[1] = __half2float(__ushort_as_half((uint16_t)(sv.x >> 16)));
-            sc4[2] = __half2float(__ushort_as_half((uint16_t)(sv.y & 0xffffu)));
-            sc4[3] = __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)));
-          } else {
+        if constexpr (TT > 1) {
+          // tensor path: tile (q0, jr) holds rows 4 (q0 + i) + jr, i < 16, at
+          // positions jr H/4 + q0 + i (16 bytes each: one 32-column block);
+          // after the four tiles of a group lane (g, c) holds rows
+          // 4 (q0 + g) .. + 3 and 4 (q0 + g + 8) .. + 3 of tokens 2c, 2c + 1
+          const int g = lane >> 2, cq = lane & 3;
+          const int tA = 2 * cq, tB = 2 * cq + 1;
+          uint4 bx = make_uint4(0u, 0u, 0u, 0u);
+          if (g < T) bx = M.actD[g][cq];
+          const bool liveA = tA < T && M.unit_w[ub][tA] != 0.0f;
+          const bool liveB = tB < T && M.unit_w[ub][tB] != 0.0f;
+          const float ca = tA < T ? -M.corrd[tA] : 0.0f;
+          const float cb = tB < T ? -M.corrd[tB] : 0.0f;
+          const float yA = liveA ? pow2f(M.dsh[tA]) : 0.0f;
+          const float yB = liveB ? pow2f(M.dsh[tB]) : 0.0f;
+          for (int G = warp; G < Hq / 16; G += kWarps) {
+            const int q0 = 16 * G;
+            float d[4][4];
 #pragma unroll
             for (int jr = 0; jr < 4; ++jr) {
-              const uint32_t sp = *reinterpret_cast<const uint32_t*>(dsc + ((size_t)jr * Hq + q4) * 4);
-              sc4[jr] = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sp >> 16) : (sp & 0xffffu))));
+              const unsigned char* rb = dc + ((size_t)jr * Hq + q0 + g) * 16 + 4 * cq;
+              uint32_t v0[4], v1[4];
+              unpack_biased(*reinterpret_cast<const uint32_t*>(rb), v0);
+              unpack_biased(*reinterpret_cast<const uint32_t*>(rb + 8 * 16), v1);
+              d[jr][0] = ca;
+              d[jr][1] = cb;
+              d[jr][2] = ca;
+              d[jr][3] = cb;
+              mma_16816(d[jr], v0[0], v1[0], v0[1], v1[1], bx.x, bx.y);
+              mma_16816(d[jr], v0[2], v1[2], v0[3], v1[3], bx.z, bx.w);
+            }
+            float s0[4], s1[4];  // scales of rows 4 (q0 + g) + jr and 4 (q0 + g + 8) + jr
+            if (p.down_tma) {
+              const uint2 a = *reinterpret_cast<const uint2*>(dsc + (size_t)(q0 + g) * 8);
+              const uint2 e = *reinterpret_cast<const uint2*>(dsc + (size_t)(q0 + g + 8) * 8);
+              s0[0] = __half2float(__ushort_as_half((uint16_t)(a.x & 0xffffu)));
+              s0[1] = __half2float(__ushort_as_half((uint16_t)(a.x >> 16)));
+              s0[2] = __half2float(__ushort_as_half((uint16_t)(a.y & 0xffffu)));
+              s0[3] = __half2float(__ushort_as_half((uint16_t)(a.y >> 16)));
+              s1[0] = __half2float(__ushort_as_half((uint16_t)(e.x & 0xffffu)));
+              s1[1] = __half2float(__ushort_as_half((uint16_t)(e.x >> 16)));
+              s1[2] = __half2float(__ushort_as_half((uint16_t)(e.y & 0xffffu)));
+              s1[3] = __half2float(__ushort_as_half((uint16_t)(e.y >> 16)));
+            } else {
+#pragma unroll
+              for (int jr = 0; jr < 4; ++jr) {
+                const uint32_t sa = *reinterpret_cast<const uint32_t*>(dsc + ((size_t)jr * Hq + q0 + g) * 4);
+                const uint32_t se = *reinterpret_cast<const uint32_t*>(dsc + ((size_t)jr * Hq + q0 + g + 8) * 4);
+                s0[jr] = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sa >> 16) : (sa & 0xffffu))));
+                s1[jr] = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (se >> 16) : (se & 0xffffu))));
+              }
+            }
+            if (liveA) {
+              red_add_v4(ycur + (size_t)tA * H + 4 * (q0 + g), s0[0] * d[0][0] * yA, s0[1] * d[1][0] * yA,
+                         s0[2] * d[2][0] * yA, s0[3] * d[3][0] * yA);
+              red_add_v4(ycur + (size_t)tA * H + 4 * (q0 + g + 8), s1[0] * d[0][2] * yA,
+                         s1[1] * d[1][2] * yA, s1[2] * d[2][2] * yA, s1[3] * d[3][2] * yA);
+            }
+            if (liveB) {
+              red_add_v4(ycur + (size_t)tB * H + 4 * (q0 + g), s0[0] * d[0][1] * yB, s0[1] * d[1][1] * yB,
+                         s0[2] * d[2][1] * yB, s0[3] * d[3][1] * yB);
+              red_add_v4(ycur + (size_t)tB * H + 4 * (q0 + g + 8), s1[0] * d[0][3] * yB,
+                         s1[1] * d[1][3] * yB, s1[2] * d[2][3] * yB, s1[3] * d[3][3] * yB);
             }
           }
+        } else {
+          uint4 act[TT][4];
+          float ysc[TT];
+          bool live[TT];
 #pragma unroll
-          for (int jr = 0; jr < 4; ++jr) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(dc + ((size_t)jr * Hq + q4) * 16);
-            dot_block<TT>(wv, act, d[jr]);
+          for (int t = 0; t < TT; ++t) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) act[t][qq] = M.actD[t][qq];
+            ysc[t] = pow2f(M.dsh[t]);
+            live[t] = (t < T) && M.unit_w[ub][t] != 0.0f;
           }
+          // four consecutive output rows 4 q4 .. 4 q4 + 3 per thread and step,
+          // added into the layer output with one vector reduction per token
+          for (int q4 = tid; q4 < Hq; q4 += kDecodeThreads) {
+            float d[4][TT], sc4[4];
+            if (p.down_tma) {  // rows 4 q4 .. 4 q4 + 3 of the block-major scales
+              const uint2 sv = *reinterpret_cast<const uint2*>(dsc + (size_t)q4 * 8);
+              sc4[0] = __half2float(__ushort_as_half((uint16_t)(sv.x & 0xffffu)));
+              sc4[1] = __half2float(__ushort_as_half((uint16_t)(sv.x >> 16)));
+              sc4[2] = __half2float(__ushort_as_half((uint16_t)(sv.y & 0xffffu)));
+              sc4[3] = __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)));
+            } else {
 #pragma unroll
-          for (int t = 0; t < TT; ++t)
-            if (live[t])
-              red_add_v4(ycur + (size_t)t * H + 4 * q4, sc4[0] * d[0][t] * ysc[t],
-                         sc4[1] * d[1][t] * ysc[t], sc4[2] * d[2][t] * ysc[t],
-                         sc4[3] * d[3][t] * ysc[t]);
+              for (int jr = 0; jr < 4; ++jr) {
+                const uint32_t sp = *reinterpret_cast<const uint32_t*>(dsc + ((size_t)jr * Hq + q4) * 4);
+                sc4[jr] = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (sp >> 16) : (sp & 0xffffu))));
+              }
+            }
+#pragma unroll
+            for (int jr = 0; jr < 4; ++jr) {
+              const uint4 wv = *reinterpret_cast<const uint4*>(dc + ((size_t)jr * Hq + q4) * 16);
+              dot_block<TT>(wv, act, d[jr]);
+            }
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+              if (live[t])
+                red_add_v4(ycur + (size_t)t * H + 4 * q4, sc4[0] * d[0][t] * ysc[t],
+                           sc4[1] * d[1][t] * ysc[t], sc4[2] * d[2][t] * ysc[t],
+                           sc4[3] * d[3][t] * ysc[t]);
+          }
         }
         // the copy warp refills the stage by TMA (async proxy) once every
         // warp has released it
