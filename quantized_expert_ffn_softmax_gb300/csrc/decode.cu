@@ -312,10 +312,12 @@ __device__ __forceinline__ void rank_candidates(const uint64_t (*cand)[kWarps * 
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
 struct DecodeSmem {
-  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dst, total;
+  size_t mbar, misc, slots, xb, hres, xp, wr, gbuf, dst, corrx, red, total;
   size_t g_stage;
   int nmy;
-  __host__ __device__ static DecodeSmem make(int H, int E, int TT, int grid, int g_stages) {
+  // gu: gate/up items by the tensor-core path (more than one token), which
+  // adds the activations' code-bias sums and the items' cross-warp sums
+  __host__ __device__ static DecodeSmem make(int H, int E, int TT, int grid, int g_stages, int gu) {
     DecodeSmem s;
     const int C = H / 32;
     s.nmy = (E + 1 + grid - 1) / grid;  // router rows per CTA, with room for the gate row
@@ -340,6 +342,14 @@ struct DecodeSmem {
     o = (o + 127) & ~(size_t)127;
     s.dst = o;  // down block of a work unit: 16 code bytes + a 4-byte scale pair per output row
     o += (size_t)H * 20;
+    o = (o + 127) & ~(size_t)127;
+    s.corrx = s.red = o;
+    if (gu) {
+      o += (size_t)C * 16;  // [C][4] fp32: per block and token
+      o = (o + 127) & ~(size_t)127;
+      s.red = o;            // [2][kWarps][32 rows][TT] fp32, by item parity
+      o += (size_t)2 * kWarps * 32 * TT * 4;
+    }
     s.total = (o + 127) & ~(size_t)127;
     return s;
   }
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   const int CF = F / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x;
-  const DecodeSmem L = DecodeSmem::make(H, E, TT, grid, p.g_stages);
+  const DecodeSmem L = DecodeSmem::make(H, E, TT, grid, p.g_stages, p.gu_mma);
   const int NG = p.g_stages;  // 1 or 2
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
   DecodeMisc& M = *reinterpret_cast<DecodeMisc*>(smem + L.misc);
@@ -474,6 +484,10 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
   float* wr = reinterpret_cast<float*>(smem + L.wr);
   unsigned char* gbuf = smem + L.gbuf;
   unsigned char* dst_s = smem + L.dst;
+  float* corrx = reinterpret_cast<float*>(smem + L.corrx);  // tensor path: [C][4]
+  float* gred = reinterpret_cast<float*>(smem + L.red);     // tensor path: item sums
+  // gate/up items by the tensor cores: more than one token, hidden % 256 == 0
+  const bool gu_mma = TT > 1 && p.gu_mma != 0;
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i)
@@ -561,16 +575,19 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       const uint16_t* gs;
       const uint8_t* uq;
       const uint16_t* us;
+      int row0;  // the item's first row in its tensors
       if (it < n_routed * ipu) {
         const int u = it / ipu;
         const int f0 = (it - u * ipu) * 16;
         const size_t slot = (size_t)M.unit_slot[u];
+        row0 = (int)slot * F + f0;
         gq = W.gate_q + (slot * F + f0) * (H / 2);
         uq = W.up_q + (slot * F + f0) * (H / 2);
         gs = W.gate_s + (slot * F + f0) * C;
         us = W.up_s + (slot * F + f0) * C;
       } else {
         const int f0 = (it - n_routed * ipu) * 16;
+        row0 = f0;
         gq = W.sh_gate_q + (size_t)f0 * (H / 2);
         uq = W.sh_up_q + (size_t)f0 * (H / 2);
         gs = W.sh_gate_s + (size_t)f0 * C;
@@ -580,10 +597,20 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       uint64_t* bar = &mbar[kBarG0 + (q % NG)];
       if (elect_one()) {
         mbar_expect_tx(bar, (uint32_t)L.g_stage);
-        bulk_g2s(st, gq, 16u * (H / 2), bar);
-        bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
-        bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
-        bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
+        if (gu_mma) {
+          // the same bytes, block-major: codes [C][16 rows][16 B], scales
+          // [C/8][16 rows][8] (the tensor path's conflict-free layout)
+          const CUtensorMap* tm = W.tm_gu + (it < n_routed * ipu ? 0 : 2);
+          tma_load_3d(st, tm, 0, row0, 0, bar);
+          tma_load_3d(st + 16 * (H / 2), tm + 1, 0, row0, 0, bar);
+          tma_load_3d(st + 16 * H, tm + 4, 0, row0, 0, bar);
+          tma_load_3d(st + 16 * H + 32 * C, tm + 5, 0, row0, 0, bar);
+        } else {
+          bulk_g2s(st, gq, 16u * (H / 2), bar);
+          bulk_g2s(st + 16 * (H / 2), uq, 16u * (H / 2), bar);
+          bulk_g2s(st + 16 * H, gs, 16u * C * 2u, bar);
+          bulk_g2s(st + 16 * H + 32 * C, us, 16u * C * 2u, bar);
+        }
       }
       __syncwarp();
     };
@@ -799,7 +826,24 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
           __half2 hh = __floats2half2_rn(e[j] * sc_t, e[j + 4] * sc_t);
           out[j] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        xp[(t * 4 + (g & 3)) * C + (g >> 2)] = make_uint4(out[0], out[1], out[2], out[3]);
+        if (gu_mma) {
+          // tensor path: planes [t][block][word] (this step's index), and
+          // per block and token the bias sum of the unpacked codes, 1032 on
+          // pairs 0, 2 and 72 on pairs 1, 3 of every word; the block's four
+          // words are in lanes L, L^8, L^16, L^24 (full 32-step groups here)
+          xp[i] = make_uint4(out[0], out[1], out[2], out[3]);
+          float cbs = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&out[j]));
+            cbs += ((j & 1) ? 72.0f : 1032.0f) * (f.x + f.y);
+          }
+          cbs += __shfl_xor_sync(0xffffffffu, cbs, 8);
+          cbs += __shfl_xor_sync(0xffffffffu, cbs, 16);
+          if (L < 8) corrx[(g >> 2) * 4 + t] = cbs;
+        } else {
+          xp[(t * 4 + (g & 3)) * C + (g >> 2)] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
       }
       cta_sync();
     }
@@ -1141,52 +1185,124 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
         else ++gcount0;
         const unsigned char* st = gbuf + (size_t)sg * L.g_stage;
         mbar_wait(&mbar[kBarG0 + sg], par, p.err, tmo);
-        float acc[4][TT];  // rows: gate 2w, gate 2w+1, up 2w, up 2w+1
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int t = 0; t < TT; ++t) acc[r][t] = 0.0f;
-        for (int c = lane; c < C; c += 32) {
-          uint4 act[TT][4];
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) act[t][qq] = xp[(t * 4 + qq) * C + c];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int mat = r >> 1, row = 2 * warp + (r & 1);
-            const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)mat * 16 * (H / 2) +
-                                                             (size_t)row * (H / 2) + c * 16);
-            const float s =
-                __half2float(reinterpret_cast<const __half*>(st + 16 * H + mat * 32 * C)[row * C + c]);
-            float d[TT];
-            dot_block<TT>(wv, act, d);
-#pragma unroll
-            for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(s, d[t], acc[r][t]);
+        if (gu_mma) {
+          // tensor path: warp w takes blocks w, w + 8, ... of all 32 rows;
+          // lane (g, c) ends with rows g, g + 8 of gate and of up for
+          // tokens 2c, 2c + 1, summed over its blocks
+          const int g = lane >> 2, cq = lane & 3;
+          float ag[4] = {0.0f, 0.0f, 0.0f, 0.0f}, au[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          for (int b = warp; b < C; b += kWarps) {
+            uint4 bx = make_uint4(0u, 0u, 0u, 0u);
+            if (g < T) bx = xp[(g * C + b) * 4 + cq];
+            float2 cr = make_float2(0.0f, 0.0f);
+            if (2 * cq < TT) cr = *reinterpret_cast<const float2*>(corrx + b * 4 + 2 * cq);
+            const unsigned char* cg = st + (size_t)b * 256 + g * 16 + 4 * cq;  // gate codes, row g
+            const unsigned char* cu = cg + 16 * (H / 2);                       // up codes, row g
+            uint32_t v0[4], v1[4];
+            float dg[4] = {-cr.x, -cr.y, -cr.x, -cr.y}, du[4] = {-cr.x, -cr.y, -cr.x, -cr.y};
+            unpack_biased(*reinterpret_cast<const uint32_t*>(cg), v0);
+            unpack_biased(*reinterpret_cast<const uint32_t*>(cg + 128), v1);
+            mma_16816(dg, v0[0], v1[0], v0[1], v1[1], bx.x, bx.y);
+            mma_16816(dg, v0[2], v1[2], v0[3], v1[3], bx.z, bx.w);
+            unpack_biased(*reinterpret_cast<const uint32_t*>(cu), v0);
+            unpack_biased(*reinterpret_cast<const uint32_t*>(cu + 128), v1);
+            mma_16816(du, v0[0], v1[0], v0[1], v1[1], bx.x, bx.y);
+            mma_16816(du, v0[2], v1[2], v0[3], v1[3], bx.z, bx.w);
+            // scales of (row g, block b) and (row g + 8, block b)
+            const unsigned char* sc0 = st + 16 * H + ((size_t)(b >> 3) * 16 + g) * 16 + (b & 7) * 2;
+            const float sg0 = __half2float(*reinterpret_cast<const __half*>(sc0));
+            const float sg1 = __half2float(*reinterpret_cast<const __half*>(sc0 + 128));
+            const float su0 = __half2float(*reinterpret_cast<const __half*>(sc0 + 32 * C));
+            const float su1 = __half2float(*reinterpret_cast<const __half*>(sc0 + 32 * C + 128));
+            ag[0] = fmaf(sg0, dg[0], ag[0]);
+            ag[1] = fmaf(sg0, dg[1], ag[1]);
+            ag[2] = fmaf(sg1, dg[2], ag[2]);
+            ag[3] = fmaf(sg1, dg[3], ag[3]);
+            au[0] = fmaf(su0, du[0], au[0]);
+            au[1] = fmaf(su0, du[1], au[1]);
+            au[2] = fmaf(su1, du[2], au[2]);
+            au[3] = fmaf(su1, du[3], au[3]);
           }
-        }
-        // the stage is refilled by bulk copies (async proxy): fence this
-        // warp's generic reads of it before handing it back
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&mbar[kBarE0 + sg]);  // this warp is done with the stage
-        float v[4 * TT];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mbar[kBarE0 + sg]);  // this warp is done with the stage
+          // this warp's sums of the item's 32 rows (gate 0..15, up 16..31)
+          float* rw = gred + (size_t)(q & 1) * (kWarps * 32 * TT) + (size_t)warp * 32 * TT;
+          if (2 * cq < TT) {
+            rw[g * TT + 2 * cq] = ag[0];
+            rw[(g + 8) * TT + 2 * cq] = ag[2];
+            rw[(16 + g) * TT + 2 * cq] = au[0];
+            rw[(24 + g) * TT + 2 * cq] = au[2];
+            if (2 * cq + 1 < TT) {
+              rw[g * TT + 2 * cq + 1] = ag[1];
+              rw[(g + 8) * TT + 2 * cq + 1] = ag[3];
+              rw[(16 + g) * TT + 2 * cq + 1] = au[1];
+              rw[(24 + g) * TT + 2 * cq + 1] = au[3];
+            }
+          }
+          cta_sync();  // every warp's sums of the item are in place
+          if (tid < 16 * TT) {
+            const int r = tid / TT, t = tid - (tid / TT) * TT;
+            const float* ri = gred + (size_t)(q & 1) * (kWarps * 32 * TT);
+            float gs = 0.0f, us = 0.0f;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+            for (int w = 0; w < kWarps; ++w) {
+              gs += ri[(w * 32 + r) * TT + t];
+              us += ri[(w * 32 + 16 + r) * TT + t];
+            }
+            const float xs = pow2f(M.x_shift[t]);
+            const float gv = gs * xs, uv = us * xs;
+            const float h = gv / (1.0f + __expf(-gv)) * uv;
+            M.hst[q & 1][r][t] = h * M.unit_w[u][t];
+          }
+        } else {
+          float acc[4][TT];  // rows: gate 2w, gate 2w+1, up 2w, up 2w+1
 #pragma unroll
-          for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
-        // value idx = r*TT + t ends in lanes [idx*REP, (idx+1)*REP); the up row
-        // of the same (row pair, token) is 2*TT indices on: 16 lanes further
-        const float s = warp_reduce_scatter<4 * TT>(v, lane);
-        const float up = __shfl_down_sync(0xffffffffu, s, 16);
-        constexpr int REP = 32 / (4 * TT);
-        if (lane < 16 && (lane & (REP - 1)) == 0) {
-          const int idx = lane / REP;
-          const int rp = idx / TT, t = idx - (idx / TT) * TT;
-          const float xs = pow2f(M.x_shift[t]);
-          const float g = s * xs, uu = up * xs;
-          const float h = g / (1.0f + __expf(-g)) * uu;
-          M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) acc[r][t] = 0.0f;
+          for (int c = lane; c < C; c += 32) {
+            uint4 act[TT][4];
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) act[t][qq] = xp[(t * 4 + qq) * C + c];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int mat = r >> 1, row = 2 * warp + (r & 1);
+              const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)mat * 16 * (H / 2) +
+                                                               (size_t)row * (H / 2) + c * 16);
+              const float s =
+                  __half2float(reinterpret_cast<const __half*>(st + 16 * H + mat * 32 * C)[row * C + c]);
+              float d[TT];
+              dot_block<TT>(wv, act, d);
+#pragma unroll
+              for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(s, d[t], acc[r][t]);
+            }
+          }
+          // the stage is refilled by bulk copies (async proxy): fence this
+          // warp's generic reads of it before handing it back
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mbar[kBarE0 + sg]);  // this warp is done with the stage
+          float v[4 * TT];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
+          // value idx = r*TT + t ends in lanes [idx*REP, (idx+1)*REP); the up row
+          // of the same (row pair, token) is 2*TT indices on: 16 lanes further
+          const float s = warp_reduce_scatter<4 * TT>(v, lane);
+          const float up = __shfl_down_sync(0xffffffffu, s, 16);
+          constexpr int REP = 32 / (4 * TT);
+          if (lane < 16 && (lane & (REP - 1)) == 0) {
+            const int idx = lane / REP;
+            const int rp = idx / TT, t = idx - (idx / TT) * TT;
+            const float xs = pow2f(M.x_shift[t]);
+            const float g = s * xs, uu = up * xs;
+            const float h = g / (1.0f + __expf(-g)) * uu;
+            M.hst[q & 1][2 * warp + rp][t] = h * M.unit_w[u][t];
+          }
         }
         // the down block after the odd item reads both items' rows: the
         // even item needs no barrier of its own (the next item writes the
@@ -1401,6 +1517,31 @@ static bool encode_down_map(CUtensorMap* m, const void* base, int H, int Fd, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D maps over one gate or up matrix of `rows` rows for the tensor path's
+// block-major stage.  Codes [rows][H/2] bytes as (byte, row, block): dims
+// {16, rows, H/32}, strides {H/2, 16}, box {16, 16, H/32} lands 16 rows as
+// [block][row][16 B].  Scales [rows][H/32] fp16 as (half, row, 8-block
+// chunk): dims {8, rows, H/256}, strides {H/16, 16}, box {8, 16, H/256}
+// lands them as [chunk][row][8].
+static bool encode_gu_maps(CUtensorMap* codes, CUtensorMap* scales, const void* q, const void* sc,
+                           int H, int rows) {
+  auto enc = tmap_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dq[3] = {16, (cuuint64_t)rows, (cuuint64_t)H / 32};
+  cuuint64_t sq[2] = {(cuuint64_t)H / 2, 16};
+  cuuint32_t bq[3] = {16, 16, (cuuint32_t)H / 32};
+  cuuint64_t ds[3] = {8, (cuuint64_t)rows, (cuuint64_t)H / 256};
+  cuuint64_t ss[2] = {(cuuint64_t)H / 16, 16};
+  cuuint32_t bs[3] = {8, 16, (cuuint32_t)H / 256};
+  cuuint32_t e1[3] = {1, 1, 1};
+  return enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q), dq, sq, bq, e1,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+         enc(scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(sc), ds, ss, bs, e1,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status decode_prepare(moe_layer* L, const char** why) {
   const moe_layer_config& c = L->cfg;
   const bool sh = c.shared_ffn > 0;
@@ -1410,12 +1551,35 @@ moe_status decode_prepare(moe_layer* L, const char** why) {
     *why = "cuTensorMapEncodeTiled failed (decode down codes)";
     return MOE_ERR_CUDA;
   }
+  L->dev.tm_gu = nullptr;
+  if (c.hidden % 256 == 0) {
+    // gate, up, shared gate, shared up: codes in maps 0-3, scales in 4-7
+    // (without a shared expert, 2, 3, 6, 7 repeat the routed ones unused)
+    CUtensorMap m[8];
+    const int R = c.n_slots * c.ffn, Rs = sh ? c.shared_ffn : R;
+    const LayerDev& D = L->dev;
+    if (!encode_gu_maps(&m[0], &m[4], D.gate_q, D.gate_s, c.hidden, R) ||
+        !encode_gu_maps(&m[1], &m[5], D.up_q, D.up_s, c.hidden, R) ||
+        !encode_gu_maps(&m[2], &m[6], sh ? D.sh_gate_q : D.gate_q, sh ? D.sh_gate_s : D.gate_s,
+                        c.hidden, Rs) ||
+        !encode_gu_maps(&m[3], &m[7], sh ? D.sh_up_q : D.up_q, sh ? D.sh_up_s : D.up_s, c.hidden, Rs)) {
+      *why = "cuTensorMapEncodeTiled failed (decode gate/up codes)";
+      return MOE_ERR_CUDA;
+    }
+    if (cudaMalloc(&L->tm_gu_block, sizeof m) != cudaSuccess ||
+        cudaMemcpy(L->tm_gu_block, m, sizeof m, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      *why = "gate/up tensor maps to device memory";
+      return MOE_ERR_CUDA;
+    }
+    L->dev.tm_gu = static_cast<const CUtensorMap*>(L->tm_gu_block);
+  }
   return MOE_OK;
 }
 
 size_t decode_smem_bytes(const DecodeParams& p, int num_sms) {
   const int TT = p.T == 1 ? 1 : (p.T == 2 ? 2 : 4);
-  return DecodeSmem::make(p.H, p.E, TT, num_sms, 1).total;
+  return DecodeSmem::make(p.H, p.E, TT, num_sms, 1, 0).total;
 }
 
 template <int TT>
@@ -1426,13 +1590,25 @@ static moe_status launch_tt(const DecodeParams& p_in, cudaStream_t stream, int n
   auto kern = var ? moe_decode_kernel<TT, true> : moe_decode_kernel<TT, false>;
   DecodeParams p = p_in;
   const int grid = num_sms;  // one CTA per SM
-  // two gate/up stages when they fit, else one
+  // gate/up items by the tensor cores for more than one token when every
+  // layer has the block-major maps and two stages still fit; otherwise the
+  // fp16 path with two gate/up stages when they fit, else one
   const size_t cap = (size_t)227 * 1024;
+  bool gu = TT > 1 && p.H % 256 == 0;
+  for (int l = 0; l < p.n_layers; ++l) gu = gu && p.layers[l].tm_gu != nullptr;
   p.g_stages = 2;
-  DecodeSmem sm = DecodeSmem::make(p.H, p.E, TT, grid, 2);
+  p.gu_mma = 0;
+  DecodeSmem sm = DecodeSmem::make(p.H, p.E, TT, grid, 2, 0);
+  if (gu) {
+    const DecodeSmem sg = DecodeSmem::make(p.H, p.E, TT, grid, 2, 1);
+    if (sg.total <= cap) {
+      p.gu_mma = 1;
+      sm = sg;
+    }
+  }
   if (sm.total > cap) {
     p.g_stages = 1;
-    sm = DecodeSmem::make(p.H, p.E, TT, grid, 1);
+    sm = DecodeSmem::make(p.H, p.E, TT, grid, 1, 0);
   }
   if (sm.total > cap) {
     *why = "decode shared-memory footprint exceeds 227 KB for this shape";

@@ -619,6 +619,7 @@ void moe_layer_destroy(moe_layer* layer) {
   if (layer->weights_block) cudaFree(layer->weights_block);
   if (layer->ws_block) cudaFree(layer->ws_block);
   if (layer->cache_dev) cudaFree(layer->cache_dev);
+  if (layer->tm_gu_block) cudaFree(layer->tm_gu_block);
   if (layer->host_tier) cudaFreeHost(layer->host_tier);
   stream_release(layer);
   cudaGetLastError();

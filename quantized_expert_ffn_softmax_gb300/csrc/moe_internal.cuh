@@ -62,6 +62,12 @@ struct LayerDev {
   // partially resident layers: the cache (device memory); slot_of then holds
   // each expert's slot or -1 and is rewritten by the decode kernel
   const CacheDev* cache;
+  // library layers with hidden % 256 == 0: eight 3-D tensor maps (device
+  // memory) that land a gate/up item block-major for the decode kernel's
+  // tensor-core path: codes of gate, up, shared gate, shared up as
+  // [H/32 blocks][16 rows][16 B], then their scales as [H/256][16 rows][8];
+  // null otherwise
+  const CUtensorMap* tm_gu;
 };
 
 // Generation-counting grid barrier state (one per workspace, 128-B aligned).
@@ -103,6 +109,7 @@ struct DecodeParams {
   // grid has, so the bounded wait runs out and records MOE_ERR_TIMEOUT.
   int debug_extra_arrivals;
   int g_stages;        // set by the launcher: gate/up shared-memory stages (1 or 2)
+  int gu_mma;          // set by the launcher: gate/up items by the tensor-core path (T > 1)
   LayerDev layers[kMaxLayersPerLaunch];
   // per layer: MOE_ROUTING_* bits and the shared-expert gate vector [H]
   // (MOE_ROUTING_SHARED_GATE), kept apart from the weight pointers
@@ -167,6 +174,7 @@ struct moe_layer {
   CUtensorMap tmap_sh_down;  // shared expert [H][Fs/2]
   CUtensorMap tm_dec_down;     // decode: 4-D view of down codes (see DecodeParams::tm_down)
   CUtensorMap tm_dec_sh_down;  // decode: the same over the shared expert's down codes
+  void* tm_gu_block = nullptr;  // device copy of the decode gate/up maps (LayerDev::tm_gu)
   int router_shift = 0;               // router weights are scaled by 2^router_shift
   const float* sh_gate_w = nullptr;   // [H] device copy of the shared-expert gate vector, or null
   void* weights_block = nullptr;  // one allocation holding all weight copies

@@ -93,11 +93,25 @@ def test_variant_noalloc_matches_layer(cuda_device):
          for k, v in host_weights(Ld).items()}
     config = config_dict(cfg, 4)
     for T in (1, 4):
-        x = to_dev(W.activations(cfg, 9, n_tokens=T))
+        xh = W.activations(cfg, 9, n_tokens=T)
+        x = to_dev(xh)
         y = torch.empty_like(x)
         moe.moe_forward_noalloc(config, w, x, T, y)
         torch.cuda.synchronize()
-        # same kernel; the fp32 reductions may add in another order
         a, b = bf16_f64(to_host_bits(y)), bf16_f64(to_host_bits(layer.forward(x)))
-        assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-30)
+        if T == 1:
+            # same kernel path; the fp32 reductions may add in another order
+            assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-30)
+        else:
+            # more than one token: the library layer runs its gate/up items on
+            # the tensor cores (block-major tensor maps it owns), the
+            # allocation-free call keeps the fp16 path (caller-owned weights,
+            # no maps): each within the y tolerance of the oracle
+            ids, _ = layer.route(x)
+            ids = ids.cpu().numpy()
+            z = oracle.router_logits(Ld["router_w"], Ld["router_b"], xh)
+            adopt = [check_topk(ids[t], z[t], cfg.top_k) for t in range(T)]
+            y_ref = oracle.moe_forward(Ld, cfg.top_k, xh, forced_ids=ids if any(adopt) else None)[0]
+            for yv in (a, b):
+                assert np.max(np.abs(yv - y_ref)) <= y_tol(y_ref)
     layer.close()
