@@ -233,43 +233,53 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // r-th selection.
 // A candidate is the 64-bit key (order_key(z) << 32) | ~e (0 = empty), so
 // candidates compare as plain integers and never tie.
-template <int NPL>
+template <int NPL, int TT>
 __device__ __forceinline__ void topk_level1(const float* z, int T, int E, int k,
                                             uint64_t (*cand)[kWarps * kMaxTopK]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t key[kMaxDecodeTokens][NPL];
+  // the tokens' ranks are independent: one pass over the source lanes ranks
+  // G tokens at once (G * NPL <= 4 keeps the keys and ranks in registers;
+  // tokens past T rank zeros and are dropped)
+  constexpr int G = (TT * NPL <= 4) ? TT : ((4 / NPL) < 1 ? 1 : (4 / NPL));
 #pragma unroll
-  for (int t = 0; t < kMaxDecodeTokens; ++t)
+  for (int t0 = 0; t0 < TT; t0 += G) {
+    if (t0 >= T) break;
+    uint32_t key[G][NPL];
+    int rank[G][NPL];
 #pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-      const int e = 32 * warp + lane + 256 * j;
-      key[t][j] = (t < T && e < E) ? order_key(__ldcg(z + (size_t)t * E + e)) : 0u;
-    }
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-  for (int t = 0; t < kMaxDecodeTokens; ++t) {
-    if (t >= T) break;
-    int rank[NPL];
-#pragma unroll
-    for (int j = 0; j < NPL; ++j) rank[j] = 0;
+      for (int j = 0; j < NPL; ++j) {
+        const int t = t0 + g, e = 32 * warp + lane + 256 * j;
+        key[g][j] = (t < T && e < E) ? order_key(__ldcg(z + (size_t)t * E + e)) : 0u;
+        rank[g][j] = 0;
+      }
 #pragma unroll 8
     for (int src = 0; src < 32; ++src) {
 #pragma unroll
-      for (int jj = 0; jj < NPL; ++jj) {
-        const uint32_t ks = __shfl_sync(0xffffffffu, key[t][jj], src);
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int j = 0; j < NPL; ++j) {
-          // logit (src, jj) has the lower expert id iff jj < j, or jj == j and src < lane
-          const bool lower_id = (jj < j) || (jj == j && src < lane);
-          rank[j] += (ks > key[t][j] || (ks == key[t][j] && lower_id)) ? 1 : 0;
+        for (int jj = 0; jj < NPL; ++jj) {
+          const uint32_t ks = __shfl_sync(0xffffffffu, key[g][jj], src);
+#pragma unroll
+          for (int j = 0; j < NPL; ++j) {
+            // logit (src, jj) has the lower expert id iff jj < j, or jj == j and src < lane
+            const bool lower_id = (jj < j) || (jj == j && src < lane);
+            rank[g][j] += (ks > key[g][j] || (ks == key[g][j] && lower_id)) ? 1 : 0;
+          }
         }
-      }
     }
 #pragma unroll
-    for (int j = 0; j < NPL; ++j)
-      if (rank[j] < k) {
-        const uint32_t e = (uint32_t)(32 * warp + lane + 256 * j);
-        cand[t][warp * k + rank[j]] = key[t][j] ? (((uint64_t)key[t][j] << 32) | (uint64_t)(~e)) : 0ull;
-      }
+    for (int g = 0; g < G; ++g) {
+      const int t = t0 + g;
+      if (t >= T) break;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j)
+        if (rank[g][j] < k) {
+          const uint32_t e = (uint32_t)(32 * warp + lane + 256 * j);
+          cand[t][warp * k + rank[g][j]] = key[g][j] ? (((uint64_t)key[g][j] << 32) | (uint64_t)(~e)) : 0ull;
+        }
+    }
   }
 }
 
@@ -704,55 +714,77 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
       float ss[TT], mx[TT];
 #pragma unroll
       for (int t = 0; t < TT; ++t) ss[t] = mx[t] = 0.0f;
-      for (int i = tid; i < TT * (H / 8); i += kDecodeThreads) {
-        const int t = i / (H / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t < T) {
-          const int g8 = i - t * (H / 8);
-          if (l == 0) {
-            v = __ldcg(reinterpret_cast<const uint4*>(p.x_in + (size_t)t * H) + g8);
-          } else {
-            // residual: h_l = bf16(h_{l-1} + bf16(y_{l-1})); h_{l-1} is still
-            // staged here (stacks only: a single layer has no layer 1)
-            const uint4 hv = reinterpret_cast<const uint4*>(hres)[i];
-            const float4 y0 = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8);
-            const float4 y1 = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8 + 1);
-            const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-            uint32_t o[4], yo[4];
+      // steps in batches of TT, each batch's global loads issued before any
+      // of them is used: one L2 round trip per batch rather than per step
+      const int NI1 = TT * (H / 8);
+      for (int i0 = tid; i0 < NI1; i0 += TT * kDecodeThreads) {
+        uint4 xin[TT], hv[TT];
+        float4 ya[TT], yb[TT];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
-              const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
-              const float lo = __uint_as_float(hw[q] << 16) + __bfloat162float(ylo);
-              const float hi = __uint_as_float(hw[q] & 0xffff0000u) + __bfloat162float(yhi);
-              o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-                     ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-              yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
+        for (int k = 0; k < TT; ++k) {
+          const int i = i0 + k * kDecodeThreads, t = i / (H / 8);
+          xin[k] = hv[k] = make_uint4(0, 0, 0, 0);
+          ya[k] = yb[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (i < NI1 && t < T) {
+            const int g8 = i - t * (H / 8);
+            if (l == 0) {
+              xin[k] = __ldcg(reinterpret_cast<const uint4*>(p.x_in + (size_t)t * H) + g8);
+            } else {
+              hv[k] = reinterpret_cast<const uint4*>(hres)[i];
+              ya[k] = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8);
+              yb[k] = __ldcg(reinterpret_cast<const float4*>(yprev + (size_t)t * H) + 2 * g8 + 1);
             }
-            v = make_uint4(o[0], o[1], o[2], o[3]);
-            if (blockIdx.x == 0 && p.h_trace)
-              reinterpret_cast<uint4*>(p.h_trace + ((size_t)(l - 1) * T + t) * H)[g8] = v;
-            if (blockIdx.x == 0 && p.y_trace)
-              reinterpret_cast<uint4*>(p.y_trace + ((size_t)(l - 1) * T + t) * H)[g8] =
-                  make_uint4(yo[0], yo[1], yo[2], yo[3]);
           }
         }
-        reinterpret_cast<uint4*>(stage_dst)[i] = v;
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float a = 0.0f, m = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
-          a = fmaf(lo, lo, fmaf(hi, hi, a));
-          m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
-        }
+        for (int k = 0; k < TT; ++k) {
+          const int i = i0 + k * kDecodeThreads, t = i / (H / 8);
+          if (i >= NI1) break;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (t < T) {
+            const int g8 = i - t * (H / 8);
+            if (l == 0) {
+              v = xin[k];
+            } else {
+              // residual: h_l = bf16(h_{l-1} + bf16(y_{l-1})); h_{l-1} is still
+              // staged here (stacks only: a single layer has no layer 1)
+              const float yy[8] = {ya[k].x, ya[k].y, ya[k].z, ya[k].w, yb[k].x, yb[k].y, yb[k].z, yb[k].w};
+              const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
+              uint32_t o[4], yo[4];
 #pragma unroll
-        for (int tt = 0; tt < TT; ++tt)
-          if (tt == t) {
-            ss[tt] += a;
-            mx[tt] = fmaxf(mx[tt], m);
+              for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat16 ylo = __float2bfloat16_rn(yy[2 * q]);
+                const __nv_bfloat16 yhi = __float2bfloat16_rn(yy[2 * q + 1]);
+                const float lo = __uint_as_float(hw[q] << 16) + __bfloat162float(ylo);
+                const float hi = __uint_as_float(hw[q] & 0xffff0000u) + __bfloat162float(yhi);
+                o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+                yo[q] = (uint32_t)__bfloat16_as_ushort(ylo) | ((uint32_t)__bfloat16_as_ushort(yhi) << 16);
+              }
+              v = make_uint4(o[0], o[1], o[2], o[3]);
+              if (blockIdx.x == 0 && p.h_trace)
+                reinterpret_cast<uint4*>(p.h_trace + ((size_t)(l - 1) * T + t) * H)[g8] = v;
+              if (blockIdx.x == 0 && p.y_trace)
+                reinterpret_cast<uint4*>(p.y_trace + ((size_t)(l - 1) * T + t) * H)[g8] =
+                    make_uint4(yo[0], yo[1], yo[2], yo[3]);
+            }
           }
+          reinterpret_cast<uint4*>(stage_dst)[i] = v;
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          float a = 0.0f, m = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+            a = fmaf(lo, lo, fmaf(hi, hi, a));
+            m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+          }
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt)
+            if (tt == t) {
+              ss[tt] += a;
+              mx[tt] = fmaxf(mx[tt], m);
+            }
+        }
       }
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
@@ -910,9 +942,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
     // ------------------------------------------------ top-k + softmax + units
     // (every CTA computes it redundantly from the logits in L2)
     if (tid < kMaxDecodeTokens * kMaxTopK) (&M.sel_key[0][0])[tid] = 0ull;
-    if (E <= 256) topk_level1<1>(p.z, T, E, k, M.cand);
-    else if (E <= 512) topk_level1<2>(p.z, T, E, k, M.cand);
-    else topk_level1<4>(p.z, T, E, k, M.cand);
+    if (E <= 256) topk_level1<1, TT>(p.z, T, E, k, M.cand);
+    else if (E <= 512) topk_level1<2, TT>(p.z, T, E, k, M.cand);
+    else topk_level1<4, TT>(p.z, T, E, k, M.cand);
     cta_sync();
     if (kWarps * k <= 64) rank_candidates<4>(M.cand, M.sel_key, T, k, tid);
     else rank_candidates<2>(M.cand, M.sel_key, T, k, tid);
