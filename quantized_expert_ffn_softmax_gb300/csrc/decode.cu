@@ -318,6 +318,29 @@ __device__ __forceinline__ void rank_candidates(const uint64_t (*cand)[kWarps * 
   }
 }
 
+// The same ranking for several tokens at once, when a token has at most 64
+// candidates: one thread per (token, candidate), tokens tid / 64; each
+// thread counts the larger keys among its token's candidates (every lane of
+// a warp reads the same entry: a broadcast).
+__device__ __forceinline__ void rank_candidates_tokens(const uint64_t (*cand)[kWarps * kMaxTopK],
+                                                       uint64_t (*sel_key)[kMaxTopK], int T, int k,
+                                                       int tid) {
+  static_assert(kDecodeThreads >= 64 * kMaxDecodeTokens, "a thread per token and candidate");
+  const int t = tid >> 6, c = tid & 63;
+  const int nc = kWarps * k;
+  if (t >= T) return;
+  const uint64_t mine = (c < nc) ? cand[t][c] : 0ull;
+  int r = 0;
+  const ulonglong2* src = reinterpret_cast<const ulonglong2*>(&cand[t][0]);
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    const ulonglong2 o = src[q];
+    r += (2 * q < nc && o.x > mine) ? 1 : 0;
+    r += (2 * q + 1 < nc && o.y > mine) ? 1 : 0;
+  }
+  if (c < nc && r < k && mine != 0ull) sel_key[t][r] = mine;
+}
+
 }  // namespace
 
 // Shared-memory carve of the decode kernel (mirrored on the host).
@@ -946,7 +969,8 @@ __global__ void __launch_bounds__(kDecodeBlock, 1)
     else if (E <= 512) topk_level1<2, TT>(p.z, T, E, k, M.cand);
     else topk_level1<4, TT>(p.z, T, E, k, M.cand);
     cta_sync();
-    if (kWarps * k <= 64) rank_candidates<4>(M.cand, M.sel_key, T, k, tid);
+    if (TT > 1 && kWarps * k <= 64) rank_candidates_tokens(M.cand, M.sel_key, T, k, tid);
+    else if (kWarps * k <= 64) rank_candidates<4>(M.cand, M.sel_key, T, k, tid);
     else rank_candidates<2>(M.cand, M.sel_key, T, k, tid);
     cta_sync();
     // the slot table of this layer (bulk-copied during the previous layer)

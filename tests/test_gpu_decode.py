@@ -99,8 +99,8 @@ def test_tiny_host_pointers_match_device_pointers(cuda_device):
 def test_tiny_pinned_host_buffers_read_and_written_in_place(cuda_device):
     """Decode-sized calls read a pinned host x and write a pinned host y
     through their device addresses (no staging copies); the results equal the
-    device-pointer calls up to the order of the fp32 reductions, for a layer,
-    a stack, and a stack with x == y."""
+    device-pointer calls up to the order of the fp32 reductions (one bf16
+    rounding per layer), for a layer, a stack, and a stack with x == y."""
     cfg = _tiny()
     L = 3
     made = [make_layer_host(cfg, l) for l in range(L)]
@@ -109,9 +109,20 @@ def test_tiny_pinned_host_buffers_read_and_written_in_place(cuda_device):
     x = W.activations(cfg, 6)
     T = x.shape[0]
 
-    def close(a_bits, b_bits):
+    def close(a_bits, b_bits, layers=1):
+        # one bf16 rounding per layer (the fp32 reductions add in a
+        # run-dependent order, and a stack feeds each layer's rounding into
+        # the next layer's input), plus one rounding of the largest element
+        # for entries the residual sum brings near zero
         a, b = bf16_f64(a_bits), bf16_f64(b_bits)
-        return np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-30)
+        bound = layers * 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b))
+        if layers > 1:
+            bound = bound + 2.0 ** -7 * np.abs(b).max()
+        ok = np.all(np.abs(a - b) <= bound + 1e-30)
+        if not ok:
+            i = np.unravel_index(np.argmax(np.abs(a - b) - bound), a.shape)
+            print("worst", i, a[i], b[i], bound[i], "max|b|", np.abs(b).max())
+        return ok
 
     xp = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
     yp = torch.zeros_like(xp).pin_memory()
@@ -123,9 +134,9 @@ def test_tiny_pinned_host_buffers_read_and_written_in_place(cuda_device):
     ys_dev = to_host_bits(yd)
     yp.zero_()
     moe.moe_stack_forward(hs, L, xp, T, yp)
-    assert close(yp.numpy().view(np.uint16), ys_dev)
+    assert close(yp.numpy().view(np.uint16), ys_dev, L)
     moe.moe_stack_forward(hs, L, xp, T, xp)  # in place: x == y
-    assert close(xp.numpy().view(np.uint16), ys_dev)
+    assert close(xp.numpy().view(np.uint16), ys_dev, L)
     for l in layers:
         l.close()
 
