@@ -13,12 +13,13 @@
 //            the expert-unit list.  Computed redundantly by every CTA.
 //   units    a work unit is (expert unit, 32-row block of its F); CTA c
 //            takes units c, c + grid, ...  Per unit: the block's gate/up
-//            rows (two 16-row items, bulk copies into a 2-deep stage ring),
-//            fused dequant GEMV + SwiGLU -> 32 values of w*h per token; then
-//            the block's 32 columns of the down matrix (copied per thread
-//            with async 16-byte copies, straight from the packed rows)
-//            against all H outputs, added into the layer's fp32 output in
-//            L2 with reductions
+//            rows (two 16-row items copied into a 2-deep stage ring by a
+//            dedicated copy warp), fused dequant GEMV + SwiGLU -> 32 values
+//            of w*h per token; then the block's 32 columns of the down
+//            matrix (one 5-D TMA box for library layers, per-thread async
+//            copies for the allocation-free entry point) against all H
+//            outputs, added into the layer's fp32 output in L2 with
+//            reductions
 //   barrier
 //
 // Only the router logits and the layer output cross between CTAs (through
@@ -26,11 +27,13 @@
 // arrive in any order, so the last bit may differ between runs.  Packed
 // 4-bit codes become fp16 pairs with a
 // magic-exponent OR (0x6400 | n = 1024 + n, minus 1032 = n - 8, exact; a
-// nibble one position higher goes into 0x5400 = 64.0 instead);
+// nibble one position higher goes into 0x5400 = 64.0 instead).  One token:
 // products with the fp16 activations are exact and summed within a
 // 32-weight block in fp16, then scaled by the block scale and summed in
-// fp32.  Activations are rescaled by a per-token power of two before the
-// fp16 conversion, so their range never overflows fp16.
+// fp32.  Two to four tokens: the biased codes and the activations go
+// through mma.sync tiles with fp32 accumulation (see mma_16816).
+// Activations are rescaled by a per-token power of two before the fp16
+// conversion, so their range never overflows fp16.
 #include <math.h>
 
 #include <mutex>
