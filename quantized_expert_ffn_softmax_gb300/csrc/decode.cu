@@ -1625,8 +1625,13 @@ moe_status decode_prepare(moe_layer* L, const char** why) {
       *why = "cuTensorMapEncodeTiled failed (decode gate/up codes)";
       return MOE_ERR_CUDA;
     }
-    if (cudaMalloc(&L->tm_gu_block, sizeof m) != cudaSuccess ||
-        cudaMemcpy(L->tm_gu_block, m, sizeof m, cudaMemcpyHostToDevice) != cudaSuccess) {
+    if (cudaMalloc(&L->tm_gu_block, sizeof m) != cudaSuccess) {
+      L->tm_gu_block = nullptr;
+      cudaGetLastError();
+      *why = "device memory for the gate/up tensor maps";
+      return MOE_ERR_OOM;
+    }
+    if (cudaMemcpy(L->tm_gu_block, m, sizeof m, cudaMemcpyHostToDevice) != cudaSuccess) {
       cudaGetLastError();
       *why = "gate/up tensor maps to device memory";
       return MOE_ERR_CUDA;
